@@ -1,0 +1,219 @@
+"""ctypes binding of the CPU oracle (``moe_oracle.cpp``).
+
+TEST INFRASTRUCTURE ONLY: imported by tests/, the smoke check and the
+benchmark's CPU-baseline leg.  The CUDA library never imports this package.
+
+The shared object is compiled from source with the host compiler on first use
+(or by the top-level ``build()``), with floating-point contraction off so the
+fp64 results are the same on x86-64 and AArch64 hosts.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.cpp")
+_LIB = os.path.join(_HERE, "libmoe_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into a shared object next to its source."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-ffp-contract=off",
+               "-fno-fast-math", _SRC, "-o", tmp]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ctypes.CDLL(build())
+            d, i32, i64, p = ctypes.c_double, ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+            L.oracle_e2m1_value.restype = d
+            L.oracle_e2m1_value.argtypes = [ctypes.c_int]
+            L.oracle_e8m0_value.restype = d
+            L.oracle_e8m0_value.argtypes = [ctypes.c_int]
+            L.oracle_e4m3_value.restype = d
+            L.oracle_e4m3_value.argtypes = [ctypes.c_int]
+            L.oracle_e4m3_encode.restype = ctypes.c_int
+            L.oracle_e4m3_encode.argtypes = [d]
+            L.oracle_bf16_value.restype = d
+            L.oracle_bf16_value.argtypes = [ctypes.c_uint16]
+            L.oracle_bf16_round.restype = ctypes.c_uint16
+            L.oracle_bf16_round.argtypes = [d]
+            L.oracle_silu.restype = d
+            L.oracle_silu.argtypes = [d]
+            L.oracle_dequant_mxfp4.restype = None
+            L.oracle_dequant_mxfp4.argtypes = [p, p, i64, i64, p]
+            L.oracle_mxfp8_quantize.restype = None
+            L.oracle_mxfp8_quantize.argtypes = [p, i64, p, p]
+            L.oracle_route.restype = None
+            L.oracle_route.argtypes = [p, p, p, i64, i64, i64, i32, p, p, p]
+            L.oracle_permute.restype = None
+            L.oracle_permute.argtypes = [p, i64, i32, i32, p, p, p, p]
+            L.oracle_expert_mlp.restype = None
+            L.oracle_expert_mlp.argtypes = [p, p, i64, i64, p, p, p, p, p, p, p, p, p, p, p]
+            L.oracle_moe_forward.restype = None
+            L.oracle_moe_forward.argtypes = [p, i64, i64, i64, i64, i32, p, p, p, p, p, p, p, p,
+                                             p, p, p, p, p, p]
+            L.oracle_rmsnorm_bf16.restype = None
+            L.oracle_rmsnorm_bf16.argtypes = [p, i64, i64, d, p]
+            _lib = L
+    return _lib
+
+
+def _np(a, dtype):
+    """Contiguous numpy view of a CPU torch tensor or array, with the given dtype."""
+    try:
+        import torch
+        if isinstance(a, torch.Tensor):
+            a = a.detach().cpu().contiguous()
+            if a.dtype == torch.bfloat16:
+                a = a.view(torch.int16)
+            a = a.numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(a)
+    if a.dtype != dtype:
+        a = a.view(dtype) if a.dtype.itemsize == np.dtype(dtype).itemsize else a.astype(dtype)
+    return a
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+# --- scalar codecs -------------------------------------------------------------------------
+def e2m1_value(code: int) -> float:
+    return lib().oracle_e2m1_value(code)
+
+
+def e8m0_value(code: int) -> float:
+    return lib().oracle_e8m0_value(code)
+
+
+def e4m3_value(code: int) -> float:
+    return lib().oracle_e4m3_value(code)
+
+
+def e4m3_encode(v: float) -> int:
+    return lib().oracle_e4m3_encode(float(v))
+
+
+def bf16_value(bits: int) -> float:
+    return lib().oracle_bf16_value(bits)
+
+
+def bf16_round(v: float) -> int:
+    return lib().oracle_bf16_round(float(v))
+
+
+def silu(z: float) -> float:
+    return lib().oracle_silu(float(z))
+
+
+# --- array routines ------------------------------------------------------------------------
+def dequant_mxfp4(blocks, scales) -> np.ndarray:
+    """[rows, K/32, 16] uint8 + [rows, K/32] uint8 -> fp64 [rows, K]."""
+    b = _np(blocks, np.uint8)
+    s = _np(scales, np.uint8)
+    rows, nb = s.shape[-2], s.shape[-1]
+    W = np.empty((rows, nb * 32), np.float64)
+    lib().oracle_dequant_mxfp4(_ptr(b), _ptr(s), rows, nb * 32, _ptr(W))
+    return W
+
+
+def mxfp8_quantize(v):
+    """fp64 values (last dim a multiple of 32) -> (e4m3 codes uint8, e8m0 scale codes uint8)."""
+    a = _np(v, np.float64)
+    q = np.empty(a.shape, np.uint8)
+    s = np.empty(a.shape[:-1] + (a.shape[-1] // 32,), np.uint8)
+    lib().oracle_mxfp8_quantize(_ptr(a), a.size, _ptr(q), _ptr(s))
+    return q, s
+
+
+def route(x, router_w, router_b, k: int):
+    """-> (logits fp64 [T,E], ids int32 [T,k], w fp64 [T,k])."""
+    xx = _np(x, np.uint16)
+    wr = _np(router_w, np.uint16)
+    br = _np(router_b, np.uint16)
+    T, H = xx.shape
+    E = wr.shape[0]
+    logits = np.empty((T, E), np.float64)
+    ids = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float64)
+    lib().oracle_route(_ptr(xx), _ptr(wr), _ptr(br), T, H, E, k, _ptr(logits), _ptr(ids), _ptr(w))
+    return logits, ids, w
+
+
+def permute(ids, E: int):
+    """-> (cnt [E], off [E+1], sorted_rows [T*k], inv_pos [T,k]), all int32."""
+    a = _np(ids, np.int32)
+    T, k = a.shape
+    cnt = np.empty(E, np.int32)
+    off = np.empty(E + 1, np.int32)
+    sr = np.empty(T * k, np.int32)
+    inv = np.empty((T, k), np.int32)
+    lib().oracle_permute(_ptr(a), T, k, E, _ptr(cnt), _ptr(off), _ptr(sr), _ptr(inv))
+    return cnt, off, sr, inv
+
+
+def expert_mlp(xq, xs, gu_blocks, gu_scales, gu_bias, d_blocks, d_scales, d_bias):
+    """One expert on one quantised row -> dict(g, h, hq, hs, y)."""
+    xq = _np(xq, np.uint8)
+    xs = _np(xs, np.uint8)
+    gub, gus, gubias = _np(gu_blocks, np.uint8), _np(gu_scales, np.uint8), _np(gu_bias, np.uint16)
+    db, ds, dbias = _np(d_blocks, np.uint8), _np(d_scales, np.uint8), _np(d_bias, np.uint16)
+    H = xq.shape[-1]
+    I = gus.shape[0] // 2
+    g = np.empty(2 * I, np.float64)
+    h = np.empty(I, np.float64)
+    hq = np.empty(I, np.uint8)
+    hs = np.empty(I // 32, np.uint8)
+    y = np.empty(H, np.float64)
+    lib().oracle_expert_mlp(_ptr(xq), _ptr(xs), H, I, _ptr(gub), _ptr(gus), _ptr(gubias),
+                            _ptr(db), _ptr(ds), _ptr(dbias), _ptr(g), _ptr(h), _ptr(hq), _ptr(hs),
+                            _ptr(y))
+    return dict(g=g, h=h, hq=hq, hs=hs, y=y)
+
+
+def moe_forward(x, router_w, router_b, gu_blocks, gu_scales, gu_bias, d_blocks, d_scales, d_bias,
+                k: int):
+    """The whole layer -> dict(out fp64 [T,H], logits, ids, w, xq, xs)."""
+    xx = _np(x, np.uint16)
+    wr, br = _np(router_w, np.uint16), _np(router_b, np.uint16)
+    gub, gus, gubias = _np(gu_blocks, np.uint8), _np(gu_scales, np.uint8), _np(gu_bias, np.uint16)
+    db, ds, dbias = _np(d_blocks, np.uint8), _np(d_scales, np.uint8), _np(d_bias, np.uint16)
+    T, H = xx.shape
+    E = wr.shape[0]
+    I = gus.shape[1] // 2
+    out = np.empty((T, H), np.float64)
+    logits = np.empty((T, E), np.float64)
+    ids = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float64)
+    xq = np.empty((T, H), np.uint8)
+    xs = np.empty((T, H // 32), np.uint8)
+    lib().oracle_moe_forward(_ptr(xx), T, H, I, E, k, _ptr(wr), _ptr(br), _ptr(gub), _ptr(gus),
+                             _ptr(gubias), _ptr(db), _ptr(ds), _ptr(dbias), _ptr(out),
+                             _ptr(logits), _ptr(ids), _ptr(w), _ptr(xq), _ptr(xs))
+    return dict(out=out, logits=logits, ids=ids, w=w, xq=xq, xs=xs)
+
+
+def rmsnorm_bf16(x, eps: float = 1e-5) -> np.ndarray:
+    """fp64 [T,H] -> bf16 bits uint16 [T,H]."""
+    a = _np(x, np.float64)
+    T, H = a.shape
+    out = np.empty((T, H), np.uint16)
+    lib().oracle_rmsnorm_bf16(_ptr(a), T, H, eps, _ptr(out))
+    return out
