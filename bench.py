@@ -1,0 +1,418 @@
+#!/usr/bin/env python
+"""Benchmark of the MXFP4 MoE layer on GB300.
+
+Headline workload: one gpt-oss-120b-shaped MoE layer in decode, T = 4 tokens,
+H = I = 2880, E = 128, top-4 (bf16 hidden and router, MXFP4 experts, MXFP8
+activations).  A step is one full forward of the layer (router, top-k, grouping,
+gather, gate_up GEMM + SwiGLU + MXFP8, down GEMM, combine) through the C ABI.
+Steps rotate over independently seeded layers whose packed weights (1.73 GB
+each) together exceed L2 many times, so every step streams its experts from HBM.
+
+The JSON line also carries the batched-decode (T = 32, skewed routing) and the
+prefill (T = 2048) workloads, an end-to-end number with host buffers, the
+roofline of the dominant kernel, the CPU oracle baseline and the SM clocks seen
+during the timed region.  ``--impl reference`` times the CPU oracle instead.
+Under torchrun every rank runs an independent replica (the layer needs no
+collective); the value is the tokens of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import moe_synth as ms  # noqa: E402
+
+METRIC = "MoE-layer tokens/s on 1 GB300; decode HBM GB/s, prefill TFLOPS vs peak"
+H = I = 2880
+E = 128
+K_TOP = 4
+# checkpoint-format bytes of one expert (packed E2M1 + E8M0 scales + bf16 bias)
+GU_BYTES = 2 * I * (H // 2) + 2 * I * (H // 32) + 2 * I * 2
+D_BYTES = H * (I // 2) + H * (I // 32) + H * 2
+FLOP_PER_ROW = 2 * (H * 2 * I + I * H)
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], p.get("bf16_tflops_sustained", p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"moe_bench_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) >= 9:
+                    rows.append(p)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        busy = sorted(sm)[len(sm) // 2:] if sm else []
+        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        return dist, dist.get_rank(), ws, int(os.environ.get("LOCAL_RANK", "0"))
+    return None, 0, 1, 0
+
+
+def _max_over_ranks(dist, v: float, device) -> float:
+    if dist is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def _oracle_tokens_per_s(T_sample: int, budget_s: float, seed: int = 0):
+    """Single-threaded CPU oracle on the first tokens of the decode workload."""
+    import oracle
+    x = ms.make_tokens(seed, T_sample, H)
+    rw, rb = ms.make_router(seed, H, E)
+    _, ids, _ = oracle.route(x, rw, rb, K_TOP)
+    need = sorted(set(ids.reshape(-1).tolist()))
+    w = ms.make_expert_weights(seed, H, I, E, experts=need)
+    full = []
+    for t_sub in w:  # full-size arrays; experts not routed to stay zero and are never read
+        z = torch.zeros((E,) + tuple(t_sub.shape[1:]), dtype=t_sub.dtype)
+        z[need] = t_sub
+        full.append(z)
+    done, t0 = 0, time.perf_counter()
+    while done < T_sample:
+        oracle.moe_forward(x[done:done + 1], rw, rb, *full, k=K_TOP)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    el = time.perf_counter() - t0
+    return done / el, done, el
+
+
+def run_reference(args):
+    dist, rank, world, _ = _dist()
+    if rank != 0:
+        return
+    per_step = 1
+    import oracle
+    oracle.build()
+    x = ms.make_tokens(0, args.warmup + args.steps, H)
+    rw, rb = ms.make_router(0, H, E)
+    _, ids, _ = oracle.route(x, rw, rb, K_TOP)
+    need = sorted(set(ids.reshape(-1).tolist()))
+    w = ms.make_expert_weights(0, H, I, E, experts=need)
+    full = []
+    for t_sub in w:
+        z = torch.zeros((E,) + tuple(t_sub.shape[1:]), dtype=t_sub.dtype)
+        z[need] = t_sub
+        full.append(z)
+    for i in range(args.warmup):
+        oracle.moe_forward(x[i:i + 1], rw, rb, *full, k=K_TOP)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        j = args.warmup + i
+        oracle.moe_forward(x[j:j + 1], rw, rb, *full, k=K_TOP)
+    el = time.perf_counter() - t0
+    v = args.steps * per_step / el
+    line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": "decode_t4: gpt-oss-120b-shaped MoE layer, H=I=2880, E=128, top-4; "
+                                   "each step one token of the workload through the CPU oracle"},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{args.steps} tokens of the T=4 decode workload, one per step"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+class Layers:
+    """Independently seeded packed layers rotated through the steps."""
+
+    def __init__(self, n: int, device, seed: int = 0):
+        import mxfp4_mixture_experts_gemv_gb300 as moe
+        self.moe = moe
+        self.dims = moe.LayerDims(E, H, I)
+        self.packed, self.router = [], []
+        for l in range(n):
+            w = ms.make_expert_weights(seed, H, I, E, layer=l, device=device)
+            self.packed.append(moe.pack_weights(self.dims, *w))
+            torch.cuda.synchronize()
+            del w
+        self.n = n
+
+    def routers(self, hot=0, hot_bias=0.0, device="cuda", seed=0):
+        return [tuple(t.to(device) for t in ms.make_router(seed, H, E, layer=l, hot_experts=hot,
+                                                            hot_bias=hot_bias)) for l in range(self.n)]
+
+
+def _active_bytes(moe, ws, layout, n_active_out):
+    cnt = moe.view(ws, layout.counts, (E,), torch.int32)
+    n_active_out.append(int((cnt > 0).sum().item()))
+
+
+def _workload(layers: Layers, T: int, hot: int, hot_bias: float, steps: int, warmup: int, device, dist,
+              profile=True, seed=0):
+    """Time `steps` forwards of T tokens rotating over the layers; returns a stats dict."""
+    moe = layers.moe
+    routers = layers.routers(hot, hot_bias, device, seed)
+    xs = [ms.make_tokens(seed, T, H, layer=l).to(device) for l in range(layers.n)]
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+    ws = moe.alloc_workspace(layers.dims, T, K_TOP, device)
+    layout = moe.workspace_layout(layers.dims, T, K_TOP)
+    # routing statistics per layer (active experts -> algorithmic bytes)
+    act = []
+    for l in range(layers.n):
+        moe.forward(layers.dims, xs[l], routers[l][0], routers[l][1], layers.packed[l], K_TOP, out=out, workspace=ws)
+        _active_bytes(moe, ws, layout, act)
+    st = moe.device_status(ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status {moe.STATUS_NAMES.get(st, st)}: {moe.lib().moe_last_error().decode()}")
+    for i in range(warmup):
+        l = i % layers.n
+        moe.forward(layers.dims, xs[l], routers[l][0], routers[l][1], layers.packed[l], K_TOP, out=out, workspace=ws)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    _barrier(dist)
+    if profile:
+        moe.profile_begin(steps)
+    clocks = ClockSampler(torch.cuda.current_device())
+    with clocks:
+        e0.record(stream)
+        for i in range(steps):
+            l = i % layers.n
+            moe.forward(layers.dims, xs[l], routers[l][0], routers[l][1], layers.packed[l], K_TOP, out=out,
+                        workspace=ws)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    _barrier(dist)
+    ms_total = e0.elapsed_time(e1)
+    stage_ms, calls = moe.profile_end() if profile else ({}, 0)
+    st = moe.device_status(ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status {moe.STATUS_NAMES.get(st, st)}")
+    ms_step = _max_over_ranks(dist, ms_total / steps, device)
+    seq = [act[i % layers.n] for i in range(steps)]
+    n_act = sum(seq) / len(seq)
+    gu_bytes = n_act * GU_BYTES
+    d_bytes = n_act * D_BYTES
+    step_bytes = gu_bytes + d_bytes + E * H * 2 + E * 2 + 2 * T * H * 2
+    flop = T * K_TOP * FLOP_PER_ROW + 2 * T * E * H
+    stage_avg = {k: v / max(calls, 1) for k, v in stage_ms.items()}
+    return dict(T=T, ms_per_step=ms_step, tokens_per_s=T / (ms_step * 1e-3), active_experts=n_act,
+                step_bytes=step_bytes, gu_bytes=gu_bytes, d_bytes=d_bytes, flop=flop,
+                gbs=step_bytes / (ms_step * 1e-3) / 1e9, tflops=flop / (ms_step * 1e-3) / 1e12,
+                stage_ms=stage_avg, clocks=clocks.summary(), xs=xs, routers=routers, out=out, ws=ws)
+
+
+def _e2e(layers: Layers, w: dict, steps: int, warmup: int, device, dist):
+    """Same workload through the C ABI with pinned host buffers: H2D of x and D2H of out each step."""
+    moe = layers.moe
+    T = w["T"]
+    hx = [x.cpu().pin_memory() for x in w["xs"]]
+    hout = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    dx = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+    out, ws, routers = w["out"], w["ws"], w["routers"]
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        l = i % layers.n
+        dx.copy_(hx[l], non_blocking=True)
+        moe.forward(layers.dims, dx, routers[l][0], routers[l][1], layers.packed[l], K_TOP, out=out, workspace=ws)
+        hout.copy_(out, non_blocking=True)
+
+    for i in range(warmup):
+        step(i)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    _barrier(dist)
+    e0.record(stream)
+    for i in range(steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    _barrier(dist)
+    ms_step = _max_over_ranks(dist, e0.elapsed_time(e1) / steps, device)
+    return {"value": T / (ms_step * 1e-3), "unit": "tokens/s", "ms_per_step": ms_step,
+            "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2}
+
+
+def _traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[f"{kernel}@{workload}"]
+        src = os.path.join(ROOT, "mxfp4_mixture_experts_gemv_gb300", "csrc", rec["source"])
+        with open(src, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest()[:16] != rec["source_sha256_16"]:
+                return None
+        return rec["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+def run_ours(args):
+    dist, rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import mxfp4_mixture_experts_gemv_gb300 as moe
+    if not os.path.exists(moe.LIB_PATH):
+        from mxfp4_mixture_experts_gemv_gb300 import build as b
+        b.build()
+    moe.lib()
+    hbm_peak, bf16_peak, bf16_sust, peak_src = _peaks()
+    fp8_peak = 2 * bf16_peak  # kind::mxf8f6f4 runs at the fp8 rate: 2x the bf16 dense rate (nominal ratio)
+    t_gen = time.perf_counter()
+    layers = Layers(args.layers, device)
+    t_gen = time.perf_counter() - t_gen
+
+    main = _workload(layers, 4, 0, 0.0, args.steps, args.warmup, device, dist)
+    e2e = _e2e(layers, main, args.steps, args.warmup, device, dist)
+    extra = {}
+    if not args.no_extra:
+        for name, T, hot, hb, n in (("decode_t32_skewed", 32, 16, 1.0, args.steps),
+                                    ("prefill_t2048", 2048, 0, 0.0, max(10, args.steps // 5))):
+            w = _workload(layers, T, hot, hb, n, min(args.warmup, 3), device, dist)
+            gu_ms = w["stage_ms"].get("gate_up_gemm", 0) or float("nan")
+            d_ms = w["stage_ms"].get("down_gemm", 0) or float("nan")
+            expert_flop = T * K_TOP * FLOP_PER_ROW
+            extra[name] = {
+                "T": T, "tokens_per_s": world * w["tokens_per_s"], "ms_per_step": w["ms_per_step"],
+                "active_experts": w["active_experts"], "algorithmic_bytes": w["step_bytes"],
+                "gbs": w["gbs"], "tflops": w["tflops"],
+                "gemm_gbs": (w["gu_bytes"] + w["d_bytes"]) / ((gu_ms + d_ms) * 1e-3) / 1e9,
+                "gemm_tflops": expert_flop / ((gu_ms + d_ms) * 1e-3) / 1e12,
+                "gemm_tflops_frac_of_fp8_peak": expert_flop / ((gu_ms + d_ms) * 1e-3) / 1e12 / fp8_peak,
+                "stage_ms": w["stage_ms"], "clocks": w["clocks"]}
+            del w
+
+    cpu_v, cpu_n, cpu_s = (None, 0, 0.0)
+    if rank == 0 and not args.no_cpu:
+        cpu_v, cpu_n, cpu_s = _oracle_tokens_per_s(64, args.cpu_budget)
+
+    gu_ms = main["stage_ms"].get("gate_up_gemm", 0.0)
+    achieved = main["gu_bytes"] / (gu_ms * 1e-3) / 1e9 if gu_ms else None
+    value = world * main["tokens_per_s"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": main["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 x e2m1 block-scaled (E8M0), fp32 accumulate", "data": "synthetic",
+        "config": {"workload": "decode_t4: one gpt-oss-120b-shaped MoE layer, T=4 tokens, H=I=2880, E=128, "
+                               "top-4, bf16 hidden/router, MXFP4 experts, MXFP8 activations",
+                   "layers_rotated": args.layers,
+                   "l2": f"inputs larger than L2: {args.layers} independently seeded layers "
+                         f"({args.layers * moe.packed_size(layers.dims) / 1e9:.1f} GB packed) rotated per step",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "decode_hbm_gbs": main["gbs"], "decode_hbm_frac": main["gbs"] / hbm_peak,
+        "active_experts_per_step": main["active_experts"],
+        "roofline": {"kernel": "expert_gemm gate_up (tcgen05 kind::mxf8f6f4)", "bound": "hbm",
+                     "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": (achieved / hbm_peak) if achieved else None,
+                     "traffic": _traffic("expert_gemm_gate_up", "decode_t4"),
+                     "algorithmic_bytes_per_launch": main["gu_bytes"],
+                     "peak_source": f"{peak_src} hbm_gbs (copy)"},
+        "stage_ms": main["stage_ms"],
+        "e2e": e2e,
+        "gpu_launches": 7 * args.steps,
+        "clocks": main["clocks"],
+        "cpu_baseline": ({"value": cpu_v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                          "sample": f"{cpu_n} tokens of the decode workload ({cpu_s:.1f} s, single-threaded fp64)"}
+                         if cpu_v else None),
+        "workloads": extra,
+        "peaks": {"hbm_gbs": hbm_peak, "fp8_tflops": fp8_peak, "source": peak_src},
+        "setup_s": t_gen,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=8, help="independently seeded layers rotated per step")
+    ap.add_argument("--no-extra", action="store_true", help="only the headline decode workload")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of CPU oracle work")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

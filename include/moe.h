@@ -1,0 +1,175 @@
+/*
+ * moe.h — C ABI of the GB300 (sm_103a) MXFP4 mixture-of-experts layer.
+ *
+ * The layer (gpt-oss-style MoE block):
+ *   logits = x . Wr^T + br                        router GEMV, bf16 in, fp32 accumulate
+ *   ids    = top-k experts by logit (desc; lower index first on ties)
+ *   w      = softmax over the k selected logits
+ *   xq     = MXFP8(x)                              E4M3 elements, one E8M0 scale per 32
+ *   for each (token, slot j), e = ids[t][j]:
+ *     g    = xq . Wgu[e]^T + bgu[e]                MXFP4 weights, 2I outputs
+ *     h    = silu(g[0:I]) * g[I:2I]                SwiGLU
+ *     hq   = MXFP8(h)
+ *     y    = hq . Wd[e]^T + bd[e]                  MXFP4 weights, H outputs
+ *   out[t] = bf16( sum_j w[t][j] * y(t, j) )
+ *
+ * Sources: "GPT-OSS-120B on DGX Spark: From MXFP4 to NVFP4 — A Deep-Dive
+ * Benchmark", sections "GPT-OSS-120B Architecture" (128 experts, 4 active,
+ * hidden 2880, router in BF16) and "MXFP4 Tensor Structure" (the weight
+ * layout below, E2M1 values, E8M0 scales with bias 127); "GPT-OSS-120B with
+ * MXFP4 on DGX Spark (SM121/GB10)", section "What's Included" (the MoE layer
+ * as an FP8-activation x FP4-weight grouped GEMM) and "Numerical Accuracy"
+ * (full-scale block activation quantisation).  The routing rule, SwiGLU form,
+ * MXFP8 scale rule, nibble order and gate/up row order are readings of those
+ * pages, documented with the oracle.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    never allocates or frees device memory and keeps no pointer after return.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
+ *    enqueued asynchronously; no entry point synchronises the host except
+ *    moe_get_device_status.
+ *  - Argument errors are detected on the host before anything is enqueued and
+ *    return a non-zero moe_status; moe_last_error() gives the message.
+ *  - bf16 values are passed as uint16_t bit patterns.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,         /* null pointer, T < 0, top_k out of range, ... */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2,   /* H or I not a multiple of 32, I not a multiple of 64, E > 256 */
+  MOE_ERR_ALIGNMENT = 3,           /* a pointer is not 256-byte (packed/workspace) or 16-byte aligned */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace_bytes < moe_workspace_size(...) */
+  MOE_ERR_BAD_PACKED_HEADER = 5,   /* packed buffer too small for these dims */
+  MOE_ERR_CUDA = 6,                /* a CUDA runtime/driver call failed */
+  MOE_ERR_TIMEOUT = 7              /* a device-side bounded wait expired (see moe_get_device_status) */
+} moe_status;
+
+/* Layer dimensions: E experts, hidden size H, expert intermediate size I. */
+typedef struct {
+  int32_t E;
+  int32_t H;
+  int32_t I;
+} moe_dims;
+
+/*
+ * Expert weights in the checkpoint layout of the MXFP4 gpt-oss release
+ * ("MXFP4 Tensor Structure"): per projection a *_blocks tensor
+ * uint8 [E, out, in/32, 16] of packed E2M1 codes (two per byte, low nibble =
+ * even element), a *_scales tensor uint8 [E, out, in/32] of E8M0 codes
+ * (value 2^(code-127)), and a *_bias tensor bf16 [E, out].
+ * gate_up: out = 2I (rows [0, I) gate, [I, 2I) up), in = H.
+ * down:    out = H, in = I.
+ */
+typedef struct {
+  const uint8_t *gate_up_blocks;  /* [E, 2I, H/32, 16] */
+  const uint8_t *gate_up_scales;  /* [E, 2I, H/32]     */
+  const uint16_t *gate_up_bias;   /* bf16 [E, 2I]      */
+  const uint8_t *down_blocks;     /* [E, H, I/32, 16]  */
+  const uint8_t *down_scales;     /* [E, H, I/32]      */
+  const uint16_t *down_bias;      /* bf16 [E, H]       */
+} moe_mxfp4_weights;
+
+/* Byte offsets of the intermediates inside a forward workspace (for tests
+ * and debugging; all relative to the workspace base). */
+typedef struct {
+  size_t status;       /* uint32 [4]: device status words (0 = ok)                  */
+  size_t logits;       /* fp32 [T, E] router logits                                 */
+  size_t topk_ids;     /* int32 [T, k]                                              */
+  size_t topk_w;       /* fp32 [T, k]                                               */
+  size_t xq;           /* uint8 [T, H] E4M3 codes of x                              */
+  size_t xs;           /* uint8 [T, H/32] E8M0 scale codes of x                     */
+  size_t counts;       /* int32 [E] tokens per expert                               */
+  size_t offsets;      /* int32 [E+1] exclusive prefix of counts                    */
+  size_t sorted_rows;  /* int32 [T*k] flat (t*k+j) index at each grouped position   */
+  size_t inv_pos;      /* int32 [T*k] grouped position of each flat index           */
+  size_t tiles;        /* int32 [4 + 4*max_tiles]: count, 3 pad, then {expert,row0,rows,0} */
+  size_t xp;           /* uint8 [T*k, H] x codes in grouped order                   */
+  size_t xp_sf;        /* uint8 [max_tiles, ceil(H/128), 512] scale atoms of xp     */
+  size_t hq;           /* uint8 [T*k, I] E4M3 codes of h                            */
+  size_t hq_sf;        /* uint8 [max_tiles, ceil(I/128), 512] scale atoms of hq     */
+  size_t y;            /* fp32 [T*k, H] per-(token, slot) expert outputs            */
+  size_t total;        /* bytes needed                                              */
+  int32_t max_tiles;   /* capacity of the tile list                                 */
+  int32_t tile_rows;   /* token rows per tile used for this T                       */
+} moe_workspace_layout;
+
+/* Bytes of the packed (repacked) weight buffer for these dims; 0 if the
+ * dims are unsupported. */
+size_t moe_packed_size(moe_dims d);
+
+/*
+ * Repack checkpoint-layout MXFP4 expert weights into the layout the forward
+ * kernels stream: rows padded along the contraction axis to a multiple of
+ * 128 elements, gate and up rows interleaved per 128-row tile, E8M0 scales
+ * rearranged into the tensor-core scale-factor atoms, biases widened to fp32.
+ * The source tensors are only read.  `packed` (device, 256-byte aligned,
+ * >= moe_packed_size(d) bytes) is fully written, header included.
+ * Asynchronous on `stream`; the source must stay valid until the work ends.
+ */
+moe_status moe_pack_weights(moe_dims d, const moe_mxfp4_weights *src, void *packed,
+                            size_t packed_bytes, void *stream);
+
+/* Workspace bytes moe_forward needs for up to T tokens with top_k. */
+size_t moe_workspace_size(moe_dims d, int32_t T, int32_t top_k);
+
+/* Offsets of the intermediates for T tokens (same layout moe_forward uses). */
+moe_status moe_workspace_layout_get(moe_dims d, int32_t T, int32_t top_k,
+                                    moe_workspace_layout *out);
+
+/*
+ * One MoE layer forward for T tokens.
+ *   hidden    bf16 [T, H]            (16-byte aligned)
+ *   router_w  bf16 [E, H]            (16-byte aligned)
+ *   router_b  bf16 [E]
+ *   packed    output of moe_pack_weights for the same dims
+ *   top_k     1 <= top_k <= min(E, 8)
+ *   out       bf16 [T, H]            (written; may not alias the inputs)
+ *   workspace device scratch, 256-byte aligned, >= moe_workspace_size(d, T, top_k)
+ * T = 0 is a no-op returning MOE_OK.  Nothing is allocated; no host
+ * synchronisation happens, so the call can be captured into a CUDA graph.
+ * Device-side bounded waits that expire set a status word in the workspace
+ * (read it with moe_get_device_status) and the kernels return early; they
+ * never trap or hang.
+ */
+moe_status moe_forward(moe_dims d, const void *hidden, int32_t T, const void *router_w,
+                       const void *router_b, const void *packed, int32_t top_k, void *out,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
+/* Synchronise `stream`, then read the workspace status words: MOE_OK, or
+ * MOE_ERR_TIMEOUT if a kernel of the last forward gave up on a wait. */
+moe_status moe_get_device_status(const void *workspace, void *stream);
+
+/*
+ * Optional per-stage timing of moe_forward with CUDA events (host-side event
+ * objects only; no device memory).  moe_profile_begin(n) arms event recording
+ * for the next n forward calls; moe_profile_end synchronises on the recorded
+ * events and writes, per stage, the summed milliseconds over the recorded calls
+ * into stage_ms[0..6] and the number of calls into *calls.  Stages: 0 router
+ * GEMV, 1 top-k + softmax + MXFP8 of x, 2 grouping, 3 gather, 4 gate_up GEMM,
+ * 5 down GEMM, 6 combine.  Each stage's events are recorded on the stream the
+ * forward runs on, around that stage's launch.  Not thread-safe; not for use
+ * while a forward is being captured into a CUDA graph.
+ */
+moe_status moe_profile_begin(int32_t max_calls);
+moe_status moe_profile_end(double *stage_ms, int32_t *calls);
+
+/* Thread-local message of the last non-OK status returned on this thread. */
+const char *moe_last_error(void);
+
+/* Library version (packed layout version in the low 16 bits). */
+uint32_t moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,208 @@
+"""Python binding of the GB300 MXFP4 mixture-of-experts layer.
+
+Argument marshalling only: every step of the layer runs in the CUDA kernels of
+``libmoe_gb300.so`` (see ``include/moe.h``).  torch supplies device memory and
+the current stream.  There is no fallback: if the shared library is missing or
+a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
+
+MOE_OK = 0
+STATUS_NAMES = {
+    0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE", 3: "MOE_ERR_ALIGNMENT",
+    4: "MOE_ERR_WORKSPACE_TOO_SMALL", 5: "MOE_ERR_BAD_PACKED_HEADER", 6: "MOE_ERR_CUDA",
+    7: "MOE_ERR_TIMEOUT",
+}
+
+# Every symbol the C ABI exports (include/moe.h).
+EXPORTED = ["moe_packed_size", "moe_pack_weights", "moe_workspace_size", "moe_workspace_layout_get",
+            "moe_forward", "moe_get_device_status", "moe_profile_begin", "moe_profile_end",
+            "moe_last_error", "moe_version"]
+STAGES = ["router", "topk_quant", "grouping", "gather", "gate_up_gemm", "down_gemm", "combine"]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("E", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32)]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("gate_up_blocks", "gate_up_scales", "gate_up_bias",
+                                                "down_blocks", "down_scales", "down_bias")]
+
+
+class WorkspaceLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in (
+        "status", "logits", "topk_ids", "topk_w", "xq", "xs", "counts", "offsets", "sorted_rows",
+        "inv_pos", "tiles", "xp", "xp_sf", "hq", "hq_sf", "y", "total")] + [
+        ("max_tiles", ctypes.c_int32), ("tile_rows", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load the shared library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: run __graft_entry__.build() (or "
+                               "python -m mxfp4_mixture_experts_gemv_gb300.build) first")
+        L = ctypes.CDLL(LIB_PATH)
+        sz, st, vp, i32 = ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p, ctypes.c_int32
+        L.moe_packed_size.restype = sz
+        L.moe_packed_size.argtypes = [Dims]
+        L.moe_pack_weights.restype = st
+        L.moe_pack_weights.argtypes = [Dims, ctypes.POINTER(Weights), vp, sz, vp]
+        L.moe_workspace_size.restype = sz
+        L.moe_workspace_size.argtypes = [Dims, i32, i32]
+        L.moe_workspace_layout_get.restype = st
+        L.moe_workspace_layout_get.argtypes = [Dims, i32, i32, ctypes.POINTER(WorkspaceLayout)]
+        L.moe_forward.restype = st
+        L.moe_forward.argtypes = [Dims, vp, i32, vp, vp, vp, i32, vp, vp, sz, vp]
+        L.moe_get_device_status.restype = st
+        L.moe_get_device_status.argtypes = [vp, vp]
+        L.moe_profile_begin.restype = st
+        L.moe_profile_begin.argtypes = [i32]
+        L.moe_profile_end.restype = st
+        L.moe_profile_end.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int32)]
+        L.moe_last_error.restype = ctypes.c_char_p
+        L.moe_last_error.argtypes = []
+        L.moe_version.restype = ctypes.c_uint32
+        L.moe_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != MOE_OK:
+        raise MoeError(status, lib().moe_last_error().decode())
+
+
+def _stream(stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _dev_ptr(t: torch.Tensor, name: str, dtype=None) -> int:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+@dataclasses.dataclass(frozen=True)
+class LayerDims:
+    E: int
+    H: int
+    I: int
+
+    def c(self) -> Dims:
+        return Dims(self.E, self.H, self.I)
+
+
+def packed_size(dims: LayerDims) -> int:
+    return lib().moe_packed_size(dims.c())
+
+
+def workspace_size(dims: LayerDims, T: int, top_k: int) -> int:
+    return lib().moe_workspace_size(dims.c(), T, top_k)
+
+
+def workspace_layout(dims: LayerDims, T: int, top_k: int) -> WorkspaceLayout:
+    out = WorkspaceLayout()
+    _check(lib().moe_workspace_layout_get(dims.c(), T, top_k, ctypes.byref(out)))
+    return out
+
+
+def _alloc_aligned(nbytes: int, device) -> torch.Tensor:
+    """uint8 device buffer whose data pointer is 256-byte aligned."""
+    buf = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+    off = (-buf.data_ptr()) % 256
+    return buf[off:off + nbytes]
+
+
+def pack_weights(dims: LayerDims, gate_up_blocks, gate_up_scales, gate_up_bias, down_blocks,
+                 down_scales, down_bias, packed: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Repack checkpoint-layout MXFP4 expert weights (CUDA tensors) into the forward layout."""
+    n = packed_size(dims)
+    if n == 0:
+        _check(lib().moe_pack_weights(dims.c(), None, None, 0, None))
+    if packed is None:
+        packed = _alloc_aligned(n, gate_up_blocks.device)
+    w = Weights(_dev_ptr(gate_up_blocks, "gate_up_blocks", torch.uint8),
+                _dev_ptr(gate_up_scales, "gate_up_scales", torch.uint8),
+                _dev_ptr(gate_up_bias, "gate_up_bias", torch.bfloat16),
+                _dev_ptr(down_blocks, "down_blocks", torch.uint8),
+                _dev_ptr(down_scales, "down_scales", torch.uint8),
+                _dev_ptr(down_bias, "down_bias", torch.bfloat16))
+    _check(lib().moe_pack_weights(dims.c(), ctypes.byref(w), _dev_ptr(packed, "packed"),
+                                  packed.numel() * packed.element_size(), _stream(stream)))
+    return packed
+
+
+def alloc_workspace(dims: LayerDims, T: int, top_k: int, device="cuda") -> torch.Tensor:
+    return _alloc_aligned(max(workspace_size(dims, T, top_k), 256), device)
+
+
+def forward(dims: LayerDims, hidden: torch.Tensor, router_w: torch.Tensor, router_b: torch.Tensor,
+            packed: torch.Tensor, top_k: int, out: torch.Tensor | None = None,
+            workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """One MoE layer: bf16 hidden [T, H] -> bf16 out [T, H]."""
+    T = hidden.shape[0]
+    if out is None:
+        out = torch.empty_like(hidden)
+    if workspace is None:
+        workspace = alloc_workspace(dims, T, top_k, hidden.device)
+    _check(lib().moe_forward(dims.c(), _dev_ptr(hidden, "hidden", torch.bfloat16), T,
+                             _dev_ptr(router_w, "router_w", torch.bfloat16),
+                             _dev_ptr(router_b, "router_b", torch.bfloat16),
+                             _dev_ptr(packed, "packed"), top_k, _dev_ptr(out, "out", torch.bfloat16),
+                             _dev_ptr(workspace, "workspace"),
+                             workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def profile_begin(max_calls: int):
+    """Arm per-stage event timing for the next ``max_calls`` forward calls."""
+    _check(lib().moe_profile_begin(max_calls))
+
+
+def profile_end() -> tuple[dict, int]:
+    """-> ({stage: summed ms}, calls recorded)."""
+    ms = (ctypes.c_double * 8)()
+    calls = ctypes.c_int32()
+    _check(lib().moe_profile_end(ms, ctypes.byref(calls)))
+    return {name: ms[i] for i, name in enumerate(STAGES)}, calls.value
+
+
+def device_status(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronise and return the status of the last forward that used ``workspace``."""
+    return lib().moe_get_device_status(_dev_ptr(workspace, "workspace"), _stream(stream))
+
+
+def view(workspace: torch.Tensor, offset: int, shape, dtype) -> torch.Tensor:
+    """A typed view of a workspace section (for tests and debugging)."""
+    n = 1
+    for s in shape:
+        n *= s
+    nbytes = n * torch.empty(0, dtype=dtype).element_size()
+    return workspace[offset:offset + nbytes].view(dtype).view(*shape)

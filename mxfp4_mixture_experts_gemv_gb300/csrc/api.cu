@@ -1,0 +1,233 @@
+// C ABI of the MXFP4 MoE layer: argument validation, workspace carving and the
+// launch sequence  router -> top-k/quant -> grouping -> gather -> gate_up GEMM
+// -> down GEMM -> combine, all on the caller's stream.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+moe_status fail(moe_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+moe_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(MOE_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+moe_status check_dims(const moe_dims& d) {
+  if (d.E <= 0 || d.H <= 0 || d.I <= 0) return fail(MOE_ERR_INVALID_ARG, "dims must be positive (E=%d H=%d I=%d)", d.E, d.H, d.I);
+  if (d.E > 256) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "E=%d > 256 experts", d.E);
+  if (d.H % 32) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "H=%d is not a multiple of 32", d.H);
+  if (d.I % 64) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "I=%d is not a multiple of 64", d.I);
+  return MOE_OK;
+}
+
+constexpr int kStages = 7;
+
+// Per-stage CUDA events of profiled forward calls.
+struct Profiler {
+  bool armed = false;
+  std::vector<cudaEvent_t> ev;  // (kStages + 1) events per call
+  int capacity = 0, used = 0;
+};
+Profiler g_prof;
+
+cudaEvent_t* profile_slot() {
+  if (!g_prof.armed || g_prof.used >= g_prof.capacity) return nullptr;
+  return &g_prof.ev[(size_t)(g_prof.used++) * (kStages + 1)];
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 1;
+  return n;
+}
+
+}  // namespace
+
+extern "C" {
+
+uint32_t moe_version(void) { return (1u << 16) | moe::kPackedVersion; }
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+size_t moe_packed_size(moe_dims d) {
+  moe::PackedHeader h;
+  if (check_dims(d) != MOE_OK || !moe::packed_layout(d, &h)) return 0;
+  return (size_t)h.total;
+}
+
+moe_status moe_pack_weights(moe_dims d, const moe_mxfp4_weights* src, void* packed, size_t packed_bytes,
+                            void* stream) {
+  moe_status st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if (!src || !packed) return fail(MOE_ERR_INVALID_ARG, "null src or packed pointer");
+  if (!src->gate_up_blocks || !src->gate_up_scales || !src->gate_up_bias || !src->down_blocks ||
+      !src->down_scales || !src->down_bias)
+    return fail(MOE_ERR_INVALID_ARG, "null weight tensor pointer");
+  if (!aligned(packed, 256)) return fail(MOE_ERR_ALIGNMENT, "packed buffer must be 256-byte aligned");
+  if (!aligned(src->gate_up_blocks, 16) || !aligned(src->down_blocks, 16))
+    return fail(MOE_ERR_ALIGNMENT, "*_blocks tensors must be 16-byte aligned");
+  moe::PackedHeader h;
+  moe::packed_layout(d, &h);
+  if (packed_bytes < h.total)
+    return fail(MOE_ERR_BAD_PACKED_HEADER, "packed buffer has %zu bytes, %llu needed", packed_bytes,
+                (unsigned long long)h.total);
+  cudaError_t e = moe::launch_pack(d, h, *src, static_cast<uint8_t*>(packed), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "pack kernels");
+  return MOE_OK;
+}
+
+size_t moe_workspace_size(moe_dims d, int32_t T, int32_t top_k) {
+  moe_workspace_layout l;
+  if (check_dims(d) != MOE_OK || T < 0 || top_k <= 0 || !moe::workspace_layout(d, T, top_k, &l)) return 0;
+  return l.total;
+}
+
+moe_status moe_workspace_layout_get(moe_dims d, int32_t T, int32_t top_k, moe_workspace_layout* out) {
+  moe_status st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if (!out || T < 0 || top_k <= 0 || top_k > 8 || top_k > d.E)
+    return fail(MOE_ERR_INVALID_ARG, "bad layout query (T=%d top_k=%d)", T, top_k);
+  moe::workspace_layout(d, T, top_k, out);
+  return MOE_OK;
+}
+
+moe_status moe_forward(moe_dims d, const void* hidden, int32_t T, const void* router_w, const void* router_b,
+                       const void* packed, int32_t top_k, void* out, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  moe_status st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T=%d < 0", T);
+  if (top_k < 1 || top_k > 8 || top_k > d.E) return fail(MOE_ERR_INVALID_ARG, "top_k=%d outside [1, min(E, 8)]", top_k);
+  if (T == 0) return MOE_OK;
+  if ((int64_t)T * top_k * (int64_t)(d.H > d.I ? d.H : d.I) >= (int64_t)1 << 31)
+    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "T*top_k*max(H,I) must stay below 2^31");
+  if (!hidden || !router_w || !router_b || !packed || !out || !workspace)
+    return fail(MOE_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(hidden, 16) || !aligned(router_w, 16) || !aligned(out, 16))
+    return fail(MOE_ERR_ALIGNMENT, "hidden, router_w and out must be 16-byte aligned");
+  if (!aligned(packed, 256) || !aligned(workspace, 256))
+    return fail(MOE_ERR_ALIGNMENT, "packed and workspace must be 256-byte aligned");
+  moe_workspace_layout L;
+  moe::workspace_layout(d, T, top_k, &L);
+  if (workspace_bytes < L.total)
+    return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "workspace has %zu bytes, %zu needed", workspace_bytes, L.total);
+  moe::PackedHeader h;
+  moe::packed_layout(d, &h);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const uint8_t* pk = static_cast<const uint8_t*>(packed);
+  auto at = [&](size_t off) { return ws + off; };
+  const int TK = T * top_k;
+  uint32_t* status = reinterpret_cast<uint32_t*>(at(L.status));
+  int32_t* ids = reinterpret_cast<int32_t*>(at(L.topk_ids));
+  float* w = reinterpret_cast<float*>(at(L.topk_w));
+  int32_t* tiles = reinterpret_cast<int32_t*>(at(L.tiles));
+  int32_t* inv_pos = reinterpret_cast<int32_t*>(at(L.inv_pos));
+  int32_t* sorted_rows = reinterpret_cast<int32_t*>(at(L.sorted_rows));
+  const int sms = num_sms();
+
+  cudaError_t e = cudaMemsetAsync(status, 0, 16, s);
+  if (e != cudaSuccess) return cuda_fail(e, "status reset");
+  cudaEvent_t* pev = profile_slot();
+  auto mark = [&](int i) {
+    if (pev) cudaEventRecord(pev[i], s);
+  };
+  mark(0);
+  e = moe::launch_router(static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(router_w),
+                         static_cast<const uint16_t*>(router_b), T, d.H, d.E, reinterpret_cast<float*>(at(L.logits)), s);
+  if (e != cudaSuccess) return cuda_fail(e, "router kernel");
+  mark(1);
+  e = moe::launch_topk_quant(reinterpret_cast<const float*>(at(L.logits)), static_cast<const uint16_t*>(hidden), T,
+                             d.H, d.E, top_k, ids, w, at(L.xq), at(L.xs), s);
+  if (e != cudaSuccess) return cuda_fail(e, "top-k/quantise kernel");
+  mark(2);
+  e = moe::launch_permute(ids, TK, top_k, d.E, L.tile_rows, L.max_tiles, reinterpret_cast<int32_t*>(at(L.counts)),
+                          reinterpret_cast<int32_t*>(at(L.offsets)), sorted_rows, inv_pos, tiles, s);
+  if (e != cudaSuccess) return cuda_fail(e, "grouping kernel");
+  mark(3);
+  e = moe::launch_gather(at(L.xq), at(L.xs), sorted_rows, tiles, L.max_tiles, top_k, d.H, d.I, L.tile_rows, at(L.xp),
+                         at(L.xp_sf), at(L.hq_sf), s);
+  if (e != cudaSuccess) return cuda_fail(e, "gather kernel");
+  mark(4);
+  e = moe::launch_expert_gemm(true, h, pk, at(L.xp), TK, at(L.xp_sf), tiles, L.max_tiles, L.tile_rows, at(L.hq),
+                              at(L.hq_sf), nullptr, status, sms, s);
+  if (e != cudaSuccess) return cuda_fail(e, "gate_up GEMM");
+  mark(5);
+  e = moe::launch_expert_gemm(false, h, pk, at(L.hq), TK, at(L.hq_sf), tiles, L.max_tiles, L.tile_rows, nullptr,
+                              nullptr, reinterpret_cast<float*>(at(L.y)), status, sms, s);
+  if (e != cudaSuccess) return cuda_fail(e, "down GEMM");
+  mark(6);
+  e = moe::launch_combine(reinterpret_cast<const float*>(at(L.y)), w, inv_pos, T, top_k, d.H,
+                          static_cast<uint16_t*>(out), s);
+  if (e != cudaSuccess) return cuda_fail(e, "combine kernel");
+  mark(7);
+  return MOE_OK;
+}
+
+moe_status moe_profile_begin(int32_t max_calls) {
+  if (max_calls <= 0) return fail(MOE_ERR_INVALID_ARG, "max_calls=%d", max_calls);
+  const size_t need = (size_t)max_calls * (kStages + 1);
+  while (g_prof.ev.size() < need) {
+    cudaEvent_t ev;
+    cudaError_t e = cudaEventCreate(&ev);
+    if (e != cudaSuccess) return cuda_fail(e, "event create");
+    g_prof.ev.push_back(ev);
+  }
+  g_prof.capacity = max_calls;
+  g_prof.used = 0;
+  g_prof.armed = true;
+  return MOE_OK;
+}
+
+moe_status moe_profile_end(double* stage_ms, int32_t* calls) {
+  if (!stage_ms || !calls) return fail(MOE_ERR_INVALID_ARG, "null output");
+  g_prof.armed = false;
+  for (int i = 0; i < kStages; ++i) stage_ms[i] = 0.0;
+  *calls = g_prof.used;
+  for (int c = 0; c < g_prof.used; ++c) {
+    cudaEvent_t* ev = &g_prof.ev[(size_t)c * (kStages + 1)];
+    cudaError_t e = cudaEventSynchronize(ev[kStages]);
+    if (e != cudaSuccess) return cuda_fail(e, "event synchronize");
+    for (int i = 0; i < kStages; ++i) {
+      float ms = 0.f;
+      e = cudaEventElapsedTime(&ms, ev[i], ev[i + 1]);
+      if (e != cudaSuccess) return cuda_fail(e, "event elapsed");
+      stage_ms[i] += ms;
+    }
+  }
+  g_prof.used = 0;
+  return MOE_OK;
+}
+
+moe_status moe_get_device_status(const void* workspace, void* stream) {
+  if (!workspace) return fail(MOE_ERR_INVALID_ARG, "null workspace");
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  uint32_t st[4] = {0, 0, 0, 0};
+  e = cudaMemcpy(st, workspace, sizeof(st), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (st[0] != 0)
+    return fail(MOE_ERR_TIMEOUT, "device wait expired (status bits 0x%x, first expired wait 0x%08x)", st[0], st[1]);
+  return MOE_OK;
+}
+
+}  // extern "C"

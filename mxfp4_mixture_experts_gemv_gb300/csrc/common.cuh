@@ -1,0 +1,143 @@
+// Internal definitions shared by the kernels of the MXFP4 MoE layer (sm_103a).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------------------
+// Packed weight buffer (written by moe_pack_weights).
+//
+// Expert weights are stored so each 128-row x 128-element tile can be fetched by
+// one TMA box and fed to tcgen05.mma without reshuffling:
+//   data  [E][rows][Kp/2] bytes: checkpoint rows, contraction axis padded with
+//         zero nibbles to Kp = round_up(K, 128) (TMA's 4-bit unpacking mode needs
+//         a multiple of 128 elements per row).
+//   sf    [E][ceil(rows/128)][Kp/128][512] bytes: E8M0 scales in scale-factor
+//         atoms; byte (r%32)*16 + (r/32)*4 + (kb%4) of atom (r/128, kb/4) holds the
+//         scale of row r, 32-element block kb.  Padding blocks hold code 127 (1.0).
+//   bias  [E][rows] fp32.
+// gate_up rows are interleaved: tile t holds gate rows 64t..64t+63 in tile rows
+// 0..63 and the matching up rows in tile rows 64..127, so one accumulator tile
+// carries both halves of the SwiGLU.
+// ---------------------------------------------------------------------------------------
+constexpr uint32_t kPackedMagic = 0x4D584645u;  // "EFXM"
+constexpr uint32_t kPackedVersion = 1;
+constexpr int kTileM = 128;   // weight rows per tile (MMA M)
+constexpr int kTileK = 128;   // contraction elements per pipeline stage
+constexpr int kAtomBytes = 512;
+
+struct PackedHeader {
+  uint32_t magic, version;
+  int32_t E, H, I, Hp, Ip, gu_mtiles, d_mtiles, gu_ktiles, d_ktiles, pad0;
+  uint64_t off_gu_data, off_gu_sf, off_gu_bias, off_d_data, off_d_sf, off_d_bias, total;
+};
+
+inline int64_t round_up(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
+
+inline bool packed_layout(const moe_dims& d, PackedHeader* hd) {
+  if (d.E <= 0 || d.H <= 0 || d.I <= 0) return false;
+  if (d.E > 256 || d.H % 32 || d.I % 64) return false;
+  PackedHeader h = {};
+  h.magic = kPackedMagic;
+  h.version = kPackedVersion;
+  h.E = d.E; h.H = d.H; h.I = d.I;
+  h.Hp = (int32_t)round_up(d.H, kTileK);
+  h.Ip = (int32_t)round_up(d.I, kTileK);
+  h.gu_mtiles = 2 * d.I / kTileM;
+  h.d_mtiles = (int32_t)((d.H + kTileM - 1) / kTileM);
+  h.gu_ktiles = h.Hp / kTileK;
+  h.d_ktiles = h.Ip / kTileK;
+  uint64_t off = 1024;
+  auto take = [&](uint64_t bytes) { uint64_t o = off; off = (uint64_t)round_up(off + bytes, 1024); return o; };
+  h.off_gu_data = take((uint64_t)d.E * 2 * d.I * (h.Hp / 2));
+  h.off_gu_sf = take((uint64_t)d.E * h.gu_mtiles * h.gu_ktiles * kAtomBytes);
+  h.off_gu_bias = take((uint64_t)d.E * 2 * d.I * 4);
+  h.off_d_data = take((uint64_t)d.E * d.H * (h.Ip / 2));
+  h.off_d_sf = take((uint64_t)d.E * h.d_mtiles * h.d_ktiles * kAtomBytes);
+  h.off_d_bias = take((uint64_t)d.E * d.H * 4);
+  h.total = off;
+  *hd = h;
+  return true;
+}
+
+// Token rows per tile of the grouped GEMM (MMA N upper bound) for T tokens.
+inline int tile_rows_for(int T) {
+  if (T <= 16) return 16;
+  if (T <= 32) return 32;
+  if (T <= 64) return 64;
+  return 128;
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline bool workspace_layout(const moe_dims& d, int T, int k, moe_workspace_layout* L) {
+  if (T < 0 || k <= 0) return false;
+  const int64_t TK = (int64_t)T * k;
+  const int tr = tile_rows_for(T);
+  const int64_t max_tiles = TK / tr + (TK < d.E ? TK : d.E) + 1;
+  const int64_t kth = (d.H + kTileK - 1) / kTileK, kti = (d.I + kTileK - 1) / kTileK;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t r = o; o = align256(o + bytes); return r; };
+  moe_workspace_layout l = {};
+  l.status = take(16);
+  l.logits = take((size_t)T * d.E * 4);
+  l.topk_ids = take((size_t)TK * 4);
+  l.topk_w = take((size_t)TK * 4);
+  l.xq = take((size_t)T * d.H);
+  l.xs = take((size_t)T * (d.H / 32));
+  l.counts = take((size_t)d.E * 4);
+  l.offsets = take((size_t)(d.E + 1) * 4);
+  l.sorted_rows = take((size_t)TK * 4);
+  l.inv_pos = take((size_t)TK * 4);
+  l.tiles = take((size_t)(4 + 4 * max_tiles) * 4);
+  l.xp = take((size_t)TK * d.H + 256);
+  l.xp_sf = take((size_t)max_tiles * kth * kAtomBytes);
+  l.hq = take((size_t)TK * d.I + 256);
+  l.hq_sf = take((size_t)max_tiles * kti * kAtomBytes);
+  l.y = take((size_t)TK * d.H * 4);
+  l.total = o;
+  l.max_tiles = (int32_t)max_tiles;
+  l.tile_rows = tr;
+  *L = l;
+  return true;
+}
+
+// Status words (first 16 bytes of the workspace).
+enum : uint32_t {
+  kStatusTimeoutProducer = 1u << 0,
+  kStatusTimeoutMma = 1u << 1,
+  kStatusTimeoutEpilogue = 1u << 2,
+  kStatusTimeoutDrain = 1u << 3,
+};
+
+// Bounded waits give up after this many nanoseconds (a healthy wait lasts
+// microseconds).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Kernel launchers (defined in the .cu files).
+cudaError_t launch_pack(const moe_dims& d, const PackedHeader& h, const moe_mxfp4_weights& w,
+                        uint8_t* packed, cudaStream_t s);
+cudaError_t launch_router(const uint16_t* x, const uint16_t* wr, const uint16_t* br, int T, int H,
+                          int E, float* logits, cudaStream_t s);
+cudaError_t launch_topk_quant(const float* logits, const uint16_t* x, int T, int H, int E, int k,
+                              int32_t* ids, float* w, uint8_t* xq, uint8_t* xs, cudaStream_t s);
+cudaError_t launch_permute(const int32_t* ids, int TK, int k, int E, int tile_rows, int max_tiles,
+                           int32_t* counts, int32_t* offsets, int32_t* sorted_rows,
+                           int32_t* inv_pos, int32_t* tiles, cudaStream_t s);
+cudaError_t launch_gather(const uint8_t* xq, const uint8_t* xs, const int32_t* sorted_rows,
+                          const int32_t* tiles, int max_tiles, int k, int H, int I, int tile_rows,
+                          uint8_t* xp, uint8_t* xp_sf, uint8_t* hq_sf, cudaStream_t s);
+cudaError_t launch_expert_gemm(bool gate_up, const PackedHeader& h, const uint8_t* packed,
+                               const uint8_t* b_rows, int b_rows_total, const uint8_t* b_sf,
+                               const int32_t* tiles, int max_tiles, int tile_rows, uint8_t* hq,
+                               uint8_t* hq_sf, float* y, uint32_t* status, int num_sms,
+                               cudaStream_t s);
+cudaError_t launch_combine(const float* y, const float* w, const int32_t* inv_pos, int T, int k,
+                           int H, uint16_t* out, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,151 @@
+// Expert grouping: histogram, exclusive prefix, stable permutation of the
+// (token, slot) pairs by expert, the GEMM tile list, and the gather of the
+// quantised activations into grouped order with their scale atoms.
+//
+// The grouping is deterministic: counts are order-free and every pair's
+// position is its rank among equal experts in ascending flat index t*k+j,
+// decided with warp match/popcount, never by atomics racing for slots.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kPermThreads = 1024;
+constexpr int kPermWarps = kPermThreads / 32;
+
+__global__ void __launch_bounds__(kPermThreads) permute_kernel(
+    const int32_t* __restrict__ ids, int TK, int E, int tile_rows, int max_tiles, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_rows, int32_t* __restrict__ inv_pos,
+    int32_t* __restrict__ tiles) {
+  __shared__ int hist[kPermWarps][257];
+  __shared__ int s_off[258];
+  __shared__ int s_tile_off[258];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kPermWarps * 257; i += kPermThreads) (&hist[0][0])[i] = 0;
+  __syncthreads();
+  const int chunk = (TK + kPermWarps - 1) / kPermWarps;
+  const int start = min(TK, warp * chunk), end = min(TK, start + chunk);
+  // ids come from the top-k kernel and are always in [0, E); the clamp only keeps
+  // shared-memory indexing safe whatever the input
+  for (int i = start + lane; i < end; i += 32) atomicAdd(&hist[warp][min(max(ids[i], 0), E - 1)], 1);
+  __syncthreads();
+  if (threadIdx.x < E) {
+    int c = 0;
+    for (int w = 0; w < kPermWarps; ++w) c += hist[w][threadIdx.x];
+    counts[threadIdx.x] = c;
+    s_off[threadIdx.x] = c;
+    s_tile_off[threadIdx.x] = (c + tile_rows - 1) / tile_rows;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0, trun = 0;
+    for (int e = 0; e < E; ++e) {
+      const int c = s_off[e], tc = s_tile_off[e];
+      s_off[e] = run;
+      s_tile_off[e] = trun;
+      run += c;
+      trun += tc;
+    }
+    s_off[E] = run;
+    s_tile_off[E] = trun;
+  }
+  __syncthreads();
+  if (threadIdx.x < E) {
+    const int e = threadIdx.x;
+    int run = s_off[e];
+    for (int w = 0; w < kPermWarps; ++w) {
+      const int c = hist[w][e];
+      hist[w][e] = run;
+      run += c;
+    }
+    offsets[e] = s_off[e];
+    // tile list entries of expert e
+    const int cnt = s_off[e + 1] - s_off[e];
+    int t = s_tile_off[e];
+    for (int r0 = 0; r0 < cnt && t < max_tiles; r0 += tile_rows, ++t) {
+      int4 td = make_int4(e, s_off[e] + r0, min(tile_rows, cnt - r0), 0);
+      reinterpret_cast<int4*>(tiles + 4)[t] = td;
+    }
+  }
+  if (threadIdx.x == 0) {
+    offsets[E] = s_off[E];
+    tiles[0] = min(s_tile_off[E], max_tiles);
+  }
+  __syncthreads();
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int base = start; base < end; base += 32) {
+    const int i = base + lane;
+    const bool valid = i < end;
+    const int e = valid ? min(max(ids[i], 0), E - 1) : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lt_mask);
+    if (valid) {
+      const int pos = hist[warp][e] + rank;
+      sorted_rows[pos] = i;
+      inv_pos[i] = pos;
+    }
+    __syncwarp();
+    if (valid && rank == 0) hist[warp][e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+// One CTA per tile: copy the tile's activation rows into grouped order and
+// write the tile's scale atoms (activation scales, plus the padding bytes of the
+// intermediate's atoms, whose real bytes the gate_up epilogue fills).
+__global__ void __launch_bounds__(256) gather_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs,
+                                                     const int32_t* __restrict__ sorted_rows,
+                                                     const int32_t* __restrict__ tiles, int k, int H, int I,
+                                                     uint8_t* __restrict__ xp, uint8_t* __restrict__ xp_sf,
+                                                     uint8_t* __restrict__ hq_sf) {
+  const int b = blockIdx.x;
+  if (b >= tiles[0]) return;
+  const int4 td = reinterpret_cast<const int4*>(tiles + 4)[b];
+  const int row0 = td.y, rows = td.z;
+  __shared__ int tok[128];
+  for (int r = threadIdx.x; r < rows; r += blockDim.x) tok[r] = sorted_rows[row0 + r] / k;
+  __syncthreads();
+  const int hc = H / 16;  // 16-byte chunks per row
+  for (int i = threadIdx.x; i < rows * hc; i += blockDim.x) {
+    const int r = i / hc, c = i % hc;
+    reinterpret_cast<uint4*>(xp + (int64_t)(row0 + r) * H)[c] =
+        reinterpret_cast<const uint4*>(xq + (int64_t)tok[r] * H)[c];
+  }
+  const int nbh = H / 32, nbi = I / 32;
+  const int kth = (H + kTileK - 1) / kTileK, kti = (I + kTileK - 1) / kTileK;
+  for (int i = threadIdx.x; i < kth * kAtomBytes; i += blockDim.x) {
+    const int ka = i / kAtomBytes, j = i % kAtomBytes;
+    const int r = (j >> 4) + 32 * ((j & 15) >> 2);
+    const int kb = ka * 4 + (j & 3);
+    uint8_t v = 127;
+    if (r < rows && kb < nbh) v = xs[(int64_t)tok[r] * nbh + kb];
+    xp_sf[((int64_t)b * kth + ka) * kAtomBytes + j] = v;
+  }
+  for (int i = threadIdx.x; i < kti * kAtomBytes; i += blockDim.x) {
+    const int ka = i / kAtomBytes, j = i % kAtomBytes;
+    const int r = (j >> 4) + 32 * ((j & 15) >> 2);
+    const int kb = ka * 4 + (j & 3);
+    if (r >= rows || kb >= nbi) hq_sf[((int64_t)b * kti + ka) * kAtomBytes + j] = 127;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const int32_t* ids, int TK, int k, int E, int tile_rows, int max_tiles,
+                           int32_t* counts, int32_t* offsets, int32_t* sorted_rows, int32_t* inv_pos,
+                           int32_t* tiles, cudaStream_t s) {
+  (void)k;
+  permute_kernel<<<1, kPermThreads, 0, s>>>(ids, TK, E, tile_rows, max_tiles, counts, offsets, sorted_rows,
+                                            inv_pos, tiles);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const uint8_t* xq, const uint8_t* xs, const int32_t* sorted_rows,
+                          const int32_t* tiles, int max_tiles, int k, int H, int I, int tile_rows,
+                          uint8_t* xp, uint8_t* xp_sf, uint8_t* hq_sf, cudaStream_t s) {
+  (void)tile_rows;
+  gather_kernel<<<max_tiles, 256, 0, s>>>(xq, xs, sorted_rows, tiles, k, H, I, xp, xp_sf, hq_sf);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -66,7 +66,7 @@ def lib():
             L.oracle_expert_mlp.argtypes = [p, p, i64, i64, p, p, p, p, p, p, p, p, p, p, p]
             L.oracle_moe_forward.restype = None
             L.oracle_moe_forward.argtypes = [p, i64, i64, i64, i64, i32, p, p, p, p, p, p, p, p,
-                                             p, p, p, p, p, p]
+                                             p, p, p, p, p, p, p, p, p]
             L.oracle_rmsnorm_bf16.restype = None
             L.oracle_rmsnorm_bf16.argtypes = [p, i64, i64, d, p]
             _lib = L
@@ -189,8 +189,8 @@ def expert_mlp(xq, xs, gu_blocks, gu_scales, gu_bias, d_blocks, d_scales, d_bias
 
 
 def moe_forward(x, router_w, router_b, gu_blocks, gu_scales, gu_bias, d_blocks, d_scales, d_bias,
-                k: int):
-    """The whole layer -> dict(out fp64 [T,H], logits, ids, w, xq, xs)."""
+                k: int, intermediates: bool = False):
+    """The whole layer -> dict(out fp64 [T,H], logits, ids, w, xq, xs[, h, hq, hs])."""
     xx = _np(x, np.uint16)
     wr, br = _np(router_w, np.uint16), _np(router_b, np.uint16)
     gub, gus, gubias = _np(gu_blocks, np.uint8), _np(gu_scales, np.uint8), _np(gu_bias, np.uint16)
@@ -204,10 +204,19 @@ def moe_forward(x, router_w, router_b, gu_blocks, gu_scales, gu_bias, d_blocks, 
     w = np.empty((T, k), np.float64)
     xq = np.empty((T, H), np.uint8)
     xs = np.empty((T, H // 32), np.uint8)
+    h = hq = hs = None
+    if intermediates:
+        h = np.empty((T, k, I), np.float64)
+        hq = np.empty((T, k, I), np.uint8)
+        hs = np.empty((T, k, I // 32), np.uint8)
     lib().oracle_moe_forward(_ptr(xx), T, H, I, E, k, _ptr(wr), _ptr(br), _ptr(gub), _ptr(gus),
                              _ptr(gubias), _ptr(db), _ptr(ds), _ptr(dbias), _ptr(out),
-                             _ptr(logits), _ptr(ids), _ptr(w), _ptr(xq), _ptr(xs))
-    return dict(out=out, logits=logits, ids=ids, w=w, xq=xq, xs=xs)
+                             _ptr(logits), _ptr(ids), _ptr(w), _ptr(xq), _ptr(xs), _ptr(h),
+                             _ptr(hq), _ptr(hs))
+    r = dict(out=out, logits=logits, ids=ids, w=w, xq=xq, xs=xs)
+    if intermediates:
+        r.update(h=h, hq=hq, hs=hs)
+    return r
 
 
 def rmsnorm_bf16(x, eps: float = 1e-5) -> np.ndarray:

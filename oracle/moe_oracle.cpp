@@ -238,13 +238,15 @@ void oracle_expert_mlp(const uint8_t* xq, const uint8_t* xs, int64_t H, int64_t 
 //     gu_blocks [E,2I,H/32,16], gu_scales [E,2I,H/32], gu_bias bf16 [E,2I]
 //     d_blocks  [E,H,I/32,16],  d_scales  [E,H,I/32],  d_bias  bf16 [E,H]
 //   out [T,H] fp64: sum_j w[t][j] * y(t, ids[t][j]), accumulated in slot order.
-//   Optional (may be NULL): logits [T,E], ids [T,k], w [T,k], xq [T,H], xs [T,H/32].
+//   Optional (may be NULL): logits [T,E], ids [T,k], w [T,k], xq [T,H], xs [T,H/32],
+//   and the intermediate of every (token, slot): h [T,k,I], hq [T,k,I], hs [T,k,I/32].
 void oracle_moe_forward(const uint16_t* x, int64_t T, int64_t H, int64_t I, int64_t E, int32_t k,
                         const uint16_t* router_w, const uint16_t* router_b,
                         const uint8_t* gu_blocks, const uint8_t* gu_scales, const uint16_t* gu_bias,
                         const uint8_t* d_blocks, const uint8_t* d_scales, const uint16_t* d_bias,
                         double* out, double* logits_out, int32_t* ids_out, double* w_out,
-                        uint8_t* xq_out, uint8_t* xs_out) {
+                        uint8_t* xq_out, uint8_t* xs_out, double* h_out, uint8_t* hq_out,
+                        uint8_t* hs_out) {
   std::vector<double> logits(T * E), w(T * k), xrow(H), y(H);
   std::vector<int32_t> ids(T * k);
   std::vector<uint8_t> xq(H), xs(H / 32);
@@ -258,11 +260,13 @@ void oracle_moe_forward(const uint16_t* x, int64_t T, int64_t H, int64_t I, int6
     for (int64_t c = 0; c < H; ++c) out[t * H + c] = 0.0;
     for (int32_t j = 0; j < k; ++j) {
       const int64_t e = ids[t * k + j];
+      const int64_t tj = t * k + j;
       oracle_expert_mlp(xq.data(), xs.data(), H, I,
                         gu_blocks + e * gu_rows * nbh * 16, gu_scales + e * gu_rows * nbh,
                         gu_bias + e * gu_rows,
                         d_blocks + e * H * nbi * 16, d_scales + e * H * nbi, d_bias + e * H,
-                        nullptr, nullptr, nullptr, nullptr, y.data());
+                        nullptr, h_out ? h_out + tj * I : nullptr, hq_out ? hq_out + tj * I : nullptr,
+                        hs_out ? hs_out + tj * nbi : nullptr, y.data());
       for (int64_t c = 0; c < H; ++c) out[t * H + c] += w[t * k + j] * y[c];
     }
   }

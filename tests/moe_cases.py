@@ -1,0 +1,234 @@
+"""Shared helpers of the GPU parity tests: build a case, run the C ABI, run the
+oracle, and compare stage by stage."""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+import torch
+
+import moe_synth as ms
+import oracle
+import mxfp4_mixture_experts_gemv_gb300 as moe
+
+# Output tolerances of the layer (fp32 GPU path with one bf16 rounding vs the
+# fp64 oracle): max |d| <= 2e-2 * rms(ref) and ||d||_F / ||ref||_F <= 5e-3.
+MAX_ABS_OVER_RMS = 2e-2
+REL_FRO = 5e-3
+TOPK_W_ATOL = 1e-6
+
+
+@dataclasses.dataclass
+class GpuRun:
+    dims: moe.LayerDims
+    k: int
+    out: torch.Tensor
+    ws: torch.Tensor
+    layout: moe.WorkspaceLayout
+
+    def section(self, name, shape, dtype):
+        return moe.view(self.ws, getattr(self.layout, name), shape, dtype).cpu()
+
+
+def pack(inp: ms.LayerInputs):
+    s = inp.shape
+    dims = moe.LayerDims(s.E, s.H, s.I)
+    packed = moe.pack_weights(dims, inp.gate_up_blocks, inp.gate_up_scales, inp.gate_up_bias,
+                              inp.down_blocks, inp.down_scales, inp.down_bias)
+    return dims, packed
+
+
+def run_gpu(inp: ms.LayerInputs, packed, x=None, poison: int | None = None) -> GpuRun:
+    s = inp.shape
+    dims = moe.LayerDims(s.E, s.H, s.I)
+    x = inp.x if x is None else x
+    T = x.shape[0]
+    ws = moe.alloc_workspace(dims, T, s.k, x.device)
+    if poison is not None:
+        ws.fill_(poison)
+    out = torch.full_like(x, float("nan"))
+    moe.forward(dims, x, inp.router_w, inp.router_b, packed, s.k, out=out, workspace=ws)
+    st = moe.device_status(ws)
+    assert st == moe.MOE_OK, moe.STATUS_NAMES.get(st, st)
+    return GpuRun(dims, s.k, out, ws, moe.workspace_layout(dims, T, s.k))
+
+
+def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.float().cpu().double().numpy()
+
+
+def _widen(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def check_routing(run: GpuRun, x_cpu, wr_cpu, br_cpu, logits_ref: np.ndarray):
+    """Router ids: equal to the oracle's, or a valid selection under fp32 near-ties.
+
+    Returns the set of tokens whose ids differ (accepted near-ties)."""
+    T, E = logits_ref.shape
+    k = run.k
+    ids = run.section("topk_ids", (T, k), torch.int32).numpy()
+    w = run.section("topk_w", (T, k), torch.float32).numpy().astype(np.float64)
+    xf = _widen(x_cpu.view(torch.int16).numpy().view(np.uint16))
+    wf = _widen(wr_cpu.view(torch.int16).numpy().view(np.uint16))
+    bf = _widen(br_cpu.view(torch.int16).numpy().view(np.uint16))
+    l32 = logits_ref.astype(np.float32)
+    ties = set()
+    for t in range(T):
+        order = np.lexsort((np.arange(E), -l32[t]))
+        if not np.array_equal(ids[t], order[:k]):
+            # accept only a selection that fp32 rounding can explain
+            assert len(set(ids[t].tolist())) == k, f"token {t}: repeated expert ids {ids[t]}"
+            err = (H_gamma(xf.shape[1]) * (np.abs(xf[t]) @ np.abs(wf).T) + 2 ** -23 * np.abs(logits_ref[t]) +
+                   np.abs(bf) * 2 ** -24)
+            sel = ids[t]
+            rest = np.setdiff1d(np.arange(E), sel)
+            lo_sel = min(logits_ref[t, e] + err[e] for e in sel)
+            hi_rest = max(logits_ref[t, e] - err[e] for e in rest)
+            assert lo_sel >= hi_rest, f"token {t}: ids {ids[t]} vs oracle {order[:k]} beyond fp32 error"
+            for a, b in zip(sel, sel[1:]):
+                assert logits_ref[t, a] + err[a] >= logits_ref[t, b] - err[b], f"token {t}: order"
+            ties.add(t)
+        sel_l = logits_ref[t, ids[t]]
+        ref_w = np.exp(sel_l - sel_l[0]) / np.exp(sel_l - sel_l[0]).sum()
+        np.testing.assert_allclose(w[t], ref_w, rtol=0, atol=TOPK_W_ATOL)
+    return ties
+
+
+def H_gamma(n: int) -> float:
+    u = 2.0 ** -24
+    return n * u / (1 - n * u)
+
+
+def check_quantised_x(run: GpuRun, xq_ref, xs_ref):
+    T, H = xq_ref.shape
+    xq = run.section("xq", (T, H), torch.uint8).numpy()
+    xs = run.section("xs", (T, H // 32), torch.uint8).numpy()
+    np.testing.assert_array_equal(xq, xq_ref)
+    np.testing.assert_array_equal(xs, xs_ref)
+
+
+def check_grouping(run: GpuRun, T: int):
+    E, k = run.dims.E, run.k
+    ids = run.section("topk_ids", (T, k), torch.int32).numpy()
+    cnt, off, sr, inv = oracle.permute(ids, E)
+    np.testing.assert_array_equal(run.section("counts", (E,), torch.int32).numpy(), cnt)
+    np.testing.assert_array_equal(run.section("offsets", (E + 1,), torch.int32).numpy(), off)
+    np.testing.assert_array_equal(run.section("sorted_rows", (T * k,), torch.int32).numpy(), sr)
+    np.testing.assert_array_equal(run.section("inv_pos", (T * k,), torch.int32).numpy(), inv.reshape(-1))
+    # tile list: every expert's rows covered in order by tiles of at most tile_rows
+    L = run.layout
+    tiles = run.section("tiles", (4 + 4 * L.max_tiles,), torch.int32).numpy()
+    n = tiles[0]
+    td = tiles[4:4 + 4 * n].reshape(n, 4)
+    want = []
+    for e in range(E):
+        for r0 in range(0, cnt[e], L.tile_rows):
+            want.append((e, off[e] + r0, min(L.tile_rows, cnt[e] - r0)))
+    assert [tuple(r[:3]) for r in td] == want
+    return cnt, off, sr, inv
+
+
+def compare_out(got: np.ndarray, want: np.ndarray, what="", allow=None, bf16_rounding=False):
+    """Layer tolerances: max |d| <= 2e-2 * rms(ref) and relative Frobenius <= 5e-3.
+
+    ``allow`` [T] adds, per token, the exact bound of validated MXFP8 near-midpoint
+    flips of the intermediate (see check_intermediate).  ``bf16_rounding`` adds, per
+    element, the largest error of rounding the reference to the bf16 output format
+    (2^-8 |ref|); used for the small edge-case shapes whose few outputs can sit
+    many rms above the mean, where that rounding alone can exceed 2e-2 * rms."""
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    d = got - want
+    rms = float(np.sqrt(np.mean(want ** 2)))
+    rel = float(np.linalg.norm(d) / np.linalg.norm(want))
+    lim = np.full(want.shape, MAX_ABS_OVER_RMS * rms)
+    if allow is not None:
+        lim += np.asarray(allow)[:, None]
+    if bf16_rounding:
+        lim += 2.0 ** -8 * np.abs(want)
+    over = np.abs(d) > lim
+    per_tok = np.abs(d).max(axis=1)
+    if over.any():
+        t, c = np.argwhere(over)[0]
+        raise AssertionError(f"{what}: |d| {abs(d[t, c]):.4g} at token {t} col {c} > limit {lim[t, c]:.4g} "
+                             f"(ref {want[t, c]:.4g}, rms {rms:.4g}, rel {rel:.3g})")
+    assert rel <= REL_FRO, f"{what}: rel Frobenius {rel:.4g} > {REL_FRO}"
+    # a broken FP4 GEMM shows up as rows whose every element is equal
+    if got.shape[1] > 1:
+        assert (np.ptp(got, axis=1) > 0).all(), f"{what}: constant output row"
+    return float(per_tok.max()) / rms, rel
+
+
+_E4M3 = None
+
+
+def _e4m3_table():
+    global _E4M3
+    if _E4M3 is None:
+        _E4M3 = np.array([oracle.e4m3_value(c) for c in range(256)])
+    return _E4M3
+
+
+def gpu_hq(run: GpuRun, T: int, inv: np.ndarray):
+    """GPU intermediate codes and scale codes per (token, slot): [T,k,I], [T,k,I/32]."""
+    I, k = run.dims.I, run.k
+    L = run.layout
+    TK = run.out.shape[0] * k
+    hq = run.section("hq", (TK, I), torch.uint8).numpy()
+    kti = (I + 127) // 128
+    hq_sf = run.section("hq_sf", (L.max_tiles, kti, 512), torch.uint8).numpy()
+    tiles = run.section("tiles", (4 + 4 * L.max_tiles,), torch.int32).numpy()
+    td = tiles[4:4 + 4 * tiles[0]].reshape(-1, 4)
+    pos = inv.reshape(-1).astype(np.int64)
+    b = np.searchsorted(td[:, 1], pos, side="right") - 1
+    n = pos - td[b, 1]
+    kb = np.arange(I // 32)
+    sc = hq_sf[b[:, None], kb[None, :] // 4, ((n % 32) * 16 + (n // 32) * 4)[:, None] + (kb % 4)[None, :]]
+    return hq[pos].reshape(-1, k, I), sc.reshape(-1, k, I // 32)
+
+
+def check_intermediate(run: GpuRun, ref: dict, inp_cpu: ms.LayerInputs, inv: np.ndarray, tokens=None,
+                       rel_mid=2e-4):
+    """Compare the GPU's MXFP8 intermediate with the oracle's for every (token, slot).
+
+    Codes may differ only where the oracle's h (fp32) lies within ``rel_mid`` of the
+    rounding midpoint between the two codes (or the block amax within ``rel_mid`` of
+    the power of two where the shared exponent changes): both codes are then
+    correct results of the same quantisation, taken from sums accumulated in a
+    different order.  Returns the per-token bound such flips put on the output
+    (sum over slots of w * sum |delta hq_i| * max_c |Wd[c][i]|) and the flip count."""
+    T, k, I = ref["hq"].shape
+    e4 = _e4m3_table()
+    gq, gs = gpu_hq(run, T, inv)
+    rq, rs = ref["hq"], ref["hs"]
+    gv = e4[gq] * np.ldexp(1.0, np.repeat(gs.astype(np.int64), 32, axis=-1) - 127)
+    rv = e4[rq] * np.ldexp(1.0, np.repeat(rs.astype(np.int64), 32, axis=-1) - 127)
+    h = ref["h"]
+    allow = np.zeros(T)
+    flips = 0
+    colmax = {}
+    for t, j in zip(*np.nonzero((gv != rv).any(axis=-1))):
+        e = int(ref["ids"][t, j])
+        bad = np.nonzero(gv[t, j] != rv[t, j])[0]
+        for blk in np.unique(bad // 32):
+            sl = slice(32 * blk, 32 * blk + 32)
+            if gs[t, j, blk] != rs[t, j, blk]:
+                amax = np.abs(h[t, j, sl]).max()
+                edge = 2.0 ** np.round(np.log2(amax))
+                assert abs(amax - edge) <= rel_mid * amax, f"pair {(t, j)} block {blk}: scale differs away from a power of two"
+            else:
+                for i in bad[(bad >= 32 * blk) & (bad < 32 * blk + 32)]:
+                    mid = 0.5 * (gv[t, j, i] + rv[t, j, i])
+                    step = abs(gv[t, j, i] - rv[t, j, i])
+                    assert step <= abs(rv[t, j, i]) / 4 + 2.0 ** (int(rs[t, j, blk]) - 127 - 9) * 2, \
+                        f"pair {(t, j)} elem {i}: codes not adjacent ({gv[t, j, i]} vs {rv[t, j, i]})"
+                    assert abs(h[t, j, i] - mid) <= rel_mid * abs(h[t, j, i]), \
+                        f"pair {(t, j)} elem {i}: h={h[t, j, i]!r} not at the midpoint {mid!r}"
+        if e not in colmax:
+            colmax[e] = np.abs(oracle.dequant_mxfp4(inp_cpu.down_blocks[e], inp_cpu.down_scales[e])).max(axis=0)
+        allow[t] += ref["w"][t, j] * float((np.abs(gv[t, j] - rv[t, j]) * colmax[e]).sum())
+        flips += bad.size
+    total = T * k * I
+    assert flips <= max(4, 0.002 * total), f"intermediate flips {flips}/{total}"
+    return allow, flips

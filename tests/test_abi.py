@@ -1,0 +1,122 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol,
+computes sizes, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+import mxfp4_mixture_experts_gemv_gb300 as moe
+from mxfp4_mixture_experts_gemv_gb300 import build as moe_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    moe_build.build()
+    return moe.lib()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declarations_match_binding():
+    assert _declared_functions() == sorted(moe.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", moe.LIB_PATH], capture_output=True, text=True).stdout
+    for name in _declared_functions():
+        assert re.search(rf"\bT {name}$", out, re.M), name
+
+
+def test_version(L):
+    assert L.moe_version() & 0xFFFF == 1
+
+
+GPT = moe.LayerDims(E=128, H=2880, I=2880)
+
+
+def test_packed_size_layout():
+    # data rows padded to 2944 elements (1472 bytes), scale atoms of 512 bytes per
+    # 128 rows x 128 columns, fp32 biases, each section 1024-aligned after a 1 KB header
+    def r(x):
+        return (x + 1023) // 1024 * 1024
+    gu_data = 128 * 5760 * 1472
+    gu_sf = 128 * 45 * 23 * 512
+    gu_b = 128 * 5760 * 4
+    d_data = 128 * 2880 * 1472
+    d_sf = 128 * 23 * 23 * 512
+    d_b = 128 * 2880 * 4
+    want = 1024 + sum(r(x) for x in (gu_data, gu_sf, gu_b, d_data, d_sf, d_b))
+    assert moe.packed_size(GPT) == want
+    assert moe.packed_size(moe.LayerDims(8, 100, 256)) == 0   # H not a multiple of 32
+    assert moe.packed_size(moe.LayerDims(8, 256, 96)) == 0    # I not a multiple of 64
+    assert moe.packed_size(moe.LayerDims(300, 256, 256)) == 0  # E > 256
+
+
+def test_workspace_layout_sections_are_disjoint_and_aligned():
+    for T in (1, 4, 32, 2048, 8192):
+        lay = moe.workspace_layout(GPT, T, 4)
+        names = [f[0] for f in moe.WorkspaceLayout._fields_[:-3]]
+        offs = [getattr(lay, n) for n in names]
+        assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+        assert lay.total == moe.workspace_size(GPT, T, 4)
+        assert lay.tile_rows == (16 if T <= 16 else 32 if T <= 32 else 64 if T <= 64 else 128)
+        # enough tiles for any routing: every expert's partial tile plus full tiles
+        assert lay.max_tiles >= T * 4 // lay.tile_rows + min(T * 4, 128)
+
+
+FAKE = 1 << 20  # never dereferenced: every call below fails validation first
+
+
+def _fwd(L, dims=GPT, hidden=FAKE, T=4, rw=FAKE, rb=FAKE, packed=FAKE, k=4, out=FAKE, ws=FAKE,
+         ws_bytes=1 << 40):
+    return L.moe_forward(dims.c(), hidden, T, rw, rb, packed, k, out, ws, ws_bytes, None)
+
+
+def test_forward_rejects_bad_arguments_on_host(L):
+    assert _fwd(L, k=0) == 1 and b"top_k" in L.moe_last_error()
+    assert _fwd(L, k=9) == 1
+    assert _fwd(L, dims=moe.LayerDims(4, 64, 128), k=5) == 1        # k > E
+    assert _fwd(L, T=-1) == 1
+    assert _fwd(L, dims=moe.LayerDims(128, 2888, 2880)) == 2         # H % 32
+    assert _fwd(L, dims=moe.LayerDims(128, 2880, 2880 + 32)) == 2    # I % 64
+    assert _fwd(L, dims=moe.LayerDims(257, 2880, 2880)) == 2
+    assert _fwd(L, hidden=0) == 1
+    assert _fwd(L, out=0) == 1
+    assert _fwd(L, hidden=FAKE + 8) == 3
+    assert _fwd(L, ws=FAKE + 16) == 3
+    assert _fwd(L, packed=FAKE + 128) == 3
+    need = moe.workspace_size(GPT, 4, 4)
+    assert _fwd(L, ws_bytes=need - 1) == 4 and b"workspace" in L.moe_last_error()
+    assert _fwd(L, T=0) == 0  # no-op, nothing launched
+    assert _fwd(L, T=1 << 24) == 2  # T*k*H beyond 32-bit indexing
+
+
+def test_pack_rejects_bad_arguments_on_host(L):
+    w = moe.Weights(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)
+    n = moe.packed_size(GPT)
+    assert L.moe_pack_weights(GPT.c(), None, FAKE, n, None) == 1
+    assert L.moe_pack_weights(GPT.c(), ctypes.byref(w), FAKE + 64, n, None) == 3
+    assert L.moe_pack_weights(GPT.c(), ctypes.byref(w), FAKE, n - 1, None) == 5
+    w2 = moe.Weights(FAKE + 4, FAKE, FAKE, FAKE, FAKE, FAKE)
+    assert L.moe_pack_weights(GPT.c(), ctypes.byref(w2), FAKE, n, None) == 3
+    w3 = moe.Weights(FAKE, 0, FAKE, FAKE, FAKE, FAKE)
+    assert L.moe_pack_weights(GPT.c(), ctypes.byref(w3), FAKE, n, None) == 1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU failure path")
+def test_forward_fails_loudly_without_a_gpu(L):
+    # valid arguments on a host with no CUDA device: the library reports a CUDA
+    # error instead of computing anything on the CPU
+    assert _fwd(L) == 6
+    assert b"status reset" in L.moe_last_error()

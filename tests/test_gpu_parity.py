@@ -1,0 +1,171 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, stage by
+stage (router ids and weights, MXFP8 codes of x, grouping, hq) and end to end."""
+import numpy as np
+import pytest
+import torch
+
+import moe_synth as ms
+import oracle
+import mxfp4_mixture_experts_gemv_gb300 as moe
+from tests import moe_cases as mc
+
+pytestmark = pytest.mark.gpu
+
+# Small shapes that the oracle finishes in well under a second but that span
+# several weight tiles, ragged token tiles and the padded contraction tails.
+SMALL_CASES = {
+    "tiny_T8_k2": (ms.LayerShape(T=8, H=256, I=256, E=8, k=2), 0),
+    "T1_k1": (ms.LayerShape(T=1, H=256, I=256, E=8, k=1), 3),
+    "ragged_T37_k4": (ms.LayerShape(T=37, H=256, I=256, E=8, k=4), 4),
+    "many_tiles_T300": (ms.LayerShape(T=300, H=256, I=128, E=8, k=2), 5),
+    "tails_H288_I192": (ms.LayerShape(T=50, H=288, I=192, E=6, k=3), 6),
+    "k8_E16": (ms.LayerShape(T=20, H=128, I=64, E=16, k=8), 7),
+}
+
+
+def _full_check(inp_cpu, run, strict=True):
+    s = inp_cpu.shape
+    ref = oracle.moe_forward(inp_cpu.x, inp_cpu.router_w, inp_cpu.router_b, inp_cpu.gate_up_blocks,
+                             inp_cpu.gate_up_scales, inp_cpu.gate_up_bias, inp_cpu.down_blocks,
+                             inp_cpu.down_scales, inp_cpu.down_bias, k=s.k, intermediates=True)
+    ties = mc.check_routing(run, inp_cpu.x, inp_cpu.router_w, inp_cpu.router_b, ref["logits"])
+    assert not ties, f"near-tie tokens {sorted(ties)}"
+    mc.check_quantised_x(run, ref["xq"], ref["xs"])
+    cnt, off, sr, inv = mc.check_grouping(run, s.T)
+    allow, flips = mc.check_intermediate(run, ref, inp_cpu, inv)
+    got = mc.bf16_to_f64(run.out)
+    mc.compare_out(got, ref["out"], "out", allow=allow, bf16_rounding=not strict)
+    return ref
+
+
+@pytest.mark.parametrize("name", list(SMALL_CASES))
+def test_small_layer_parity(name):
+    shape, seed = SMALL_CASES[name]
+    inp = ms.make_layer(shape, seed=seed)
+    dev = inp.to("cuda")
+    _, packed = mc.pack(dev)
+    run = mc.run_gpu(dev, packed)
+    _full_check(inp, run, strict=False)
+
+
+def test_pack_is_a_bijection_with_deterministic_padding():
+    shape = ms.LayerShape(T=1, H=288, I=192, E=3, k=1)
+    inp = ms.make_layer(shape, seed=9)
+    dev = inp.to("cuda")
+    _, packed = mc.pack(dev)
+    pk = packed.cpu().numpy()
+    E, H, I = shape.E, shape.H, shape.I
+    Hp, Ip = 384, 256
+    hdr = pk[:64].view(np.uint32)
+    assert hdr[0] == 0x4D584645 and hdr[1] == 1 and tuple(hdr[2:5]) == (E, H, I)
+    offs = pk[48:104].view(np.uint64)
+    gu_data, gu_sf, gu_b, d_data, d_sf, d_b, total = (int(o) for o in offs)
+    assert total == moe.packed_size(moe.LayerDims(E, H, I))
+    # gate_up rows: tile t = gate rows 64t.., then up rows I+64t..
+    src_row = np.array([(64 * (r // 128) + r % 128) if r % 128 < 64 else (I + 64 * (r // 128) + r % 128 - 64)
+                        for r in range(2 * I)])
+    gub = inp.gate_up_blocks.numpy().reshape(E, 2 * I, H // 2)
+    got = pk[gu_data:gu_data + E * 2 * I * Hp // 2].reshape(E, 2 * I, Hp // 2)
+    np.testing.assert_array_equal(got[:, :, :H // 2], gub[:, src_row])
+    assert (got[:, :, H // 2:] == 0).all()
+    db = inp.down_blocks.numpy().reshape(E, H, I // 2)
+    got = pk[d_data:d_data + E * H * Ip // 2].reshape(E, H, Ip // 2)
+    np.testing.assert_array_equal(got[:, :, :I // 2], db)
+    assert (got[:, :, I // 2:] == 0).all()
+
+    def atoms(base, rows, nb, kt, src):
+        mt = (rows + 127) // 128
+        a = pk[base:base + E * mt * kt * 512].reshape(E, mt, kt, 512)
+        full = np.full((E, mt * 128, kt * 4), 127, np.uint8)
+        j = np.arange(512)
+        r = (j >> 4) + 32 * ((j & 15) >> 2)
+        kb = j & 3
+        for m in range(mt):
+            for kk in range(kt):
+                full[:, m * 128 + r, kk * 4 + kb] = a[:, m, kk, j]
+        assert (full[:, :rows, :nb] == src).all()
+        assert (full[:, rows:, :] == 127).all() and (full[:, :, nb:] == 127).all()
+
+    atoms(gu_sf, 2 * I, H // 32, Hp // 128, inp.gate_up_scales.numpy()[:, src_row])
+    atoms(d_sf, H, I // 32, Ip // 128, inp.down_scales.numpy())
+    bias = pk[gu_b:gu_b + E * 2 * I * 4].view(np.float32).reshape(E, 2 * I)
+    np.testing.assert_array_equal(bias, inp.gate_up_bias.float().numpy()[:, src_row])
+    bias = pk[d_b:d_b + E * H * 4].view(np.float32).reshape(E, H)
+    np.testing.assert_array_equal(bias, inp.down_bias.float().numpy())
+
+
+def test_deterministic_and_independent_of_workspace_contents():
+    shape = ms.LayerShape(T=64, H=256, I=256, E=8, k=4)
+    inp = ms.make_layer(shape, seed=11).to("cuda")
+    _, packed = mc.pack(inp)
+    a = mc.run_gpu(inp, packed, poison=0x00)
+    b = mc.run_gpu(inp, packed, poison=0xFF)
+    c = mc.run_gpu(inp, packed, poison=0x7F)
+    for r in (b, c):
+        assert torch.equal(a.out.view(torch.int16), r.out.view(torch.int16))
+        for name, shp in [("topk_ids", (64 * 4,)), ("sorted_rows", (64 * 4,)), ("inv_pos", (64 * 4,))]:
+            assert torch.equal(a.section(name, shp, torch.int32), r.section(name, shp, torch.int32))
+
+
+def test_zero_tokens_is_a_noop():
+    shape = ms.LayerShape(T=4, H=256, I=256, E=8, k=2)
+    inp = ms.make_layer(shape, seed=1).to("cuda")
+    dims, packed = mc.pack(inp)
+    out = torch.full((0, 256), 1.0, dtype=torch.bfloat16, device="cuda")
+    ws = moe.alloc_workspace(dims, 1, 2)
+    moe.forward(dims, inp.x[:0], inp.router_w, inp.router_b, packed, 2, out=out, workspace=ws)
+    torch.cuda.synchronize()
+
+
+# ----------------------------------------------------------------------- gpt-oss-shaped layer
+@pytest.fixture(scope="module")
+def gpt_layer():
+    H = I = 2880
+    E = 128
+    w = ms.make_expert_weights(0, H, I, E, device="cuda")
+    dims = moe.LayerDims(E, H, I)
+    packed = moe.pack_weights(dims, *w)
+    cpu = [t.cpu() for t in w]
+    return dims, packed, w, cpu
+
+
+def _gpt_inputs(gpt_layer, T, hot=0, hot_bias=0.0):
+    dims, packed, w, cpu = gpt_layer
+    shape = ms.LayerShape(T=T, H=dims.H, I=dims.I, E=dims.E, k=4)
+    x = ms.make_tokens(0, T, dims.H)
+    rw, rb = ms.make_router(0, dims.H, dims.E, hot_experts=hot, hot_bias=hot_bias)
+    cpu_inp = ms.LayerInputs(shape, x, rw, rb, *cpu)
+    dev_inp = ms.LayerInputs(shape, x.cuda(), rw.cuda(), rb.cuda(), *w)
+    return cpu_inp, dev_inp, packed
+
+
+@pytest.mark.parametrize("T,hot", [(4, 0), (32, 16)], ids=["decode_t4", "decode_t32_skewed"])
+def test_gpt_oss_decode_parity(gpt_layer, T, hot):
+    cpu_inp, dev_inp, packed = _gpt_inputs(gpt_layer, T, hot, 1.0 if hot else 0.0)
+    run = mc.run_gpu(dev_inp, packed)
+    _full_check(cpu_inp, run)
+
+
+def test_gpt_oss_prefill_sampled_parity(gpt_layer):
+    """T = 2048 with the launch configuration of the benchmark; all ids and the
+    whole grouping are checked, the output on a sample of tokens."""
+    T = 2048
+    cpu_inp, dev_inp, packed = _gpt_inputs(gpt_layer, T)
+    run = mc.run_gpu(dev_inp, packed)
+    logits, ids_ref, _ = oracle.route(cpu_inp.x, cpu_inp.router_w, cpu_inp.router_b, 4)
+    ties = mc.check_routing(run, cpu_inp.x, cpu_inp.router_w, cpu_inp.router_b, logits)
+    cnt, off, sr, inv = mc.check_grouping(run, T)
+    # sample: spread tokens plus the tokens of the most loaded expert's last tile
+    e_max = int(np.argmax(cnt))
+    last = [int(sr[p]) // 4 for p in range(off[e_max + 1] - 3, off[e_max + 1])]
+    sample = sorted(set(list(range(0, T, 257)) + last + [T - 1]) - ties)
+    sub = cpu_inp.x[sample]
+    ref = oracle.moe_forward(sub, cpu_inp.router_w, cpu_inp.router_b, *cpu_inp_weights(cpu_inp), k=4,
+                             intermediates=True)
+    allow, _ = mc.check_intermediate(run, ref, cpu_inp, inv.reshape(T, 4)[sample])
+    got = mc.bf16_to_f64(run.out)[sample]
+    mc.compare_out(got, ref["out"], "prefill sample", allow=allow)
+
+
+def cpu_inp_weights(c):
+    return (c.gate_up_blocks, c.gate_up_scales, c.gate_up_bias, c.down_blocks, c.down_scales, c.down_bias)
