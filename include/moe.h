@@ -145,6 +145,33 @@ moe_status moe_forward(moe_dims d, const void *hidden, int32_t T, const void *ro
                        const void *router_b, const void *packed, int32_t top_k, void *out,
                        void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * Allocation-free forward.  This entry point has no counterpart in the pages
+ * the layer follows; it exists for callers that cannot allocate device memory
+ * themselves: code whose device memory is owned by a host runtime that forbids
+ * or budgets cudaMalloc (plugins, fixed-pool serving runtimes), or code that
+ * must not call an allocator in its launch path because cudaMalloc can
+ * synchronise the device.  It computes exactly what moe_forward computes, with
+ * the same arguments minus the workspace: its scratch is a file-scope device
+ * array of MOE_STATIC_SCRATCH_BYTES inside this library (held by every GPU that
+ * loads the library until the process exits; enough for a gpt-oss-sized layer
+ * up to T = 64 with top_k = 4).
+ *  - A call whose scratch need (moe_workspace_size) exceeds that size returns
+ *    MOE_ERR_WORKSPACE_TOO_SMALL with a message; nothing is enqueued.
+ *  - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture on the device.
+ *  - Every call on a device shares the one array, which keeps the last call's
+ *    contents (the forward resets the words it needs zeroed itself).  Calls that
+ *    overlap on the GPU (concurrent streams or host threads) race on it:
+ *    serialise them.
+ */
+#define MOE_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
+moe_status moe_forward_static_scratch(moe_dims d, const void *hidden, int32_t T, const void *router_w,
+                                      const void *router_b, const void *packed, int32_t top_k, void *out,
+                                      void *stream);
+
 /* Synchronise `stream`, then read the workspace status words: MOE_OK, or
  * MOE_ERR_TIMEOUT if a kernel of the last forward gave up on a wait. */
 moe_status moe_get_device_status(const void *workspace, void *stream);

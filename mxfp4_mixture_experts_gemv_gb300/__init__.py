@@ -25,7 +25,8 @@ STATUS_NAMES = {
 
 # Every symbol the C ABI exports (include/moe.h).
 EXPORTED = ["moe_packed_size", "moe_pack_weights", "moe_workspace_size", "moe_workspace_layout_get",
-            "moe_forward", "moe_get_device_status", "moe_profile_begin", "moe_profile_end",
+            "moe_forward", "moe_forward_static_scratch", "moe_get_device_status", "moe_profile_begin",
+            "moe_profile_end",
             "moe_last_error", "moe_version"]
 STAGES = ["router", "topk_quant", "grouping", "gather", "gate_up_gemm", "down_gemm", "combine"]
 
@@ -74,6 +75,8 @@ def lib() -> ctypes.CDLL:
         L.moe_workspace_layout_get.argtypes = [Dims, i32, i32, ctypes.POINTER(WorkspaceLayout)]
         L.moe_forward.restype = st
         L.moe_forward.argtypes = [Dims, vp, i32, vp, vp, vp, i32, vp, vp, sz, vp]
+        L.moe_forward_static_scratch.restype = st
+        L.moe_forward_static_scratch.argtypes = [Dims, vp, i32, vp, vp, vp, i32, vp, vp]
         L.moe_get_device_status.restype = st
         L.moe_get_device_status.argtypes = [vp, vp]
         L.moe_profile_begin.restype = st
@@ -178,6 +181,23 @@ def forward(dims: LayerDims, hidden: torch.Tensor, router_w: torch.Tensor, route
                              _dev_ptr(packed, "packed"), top_k, _dev_ptr(out, "out", torch.bfloat16),
                              _dev_ptr(workspace, "workspace"),
                              workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+STATIC_SCRATCH_BYTES = 8 << 20
+
+
+def forward_static_scratch(dims: LayerDims, hidden: torch.Tensor, router_w: torch.Tensor,
+                           router_b: torch.Tensor, packed: torch.Tensor, top_k: int,
+                           out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The layer forward through the allocation-free entry point (library-owned scratch)."""
+    if out is None:
+        out = torch.empty_like(hidden)
+    _check(lib().moe_forward_static_scratch(dims.c(), _dev_ptr(hidden, "hidden", torch.bfloat16), hidden.shape[0],
+                                            _dev_ptr(router_w, "router_w", torch.bfloat16),
+                                            _dev_ptr(router_b, "router_b", torch.bfloat16),
+                                            _dev_ptr(packed, "packed"), top_k,
+                                            _dev_ptr(out, "out", torch.bfloat16), _stream(stream)))
     return out
 
 

@@ -61,6 +61,18 @@ int num_sms() {
 
 }  // namespace
 
+namespace moe {
+moe_status report_error(moe_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+}  // namespace moe
+
 extern "C" {
 
 uint32_t moe_version(void) { return (1u << 16) | moe::kPackedVersion; }

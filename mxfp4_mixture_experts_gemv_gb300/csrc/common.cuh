@@ -119,6 +119,9 @@ enum : uint32_t {
 // microseconds).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// Record a status and its message for moe_last_error (defined with the C ABI).
+moe_status report_error(moe_status st, const char* fmt, ...);
+
 // Kernel launchers (defined in the .cu files).
 cudaError_t launch_pack(const moe_dims& d, const PackedHeader& h, const moe_mxfp4_weights& w,
                         uint8_t* packed, cudaStream_t s);
