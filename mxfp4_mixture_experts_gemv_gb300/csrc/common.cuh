@@ -10,30 +10,34 @@
 namespace moe {
 
 // ---------------------------------------------------------------------------------------
-// Packed weight buffer (written by moe_pack_weights).
+// Packed weight buffer (written by moe_pack_weights), layout version 2.
 //
-// Expert weights are stored so each 128-row x 128-element tile can be fetched by
-// one TMA box and fed to tcgen05.mma without reshuffling:
-//   data  [E][rows][Kp/2] bytes: checkpoint rows, contraction axis padded with
-//         zero nibbles to Kp = round_up(K, 128) (TMA's 4-bit unpacking mode needs
-//         a multiple of 128 elements per row).
-//   sf    [E][ceil(rows/128)][Kp/128][512] bytes: E8M0 scales in scale-factor
-//         atoms; byte (r%32)*16 + (r/32)*4 + (kb%4) of atom (r/128, kb/4) holds the
-//         scale of row r, 32-element block kb.  Padding blocks hold code 127 (1.0).
+// Expert weights are stored tile-contiguous so that every pipeline stage of the
+// grouped GEMM fetches one contiguous block with one TMA box:
+//   data  [E][m_tile][k_tile][rows_m][64 B]: 128 weight rows (64 for a tail
+//         m-tile) x 128 contraction elements of packed E2M1 per tile, 8 KB.
+//         The contraction axis is padded with zero nibbles to Kp = round_up(K, 128)
+//         (TMA's 4-bit unpacking mode works on 128-element rows); the row count per
+//         expert is padded to a multiple of 64 with zero rows.
+//   sf    [E][m_tile][k_tile][512 B]: E8M0 scales in scale-factor atoms; byte
+//         (r%32)*16 + (r/32)*4 + (kb%4) holds the scale of tile row r, 32-element
+//         block kb of the tile.  Padding holds code 127 (1.0).
 //   bias  [E][rows] fp32.
-// gate_up rows are interleaved: tile t holds gate rows 64t..64t+63 in tile rows
+// gate_up rows are interleaved: m-tile t holds gate rows 64t..64t+63 in tile rows
 // 0..63 and the matching up rows in tile rows 64..127, so one accumulator tile
 // carries both halves of the SwiGLU.
 // ---------------------------------------------------------------------------------------
 constexpr uint32_t kPackedMagic = 0x4D584645u;  // "EFXM"
-constexpr uint32_t kPackedVersion = 1;
+constexpr uint32_t kPackedVersion = 2;
 constexpr int kTileM = 128;   // weight rows per tile (MMA M)
 constexpr int kTileK = 128;   // contraction elements per pipeline stage
 constexpr int kAtomBytes = 512;
+constexpr int kTileRowBytes = kTileK / 2;  // packed bytes of one tile row
 
 struct PackedHeader {
   uint32_t magic, version;
-  int32_t E, H, I, Hp, Ip, gu_mtiles, d_mtiles, gu_ktiles, d_ktiles, pad0;
+  int32_t E, H, I, Hp, Ip, gu_mtiles, d_mtiles, gu_ktiles, d_ktiles;
+  int32_t gu_rows_stored, d_rows_stored, pad0;
   uint64_t off_gu_data, off_gu_sf, off_gu_bias, off_d_data, off_d_sf, off_d_bias, total;
 };
 
@@ -52,17 +56,26 @@ inline bool packed_layout(const moe_dims& d, PackedHeader* hd) {
   h.d_mtiles = (int32_t)((d.H + kTileM - 1) / kTileM);
   h.gu_ktiles = h.Hp / kTileK;
   h.d_ktiles = h.Ip / kTileK;
+  h.gu_rows_stored = 2 * d.I;
+  h.d_rows_stored = (int32_t)round_up(d.H, 64);
   uint64_t off = 1024;
   auto take = [&](uint64_t bytes) { uint64_t o = off; off = (uint64_t)round_up(off + bytes, 1024); return o; };
-  h.off_gu_data = take((uint64_t)d.E * 2 * d.I * (h.Hp / 2));
+  h.off_gu_data = take((uint64_t)d.E * h.gu_rows_stored * h.gu_ktiles * kTileRowBytes);
   h.off_gu_sf = take((uint64_t)d.E * h.gu_mtiles * h.gu_ktiles * kAtomBytes);
   h.off_gu_bias = take((uint64_t)d.E * 2 * d.I * 4);
-  h.off_d_data = take((uint64_t)d.E * d.H * (h.Ip / 2));
+  h.off_d_data = take((uint64_t)d.E * h.d_rows_stored * h.d_ktiles * kTileRowBytes);
   h.off_d_sf = take((uint64_t)d.E * h.d_mtiles * h.d_ktiles * kAtomBytes);
   h.off_d_bias = take((uint64_t)d.E * d.H * 4);
   h.total = off;
   *hd = h;
   return true;
+}
+
+// Row (in 64-byte units) of the first row of data tile (e, m, kt) in the
+// tile-contiguous layout; `rows_stored` rows per expert, the last m-tile may be short.
+__host__ __device__ inline int64_t tile_row0(int e, int m, int kt, int rows_stored, int k_tiles) {
+  const int rows_m = (rows_stored - m * kTileM) < kTileM ? (rows_stored - m * kTileM) : kTileM;
+  return ((int64_t)e * rows_stored + (int64_t)m * kTileM) * k_tiles + (int64_t)kt * rows_m;
 }
 
 // Token rows per tile of the grouped GEMM (MMA N upper bound) for T tokens.

@@ -17,26 +17,35 @@ struct PackArgs {
   uint8_t* packed;
 };
 
-// Data rows: one thread per 16-byte chunk of a packed row.
+// Data tiles: one thread per 16-byte chunk (32 elements) of the tile-contiguous layout.
 __global__ void pack_data_kernel(PackArgs a, int gate_up) {
   const PackedHeader& h = a.h;
   const int rows = gate_up ? 2 * h.I : h.H;
+  const int rows_stored = gate_up ? h.gu_rows_stored : h.d_rows_stored;
   const int K = gate_up ? h.H : h.I;
-  const int Kp = gate_up ? h.Hp : h.Ip;
-  const int nb = K / 32, nbp = Kp / 32;
+  const int kt_n = gate_up ? h.gu_ktiles : h.d_ktiles;
+  const int nb = K / 32;
   const uint4* src = reinterpret_cast<const uint4*>(gate_up ? a.w.gate_up_blocks : a.w.down_blocks);
   uint4* dst = reinterpret_cast<uint4*>(a.packed + (gate_up ? h.off_gu_data : h.off_d_data));
-  const int64_t total = (int64_t)h.E * rows * nbp;
+  const int64_t per_expert = (int64_t)rows_stored * kt_n * 4;  // chunks
+  const int64_t per_mtile = (int64_t)kTileM * kt_n * 4;
+  const int64_t total = (int64_t)h.E * per_expert;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const int c = (int)(i % nbp);
-    const int64_t er = i / nbp;
-    const int pr = (int)(er % rows);
-    const int e = (int)(er / rows);
+    const int e = (int)(i / per_expert);
+    const int64_t q = i - (int64_t)e * per_expert;
+    const int m = (int)(q / per_mtile);
+    const int rows_m = min(kTileM, rows_stored - m * kTileM);
+    const int64_t rem = q - (int64_t)m * per_mtile;
+    const int kt = (int)(rem / (rows_m * 4));
+    const int rem2 = (int)(rem - (int64_t)kt * rows_m * 4);
+    const int r = rem2 >> 2, j = rem2 & 3;
+    const int pr = m * kTileM + r;          // packed row
+    const int kb = kt * 4 + j;              // source 32-element block
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (c < nb) {
+    if (pr < rows && kb < nb) {
       const int sr = gate_up ? gu_source_row(pr, h.I) : pr;
-      v = src[((int64_t)e * rows + sr) * nb + c];
+      v = src[((int64_t)e * rows + sr) * nb + kb];
     }
     dst[i] = v;
   }

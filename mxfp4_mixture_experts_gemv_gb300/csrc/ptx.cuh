@@ -16,6 +16,17 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// One lane of a converged warp (the lowest active one) gets true.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|P, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ----------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -56,6 +67,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
     if (mbar_try_wait(a, parity)) return true;
     if (global_timer_ns() - t0 > limit_ns) return false;
   }
+}
+
+// Warp-uniform bounded wait: every lane polls, the warp agrees on the outcome.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  return __any_sync(0xffffffffu, mbar_wait(bar, parity, limit_ns));
 }
 
 // ----------------------------------------------------------------- TMA / bulk copies

@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_version(L):
-    assert L.moe_version() & 0xFFFF == 1
+    assert L.moe_version() & 0xFFFF == 2
 
 
 GPT = moe.LayerDims(E=128, H=2880, I=2880)
@@ -50,10 +50,10 @@ def test_packed_size_layout():
     # 128 rows x 128 columns, fp32 biases, each section 1024-aligned after a 1 KB header
     def r(x):
         return (x + 1023) // 1024 * 1024
-    gu_data = 128 * 5760 * 1472
+    gu_data = 128 * 5760 * 1472   # tile-contiguous, K padded to 2944
     gu_sf = 128 * 45 * 23 * 512
     gu_b = 128 * 5760 * 4
-    d_data = 128 * 2880 * 1472
+    d_data = 128 * 2880 * 1472    # 2880 rows = 22 full tiles + one 64-row tile
     d_sf = 128 * 23 * 23 * 512
     d_b = 128 * 2880 * 4
     want = 1024 + sum(r(x) for x in (gu_data, gu_sf, gu_b, d_data, d_sf, d_b))

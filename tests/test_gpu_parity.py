@@ -48,6 +48,22 @@ def test_small_layer_parity(name):
     _full_check(inp, run, strict=False)
 
 
+def _untile(flat, E, rows_stored, Kp):
+    """Tile-contiguous data ([E][m][kt][rows_m][64 B]) back to [E][rows_stored][Kp/2] bytes."""
+    kt_n = Kp // 128
+    out = np.zeros((E, rows_stored, Kp // 2), np.uint8)
+    pos = 0
+    for e in range(E):
+        for m in range(0, rows_stored, 128):
+            rows_m = min(128, rows_stored - m)
+            for kt in range(kt_n):
+                n = rows_m * 64
+                out[e, m:m + rows_m, kt * 64:(kt + 1) * 64] = flat[pos:pos + n].reshape(rows_m, 64)
+                pos += n
+    assert pos == flat.size
+    return out
+
+
 def test_pack_is_a_bijection_with_deterministic_padding():
     shape = ms.LayerShape(T=1, H=288, I=192, E=3, k=1)
     inp = ms.make_layer(shape, seed=9)
@@ -56,22 +72,24 @@ def test_pack_is_a_bijection_with_deterministic_padding():
     pk = packed.cpu().numpy()
     E, H, I = shape.E, shape.H, shape.I
     Hp, Ip = 384, 256
+    Hs = 320  # down rows stored: H rounded up to 64
     hdr = pk[:64].view(np.uint32)
-    assert hdr[0] == 0x4D584645 and hdr[1] == 1 and tuple(hdr[2:5]) == (E, H, I)
-    offs = pk[48:104].view(np.uint64)
+    assert hdr[0] == 0x4D584645 and hdr[1] == 2 and tuple(hdr[2:5]) == (E, H, I)
+    assert tuple(hdr[11:13]) == (2 * I, Hs)
+    offs = pk[56:112].view(np.uint64)
     gu_data, gu_sf, gu_b, d_data, d_sf, d_b, total = (int(o) for o in offs)
     assert total == moe.packed_size(moe.LayerDims(E, H, I))
     # gate_up rows: tile t = gate rows 64t.., then up rows I+64t..
     src_row = np.array([(64 * (r // 128) + r % 128) if r % 128 < 64 else (I + 64 * (r // 128) + r % 128 - 64)
                         for r in range(2 * I)])
     gub = inp.gate_up_blocks.numpy().reshape(E, 2 * I, H // 2)
-    got = pk[gu_data:gu_data + E * 2 * I * Hp // 2].reshape(E, 2 * I, Hp // 2)
+    got = _untile(pk[gu_data:gu_data + E * 2 * I * Hp // 2], E, 2 * I, Hp)
     np.testing.assert_array_equal(got[:, :, :H // 2], gub[:, src_row])
     assert (got[:, :, H // 2:] == 0).all()
     db = inp.down_blocks.numpy().reshape(E, H, I // 2)
-    got = pk[d_data:d_data + E * H * Ip // 2].reshape(E, H, Ip // 2)
-    np.testing.assert_array_equal(got[:, :, :I // 2], db)
-    assert (got[:, :, I // 2:] == 0).all()
+    got = _untile(pk[d_data:d_data + E * Hs * Ip // 2], E, Hs, Ip)
+    np.testing.assert_array_equal(got[:, :H, :I // 2], db)
+    assert (got[:, :, I // 2:] == 0).all() and (got[:, H:, :] == 0).all()
 
     def atoms(base, rows, nb, kt, src):
         mt = (rows + 127) // 128
