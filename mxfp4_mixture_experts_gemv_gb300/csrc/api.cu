@@ -37,7 +37,7 @@ moe_status check_dims(const moe_dims& d) {
   return MOE_OK;
 }
 
-constexpr int kStages = 7;
+constexpr int kStages = 5;
 
 // Per-stage CUDA events of profiled forward calls.
 struct Profiler {
@@ -157,7 +157,7 @@ moe_status moe_forward(moe_dims d, const void* hidden, int32_t T, const void* ro
   int32_t* sorted_rows = reinterpret_cast<int32_t*>(at(L.sorted_rows));
   const int sms = num_sms();
 
-  cudaError_t e = cudaMemsetAsync(status, 0, 16, s);
+  cudaError_t e = cudaMemsetAsync(ws, 0, L.zero_bytes, s);
   if (e != cudaSuccess) return cuda_fail(e, "status reset");
   cudaEvent_t* pev = profile_slot();
   auto mark = [&](int i) {
@@ -180,18 +180,23 @@ moe_status moe_forward(moe_dims d, const void* hidden, int32_t T, const void* ro
                          at(L.xp_sf), at(L.hq_sf), s);
   if (e != cudaSuccess) return cuda_fail(e, "gather kernel");
   mark(4);
-  e = moe::launch_expert_gemm(true, h, pk, at(L.xp), TK, at(L.xp_sf), tiles, L.max_tiles, L.tile_rows, at(L.hq),
-                              at(L.hq_sf), nullptr, status, sms, s);
-  if (e != cudaSuccess) return cuda_fail(e, "gate_up GEMM");
+  moe::ExpertMlpBuffers b;
+  b.xp = at(L.xp);
+  b.xp_sf = at(L.xp_sf);
+  b.hq = at(L.hq);
+  b.hq_sf = at(L.hq_sf);
+  b.y = reinterpret_cast<float*>(at(L.y));
+  b.out = static_cast<uint16_t*>(out);
+  b.tiles = tiles;
+  b.sorted_rows = sorted_rows;
+  b.inv_pos = inv_pos;
+  b.topk_w = w;
+  b.done_gu = reinterpret_cast<int32_t*>(at(L.done_gu));
+  b.done_tok = reinterpret_cast<int32_t*>(at(L.done_tok));
+  b.status = status;
+  e = moe::launch_expert_mlp(h, pk, b, T, top_k, L.max_tiles, L.tile_rows, sms, s);
+  if (e != cudaSuccess) return cuda_fail(e, "expert MLP kernel");
   mark(5);
-  e = moe::launch_expert_gemm(false, h, pk, at(L.hq), TK, at(L.hq_sf), tiles, L.max_tiles, L.tile_rows, nullptr,
-                              nullptr, reinterpret_cast<float*>(at(L.y)), status, sms, s);
-  if (e != cudaSuccess) return cuda_fail(e, "down GEMM");
-  mark(6);
-  e = moe::launch_combine(reinterpret_cast<const float*>(at(L.y)), w, inv_pos, T, top_k, d.H,
-                          static_cast<uint16_t*>(out), s);
-  if (e != cudaSuccess) return cuda_fail(e, "combine kernel");
-  mark(7);
   return MOE_OK;
 }
 

@@ -98,6 +98,9 @@ inline bool workspace_layout(const moe_dims& d, int T, int k, moe_workspace_layo
   auto take = [&](size_t bytes) { size_t r = o; o = align256(o + bytes); return r; };
   moe_workspace_layout l = {};
   l.status = take(16);
+  l.done_gu = take((size_t)max_tiles * 4);
+  l.done_tok = take((size_t)T * ((d.H + kTileM - 1) / kTileM) * 4);
+  l.zero_bytes = o;  // status words and the counters above start at zero every forward
   l.logits = take((size_t)T * d.E * 4);
   l.topk_ids = take((size_t)TK * 4);
   l.topk_w = take((size_t)TK * 4);
@@ -148,12 +151,22 @@ cudaError_t launch_permute(const int32_t* ids, int TK, int k, int E, int tile_ro
 cudaError_t launch_gather(const uint8_t* xq, const uint8_t* xs, const int32_t* sorted_rows,
                           const int32_t* tiles, int max_tiles, int k, int H, int I, int tile_rows,
                           uint8_t* xp, uint8_t* xp_sf, uint8_t* hq_sf, cudaStream_t s);
-cudaError_t launch_expert_gemm(bool gate_up, const PackedHeader& h, const uint8_t* packed,
-                               const uint8_t* b_rows, int b_rows_total, const uint8_t* b_sf,
-                               const int32_t* tiles, int max_tiles, int tile_rows, uint8_t* hq,
-                               uint8_t* hq_sf, float* y, uint32_t* status, int num_sms,
-                               cudaStream_t s);
-cudaError_t launch_combine(const float* y, const float* w, const int32_t* inv_pos, int T, int k,
-                           int H, uint16_t* out, cudaStream_t s);
+struct ExpertMlpBuffers {
+  const uint8_t* xp;        // gate_up B rows [TK][H]
+  const uint8_t* xp_sf;     // gate_up B scale atoms
+  uint8_t* hq;              // [TK][I]
+  uint8_t* hq_sf;           // down B scale atoms
+  float* y;                 // [TK][H]
+  uint16_t* out;            // bf16 [T][H]
+  const int32_t* tiles;
+  const int32_t* sorted_rows;
+  const int32_t* inv_pos;
+  const float* topk_w;
+  int32_t* done_gu;
+  int32_t* done_tok;
+  uint32_t* status;
+};
+cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, const ExpertMlpBuffers& b, int T, int k,
+                              int max_tiles, int tile_rows, int num_sms, cudaStream_t s);
 
 }  // namespace moe

@@ -1,10 +1,12 @@
-// Block-scaled grouped GEMM of the expert MLP on tcgen05 (kind::mxf8f6f4):
-// E2M1 weights (A, 128 rows per tile) x E4M3 activations (B, up to BN token rows
-// per tile), one E8M0 scale per 32 contraction elements on both sides, fp32
-// accumulation in tensor memory.
+// The expert MLP of the MoE layer in one persistent kernel on tcgen05
+// (kind::mxf8f6f4 block-scaled MMA): E2M1 weights (A, 128 rows per tile) x E4M3
+// activations (B, up to BN token rows per tile), one E8M0 scale per 32
+// contraction elements on both sides, fp32 accumulation in tensor memory.
 //
-//   gate_up: g = Xp . Wgu[e]^T + bgu[e]; epilogue h = silu(gate) * up, MXFP8(h)
-//   down:    y = hq . Wd[e]^T + bd[e];   epilogue adds the bias, writes fp32
+//   gate_up tiles: g = Xp . Wgu[e]^T + bgu[e]; epilogue h = silu(gate) * up, MXFP8(h)
+//   down tiles:    y = hq . Wd[e]^T + bd[e];   epilogue writes y, then the
+//                  routing-weighted combine of every (token, 128-feature block)
+//                  whose k contributions are complete
 //
 // The MoE layer as an FP8-activation x FP4-weight grouped GEMM follows "GPT-OSS-
 // 120B with MXFP4 on DGX Spark (SM121/GB10)", "What's Included"; that page's
@@ -12,15 +14,22 @@
 // slot (swap-AB) because an expert sees few tokens, and the token count of a
 // tile sets the MMA N at run time (16..BN, step 16).
 //
-// Warp roles (192 threads, one CTA per SM, persistent over the tile list):
-//   warp 0      TMA producer: weight tile (4-bit, unpacked to the 16-byte
-//               aligned smem form), activation tile, both scale atoms
-//   warp 1      TMEM allocation; one thread issues tcgen05.cp (scales ->
-//               tmem) and tcgen05.mma, commits to mbarriers
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator, bias, SwiGLU +
-//               MXFP8 (gate_up) or fp32 store (down)
-// Every mbarrier wait is bounded; an expired wait records a status bit and the
-// roles wind down without hanging.
+// One launch walks the tile list: every gate_up tile first, then every down
+// tile.  A down tile needs the whole intermediate of its token rows, i.e. all
+// gate_up m-tiles of the same token tile; their epilogues count themselves in a
+// per-token-tile counter that the down tile's producer waits on (acquire) before
+// it streams hq.  CTAs are launched cooperatively (all resident), each walks its
+// tiles in increasing order and finishes every gate_up tile it owns before its
+// first down tile, so every wait is on work that is already in progress.
+//
+// Warp roles (192 threads, one CTA per SM):
+//   warp 0      TMA producer (whole warp walks the schedule, one elected lane issues)
+//   warp 1      TMEM allocation; elected lane issues tcgen05.cp / tcgen05.mma / commits
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator, bias, SwiGLU + MXFP8 (gate_up)
+//               or fp32 y + combine (down)
+// Every wait (mbarrier or global counter) is bounded; an expired wait records a
+// status bit and the roles wind down without hanging.
+#include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -46,29 +55,59 @@ struct GemmCfg {
   static constexpr uint32_t kB = kKS * kB1;
   static constexpr uint32_t kSF = 2 * kKS * kAtomBytes;  // scale atoms of A (first half) and B
   static constexpr uint32_t kStage = kA + kB + kSF;
-  static constexpr uint32_t kXbuf = 64 * 33 * 4;    // gate_up: up-half exchange
-  static constexpr uint32_t kBars = 256;
+  static constexpr uint32_t kXbuf = 128 * 33 * 4;   // gate_up: the accumulator chunk exchanged through smem
+  static constexpr uint32_t kBars = 1024;
   static constexpr uint32_t kBudget = 227 * 1024 - 1024 - kXbuf - kBars;
   static constexpr int kStages = (kBudget / kStage) > 8 ? 8 : (int)(kBudget / kStage);
   static constexpr uint32_t kSmem = 1024 + kStages * kStage + kBars + kXbuf;
   static_assert(kStages >= 2, "pipeline too shallow");
   static_assert(256 + 8 * kKS * kStages <= 512, "tmem columns");
+  static_assert((2 * kStages + 5) * 8 + 16 + 4 * (BN + 1) <= kBars, "barrier area");
 };
 
-struct GemmParams {
-  const uint8_t* sfa;      // weight scale atoms [E][m_tiles][k_tiles][512]
-  const float* bias;       // [E][out_rows] fp32 (gate_up rows interleaved)
-  const uint8_t* sfb;      // activation scale atoms [tiles][k_tiles][512]
-  const int32_t* tiles;    // [0] = count; tile i at 4 + 4i: {expert, row0, rows, 0}
-  uint8_t* hq;             // gate_up out: E4M3 codes [TK][I]
-  uint8_t* hq_sf;          // gate_up out: scale atoms [tiles][hq_ktiles][512]
-  float* y;                // down out: [TK][H]
+struct MlpParams {
+  const uint8_t* gu_sfa;     // gate_up weight scale atoms [E][gu_mtiles][gu_ktiles][512]
+  const float* gu_bias;      // [E][2I] fp32, rows interleaved like the weights
+  const uint8_t* d_sfa;      // down weight scale atoms [E][d_mtiles][d_ktiles][512]
+  const float* d_bias;       // [E][H] fp32
+  const uint8_t* xp_sf;      // gate_up B scale atoms [tiles][gu_ktiles][512]
+  uint8_t* hq;               // gate_up out / down B: E4M3 codes [TK][I]
+  uint8_t* hq_sf;            // gate_up out / down B: scale atoms [tiles][d_ktiles][512]
+  float* y;                  // down out: [TK][H]
+  uint16_t* out;             // combine out: bf16 [T][H]
+  const int32_t* tiles;      // [0] = count; tile i at 4 + 4i: {expert, row0, rows, 0}
+  const int32_t* sorted_rows;  // grouped position -> flat (t*k + j)
+  const int32_t* inv_pos;      // flat (t*k + j) -> grouped position
+  const float* topk_w;         // [T][k]
+  int32_t* done_gu;          // [tiles] gate_up m-tiles finished per token tile
+  int32_t* done_tok;         // [T][d_mtiles] down contributions finished per (token, feature block)
   uint32_t* status;
-  int m_tiles, k_tiles, out_rows, rows_stored, I, H, hq_ktiles;
+  int gu_mtiles, gu_ktiles, gu_rows_stored;
+  int d_mtiles, d_ktiles, d_rows_stored;
+  int I, H, k;
 };
+
+struct TileRef {
+  bool gu;      // gate_up tile (else down)
+  int b, m;     // token tile, weight m-tile
+};
+
+__device__ __forceinline__ TileRef tile_ref(int tile, int n_gu, const MlpParams& p) {
+  TileRef r;
+  r.gu = tile < n_gu;
+  if (r.gu) {
+    r.b = tile / p.gu_mtiles;
+    r.m = tile - r.b * p.gu_mtiles;
+  } else {
+    const int t = tile - n_gu;
+    r.b = t / p.d_mtiles;
+    r.m = t - r.b * p.d_mtiles;
+  }
+  return r;
+}
 
 // Where a bounded wait expired: role (1 producer/empty, 2 mma/accumulator, 3 mma/full,
-// 4 epilogue), tile and k-step, packed for the second status word.
+// 4 epilogue, 5 producer/dependency), tile and k-step, packed for the second status word.
 __device__ __forceinline__ uint32_t wait_site(uint32_t role, int tile, int kt) {
   return (role << 28) | ((uint32_t)min(tile, 0xFFFF) << 12) | (uint32_t)min(kt, 0xFFF);
 }
@@ -79,11 +118,38 @@ __device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
   return r;
 }
 
-template <int BN, bool GATE_UP>
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Bounded wait (all lanes of the warp) until *ctr >= target.
+__device__ __forceinline__ bool wait_counter_warp(const int32_t* ctr, int target, uint64_t limit_ns) {
+  bool ok = ld_acquire_gpu(ctr) >= target;
+  if (!__all_sync(0xffffffffu, ok)) {
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+      ok = ld_acquire_gpu(ctr) >= target;
+      if (__all_sync(0xffffffffu, ok)) break;
+      if (global_timer_ns() - t0 > limit_ns) return false;
+      __nanosleep(64);
+    }
+  }
+  return true;
+}
+
+template <int BN>
 __global__ void __launch_bounds__(192, 1)
-    expert_gemm_kernel(const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmA,
-                       const __grid_constant__ CUtensorMap tmAt, const __grid_constant__ CUtensorMap tmB,
-                       const GemmParams p) {
+    expert_mlp_kernel(const __grid_constant__ CUtensorMap tmGu2, const __grid_constant__ CUtensorMap tmGu,
+                      const __grid_constant__ CUtensorMap tmGuT, const __grid_constant__ CUtensorMap tmXp,
+                      const __grid_constant__ CUtensorMap tmD2, const __grid_constant__ CUtensorMap tmD,
+                      const __grid_constant__ CUtensorMap tmDT, const __grid_constant__ CUtensorMap tmHq,
+                      const MlpParams p) {
   using C = GemmCfg<BN>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -97,6 +163,7 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* comb_list = reinterpret_cast<int*>(tmem_slot + 4);  // [BN + 1]: count, tokens to combine
   float* xbuf = reinterpret_cast<float*>(sSF + S * C::kSF + C::kBars);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -121,18 +188,20 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int n_btiles = p.tiles[0];
-  const int total = n_btiles * p.m_tiles;
+  const int n_gu = n_btiles * p.gu_mtiles;
+  const int total = n_gu + n_btiles * p.d_mtiles;
   const int4* tl = reinterpret_cast<const int4*>(p.tiles + 4);
 
   if (warp == 0) {
     // -------------------------------------------------------------- producer
-    // The whole warp walks the schedule (so every operand stays warp-uniform);
-    // one elected lane issues the copies.
     if (elect_one()) {
-      tma_prefetch_desc(&tmA);
-      tma_prefetch_desc(&tmA2);
-      tma_prefetch_desc(&tmAt);
-      tma_prefetch_desc(&tmB);
+      tma_prefetch_desc(&tmGu2);
+      tma_prefetch_desc(&tmGu);
+      tma_prefetch_desc(&tmXp);
+      tma_prefetch_desc(&tmD2);
+      tma_prefetch_desc(&tmD);
+      tma_prefetch_desc(&tmDT);
+      tma_prefetch_desc(&tmHq);
     }
     __syncwarp();
     int s = 0;
@@ -140,13 +209,29 @@ __global__ void __launch_bounds__(192, 1)
     int64_t issued = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      const int b = tile / p.m_tiles, m = tile - b * p.m_tiles;
-      const int4 td = tl[b];
-      const uint8_t* sfa = p.sfa + ((int64_t)td.x * p.m_tiles + m) * p.k_tiles * kAtomBytes;
-      const uint8_t* sfb = p.sfb + (int64_t)b * p.k_tiles * kAtomBytes;
-      const int rows_m = min(kTileM, p.rows_stored - m * kTileM);  // 64 for a tail m-tile
-      for (int kt = 0; kt < p.k_tiles; kt += kKS) {
-        const int nk = min(kKS, p.k_tiles - kt);
+      const TileRef r = tile_ref(tile, n_gu, p);
+      const int4 td = tl[r.b];
+      const int k_tiles = r.gu ? p.gu_ktiles : p.d_ktiles;
+      const int m_tiles = r.gu ? p.gu_mtiles : p.d_mtiles;
+      const int rows_stored = r.gu ? p.gu_rows_stored : p.d_rows_stored;
+      const uint8_t* sfa = (r.gu ? p.gu_sfa : p.d_sfa) + ((int64_t)td.x * m_tiles + r.m) * k_tiles * kAtomBytes;
+      const uint8_t* sfb = (r.gu ? p.xp_sf : p.hq_sf) + (int64_t)r.b * k_tiles * kAtomBytes;
+      const int rows_m = min(kTileM, rows_stored - r.m * kTileM);  // 64 for a tail m-tile
+      const CUtensorMap* bmap = r.gu ? &tmXp : &tmHq;
+      if (!r.gu) {
+        // the intermediate of this token tile must be complete (all gate_up m-tiles)
+        if (!wait_counter_warp(p.done_gu + r.b, p.gu_mtiles, kWaitLimitNs)) {
+          if (lane == 0) {
+            atomicOr(p.status, kStatusTimeoutProducer);
+            atomicCAS(p.status + 1, 0u, wait_site(5, tile, 0));
+          }
+          ok = false;
+          break;
+        }
+        fence_proxy_async_global();  // hq was written by generic stores; TMA reads it
+      }
+      for (int kt = 0; kt < k_tiles; kt += kKS) {
+        const int nk = min(kKS, k_tiles - kt);
         if (!mbar_wait_warp(&empty[s], ph ^ 1u, kWaitLimitNs)) {
           if (lane == 0) {
             atomicOr(p.status, kStatusTimeoutProducer);
@@ -158,11 +243,12 @@ __global__ void __launch_bounds__(192, 1)
         if (elect_one()) {
           // the nk weight tiles are rows_m * nk consecutive 64-byte rows: one box
           const int box_rows = rows_m * nk;
-          const CUtensorMap* amap = box_rows == 256 ? &tmA2 : (box_rows == 128 ? &tmA : &tmAt);
+          const CUtensorMap* amap = r.gu ? (box_rows == 256 ? &tmGu2 : (box_rows == 128 ? &tmGu : &tmGuT))
+                                         : (box_rows == 256 ? &tmD2 : (box_rows == 128 ? &tmD : &tmDT));
           mbar_arrive_expect_tx(&full[s], (uint32_t)(box_rows * kTileRowBytes + nk * (C::kB1 + 2 * kAtomBytes)));
-          tma_load_2d(sA + s * C::kA, amap, &full[s], 0, (int)tile_row0(td.x, m, kt, p.rows_stored, p.k_tiles));
+          tma_load_2d(sA + s * C::kA, amap, &full[s], 0, (int)tile_row0(td.x, r.m, kt, rows_stored, k_tiles));
           for (int j = 0; j < nk; ++j)
-            tma_load_2d(sB + s * C::kB + j * C::kB1, &tmB, &full[s], (kt + j) * kTileK, td.y);
+            tma_load_2d(sB + s * C::kB + j * C::kB1, bmap, &full[s], (kt + j) * kTileK, td.y);
           uint8_t* sf = sSF + s * C::kSF;
           bulk_g2s(sf, sfa + kt * kAtomBytes, nk * kAtomBytes, &full[s]);
           bulk_g2s(sf + kKS * kAtomBytes, sfb + kt * kAtomBytes, nk * kAtomBytes, &full[s]);
@@ -183,13 +269,14 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
-    // Warp-uniform loop; the elected lane (always the same one, the lowest) issues
-    // tcgen05.cp / tcgen05.mma and the commits that track them.
     int s = 0, acc = 0;
     uint32_t ph = 0, aph = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      const int4 td = tl[tile / p.m_tiles];
+      const TileRef r = tile_ref(tile, n_gu, p);
+      const int4 td = tl[r.b];
+      const int k_tiles = r.gu ? p.gu_ktiles : p.d_ktiles;
+      const int rows_m = min(kTileM, (r.gu ? p.gu_rows_stored : p.d_rows_stored) - r.m * kTileM);
       if (!mbar_wait_warp(&tempty[acc], aph ^ 1u, kWaitLimitNs)) {
         if (lane == 0) {
           atomicOr(p.status, kStatusTimeoutMma);
@@ -201,9 +288,8 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t n_mma = (uint32_t)min(BN, max(16, (td.z + 15) & ~15));
       const uint32_t d_tmem = tmem + (uint32_t)acc * 128u;
       const uint32_t idesc0 = idesc_mxf8f6f4(128, n_mma, 5 /*E2M1*/, 0 /*E4M3*/, 0, 0);
-      const int rows_m = min(kTileM, p.rows_stored - (tile % p.m_tiles) * kTileM);
-      for (int kt = 0; kt < p.k_tiles; kt += kKS) {
-        const int nk = min(kKS, p.k_tiles - kt);
+      for (int kt = 0; kt < k_tiles; kt += kKS) {
+        const int nk = min(kKS, k_tiles - kt);
         if (!mbar_wait_warp(&full[s], ph, kWaitLimitNs)) {
           if (lane == 0) {
             atomicOr(p.status, kStatusTimeoutMma);
@@ -254,16 +340,17 @@ __global__ void __launch_bounds__(192, 1)
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;              // tmem lane quadrant this warp may read
     const int row = 32 * q + lane;       // tile row == tmem lane
+    const int et = threadIdx.x - 64;     // 0..127 within the epilogue warps
     int acc = 0;
     uint32_t aph = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const int b = tile / p.m_tiles, m = tile - b * p.m_tiles;
-      const int4 td = tl[b];
+      const TileRef r = tile_ref(tile, n_gu, p);
+      const int4 td = tl[r.b];
       const int rows = td.z;
       if (ok) {
         // all lanes take the same decision, so the warp-collective tcgen05.ld stays uniform
-        ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], aph, kWaitLimitNs));
+        ok = mbar_wait_warp(&tfull[acc], aph, kWaitLimitNs);
         if (!ok && lane == 0) {
           atomicOr(p.status, kStatusTimeoutEpilogue);
           atomicCAS(p.status + 1, 0u, wait_site(4, tile, 0));
@@ -271,9 +358,13 @@ __global__ void __launch_bounds__(192, 1)
       }
       tc_fence_after();
       const uint32_t tb = tmem + (uint32_t)acc * 128u + ((uint32_t)(32 * q) << 16);
-      if constexpr (GATE_UP) {
-        const float bias_v = p.bias[(int64_t)td.x * p.out_rows + m * kTileM + row];
-        const int kb = 2 * m + q;  // MX block of the intermediate this gate warp covers
+      if (r.gu) {
+        // accumulator rows 0..63 = gate, 64..127 = up of intermediate columns 64m..64m+63
+        const float bias_v = p.gu_bias[(int64_t)td.x * 2 * p.I + r.m * kTileM + row];
+        // work split of a 32-column chunk: warp w quantises gate block (w & 1) for
+        // columns 16 * (w >> 1) .. +16 (a 32-row block is one MX block of h)
+        const int wq = warp - 2, rb = wq & 1, jc = (wq >> 1) * 16;
+        const int kb = 2 * r.m + rb;  // MX block of the intermediate
         for (int c0 = 0; c0 < rows; c0 += 32) {
           uint32_t r0[16], r1[16];
           if (ok) {
@@ -284,38 +375,42 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) r0[j] = r1[j] = 0;
           }
-          if (q >= 2) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              xbuf[(row - 64) * 33 + j] = __uint_as_float(j < 16 ? r0[j] : r1[j - 16]) + bias_v;
-          }
+          for (int j = 0; j < 32; ++j) xbuf[row * 33 + j] = __uint_as_float(j < 16 ? r0[j] : r1[j - 16]) + bias_v;
           named_barrier_sync(1, 128);
-          if (q < 2) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int n = c0 + j;
-              if (n < rows) {
-                const float g = __uint_as_float(j < 16 ? r0[j] : r1[j - 16]) + bias_v;
-                const float u = xbuf[row * 33 + j];
-                const float h = g / (1.0f + expf(-g)) * u;
-                const uint32_t amax = warp_max_u32(__float_as_uint(fabsf(h)));
-                const int sx = mx_scale_exp(__uint_as_float(amax));
-                const uint8_t code = (uint8_t)(cvt_e4m3x2(h * mx_pow2_neg(sx), 0.0f) & 0xFFu);
-                if (ok) {
-                  p.hq[(int64_t)(td.y + n) * p.I + m * 64 + row] = code;
-                  if (lane == 0)
-                    p.hq_sf[((int64_t)b * p.hq_ktiles + (kb >> 2)) * kAtomBytes + (n & 31) * 16 + (n >> 5) * 4 +
-                            (kb & 3)] = (uint8_t)(sx + 127);
-                }
+#pragma unroll 4
+          for (int jj = 0; jj < 16; ++jj) {
+            const int j = jc + jj, n = c0 + j;
+            if (n < rows) {
+              const float g = xbuf[(32 * rb + lane) * 33 + j];
+              const float u = xbuf[(64 + 32 * rb + lane) * 33 + j];
+              const float h = g / (1.0f + expf(-g)) * u;
+              const uint32_t amax = warp_max_u32(__float_as_uint(fabsf(h)));
+              const int sx = mx_scale_exp(__uint_as_float(amax));
+              const uint8_t code = (uint8_t)(cvt_e4m3x2(h * mx_pow2_neg(sx), 0.0f) & 0xFFu);
+              if (ok) {
+                p.hq[(int64_t)(td.y + n) * p.I + r.m * 64 + 32 * rb + lane] = code;
+                if (lane == 0)
+                  p.hq_sf[((int64_t)r.b * p.d_ktiles + (kb >> 2)) * kAtomBytes + (n & 31) * 16 + (n >> 5) * 4 +
+                          (kb & 3)] = (uint8_t)(sx + 127);
               }
             }
           }
           named_barrier_sync(1, 128);
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        // every hq byte of this m-tile is stored (the last barrier above): count it
+        if (et == 0 && ok) {
+          __threadfence();
+          fence_proxy_async_global();
+          atomicAdd(p.done_gu + r.b, 1);
+        }
       } else {
-        const int orow = m * kTileM + row;
+        const int orow = r.m * kTileM + row;
         const bool rv = orow < p.H;
-        const float bias_v = rv ? p.bias[(int64_t)td.x * p.H + orow] : 0.0f;
+        const float bias_v = rv ? p.d_bias[(int64_t)td.x * p.H + orow] : 0.0f;
         for (int c0 = 0; c0 < rows; c0 += 32) {
           uint32_t r0[16], r1[16];
           if (ok) {
@@ -326,15 +421,54 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
                 const int n = c0 + j;
-                if (n < rows) p.y[(int64_t)(td.y + n) * p.H + orow] = __uint_as_float(j < 16 ? r0[j] : r1[j - 16]) + bias_v;
+                if (n < rows)
+                  p.y[(int64_t)(td.y + n) * p.H + orow] = __uint_as_float(j < 16 ? r0[j] : r1[j - 16]) + bias_v;
               }
             }
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        // combine: each token of the tile has one more of its k contributions to
+        // feature block m; the epilogue that completes the k-th sums them (slot order)
+        if (et == 0) comb_list[0] = 0;
+        named_barrier_sync(1, 128);
+        if (et < rows && ok) {
+          const int flat = p.sorted_rows[td.y + et];
+          const int t = flat / p.k;
+          __threadfence();
+          const int prev = atomicAdd(p.done_tok + (int64_t)t * p.d_mtiles + r.m, 1);
+          if (prev == p.k - 1) {
+            __threadfence();
+            comb_list[1 + atomicAdd(comb_list, 1)] = t;
+          }
+        }
+        named_barrier_sync(1, 128);
+        const int ncomb = comb_list[0];
+        for (int i = warp - 2; i < ncomb; i += 4) {
+          const int t = comb_list[1 + i];
+          const int f = r.m * kTileM + 4 * lane;
+          if (f < p.H) {
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < p.k; ++j) {
+              const float wj = p.topk_w[(int64_t)t * p.k + j];
+              const int64_t pos = p.inv_pos[(int64_t)t * p.k + j];
+              const float4 v = __ldcg(reinterpret_cast<const float4*>(p.y + pos * p.H + f));
+              a.x = fmaf(wj, v.x, a.x);
+              a.y = fmaf(wj, v.y, a.y);
+              a.z = fmaf(wj, v.z, a.z);
+              a.w = fmaf(wj, v.w, a.w);
+            }
+            const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a.x)) |
+                                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a.y)) << 16);
+            const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a.z)) |
+                                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a.w)) << 16);
+            *reinterpret_cast<uint2*>(p.out + (int64_t)t * p.H + f) = make_uint2(lo, hi);
+          }
+        }
+        named_barrier_sync(1, 128);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
       acc ^= 1;
       if (acc == 0) aph ^= 1u;
     }
@@ -360,7 +494,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Weights: the tile-contiguous layout seen as a 2-D array of 128-element (64-byte)
-// rows of 4-bit codes; one box is one tile (128 rows, or 64 for a tail m-tile),
+// rows of 4-bit codes; one box is kKS adjacent tiles or fewer (256, 128 or 64 rows),
 // unpacked by TMA into the 16-byte-aligned smem form the MMA reads (16 codes in
 // each 16-byte chunk, 8 bytes used).
 bool make_weight_map(CUtensorMap* map, const uint8_t* base, int64_t total_rows, int box_rows) {
@@ -388,69 +522,81 @@ bool make_act_map(CUtensorMap* map, const uint8_t* base, int K, int rows, int bo
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, bool GU>
-cudaError_t launch_bn(const CUtensorMap& a2, const CUtensorMap& a, const CUtensorMap& at, const CUtensorMap& b,
-                      const GemmParams& p, int grid, cudaStream_t s) {
+struct Maps {
+  CUtensorMap gu2, gu, gut, xp, d2, d, dt, hq;
+};
+
+template <int BN>
+cudaError_t launch_bn(const Maps& m, const MlpParams& p, int grid, cudaStream_t s) {
   using C = GemmCfg<BN>;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(expert_gemm_kernel<BN, GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)C::kSmem);
+    cudaError_t e =
+        cudaFuncSetAttribute(expert_mlp_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  expert_gemm_kernel<BN, GU><<<grid, 192, C::kSmem, s>>>(a2, a, at, b, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeCooperative;  // every CTA resident: the tile dependencies need it
+  attrs[0].val.cooperative = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, expert_mlp_kernel<BN>, m.gu2, m.gu, m.gut, m.xp, m.d2, m.d, m.dt, m.hq, p);
 }
 
 }  // namespace
 
-cudaError_t launch_expert_gemm(bool gate_up, const PackedHeader& h, const uint8_t* packed, const uint8_t* b_rows,
-                               int b_rows_total, const uint8_t* b_sf, const int32_t* tiles, int max_tiles,
-                               int tile_rows, uint8_t* hq, uint8_t* hq_sf, float* y, uint32_t* status, int num_sms,
-                               cudaStream_t s) {
-  CUtensorMap ma2, ma, mat, mb;
-  GemmParams p{};
-  p.tiles = tiles;
-  p.status = status;
+cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, const ExpertMlpBuffers& b, int T, int k,
+                              int max_tiles, int tile_rows, int num_sms, cudaStream_t s) {
+  Maps m;
+  const int TK = T * k;
+  const int64_t gu_rows = (int64_t)h.E * h.gu_rows_stored * h.gu_ktiles;
+  const int64_t d_rows = (int64_t)h.E * h.d_rows_stored * h.d_ktiles;
+  if (!make_weight_map(&m.gu2, packed + h.off_gu_data, gu_rows, 2 * kTileM) ||
+      !make_weight_map(&m.gu, packed + h.off_gu_data, gu_rows, kTileM) ||
+      !make_weight_map(&m.gut, packed + h.off_gu_data, gu_rows, 64) ||
+      !make_weight_map(&m.d2, packed + h.off_d_data, d_rows, 2 * kTileM) ||
+      !make_weight_map(&m.d, packed + h.off_d_data, d_rows, kTileM) ||
+      !make_weight_map(&m.dt, packed + h.off_d_data, d_rows, 64) ||
+      !make_act_map(&m.xp, b.xp, h.H, TK, tile_rows) || !make_act_map(&m.hq, b.hq, h.I, TK, tile_rows))
+    return cudaErrorInvalidValue;
+  MlpParams p{};
+  p.gu_sfa = packed + h.off_gu_sf;
+  p.gu_bias = reinterpret_cast<const float*>(packed + h.off_gu_bias);
+  p.d_sfa = packed + h.off_d_sf;
+  p.d_bias = reinterpret_cast<const float*>(packed + h.off_d_bias);
+  p.xp_sf = b.xp_sf;
+  p.hq = b.hq;
+  p.hq_sf = b.hq_sf;
+  p.y = b.y;
+  p.out = b.out;
+  p.tiles = b.tiles;
+  p.sorted_rows = b.sorted_rows;
+  p.inv_pos = b.inv_pos;
+  p.topk_w = b.topk_w;
+  p.done_gu = b.done_gu;
+  p.done_tok = b.done_tok;
+  p.status = b.status;
+  p.gu_mtiles = h.gu_mtiles;
+  p.gu_ktiles = h.gu_ktiles;
+  p.gu_rows_stored = h.gu_rows_stored;
+  p.d_mtiles = h.d_mtiles;
+  p.d_ktiles = h.d_ktiles;
+  p.d_rows_stored = h.d_rows_stored;
   p.I = h.I;
   p.H = h.H;
-  p.hq_ktiles = h.d_ktiles;
-  p.hq = hq;
-  p.hq_sf = hq_sf;
-  p.y = y;
-  p.sfb = b_sf;
-  if (gate_up) {
-    const int64_t rows = (int64_t)h.E * h.gu_rows_stored * h.gu_ktiles;
-    if (!make_weight_map(&ma2, packed + h.off_gu_data, rows, 2 * kTileM)) return cudaErrorInvalidValue;
-    if (!make_weight_map(&ma, packed + h.off_gu_data, rows, kTileM)) return cudaErrorInvalidValue;
-    if (!make_weight_map(&mat, packed + h.off_gu_data, rows, 64)) return cudaErrorInvalidValue;
-    if (!make_act_map(&mb, b_rows, h.H, b_rows_total, tile_rows)) return cudaErrorInvalidValue;
-    p.sfa = packed + h.off_gu_sf;
-    p.bias = reinterpret_cast<const float*>(packed + h.off_gu_bias);
-    p.m_tiles = h.gu_mtiles;
-    p.k_tiles = h.gu_ktiles;
-    p.out_rows = 2 * h.I;
-    p.rows_stored = h.gu_rows_stored;
-  } else {
-    const int64_t rows = (int64_t)h.E * h.d_rows_stored * h.d_ktiles;
-    if (!make_weight_map(&ma2, packed + h.off_d_data, rows, 2 * kTileM)) return cudaErrorInvalidValue;
-    if (!make_weight_map(&ma, packed + h.off_d_data, rows, kTileM)) return cudaErrorInvalidValue;
-    if (!make_weight_map(&mat, packed + h.off_d_data, rows, 64)) return cudaErrorInvalidValue;
-    if (!make_act_map(&mb, b_rows, h.I, b_rows_total, tile_rows)) return cudaErrorInvalidValue;
-    p.sfa = packed + h.off_d_sf;
-    p.bias = reinterpret_cast<const float*>(packed + h.off_d_bias);
-    p.m_tiles = h.d_mtiles;
-    p.k_tiles = h.d_ktiles;
-    p.out_rows = h.H;
-    p.rows_stored = h.d_rows_stored;
-  }
-  const int grid = (int)std::min<int64_t>(num_sms, (int64_t)max_tiles * p.m_tiles);
+  p.k = k;
+  const int grid = (int)std::min<int64_t>(num_sms, (int64_t)max_tiles * (h.gu_mtiles + h.d_mtiles));
   switch (tile_rows) {
-    case 16: return gate_up ? launch_bn<16, true>(ma2, ma, mat, mb, p, grid, s) : launch_bn<16, false>(ma2, ma, mat, mb, p, grid, s);
-    case 32: return gate_up ? launch_bn<32, true>(ma2, ma, mat, mb, p, grid, s) : launch_bn<32, false>(ma2, ma, mat, mb, p, grid, s);
-    case 64: return gate_up ? launch_bn<64, true>(ma2, ma, mat, mb, p, grid, s) : launch_bn<64, false>(ma2, ma, mat, mb, p, grid, s);
-    case 128: return gate_up ? launch_bn<128, true>(ma2, ma, mat, mb, p, grid, s) : launch_bn<128, false>(ma2, ma, mat, mb, p, grid, s);
+    case 16: return launch_bn<16>(m, p, grid, s);
+    case 32: return launch_bn<32>(m, p, grid, s);
+    case 64: return launch_bn<64>(m, p, grid, s);
+    case 128: return launch_bn<128>(m, p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }
