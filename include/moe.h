@@ -85,6 +85,7 @@ typedef struct {
   size_t status;       /* uint32 [4]: device status words (0 = ok)                  */
   size_t done_gu;      /* int32 [max_tiles]: finished gate_up tiles per token tile  */
   size_t done_tok;     /* int32 [T, ceil(H/128)]: finished down slots per block     */
+  size_t grid_bar;     /* int32: arrival count of the small-batch routing kernel    */
   size_t zero_bytes;   /* bytes from offset 0 the forward zeroes before it starts   */
   size_t logits;       /* fp32 [T, E] router logits                                 */
   size_t topk_ids;     /* int32 [T, k]                                              */
@@ -182,14 +183,13 @@ moe_status moe_get_device_status(const void *workspace, void *stream);
 /*
  * Optional per-stage timing of moe_forward with CUDA events (host-side event
  * objects only; no device memory).  moe_profile_begin(n) arms event recording
- * for the next n forward calls; moe_profile_end synchronises on the recorded
- * events and writes, per stage, the summed milliseconds over the recorded calls
- * into stage_ms[0..4] and the number of calls into *calls.  Stages: 0 router
- * GEMV, 1 top-k + softmax + MXFP8 of x, 2 grouping, 3 gather, 4 expert MLP
- * (gate_up GEMM + SwiGLU + MXFP8, down GEMM, combine in one persistent kernel).
- * Each stage's events are recorded on the stream the
- * forward runs on, around that stage's launch.  Not thread-safe; not for use
- * while a forward is being captured into a CUDA graph.
+ * for the next n forward calls (three events each: start, expert-kernel start,
+ * end; inside a stream capture they become timestamping graph nodes);
+ * moe_profile_end synchronises on the recorded events and writes, per stage,
+ * the summed milliseconds over the recorded calls into stage_ms[0..1] and the
+ * number of calls into *calls.  Stages: 0 routing (router GEMV, top-k +
+ * softmax, MXFP8 of x, grouping, gather), 1 expert MLP (gate_up GEMM + SwiGLU +
+ * MXFP8, down GEMM, combine in one persistent kernel).  Not thread-safe.
  */
 moe_status moe_profile_begin(int32_t max_calls);
 moe_status moe_profile_end(double *stage_ms, int32_t *calls);

@@ -28,7 +28,7 @@ EXPORTED = ["moe_packed_size", "moe_pack_weights", "moe_workspace_size", "moe_wo
             "moe_forward", "moe_forward_static_scratch", "moe_get_device_status", "moe_profile_begin",
             "moe_profile_end",
             "moe_last_error", "moe_version"]
-STAGES = ["router", "topk_quant", "grouping", "gather", "expert_mlp"]
+STAGES = ["routing", "expert_mlp"]
 
 
 class MoeError(RuntimeError):
@@ -48,7 +48,7 @@ class Weights(ctypes.Structure):
 
 class WorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
-        "status", "done_gu", "done_tok", "zero_bytes", "logits", "topk_ids", "topk_w", "xq", "xs", "counts", "offsets", "sorted_rows",
+        "status", "done_gu", "done_tok", "grid_bar", "zero_bytes", "logits", "topk_ids", "topk_w", "xq", "xs", "counts", "offsets", "sorted_rows",
         "inv_pos", "tiles", "xp", "xp_sf", "hq", "hq_sf", "y", "total")] + [
         ("max_tiles", ctypes.c_int32), ("tile_rows", ctypes.c_int32)]
 

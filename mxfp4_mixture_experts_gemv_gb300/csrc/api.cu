@@ -37,7 +37,7 @@ moe_status check_dims(const moe_dims& d) {
   return MOE_OK;
 }
 
-constexpr int kStages = 5;
+constexpr int kStages = 2;  // routing (all routing kernels), expert MLP
 
 // Per-stage CUDA events of profiled forward calls.
 struct Profiler {
@@ -161,25 +161,48 @@ moe_status moe_forward(moe_dims d, const void* hidden, int32_t T, const void* ro
   if (e != cudaSuccess) return cuda_fail(e, "status reset");
   cudaEvent_t* pev = profile_slot();
   auto mark = [&](int i) {
-    if (pev) cudaEventRecord(pev[i], s);
+    // external record: inside a stream capture this becomes a timestamping graph node
+    if (pev) cudaEventRecordWithFlags(pev[i], s, cudaEventRecordExternal);
   };
   mark(0);
-  e = moe::launch_router(static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(router_w),
-                         static_cast<const uint16_t*>(router_b), T, d.H, d.E, reinterpret_cast<float*>(at(L.logits)), s);
-  if (e != cudaSuccess) return cuda_fail(e, "router kernel");
+  if (moe::route_small_fits(T, d.H)) {
+    // decode: routing, quantisation, grouping and gather in one launch
+    moe::RouteSmallOut o;
+    o.logits = reinterpret_cast<float*>(at(L.logits));
+    o.ids = ids;
+    o.w = w;
+    o.xq = at(L.xq);
+    o.xs = at(L.xs);
+    o.counts = reinterpret_cast<int32_t*>(at(L.counts));
+    o.offsets = reinterpret_cast<int32_t*>(at(L.offsets));
+    o.sorted_rows = sorted_rows;
+    o.inv_pos = inv_pos;
+    o.tiles = tiles;
+    o.xp = at(L.xp);
+    o.xp_sf = at(L.xp_sf);
+    o.hq_sf = at(L.hq_sf);
+    o.grid_bar = reinterpret_cast<int32_t*>(at(L.grid_bar));
+    o.status = status;
+    e = moe::launch_route_small(static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(router_w),
+                                static_cast<const uint16_t*>(router_b), T, d.H, d.E, d.I, top_k, L.tile_rows,
+                                L.max_tiles, o, s);
+    if (e != cudaSuccess) return cuda_fail(e, "small-batch routing kernel");
+  } else {
+    e = moe::launch_router(static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(router_w),
+                           static_cast<const uint16_t*>(router_b), T, d.H, d.E, reinterpret_cast<float*>(at(L.logits)),
+                           s);
+    if (e != cudaSuccess) return cuda_fail(e, "router kernel");
+    e = moe::launch_topk_quant(reinterpret_cast<const float*>(at(L.logits)), static_cast<const uint16_t*>(hidden), T,
+                               d.H, d.E, top_k, ids, w, at(L.xq), at(L.xs), s);
+    if (e != cudaSuccess) return cuda_fail(e, "top-k/quantise kernel");
+    e = moe::launch_permute(ids, TK, top_k, d.E, L.tile_rows, L.max_tiles, reinterpret_cast<int32_t*>(at(L.counts)),
+                            reinterpret_cast<int32_t*>(at(L.offsets)), sorted_rows, inv_pos, tiles, s);
+    if (e != cudaSuccess) return cuda_fail(e, "grouping kernel");
+    e = moe::launch_gather(at(L.xq), at(L.xs), sorted_rows, tiles, L.max_tiles, top_k, d.H, d.I, L.tile_rows,
+                           at(L.xp), at(L.xp_sf), at(L.hq_sf), s);
+    if (e != cudaSuccess) return cuda_fail(e, "gather kernel");
+  }
   mark(1);
-  e = moe::launch_topk_quant(reinterpret_cast<const float*>(at(L.logits)), static_cast<const uint16_t*>(hidden), T,
-                             d.H, d.E, top_k, ids, w, at(L.xq), at(L.xs), s);
-  if (e != cudaSuccess) return cuda_fail(e, "top-k/quantise kernel");
-  mark(2);
-  e = moe::launch_permute(ids, TK, top_k, d.E, L.tile_rows, L.max_tiles, reinterpret_cast<int32_t*>(at(L.counts)),
-                          reinterpret_cast<int32_t*>(at(L.offsets)), sorted_rows, inv_pos, tiles, s);
-  if (e != cudaSuccess) return cuda_fail(e, "grouping kernel");
-  mark(3);
-  e = moe::launch_gather(at(L.xq), at(L.xs), sorted_rows, tiles, L.max_tiles, top_k, d.H, d.I, L.tile_rows, at(L.xp),
-                         at(L.xp_sf), at(L.hq_sf), s);
-  if (e != cudaSuccess) return cuda_fail(e, "gather kernel");
-  mark(4);
   moe::ExpertMlpBuffers b;
   b.xp = at(L.xp);
   b.xp_sf = at(L.xp_sf);
@@ -196,7 +219,7 @@ moe_status moe_forward(moe_dims d, const void* hidden, int32_t T, const void* ro
   b.status = status;
   e = moe::launch_expert_mlp(h, pk, b, T, top_k, L.max_tiles, L.tile_rows, sms, s);
   if (e != cudaSuccess) return cuda_fail(e, "expert MLP kernel");
-  mark(5);
+  mark(2);
   return MOE_OK;
 }
 

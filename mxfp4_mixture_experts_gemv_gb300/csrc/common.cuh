@@ -78,8 +78,22 @@ __host__ __device__ inline int64_t tile_row0(int e, int m, int kt, int rows_stor
   return ((int64_t)e * rows_stored + (int64_t)m * kTileM) * k_tiles + (int64_t)kt * rows_m;
 }
 
-// Token rows per tile of the grouped GEMM (MMA N upper bound) for T tokens.
-inline int tile_rows_for(int T) {
+// Token counts up to this take the fused small-batch routing kernel.
+constexpr int kRouteSmallMaxT = 32;
+constexpr int kRouteSmallMaxH = 8192;
+// dynamic shared memory of the small-batch routing kernel: (T + 1) rows of H bf16
+constexpr size_t kRouteSmallMaxSmem = 200 * 1024;
+inline bool route_small_fits(int T, int H) {
+  return T <= kRouteSmallMaxT && H <= kRouteSmallMaxH && (size_t)(T + 1) * H * 2 <= kRouteSmallMaxSmem;
+}
+
+// Token rows per tile of the grouped GEMM (MMA N upper bound): a token visits an
+// expert at most once, so up to 64 tokens one tile of the next size covers any
+// expert; beyond that 128 (measured: smaller tiles re-read the weights of
+// experts with more rows than the tile and lose more than they gain).
+inline int tile_rows_for(int T, int k, int E) {
+  (void)k;
+  (void)E;
   if (T <= 16) return 16;
   if (T <= 32) return 32;
   if (T <= 64) return 64;
@@ -91,7 +105,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline bool workspace_layout(const moe_dims& d, int T, int k, moe_workspace_layout* L) {
   if (T < 0 || k <= 0) return false;
   const int64_t TK = (int64_t)T * k;
-  const int tr = tile_rows_for(T);
+  const int tr = tile_rows_for(T, k, d.E);
   const int64_t max_tiles = TK / tr + (TK < d.E ? TK : d.E) + 1;
   const int64_t kth = (d.H + kTileK - 1) / kTileK, kti = (d.I + kTileK - 1) / kTileK;
   size_t o = 0;
@@ -100,6 +114,7 @@ inline bool workspace_layout(const moe_dims& d, int T, int k, moe_workspace_layo
   l.status = take(16);
   l.done_gu = take((size_t)max_tiles * 4);
   l.done_tok = take((size_t)T * ((d.H + kTileM - 1) / kTileM) * 4);
+  l.grid_bar = take(16);
   l.zero_bytes = o;  // status words and the counters above start at zero every forward
   l.logits = take((size_t)T * d.E * 4);
   l.topk_ids = take((size_t)TK * 4);
@@ -151,6 +166,26 @@ cudaError_t launch_permute(const int32_t* ids, int TK, int k, int E, int tile_ro
 cudaError_t launch_gather(const uint8_t* xq, const uint8_t* xs, const int32_t* sorted_rows,
                           const int32_t* tiles, int max_tiles, int k, int H, int I, int tile_rows,
                           uint8_t* xp, uint8_t* xp_sf, uint8_t* hq_sf, cudaStream_t s);
+struct RouteSmallOut {
+  float* logits;
+  int32_t* ids;
+  float* w;
+  uint8_t* xq;
+  uint8_t* xs;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* sorted_rows;
+  int32_t* inv_pos;
+  int32_t* tiles;
+  uint8_t* xp;
+  uint8_t* xp_sf;
+  uint8_t* hq_sf;
+  int32_t* grid_bar;
+  uint32_t* status;
+};
+cudaError_t launch_route_small(const uint16_t* x, const uint16_t* wr, const uint16_t* br, int T, int H, int E, int I,
+                               int k, int tile_rows, int max_tiles, const RouteSmallOut& o, cudaStream_t s);
+
 struct ExpertMlpBuffers {
   const uint8_t* xp;        // gate_up B rows [TK][H]
   const uint8_t* xp_sf;     // gate_up B scale atoms

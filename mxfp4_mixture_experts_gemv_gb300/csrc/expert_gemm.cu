@@ -18,7 +18,7 @@
 // tile.  A down tile needs the whole intermediate of its token rows, i.e. all
 // gate_up m-tiles of the same token tile; their epilogues count themselves in a
 // per-token-tile counter that the down tile's producer waits on (acquire) before
-// it streams hq.  CTAs are launched cooperatively (all resident), each walks its
+// it streams hq.  Every CTA is resident (one per SM at most), each walks its
 // tiles in increasing order and finishes every gate_up tile it owns before its
 // first down tile, so every wait is on work that is already in progress.
 //
@@ -33,6 +33,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -112,16 +113,24 @@ __device__ __forceinline__ uint32_t wait_site(uint32_t role, int tile, int kt) {
   return (role << 28) | ((uint32_t)min(tile, 0xFFFF) << 12) | (uint32_t)min(kt, 0xFFF);
 }
 
-__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
-  uint32_t r;
-  asm("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
-  return r;
-}
-
 __device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+// Release increment: every write that happens-before it (this CTA's, ordered by
+// the preceding barrier) is visible to whoever acquires the counter.
+__device__ __forceinline__ void red_add_release_gpu(int32_t* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Increment with acquire and release: returns the previous value; the caller sees
+// every write published by earlier increments.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 
 __device__ __forceinline__ void fence_proxy_async_global() {
@@ -187,6 +196,9 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Everything above overlaps the previous kernel (programmatic dependent
+  // launch); the tile list and activations it produced are read only after this.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int n_btiles = p.tiles[0];
   const int n_gu = n_btiles * p.gu_mtiles;
   const int total = n_gu + n_btiles * p.d_mtiles;
@@ -208,9 +220,11 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t ph = 0;
     int64_t issued = 0;
     bool ok = true;
+    int4 td_next = blockIdx.x < total ? tl[tile_ref(blockIdx.x, n_gu, p).b] : make_int4(0, 0, 0, 0);
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       const TileRef r = tile_ref(tile, n_gu, p);
-      const int4 td = tl[r.b];
+      const int4 td = td_next;
+      if (tile + (int)gridDim.x < total) td_next = tl[tile_ref(tile + gridDim.x, n_gu, p).b];
       const int k_tiles = r.gu ? p.gu_ktiles : p.d_ktiles;
       const int m_tiles = r.gu ? p.gu_mtiles : p.d_mtiles;
       const int rows_stored = r.gu ? p.gu_rows_stored : p.d_rows_stored;
@@ -272,9 +286,11 @@ __global__ void __launch_bounds__(192, 1)
     int s = 0, acc = 0;
     uint32_t ph = 0, aph = 0;
     bool ok = true;
+    int4 td_next = blockIdx.x < total ? tl[tile_ref(blockIdx.x, n_gu, p).b] : make_int4(0, 0, 0, 0);
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       const TileRef r = tile_ref(tile, n_gu, p);
-      const int4 td = tl[r.b];
+      const int4 td = td_next;
+      if (tile + (int)gridDim.x < total) td_next = tl[tile_ref(tile + gridDim.x, n_gu, p).b];
       const int k_tiles = r.gu ? p.gu_ktiles : p.d_ktiles;
       const int rows_m = min(kTileM, (r.gu ? p.gu_rows_stored : p.d_rows_stored) - r.m * kTileM);
       if (!mbar_wait_warp(&tempty[acc], aph ^ 1u, kWaitLimitNs)) {
@@ -344,9 +360,28 @@ __global__ void __launch_bounds__(192, 1)
     int acc = 0;
     uint32_t aph = 0;
     bool ok = true;
+    // the next tile's descriptor and bias are fetched while this one is processed
+    auto bias_of = [&](const TileRef& rr, const int4& t4) -> float {
+      if (rr.gu) return p.gu_bias[(int64_t)t4.x * 2 * p.I + rr.m * kTileM + row];
+      const int o = rr.m * kTileM + row;
+      return o < p.H ? p.d_bias[(int64_t)t4.x * p.H + o] : 0.0f;
+    };
+    int4 td_next = make_int4(0, 0, 0, 0);
+    float bias_next = 0.f;
+    if (blockIdx.x < total) {
+      const TileRef r0 = tile_ref(blockIdx.x, n_gu, p);
+      td_next = tl[r0.b];
+      bias_next = bias_of(r0, td_next);
+    }
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const TileRef r = tile_ref(tile, n_gu, p);
-      const int4 td = tl[r.b];
+      const int4 td = td_next;
+      const float bias_v = bias_next;
+      if (tile + (int)gridDim.x < total) {
+        const TileRef rn = tile_ref(tile + gridDim.x, n_gu, p);
+        td_next = tl[rn.b];
+        bias_next = bias_of(rn, td_next);
+      }
       const int rows = td.z;
       if (ok) {
         // all lanes take the same decision, so the warp-collective tcgen05.ld stays uniform
@@ -360,10 +395,11 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t tb = tmem + (uint32_t)acc * 128u + ((uint32_t)(32 * q) << 16);
       if (r.gu) {
         // accumulator rows 0..63 = gate, 64..127 = up of intermediate columns 64m..64m+63
-        const float bias_v = p.gu_bias[(int64_t)td.x * 2 * p.I + r.m * kTileM + row];
-        // work split of a 32-column chunk: warp w quantises gate block (w & 1) for
-        // columns 16 * (w >> 1) .. +16 (a 32-row block is one MX block of h)
-        const int wq = warp - 2, rb = wq & 1, jc = (wq >> 1) * 16;
+        // SwiGLU + MXFP8 of a 32-column chunk, transposed through shared memory:
+        // thread et takes token column j = (et >> 1) & 31 and 16 rows (half hh = et & 1)
+        // of MX block rb = et >> 6 (gate rows 32rb..32rb+31); the two halves of a block
+        // are neighbouring lanes and share their amax with one shuffle.
+        const int hh = et & 1, jt = (et >> 1) & 31, rb = et >> 6;
         const int kb = 2 * r.m + rb;  // MX block of the intermediate
         for (int c0 = 0; c0 < rows; c0 += 32) {
           uint32_t r0[16], r1[16];
@@ -378,23 +414,38 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) xbuf[row * 33 + j] = __uint_as_float(j < 16 ? r0[j] : r1[j - 16]) + bias_v;
           named_barrier_sync(1, 128);
-#pragma unroll 4
-          for (int jj = 0; jj < 16; ++jj) {
-            const int j = jc + jj, n = c0 + j;
-            if (n < rows) {
-              const float g = xbuf[(32 * rb + lane) * 33 + j];
-              const float u = xbuf[(64 + 32 * rb + lane) * 33 + j];
-              const float h = g / (1.0f + expf(-g)) * u;
-              const uint32_t amax = warp_max_u32(__float_as_uint(fabsf(h)));
-              const int sx = mx_scale_exp(__uint_as_float(amax));
-              const uint8_t code = (uint8_t)(cvt_e4m3x2(h * mx_pow2_neg(sx), 0.0f) & 0xFFu);
-              if (ok) {
-                p.hq[(int64_t)(td.y + n) * p.I + r.m * 64 + 32 * rb + lane] = code;
-                if (lane == 0)
-                  p.hq_sf[((int64_t)r.b * p.d_ktiles + (kb >> 2)) * kAtomBytes + (n & 31) * 16 + (n >> 5) * 4 +
-                          (kb & 3)] = (uint8_t)(sx + 127);
-              }
+          const int n = c0 + jt;
+          float h[16];
+          float amax = 0.f;
+          if (n < rows) {  // same for both lanes of a pair
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int rr = 32 * rb + 16 * hh + i;
+              const float g = xbuf[rr * 33 + jt];
+              const float u = xbuf[(64 + rr) * 33 + jt];
+              h[i] = g / (1.0f + expf(-g)) * u;
+              amax = fmaxf(amax, fabsf(h[i]));
             }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) h[i] = 0.f;
+          }
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+          const int sx = mx_scale_exp(amax);
+          const float inv = mx_pow2_neg(sx);
+          uint32_t pk[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = cvt_e4m3x2(h[4 * i] * inv, h[4 * i + 1] * inv);
+            const uint32_t hi = cvt_e4m3x2(h[4 * i + 2] * inv, h[4 * i + 3] * inv);
+            pk[i] = lo | (hi << 16);
+          }
+          if (ok && n < rows) {
+            *reinterpret_cast<uint4*>(p.hq + (int64_t)(td.y + n) * p.I + r.m * 64 + 32 * rb + 16 * hh) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            if (hh == 0)
+              p.hq_sf[((int64_t)r.b * p.d_ktiles + (kb >> 2)) * kAtomBytes + (n & 31) * 16 + (n >> 5) * 4 + (kb & 3)] =
+                  (uint8_t)(sx + 127);
           }
           named_barrier_sync(1, 128);
         }
@@ -402,15 +453,10 @@ __global__ void __launch_bounds__(192, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
         // every hq byte of this m-tile is stored (the last barrier above): count it
-        if (et == 0 && ok) {
-          __threadfence();
-          fence_proxy_async_global();
-          atomicAdd(p.done_gu + r.b, 1);
-        }
+        if (et == 0 && ok) red_add_release_gpu(p.done_gu + r.b, 1);
       } else {
         const int orow = r.m * kTileM + row;
         const bool rv = orow < p.H;
-        const float bias_v = rv ? p.d_bias[(int64_t)td.x * p.H + orow] : 0.0f;
         for (int c0 = 0; c0 < rows; c0 += 32) {
           uint32_t r0[16], r1[16];
           if (ok) {
@@ -437,12 +483,10 @@ __global__ void __launch_bounds__(192, 1)
         if (et < rows && ok) {
           const int flat = p.sorted_rows[td.y + et];
           const int t = flat / p.k;
-          __threadfence();
-          const int prev = atomicAdd(p.done_tok + (int64_t)t * p.d_mtiles + r.m, 1);
-          if (prev == p.k - 1) {
-            __threadfence();
-            comb_list[1 + atomicAdd(comb_list, 1)] = t;
-          }
+          // y of this tile is stored (barrier above); release it, and acquire the
+          // other slots' rows if this is the last of the k contributions
+          const int prev = atom_add_acq_rel_gpu(p.done_tok + (int64_t)t * p.d_mtiles + r.m, 1);
+          if (prev == p.k - 1) comb_list[1 + atomicAdd(comb_list, 1)] = t;
         }
         named_barrier_sync(1, 128);
         const int ncomb = comb_list[0];
@@ -450,15 +494,26 @@ __global__ void __launch_bounds__(192, 1)
           const int t = comb_list[1 + i];
           const int f = r.m * kTileM + 4 * lane;
           if (f < p.H) {
+            // every slot's row is fetched before the sum (all loads in flight)
+            float4 v[8];
+            float wj[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              if (j < p.k) {
+                wj[j] = p.topk_w[(int64_t)t * p.k + j];
+                const int64_t pos = p.inv_pos[(int64_t)t * p.k + j];
+                v[j] = __ldcg(reinterpret_cast<const float4*>(p.y + pos * p.H + f));
+              }
+            }
             float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int j = 0; j < p.k; ++j) {
-              const float wj = p.topk_w[(int64_t)t * p.k + j];
-              const int64_t pos = p.inv_pos[(int64_t)t * p.k + j];
-              const float4 v = __ldcg(reinterpret_cast<const float4*>(p.y + pos * p.H + f));
-              a.x = fmaf(wj, v.x, a.x);
-              a.y = fmaf(wj, v.y, a.y);
-              a.z = fmaf(wj, v.z, a.z);
-              a.w = fmaf(wj, v.w, a.w);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              if (j < p.k) {
+                a.x = fmaf(wj[j], v[j].x, a.x);
+                a.y = fmaf(wj[j], v[j].y, a.y);
+                a.z = fmaf(wj[j], v[j].z, a.z);
+                a.w = fmaf(wj[j], v[j].w, a.w);
+              }
             }
             const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a.x)) |
                                 ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a.y)) << 16);
@@ -541,9 +596,14 @@ cudaError_t launch_bn(const Maps& m, const MlpParams& p, int grid, cudaStream_t 
   cfg.blockDim = dim3(192);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = s;
+  // Programmatic dependent launch: the CTAs start (barrier init, TMEM allocation,
+  // descriptor prefetch) while the routing kernel finishes.  The grid is at most
+  // one CTA per SM and each CTA needs most of an SM's shared memory, so every CTA
+  // becomes resident once the previous kernel's CTAs leave; the tile dependencies
+  // only ever wait on resident CTAs' work (and are bounded regardless).
   cudaLaunchAttribute attrs[1];
-  attrs[0].id = cudaLaunchAttributeCooperative;  // every CTA resident: the tile dependencies need it
-  attrs[0].val.cooperative = 1;
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, expert_mlp_kernel<BN>, m.gu2, m.gu, m.gut, m.xp, m.d2, m.d, m.dt, m.hq, p);
@@ -551,10 +611,38 @@ cudaError_t launch_bn(const Maps& m, const MlpParams& p, int grid, cudaStream_t 
 
 }  // namespace
 
+// Encoded descriptors depend only on these values, so they are reused across calls.
+struct MapKey {
+  const uint8_t* packed;
+  const uint8_t* xp;
+  const uint8_t* hq;
+  int E, H, I, TK, tile_rows;
+  bool operator==(const MapKey& o) const {
+    return packed == o.packed && xp == o.xp && hq == o.hq && E == o.E && H == o.H && I == o.I && TK == o.TK &&
+           tile_rows == o.tile_rows;
+  }
+};
+
 cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, const ExpertMlpBuffers& b, int T, int k,
                               int max_tiles, int tile_rows, int num_sms, cudaStream_t s) {
-  Maps m;
   const int TK = T * k;
+  static std::mutex mu;
+  static MapKey keys[32];
+  static Maps cache[32];
+  static int n_cached = 0, next_slot = 0;
+  const MapKey key{packed, b.xp, b.hq, h.E, h.H, h.I, TK, tile_rows};
+  Maps m;
+  bool hit = false;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < n_cached; ++i)
+      if (keys[i] == key) {
+        m = cache[i];
+        hit = true;
+        break;
+      }
+  }
+  if (!hit) {
   const int64_t gu_rows = (int64_t)h.E * h.gu_rows_stored * h.gu_ktiles;
   const int64_t d_rows = (int64_t)h.E * h.d_rows_stored * h.d_ktiles;
   if (!make_weight_map(&m.gu2, packed + h.off_gu_data, gu_rows, 2 * kTileM) ||
@@ -565,6 +653,12 @@ cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, cons
       !make_weight_map(&m.dt, packed + h.off_d_data, d_rows, 64) ||
       !make_act_map(&m.xp, b.xp, h.H, TK, tile_rows) || !make_act_map(&m.hq, b.hq, h.I, TK, tile_rows))
     return cudaErrorInvalidValue;
+    std::lock_guard<std::mutex> lk(mu);
+    keys[next_slot] = key;
+    cache[next_slot] = m;
+    next_slot = (next_slot + 1) % 32;
+    if (n_cached < 32) ++n_cached;
+  }
   MlpParams p{};
   p.gu_sfa = packed + h.off_gu_sf;
   p.gu_bias = reinterpret_cast<const float*>(packed + h.off_gu_bias);

@@ -6,6 +6,7 @@
 // position is its rank among equal experts in ascending flat index t*k+j,
 // decided with warp match/popcount, never by atomics racing for slots.
 #include "common.cuh"
+#include "quant.cuh"
 
 namespace moe {
 namespace {
@@ -20,6 +21,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(
   __shared__ int hist[kPermWarps][257];
   __shared__ int s_off[258];
   __shared__ int s_tile_off[258];
+  extern __shared__ int s_tile_e[];  // [max_tiles]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < kPermWarps * 257; i += kPermThreads) (&hist[0][0])[i] = 0;
   __syncthreads();
@@ -29,26 +31,15 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(
   // shared-memory indexing safe whatever the input
   for (int i = start + lane; i < end; i += 32) atomicAdd(&hist[warp][min(max(ids[i], 0), E - 1)], 1);
   __syncthreads();
+  __shared__ int s_cnt[257];
   if (threadIdx.x < E) {
     int c = 0;
     for (int w = 0; w < kPermWarps; ++w) c += hist[w][threadIdx.x];
     counts[threadIdx.x] = c;
-    s_off[threadIdx.x] = c;
-    s_tile_off[threadIdx.x] = (c + tile_rows - 1) / tile_rows;
+    s_cnt[threadIdx.x] = c;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = 0, trun = 0;
-    for (int e = 0; e < E; ++e) {
-      const int c = s_off[e], tc = s_tile_off[e];
-      s_off[e] = run;
-      s_tile_off[e] = trun;
-      run += c;
-      trun += tc;
-    }
-    s_off[E] = run;
-    s_tile_off[E] = trun;
-  }
+  if (warp == 0) warp_expert_scan(s_cnt, E, __ffs(tile_rows) - 1, s_off, s_tile_off, s_tile_e, lane);
   __syncthreads();
   if (threadIdx.x < E) {
     const int e = threadIdx.x;
@@ -98,6 +89,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint8_t* __restrict__
                                                      const int32_t* __restrict__ tiles, int k, int H, int I,
                                                      uint8_t* __restrict__ xp, uint8_t* __restrict__ xp_sf,
                                                      uint8_t* __restrict__ hq_sf) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int b = blockIdx.x;
   if (b >= tiles[0]) return;
   const int4 td = reinterpret_cast<const int4*>(tiles + 4)[b];
@@ -111,22 +103,28 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint8_t* __restrict__
     reinterpret_cast<uint4*>(xp + (int64_t)(row0 + r) * H)[c] =
         reinterpret_cast<const uint4*>(xq + (int64_t)tok[r] * H)[c];
   }
-  const int nbh = H / 32, nbi = I / 32;
+  const int nbh = H / 32;
   const int kth = (H + kTileK - 1) / kTileK, kti = (I + kTileK - 1) / kTileK;
-  for (int i = threadIdx.x; i < kth * kAtomBytes; i += blockDim.x) {
-    const int ka = i / kAtomBytes, j = i % kAtomBytes;
-    const int r = (j >> 4) + 32 * ((j & 15) >> 2);
-    const int kb = ka * 4 + (j & 3);
-    uint8_t v = 127;
-    if (r < rows && kb < nbh) v = xs[(int64_t)tok[r] * nbh + kb];
-    xp_sf[((int64_t)b * kth + ka) * kAtomBytes + j] = v;
+  // activation scale atoms: one 32-bit word per (atom, row) holds the row's 4 block scales
+  for (int i = threadIdx.x; i < kth * kTileM; i += blockDim.x) {
+    const int ka = i / kTileM, r = i - ka * kTileM;
+    uint32_t wv = 0x7F7F7F7Fu;
+    if (r < rows) {
+      const uint8_t* src = xs + (int64_t)tok[r] * nbh;
+      wv = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int kb = 4 * ka + j;
+        wv |= (uint32_t)(kb < nbh ? src[kb] : 127) << (8 * j);
+      }
+    }
+    *reinterpret_cast<uint32_t*>(xp_sf + ((int64_t)b * kth + ka) * kAtomBytes + (r & 31) * 16 + (r >> 5) * 4) = wv;
   }
-  for (int i = threadIdx.x; i < kti * kAtomBytes; i += blockDim.x) {
-    const int ka = i / kAtomBytes, j = i % kAtomBytes;
-    const int r = (j >> 4) + 32 * ((j & 15) >> 2);
-    const int kb = ka * 4 + (j & 3);
-    if (r >= rows || kb >= nbi) hq_sf[((int64_t)b * kti + ka) * kAtomBytes + j] = 127;
-  }
+  // intermediate scale atoms start as code 127 everywhere; the gate_up epilogue
+  // overwrites the real ones
+  uint4* hs = reinterpret_cast<uint4*>(hq_sf + (int64_t)b * kti * kAtomBytes);
+  for (int i = threadIdx.x; i < kti * kAtomBytes / 16; i += blockDim.x)
+    hs[i] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
 }
 
 }  // namespace
@@ -135,8 +133,8 @@ cudaError_t launch_permute(const int32_t* ids, int TK, int k, int E, int tile_ro
                            int32_t* counts, int32_t* offsets, int32_t* sorted_rows, int32_t* inv_pos,
                            int32_t* tiles, cudaStream_t s) {
   (void)k;
-  permute_kernel<<<1, kPermThreads, 0, s>>>(ids, TK, E, tile_rows, max_tiles, counts, offsets, sorted_rows,
-                                            inv_pos, tiles);
+  permute_kernel<<<1, kPermThreads, (size_t)max_tiles * sizeof(int), s>>>(ids, TK, E, tile_rows, max_tiles, counts,
+                                                                           offsets, sorted_rows, inv_pos, tiles);
   return cudaGetLastError();
 }
 

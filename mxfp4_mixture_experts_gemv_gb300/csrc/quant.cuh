@@ -22,4 +22,45 @@ __device__ __forceinline__ int mx_scale_exp(float amax) {
 // 2^-s as an fp32 (exact for s in [-127, 126]).
 __device__ __forceinline__ float mx_pow2_neg(int s) { return __uint_as_float((uint32_t)(127 - s) << 23); }
 
+// Exclusive prefix sums over E <= 256 counts by one warp (lane l owns entries
+// 8l..8l+7): off[e] = sum of cnt[<e], toff[e] = sum of ceil(cnt[<e] / 2^tshift);
+// off[E], toff[E] hold the totals and tile_e[t] the expert of every tile t.
+__device__ __forceinline__ void warp_expert_scan(const int* cnt, int E, int tshift, int* off, int* toff,
+                                                 int* tile_e, int lane) {
+  int c[8], tc[8], sum = 0, tsum = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = 8 * lane + i;
+    c[i] = e < E ? cnt[e] : 0;
+    tc[i] = (c[i] + (1 << tshift) - 1) >> tshift;
+    sum += c[i];
+    tsum += tc[i];
+  }
+  int incl = sum, tincl = tsum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o), tv = __shfl_up_sync(0xffffffffu, tincl, o);
+    if (lane >= o) {
+      incl += v;
+      tincl += tv;
+    }
+  }
+  int run = incl - sum, trun = tincl - tsum;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = 8 * lane + i;
+    if (e < E) {
+      off[e] = run;
+      toff[e] = trun;
+      for (int t = 0; t < tc[i]; ++t) tile_e[trun + t] = e;
+    }
+    run += c[i];
+    trun += tc[i];
+  }
+  if (lane == 31) {
+    off[E] = incl;
+    toff[E] = tincl;
+  }
+}
+
 }  // namespace moe
