@@ -34,6 +34,7 @@ moe_status check_dims(const moe_dims& d) {
   if (d.E > 256) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "E=%d > 256 experts", d.E);
   if (d.H % 32) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "H=%d is not a multiple of 32", d.H);
   if (d.I % 64) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "I=%d is not a multiple of 64", d.I);
+  if (d.H > moe::kRouteSmallMaxH) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "H=%d > %d", d.H, moe::kRouteSmallMaxH);
   return MOE_OK;
 }
 
@@ -188,18 +189,16 @@ moe_status moe_forward(moe_dims d, const void* hidden, int32_t T, const void* ro
                                 L.max_tiles, o, s);
     if (e != cudaSuccess) return cuda_fail(e, "small-batch routing kernel");
   } else {
-    e = moe::launch_router(static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(router_w),
-                           static_cast<const uint16_t*>(router_b), T, d.H, d.E, reinterpret_cast<float*>(at(L.logits)),
-                           s);
+    // larger T: tensor-core router with top-k in its epilogue, grouping, quantise-on-gather
+    e = moe::launch_router_tc(static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(router_w),
+                              static_cast<const uint16_t*>(router_b), T, d.H, d.E, top_k,
+                              reinterpret_cast<float*>(at(L.logits)), ids, w, status, s);
     if (e != cudaSuccess) return cuda_fail(e, "router kernel");
-    e = moe::launch_topk_quant(reinterpret_cast<const float*>(at(L.logits)), static_cast<const uint16_t*>(hidden), T,
-                               d.H, d.E, top_k, ids, w, at(L.xq), at(L.xs), s);
-    if (e != cudaSuccess) return cuda_fail(e, "top-k/quantise kernel");
     e = moe::launch_permute(ids, TK, top_k, d.E, L.tile_rows, L.max_tiles, reinterpret_cast<int32_t*>(at(L.counts)),
                             reinterpret_cast<int32_t*>(at(L.offsets)), sorted_rows, inv_pos, tiles, s);
     if (e != cudaSuccess) return cuda_fail(e, "grouping kernel");
-    e = moe::launch_gather(at(L.xq), at(L.xs), sorted_rows, tiles, L.max_tiles, top_k, d.H, d.I, L.tile_rows,
-                           at(L.xp), at(L.xp_sf), at(L.hq_sf), s);
+    e = moe::launch_gather_quant(static_cast<const uint16_t*>(hidden), sorted_rows, tiles, L.max_tiles, top_k, d.H,
+                                 d.I, at(L.xq), at(L.xs), at(L.xp), at(L.xp_sf), at(L.hq_sf), s);
     if (e != cudaSuccess) return cuda_fail(e, "gather kernel");
   }
   mark(1);

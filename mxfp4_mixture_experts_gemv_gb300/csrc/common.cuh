@@ -156,16 +156,15 @@ moe_status report_error(moe_status st, const char* fmt, ...);
 // Kernel launchers (defined in the .cu files).
 cudaError_t launch_pack(const moe_dims& d, const PackedHeader& h, const moe_mxfp4_weights& w,
                         uint8_t* packed, cudaStream_t s);
-cudaError_t launch_router(const uint16_t* x, const uint16_t* wr, const uint16_t* br, int T, int H,
-                          int E, float* logits, cudaStream_t s);
-cudaError_t launch_topk_quant(const float* logits, const uint16_t* x, int T, int H, int E, int k,
-                              int32_t* ids, float* w, uint8_t* xq, uint8_t* xs, cudaStream_t s);
+cudaError_t launch_router_tc(const uint16_t* x, const uint16_t* wr, const uint16_t* br, int T, int H, int E, int k,
+                             float* logits, int32_t* ids, float* w, uint32_t* status, cudaStream_t s);
 cudaError_t launch_permute(const int32_t* ids, int TK, int k, int E, int tile_rows, int max_tiles,
                            int32_t* counts, int32_t* offsets, int32_t* sorted_rows,
                            int32_t* inv_pos, int32_t* tiles, cudaStream_t s);
-cudaError_t launch_gather(const uint8_t* xq, const uint8_t* xs, const int32_t* sorted_rows,
-                          const int32_t* tiles, int max_tiles, int k, int H, int I, int tile_rows,
-                          uint8_t* xp, uint8_t* xp_sf, uint8_t* hq_sf, cudaStream_t s);
+cudaError_t launch_gather_quant(const uint16_t* x, const int32_t* sorted_rows, const int32_t* tiles, int max_tiles,
+                                int k, int H, int I, uint8_t* xq, uint8_t* xs, uint8_t* xp, uint8_t* xp_sf,
+                                uint8_t* hq_sf, cudaStream_t s);
+
 struct RouteSmallOut {
   float* logits;
   int32_t* ids;

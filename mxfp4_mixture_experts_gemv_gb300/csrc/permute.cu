@@ -81,47 +81,57 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(
   }
 }
 
-// One CTA per tile: copy the tile's activation rows into grouped order and
-// write the tile's scale atoms (activation scales, plus the padding bytes of the
-// intermediate's atoms, whose real bytes the gate_up epilogue fills).
-__global__ void __launch_bounds__(256) gather_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs,
-                                                     const int32_t* __restrict__ sorted_rows,
-                                                     const int32_t* __restrict__ tiles, int k, int H, int I,
-                                                     uint8_t* __restrict__ xp, uint8_t* __restrict__ xp_sf,
-                                                     uint8_t* __restrict__ hq_sf) {
+// One CTA per tile: quantise the tile's token rows to MXFP8 straight into grouped
+// order (x -> Xp rows and their scale atoms); the row of a token's first slot also
+// publishes the token's codes (xq, xs).  Padding words of the tile's atoms are
+// code 127; the intermediate's atoms start as all-127 (the gate_up epilogue
+// writes the real ones).
+__global__ void __launch_bounds__(256) gather_quant_kernel(const uint16_t* __restrict__ x,
+                                                           const int32_t* __restrict__ sorted_rows,
+                                                           const int32_t* __restrict__ tiles, int k, int H, int I,
+                                                           uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
+                                                           uint8_t* __restrict__ xp, uint8_t* __restrict__ xp_sf,
+                                                           uint8_t* __restrict__ hq_sf) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int b = blockIdx.x;
   if (b >= tiles[0]) return;
   const int4 td = reinterpret_cast<const int4*>(tiles + 4)[b];
   const int row0 = td.y, rows = td.z;
-  __shared__ int tok[128];
-  for (int r = threadIdx.x; r < rows; r += blockDim.x) tok[r] = sorted_rows[row0 + r] / k;
-  __syncthreads();
-  const int hc = H / 16;  // 16-byte chunks per row
-  for (int i = threadIdx.x; i < rows * hc; i += blockDim.x) {
-    const int r = i / hc, c = i % hc;
-    reinterpret_cast<uint4*>(xp + (int64_t)(row0 + r) * H)[c] =
-        reinterpret_cast<const uint4*>(xq + (int64_t)tok[r] * H)[c];
-  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nbh = H / 32;
   const int kth = (H + kTileK - 1) / kTileK, kti = (I + kTileK - 1) / kTileK;
-  // activation scale atoms: one 32-bit word per (atom, row) holds the row's 4 block scales
-  for (int i = threadIdx.x; i < kth * kTileM; i += blockDim.x) {
-    const int ka = i / kTileM, r = i - ka * kTileM;
-    uint32_t wv = 0x7F7F7F7Fu;
-    if (r < rows) {
-      const uint8_t* src = xs + (int64_t)tok[r] * nbh;
-      wv = 0;
+  __shared__ uint8_t s_scale[8][kRouteSmallMaxH / 32];
+  for (int r = warp; r < rows; r += 8) {
+    const int f = sorted_rows[row0 + r], t = f / k;
+    const bool first = (f % k) == 0;
+    for (int blk = lane; blk < nbh; blk += 32) {
+      uint8_t* dst = xp + (int64_t)(row0 + r) * H + blk * 32;
+      const uint8_t sc = quant_block(x + (int64_t)t * H + blk * 32, dst);
+      s_scale[warp][blk] = sc;
+      if (first) {
+        reinterpret_cast<uint4*>(xq + (int64_t)t * H + blk * 32)[0] = reinterpret_cast<const uint4*>(dst)[0];
+        reinterpret_cast<uint4*>(xq + (int64_t)t * H + blk * 32)[1] = reinterpret_cast<const uint4*>(dst)[1];
+        xs[(int64_t)t * nbh + blk] = sc;
+      }
+    }
+    __syncwarp();
+    for (int ka = lane; ka < kth; ka += 32) {
+      uint32_t wv = 0;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int kb = 4 * ka + j;
-        wv |= (uint32_t)(kb < nbh ? src[kb] : 127) << (8 * j);
+        wv |= (uint32_t)(kb < nbh ? s_scale[warp][kb] : 127) << (8 * j);
       }
+      *reinterpret_cast<uint32_t*>(xp_sf + ((int64_t)b * kth + ka) * kAtomBytes + (r & 31) * 16 + (r >> 5) * 4) = wv;
     }
-    *reinterpret_cast<uint32_t*>(xp_sf + ((int64_t)b * kth + ka) * kAtomBytes + (r & 31) * 16 + (r >> 5) * 4) = wv;
+    __syncwarp();
   }
-  // intermediate scale atoms start as code 127 everywhere; the gate_up epilogue
-  // overwrites the real ones
+  for (int i = threadIdx.x; i < kth * kTileM; i += blockDim.x) {
+    const int ka = i / kTileM, r = i - ka * kTileM;
+    if (r >= rows)
+      *reinterpret_cast<uint32_t*>(xp_sf + ((int64_t)b * kth + ka) * kAtomBytes + (r & 31) * 16 + (r >> 5) * 4) =
+          0x7F7F7F7Fu;
+  }
   uint4* hs = reinterpret_cast<uint4*>(hq_sf + (int64_t)b * kti * kAtomBytes);
   for (int i = threadIdx.x; i < kti * kAtomBytes / 16; i += blockDim.x)
     hs[i] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
@@ -138,11 +148,10 @@ cudaError_t launch_permute(const int32_t* ids, int TK, int k, int E, int tile_ro
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather(const uint8_t* xq, const uint8_t* xs, const int32_t* sorted_rows,
-                          const int32_t* tiles, int max_tiles, int k, int H, int I, int tile_rows,
-                          uint8_t* xp, uint8_t* xp_sf, uint8_t* hq_sf, cudaStream_t s) {
-  (void)tile_rows;
-  gather_kernel<<<max_tiles, 256, 0, s>>>(xq, xs, sorted_rows, tiles, k, H, I, xp, xp_sf, hq_sf);
+cudaError_t launch_gather_quant(const uint16_t* x, const int32_t* sorted_rows, const int32_t* tiles, int max_tiles,
+                                int k, int H, int I, uint8_t* xq, uint8_t* xs, uint8_t* xp, uint8_t* xp_sf,
+                                uint8_t* hq_sf, cudaStream_t s) {
+  gather_quant_kernel<<<max_tiles, 256, 0, s>>>(x, sorted_rows, tiles, k, H, I, xq, xs, xp, xp_sf, hq_sf);
   return cudaGetLastError();
 }
 

@@ -10,6 +10,8 @@
 
 #include <stdint.h>
 
+#include "ptx.cuh"
+
 namespace moe {
 
 // floor(log2(amax)) - 8, at least -127.  amax >= 0 (fp32 bit pattern ordering).
@@ -21,6 +23,43 @@ __device__ __forceinline__ int mx_scale_exp(float amax) {
 
 // 2^-s as an fp32 (exact for s in [-127, 126]).
 __device__ __forceinline__ float mx_pow2_neg(int s) { return __uint_as_float((uint32_t)(127 - s) << 23); }
+
+// Eight bf16 (one 16-byte load) to fp32.
+__device__ __forceinline__ void bf16x8(const uint4 v, float (&f)[8]) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(u[i] << 16);
+    f[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+  }
+}
+
+// Quantise one 32-element block of a bf16 row to MXFP8: 32 codes into dst, returns the scale code.
+__device__ __forceinline__ uint8_t quant_block(const uint16_t* src, uint8_t* dst) {
+  float f[32];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    float g[8];
+    bf16x8(reinterpret_cast<const uint4*>(src)[c], g);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[8 * c + i] = g[i];
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  const int s = mx_scale_exp(amax);
+  const float inv = mx_pow2_neg(s);
+  uint32_t pk[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t lo = cvt_e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv);
+    const uint32_t hi = cvt_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv);
+    pk[i] = lo | (hi << 16);
+  }
+  reinterpret_cast<uint4*>(dst)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  reinterpret_cast<uint4*>(dst)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  return (uint8_t)(s + 127);
+}
 
 // Exclusive prefix sums over E <= 256 counts by one warp (lane l owns entries
 // 8l..8l+7): off[e] = sum of cnt[<e], toff[e] = sum of ceil(cnt[<e] / 2^tshift);
