@@ -284,6 +284,69 @@ def _workload(layers: Layers, T: int, hot: int, hot_bias: float, steps: int, war
                 stage_ms=stage_avg, clocks=clocks.summary(), xs=xs, routers=routers, out=out, ws=ws)
 
 
+def _stack(layers: Layers, n_layers: int, T: int, steps: int, warmup: int, device, dist, graph: bool):
+    """x <- x + moe(rmsnorm(x)) over n_layers independently seeded layers (all resident)."""
+    moe = layers.moe
+    while len(layers.packed) < n_layers:
+        w = ms.make_expert_weights(0, H, I, E, layer=len(layers.packed), device=device)
+        layers.packed.append(moe.pack_weights(layers.dims, *w))
+        torch.cuda.synchronize()
+        del w
+    routers = [tuple(t.to(device) for t in ms.make_router(0, H, E, layer=l)) for l in range(n_layers)]
+    x0 = ms.make_tokens(0, T, H).to(device).float()
+    x_res = torch.empty_like(x0)
+    hidden = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+    ws = moe.alloc_workspace(layers.dims, T, K_TOP, device)
+    lay = moe.workspace_layout(layers.dims, T, K_TOP)
+
+    def step(count=None):
+        x_res.copy_(x0)
+        prev = None
+        for l in range(n_layers):
+            moe.residual_rmsnorm(x_res, prev, hidden)
+            moe.forward(layers.dims, hidden, routers[l][0], routers[l][1], layers.packed[l], K_TOP, out=out,
+                        workspace=ws)
+            if count is not None:
+                count.append(int((moe.view(ws, lay.counts, (E,), torch.int32) > 0).sum().item()))
+            prev = out
+        moe.residual_rmsnorm(x_res, out, hidden)
+
+    act = []
+    step(act)  # also the active experts of every layer
+    st = moe.device_status(ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"stack: device status {moe.STATUS_NAMES.get(st, st)}")
+    g = None
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+    run = g.replay if g is not None else step
+    for _ in range(warmup):
+        run()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    _barrier(dist)
+    clocks = ClockSampler(torch.cuda.current_device())
+    with clocks:
+        e0.record(stream)
+        for _ in range(steps):
+            run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    _barrier(dist)
+    ms_step = _max_over_ranks(dist, e0.elapsed_time(e1) / steps, device)
+    step_bytes = sum(a * (GU_BYTES + D_BYTES) for a in act) + n_layers * (E * H * 2 + E * 2 + 2 * T * H * 2)
+    flop = n_layers * (T * K_TOP * FLOP_PER_ROW + 2 * T * E * H)
+    return {"T": T, "layers": n_layers, "tokens_per_s": T / (ms_step * 1e-3), "ms_per_step": ms_step,
+            "ms_per_layer": ms_step / n_layers, "active_experts_per_layer": sum(act) / len(act),
+            "algorithmic_bytes": step_bytes, "gbs": step_bytes / (ms_step * 1e-3) / 1e9,
+            "tflops": flop / (ms_step * 1e-3) / 1e12, "timing": "CUDA graph of the whole step" if graph else
+            "stream of C-ABI calls", "clocks": clocks.summary()}
+
+
 def _e2e(layers: Layers, w: dict, steps: int, warmup: int, device, dist):
     """Same workload through the C ABI with pinned host buffers: H2D of x and D2H of out each step."""
     moe = layers.moe
@@ -386,6 +449,15 @@ def run_ours(args):
                 "stage_ms": w["stage_ms"], "clocks": w["clocks"]}
             del w
 
+    if not args.no_extra and not args.no_stack:
+        n_l = 36
+        pre = _stack(layers, n_l, 8192, 2, 1, device, dist, graph=False)
+        pre["tflops_frac_of_fp8_peak"] = pre["tflops"] / fp8_peak
+        extra["stack36_prefill_t8192"] = pre
+        dec = _stack(layers, n_l, 4, max(5, args.steps // 5), 2, device, dist, graph=True)
+        dec["hbm_frac"] = dec["gbs"] / hbm_peak
+        extra["stack36_decode_t4"] = dec
+
     cpu_v, cpu_n, cpu_s = (None, 0, 0.0)
     if rank == 0 and not args.no_cpu:
         cpu_v, cpu_n, cpu_s = _oracle_tokens_per_s(64, args.cpu_budget)
@@ -440,6 +512,7 @@ def main():
     ap.add_argument("--layers", type=int, default=8, help="independently seeded layers rotated per step")
     ap.add_argument("--no-extra", action="store_true", help="only the headline decode workload")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-stack", action="store_true", help="skip the 36-layer stack workloads")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of CPU oracle work")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -181,6 +181,16 @@ moe_status moe_forward_static_scratch(moe_dims d, const void *hidden, int32_t T,
 moe_status moe_get_device_status(const void *workspace, void *stream);
 
 /*
+ * Residual stream of a stack of MoE layers, x <- x + moe(rmsnorm(x)) (the
+ * stacked-layer workload; RMSNorm with unit gain): if layer_out (bf16 [T, H],
+ * the previous layer's moe_forward output) is not NULL, x_res (fp32 [T, H]) +=
+ * layer_out; then hidden (bf16 [T, H]) = bf16(x_res / sqrt(mean(x_res^2) + eps))
+ * per token, ready to be the next layer's input.  H a multiple of 4.
+ */
+moe_status moe_residual_rmsnorm(float *x_res, const void *layer_out, int32_t T, int32_t H, float eps,
+                                void *hidden, void *stream);
+
+/*
  * Optional per-stage timing of moe_forward with CUDA events (host-side event
  * objects only; no device memory).  moe_profile_begin(n) arms event recording
  * for the next n forward calls (three events each: start, expert-kernel start,

@@ -26,7 +26,7 @@ STATUS_NAMES = {
 # Every symbol the C ABI exports (include/moe.h).
 EXPORTED = ["moe_packed_size", "moe_pack_weights", "moe_workspace_size", "moe_workspace_layout_get",
             "moe_forward", "moe_forward_static_scratch", "moe_get_device_status", "moe_profile_begin",
-            "moe_profile_end",
+            "moe_profile_end", "moe_residual_rmsnorm",
             "moe_last_error", "moe_version"]
 STAGES = ["routing", "expert_mlp"]
 
@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
         L.moe_forward_static_scratch.argtypes = [Dims, vp, i32, vp, vp, vp, i32, vp, vp]
         L.moe_get_device_status.restype = st
         L.moe_get_device_status.argtypes = [vp, vp]
+        L.moe_residual_rmsnorm.restype = st
+        L.moe_residual_rmsnorm.argtypes = [vp, vp, i32, i32, ctypes.c_float, vp, vp]
         L.moe_profile_begin.restype = st
         L.moe_profile_begin.argtypes = [i32]
         L.moe_profile_end.restype = st
@@ -199,6 +201,16 @@ def forward_static_scratch(dims: LayerDims, hidden: torch.Tensor, router_w: torc
                                             _dev_ptr(packed, "packed"), top_k,
                                             _dev_ptr(out, "out", torch.bfloat16), _stream(stream)))
     return out
+
+
+def residual_rmsnorm(x_res: torch.Tensor, layer_out: torch.Tensor | None, hidden: torch.Tensor,
+                     eps: float = 1e-5, stream=None):
+    """x_res (fp32 [T, H]) += layer_out (bf16, optional); hidden (bf16) = rmsnorm(x_res)."""
+    T, H = x_res.shape
+    _check(lib().moe_residual_rmsnorm(_dev_ptr(x_res, "x_res", torch.float32),
+                                      None if layer_out is None else _dev_ptr(layer_out, "layer_out", torch.bfloat16),
+                                      T, H, eps, _dev_ptr(hidden, "hidden", torch.bfloat16), _stream(stream)))
+    return hidden
 
 
 def profile_begin(max_calls: int):

@@ -222,6 +222,19 @@ moe_status moe_forward(moe_dims d, const void* hidden, int32_t T, const void* ro
   return MOE_OK;
 }
 
+moe_status moe_residual_rmsnorm(float* x_res, const void* layer_out, int32_t T, int32_t H, float eps, void* hidden,
+                                void* stream) {
+  if (T < 0 || H <= 0 || H % 4 || !(eps > 0.f)) return fail(MOE_ERR_INVALID_ARG, "bad residual/rmsnorm arguments");
+  if (T == 0) return MOE_OK;
+  if (!x_res || !hidden) return fail(MOE_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(x_res, 16) || !aligned(hidden, 8) || (layer_out && !aligned(layer_out, 8)))
+    return fail(MOE_ERR_ALIGNMENT, "x_res must be 16-byte and hidden/layer_out 8-byte aligned");
+  cudaError_t e = moe::launch_residual_rmsnorm(x_res, static_cast<const uint16_t*>(layer_out), T, H, eps,
+                                               static_cast<uint16_t*>(hidden), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "residual/rmsnorm kernel");
+  return MOE_OK;
+}
+
 moe_status moe_profile_begin(int32_t max_calls) {
   if (max_calls <= 0) return fail(MOE_ERR_INVALID_ARG, "max_calls=%d", max_calls);
   const size_t need = (size_t)max_calls * (kStages + 1);

@@ -165,6 +165,9 @@ cudaError_t launch_gather_quant(const uint16_t* x, const int32_t* sorted_rows, c
                                 int k, int H, int I, uint8_t* xq, uint8_t* xs, uint8_t* xp, uint8_t* xp_sf,
                                 uint8_t* hq_sf, cudaStream_t s);
 
+cudaError_t launch_residual_rmsnorm(float* x_res, const uint16_t* layer_out, int T, int H, float eps,
+                                    uint16_t* hidden, cudaStream_t s);
+
 struct RouteSmallOut {
   float* logits;
   int32_t* ids;

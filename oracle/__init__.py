@@ -219,6 +219,13 @@ def moe_forward(x, router_w, router_b, gu_blocks, gu_scales, gu_bias, d_blocks, 
     return r
 
 
+def bf16_round_array(v) -> np.ndarray:
+    """fp64 array -> bf16 bit patterns (one RNE rounding per element)."""
+    a = _np(v, np.float64)
+    L = lib()
+    return np.array([L.oracle_bf16_round(float(x)) for x in a.reshape(-1)], np.uint16).reshape(a.shape)
+
+
 def rmsnorm_bf16(x, eps: float = 1e-5) -> np.ndarray:
     """fp64 [T,H] -> bf16 bits uint16 [T,H]."""
     a = _np(x, np.float64)

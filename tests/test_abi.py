@@ -122,3 +122,11 @@ def test_forward_fails_loudly_without_a_gpu(L):
     # error instead of computing anything on the CPU
     assert _fwd(L) == 6
     assert b"status reset" in L.moe_last_error()
+
+
+def test_residual_rmsnorm_rejects_bad_arguments_on_host(L):
+    assert L.moe_residual_rmsnorm(FAKE, None, 4, 2882, 1e-5, FAKE, None) == 1    # H % 4
+    assert L.moe_residual_rmsnorm(FAKE, None, 4, 2880, 0.0, FAKE, None) == 1     # eps must be > 0
+    assert L.moe_residual_rmsnorm(0, None, 4, 2880, 1e-5, FAKE, None) == 1       # null residual
+    assert L.moe_residual_rmsnorm(FAKE + 8, None, 4, 2880, 1e-5, FAKE, None) == 3
+    assert L.moe_residual_rmsnorm(FAKE, None, 0, 2880, 1e-5, FAKE, None) == 0    # T = 0: no-op
