@@ -503,6 +503,30 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_case(T: int, calls: int):
+    """A small profiling target: one layer (about 2.3 GB of packed weights on the
+    device), ``calls`` forward calls on the default stream, then the device status."""
+    import torch
+    import moe_synth as ms
+    import mxfp4_mixture_experts_gemv_gb300 as moe
+    H = I = 2880
+    E, k = 128, 4
+    dims = moe.LayerDims(E, H, I)
+    w = ms.make_expert_weights(0, H, I, E, device="cuda")
+    packed = moe.pack_weights(dims, *w)
+    del w
+    rw, rb = [t.cuda() for t in ms.make_router(0, H, E, hot_experts=16 if T == 32 else 0, hot_bias=1.0)]
+    x = ms.make_tokens(0, T, H).cuda()
+    ws = moe.alloc_workspace(dims, T, k)
+    for _ in range(calls):
+        moe.forward(dims, x, rw, rb, packed, k, workspace=ws)
+    torch.cuda.synchronize()
+    st = moe.device_status(ws)
+    print(f"case T={T}: {calls} calls, device status {st}", flush=True)
+    if st != 0:
+        raise SystemExit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -514,10 +538,15 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-stack", action="store_true", help="skip the 36-layer stack workloads")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of CPU oracle work")
+    ap.add_argument("--case", type=int, default=None, metavar="T",
+                    help="profiling run: one gpt-oss-shaped layer at T tokens, warmup + steps plain "
+                         "forward calls, no timing and no JSON line (T=32 uses the skewed router)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.case is not None:
+        run_case(args.case, args.warmup + args.steps)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

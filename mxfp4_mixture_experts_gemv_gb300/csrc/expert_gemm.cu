@@ -443,9 +443,14 @@ __global__ void __launch_bounds__(192, 1)
           if (ok && n < rows) {
             *reinterpret_cast<uint4*>(p.hq + (int64_t)(td.y + n) * p.I + r.m * 64 + 32 * rb + 16 * hh) =
                 make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            if (hh == 0)
-              p.hq_sf[((int64_t)r.b * p.d_ktiles + (kb >> 2)) * kAtomBytes + (n & 31) * 16 + (n >> 5) * 4 + (kb & 3)] =
-                  (uint8_t)(sx + 127);
+            if (hh == 0) {
+              uint8_t* wd = p.hq_sf + ((int64_t)r.b * p.d_ktiles + (kb >> 2)) * kAtomBytes + (n & 31) * 16 + (n >> 5) * 4;
+              wd[kb & 3] = (uint8_t)(sx + 127);
+              // the last real block also sets the padding blocks of its word (zero
+              // data past I; their scale must not be the NaN code)
+              if (kb == (p.I >> 5) - 1)
+                for (int j = (kb & 3) + 1; j < 4; ++j) wd[j] = 127;
+            }
           }
           named_barrier_sync(1, 128);
         }

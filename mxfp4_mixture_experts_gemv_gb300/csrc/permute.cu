@@ -83,10 +83,9 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(
 
 // One CTA per tile: quantise the tile's token rows to MXFP8 straight into grouped
 // order (x -> Xp rows and their scale atoms); the row of a token's first slot also
-// publishes the token's codes (xq, xs).  Padding words of the tile's atoms are
-// code 127; the intermediate's atoms start as all-127 (the gate_up epilogue
-// writes the real ones).
-__global__ void __launch_bounds__(256) gather_quant_kernel(const uint16_t* __restrict__ x,
+// publishes the token's codes (xq, xs).  Atom words of rows past the tile's rows
+// are left as they are: they only feed accumulator columns that are discarded.
+__global__ void __launch_bounds__(512) gather_quant_kernel(const uint16_t* __restrict__ x,
                                                            const int32_t* __restrict__ sorted_rows,
                                                            const int32_t* __restrict__ tiles, int k, int H, int I,
                                                            uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
@@ -99,9 +98,11 @@ __global__ void __launch_bounds__(256) gather_quant_kernel(const uint16_t* __res
   const int row0 = td.y, rows = td.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nbh = H / 32;
-  const int kth = (H + kTileK - 1) / kTileK, kti = (I + kTileK - 1) / kTileK;
-  __shared__ uint8_t s_scale[8][kRouteSmallMaxH / 32];
-  for (int r = warp; r < rows; r += 8) {
+  const int kth = (H + kTileK - 1) / kTileK;
+  (void)I;
+  (void)hq_sf;
+  __shared__ uint8_t s_scale[16][kRouteSmallMaxH / 32];
+  for (int r = warp; r < rows; r += 16) {
     const int f = sorted_rows[row0 + r], t = f / k;
     const bool first = (f % k) == 0;
     for (int blk = lane; blk < nbh; blk += 32) {
@@ -126,15 +127,6 @@ __global__ void __launch_bounds__(256) gather_quant_kernel(const uint16_t* __res
     }
     __syncwarp();
   }
-  for (int i = threadIdx.x; i < kth * kTileM; i += blockDim.x) {
-    const int ka = i / kTileM, r = i - ka * kTileM;
-    if (r >= rows)
-      *reinterpret_cast<uint32_t*>(xp_sf + ((int64_t)b * kth + ka) * kAtomBytes + (r & 31) * 16 + (r >> 5) * 4) =
-          0x7F7F7F7Fu;
-  }
-  uint4* hs = reinterpret_cast<uint4*>(hq_sf + (int64_t)b * kti * kAtomBytes);
-  for (int i = threadIdx.x; i < kti * kAtomBytes / 16; i += blockDim.x)
-    hs[i] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
 }
 
 }  // namespace
@@ -151,7 +143,7 @@ cudaError_t launch_permute(const int32_t* ids, int TK, int k, int E, int tile_ro
 cudaError_t launch_gather_quant(const uint16_t* x, const int32_t* sorted_rows, const int32_t* tiles, int max_tiles,
                                 int k, int H, int I, uint8_t* xq, uint8_t* xs, uint8_t* xp, uint8_t* xp_sf,
                                 uint8_t* hq_sf, cudaStream_t s) {
-  gather_quant_kernel<<<max_tiles, 256, 0, s>>>(x, sorted_rows, tiles, k, H, I, xq, xs, xp, xp_sf, hq_sf);
+  gather_quant_kernel<<<max_tiles, 512, 0, s>>>(x, sorted_rows, tiles, k, H, I, xq, xs, xp, xp_sf, hq_sf);
   return cudaGetLastError();
 }
 

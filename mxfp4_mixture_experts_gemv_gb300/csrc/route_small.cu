@@ -258,24 +258,6 @@ __global__ void __launch_bounds__(kThreads) route_small_kernel(const RouteSmallA
     }
     __syncthreads();
   }
-  // padding words of the tiles' atoms: rows past the tile's rows (both operands),
-  // and every word of the intermediate's atoms (the gate_up epilogue later
-  // overwrites the real bytes)
-  for (int b = blockIdx.x; b < n_tiles; b += gridDim.x) {
-    const int e = s_tile_e[b];
-    const int rows = min(a.tile_rows, s_cnt[e] - (b - s_toff[e]) * a.tile_rows);
-    for (int i = tid; i < kth * kTileM; i += kThreads) {
-      const int ka = i / kTileM, r = i % kTileM;
-      if (r >= rows)
-        *reinterpret_cast<uint32_t*>(a.xp_sf + ((int64_t)b * kth + ka) * kAtomBytes + (r & 31) * 16 + (r >> 5) * 4) =
-            0x7F7F7F7Fu;
-    }
-    for (int i = tid; i < kti * kTileM; i += kThreads) {
-      const int ka = i / kTileM, r = i % kTileM;
-      *reinterpret_cast<uint32_t*>(a.hq_sf + ((int64_t)b * kti + ka) * kAtomBytes + (r & 31) * 16 + (r >> 5) * 4) =
-          0x7F7F7F7Fu;
-    }
-  }
 }
 
 }  // namespace

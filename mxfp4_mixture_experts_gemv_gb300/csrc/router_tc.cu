@@ -23,7 +23,7 @@ namespace {
 
 constexpr int kRTileM = 128;   // tokens per tile (MMA M)
 constexpr int kRK = 64;        // bf16 elements per k-slice (one 128-byte swizzled row)
-constexpr int kRStages = 4;
+constexpr int kRStages = 6;
 
 struct RouterArgs {
   const uint16_t* br;
@@ -150,6 +150,8 @@ __global__ void __launch_bounds__(192, 1)
     const bool ok = mbar_wait_warp(done, 0, kWaitLimitNs);
     if (!ok && lane == 0) atomicOr(a.status, kStatusTimeoutEpilogue);
     tc_fence_after();
+    // running top-8 in registers, sorted by (logit desc, index asc): experts arrive
+    // in ascending order and only a strictly larger logit moves ahead
     float best_v[8];
     int best_i[8];
 #pragma unroll
@@ -167,21 +169,24 @@ __global__ void __launch_bounds__(192, 1)
       if (ok && t < a.T) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const int e = c0 + j;
-          if (e < a.E) {
-            float v = __uint_as_float(r[j]) + __uint_as_float((uint32_t)a.br[e] << 16);
-            a.logits[(int64_t)t * a.E + e] = v;
+          const int e0 = c0 + j;
+          if (e0 < a.E) {
+            float v = __uint_as_float(r[j]) + __uint_as_float((uint32_t)a.br[e0] << 16);
+            a.logits[(int64_t)t * a.E + e0] = v;
             if (isnan(v)) v = -INFINITY;  // a NaN logit ranks last
-            // experts arrive in ascending order, so a tie keeps the earlier (lower) index first
-            if (v > best_v[a.k - 1] || best_i[a.k - 1] == 0x7FFFFFFF) {
-              int pos = a.k - 1;
-              while (pos > 0 && (v > best_v[pos - 1] || best_i[pos - 1] == 0x7FFFFFFF)) {
-                best_v[pos] = best_v[pos - 1];
-                best_i[pos] = best_i[pos - 1];
-                --pos;
+            int e = e0;
+            const bool any = v > best_v[7] || best_i[7] == 0x7FFFFFFF;
+            if (any) {
+#pragma unroll
+              for (int s2 = 0; s2 < 8; ++s2) {
+                const bool take = v > best_v[s2] || best_i[s2] == 0x7FFFFFFF;
+                const float tv = best_v[s2];
+                const int ti = best_i[s2];
+                best_v[s2] = take ? v : tv;
+                best_i[s2] = take ? e : ti;
+                v = take ? tv : v;
+                e = take ? ti : e;
               }
-              best_v[pos] = v;
-              best_i[pos] = e;
             }
           }
         }
@@ -189,10 +194,15 @@ __global__ void __launch_bounds__(192, 1)
     }
     if (ok && t < a.T) {
       float den = 0.f;
-      for (int j = 0; j < a.k; ++j) den += expf(best_v[j] - best_v[0]);
-      for (int j = 0; j < a.k; ++j) {
-        a.ids[(int64_t)t * a.k + j] = best_i[j];
-        a.w[(int64_t)t * a.k + j] = expf(best_v[j] - best_v[0]) / den;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < a.k) den += expf(best_v[j] - best_v[0]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j < a.k) {
+          a.ids[(int64_t)t * a.k + j] = best_i[j];
+          a.w[(int64_t)t * a.k + j] = expf(best_v[j] - best_v[0]) / den;
+        }
       }
     }
   }
