@@ -234,27 +234,29 @@ def _workload(layers: Layers, T: int, hot: int, hot_bias: float, steps: int, war
     if st != moe.MOE_OK:
         raise RuntimeError(f"device status {moe.STATUS_NAMES.get(st, st)}: {moe.lib().moe_last_error().decode()}")
     # One CUDA graph per timed step, captured from the C-ABI call (the way a decode
-    # loop runs it); each capture takes one profiling slot, so the per-stage events
-    # are recorded by the replays inside the timed region.
+    # loop runs it).
     for i in range(warmup):
         l = i % layers.n
         moe.forward(layers.dims, xs[l], routers[l][0], routers[l][1], layers.packed[l], K_TOP, out=out, workspace=ws)
     torch.cuda.synchronize()
-    graphs = []
-    if profile:
-        moe.profile_begin(steps)
-    for i in range(steps):
-        l = i % layers.n
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            moe.forward(layers.dims, xs[l], routers[l][0], routers[l][1], layers.packed[l], K_TOP, out=out,
-                        workspace=ws)
-        graphs.append(g)
-    for i in range(min(warmup, steps)):
-        graphs[i].replay()
+
+    def capture():
+        graphs = []
+        for i in range(steps):
+            l = i % layers.n
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                moe.forward(layers.dims, xs[l], routers[l][0], routers[l][1], layers.packed[l], K_TOP, out=out,
+                            workspace=ws)
+            graphs.append(g)
+        for i in range(min(warmup, steps)):
+            graphs[i].replay()
+        torch.cuda.synchronize()
+        return graphs
+
+    graphs = capture()
     stream = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
     _barrier(dist)
     clocks = ClockSampler(torch.cuda.current_device())
     with clocks:
@@ -265,7 +267,19 @@ def _workload(layers: Layers, T: int, hot: int, hot_bias: float, steps: int, war
         torch.cuda.synchronize()
     _barrier(dist)
     ms_total = e0.elapsed_time(e1)
-    stage_ms, calls = moe.profile_end() if profile else ({}, 0)
+    del graphs
+    # The per-stage split comes from a second set of graphs whose captures each
+    # take one profiling slot (the stage events become graph nodes, so these
+    # replays are not the timed ones).
+    stage_ms, calls = {}, 0
+    if profile:
+        moe.profile_begin(steps)
+        graphs = capture()
+        for g in graphs:
+            g.replay()
+        torch.cuda.synchronize()
+        stage_ms, calls = moe.profile_end()
+        del graphs
     st = moe.device_status(ws)
     if st != moe.MOE_OK:
         raise RuntimeError(f"device status {moe.STATUS_NAMES.get(st, st)}")
@@ -277,7 +291,6 @@ def _workload(layers: Layers, T: int, hot: int, hot_bias: float, steps: int, war
     step_bytes = gu_bytes + d_bytes + E * H * 2 + E * 2 + 2 * T * H * 2
     flop = T * K_TOP * FLOP_PER_ROW + 2 * T * E * H
     stage_avg = {k: v / max(calls, 1) for k, v in stage_ms.items()}
-    del graphs
     return dict(T=T, ms_per_step=ms_step, tokens_per_s=T / (ms_step * 1e-3), active_experts=n_act,
                 step_bytes=step_bytes, gu_bytes=gu_bytes, d_bytes=d_bytes, flop=flop,
                 gbs=step_bytes / (ms_step * 1e-3) / 1e9, tflops=flop / (ms_step * 1e-3) / 1e12,

@@ -158,15 +158,42 @@ moe_status moe_forward(moe_dims d, const void* hidden, int32_t T, const void* ro
   int32_t* sorted_rows = reinterpret_cast<int32_t*>(at(L.sorted_rows));
   const int sms = num_sms();
 
-  cudaError_t e = cudaMemsetAsync(ws, 0, L.zero_bytes, s);
-  if (e != cudaSuccess) return cuda_fail(e, "status reset");
+  // The cluster routing kernel clears the status words and counters itself; the
+  // other paths start from a memset.
+  const bool cluster_route = moe::route_cluster_fits(T, d.E, d.H);
+  cudaError_t e = cudaSuccess;
+  if (!cluster_route) {
+    e = cudaMemsetAsync(ws, 0, L.zero_bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "status reset");
+  }
   cudaEvent_t* pev = profile_slot();
   auto mark = [&](int i) {
     // external record: inside a stream capture this becomes a timestamping graph node
     if (pev) cudaEventRecordWithFlags(pev[i], s, cudaEventRecordExternal);
   };
   mark(0);
-  if (moe::route_small_fits(T, d.H)) {
+  if (cluster_route) {
+    // a few tokens: routing, grouping and quantise-on-gather in one cluster
+    moe::RouteClusterOut o;
+    o.logits = reinterpret_cast<float*>(at(L.logits));
+    o.ids = ids;
+    o.w = w;
+    o.xq = at(L.xq);
+    o.xs = at(L.xs);
+    o.counts = reinterpret_cast<int32_t*>(at(L.counts));
+    o.offsets = reinterpret_cast<int32_t*>(at(L.offsets));
+    o.sorted_rows = sorted_rows;
+    o.inv_pos = inv_pos;
+    o.tiles = tiles;
+    o.xp = at(L.xp);
+    o.xp_sf = at(L.xp_sf);
+    o.zero = reinterpret_cast<uint32_t*>(ws);
+    o.zero_words = (int)(L.zero_bytes / 4);
+    o.status = status;
+    e = moe::launch_route_cluster(static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(router_w),
+                                  static_cast<const uint16_t*>(router_b), T, d.H, d.E, top_k, L.tile_rows, o, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cluster routing kernel");
+  } else if (moe::route_small_fits(T, d.H)) {
     // decode: routing, quantisation, grouping and gather in one launch
     moe::RouteSmallOut o;
     o.logits = reinterpret_cast<float*>(at(L.logits));

@@ -87,6 +87,12 @@ inline bool route_small_fits(int T, int H) {
   return T <= kRouteSmallMaxT && H <= kRouteSmallMaxH && (size_t)(T + 1) * H * 2 <= kRouteSmallMaxSmem;
 }
 
+// Cluster routing (a few tokens): the router rows of a CTA's experts (E / 8 of
+// them on the smallest cluster) and the T token rows sit in shared memory.
+constexpr int kRouteClusterMaxT = 8;
+constexpr size_t kRouteClusterMaxSmem = 200 * 1024;
+bool route_cluster_fits(int T, int E, int H);
+
 // Token rows per tile of the grouped GEMM (MMA N upper bound): a token visits an
 // expert at most once, so up to 64 tokens one tile of the next size covers any
 // expert; beyond that 128 (measured: smaller tiles re-read the weights of
@@ -187,6 +193,26 @@ struct RouteSmallOut {
 };
 cudaError_t launch_route_small(const uint16_t* x, const uint16_t* wr, const uint16_t* br, int T, int H, int E, int I,
                                int k, int tile_rows, int max_tiles, const RouteSmallOut& o, cudaStream_t s);
+
+struct RouteClusterOut {
+  float* logits;
+  int32_t* ids;
+  float* w;
+  uint8_t* xq;
+  uint8_t* xs;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* sorted_rows;
+  int32_t* inv_pos;
+  int32_t* tiles;
+  uint8_t* xp;
+  uint8_t* xp_sf;
+  uint32_t* zero;  // the workspace's zero-initialised words, cleared by the kernel
+  int zero_words;
+  uint32_t* status;
+};
+cudaError_t launch_route_cluster(const uint16_t* x, const uint16_t* wr, const uint16_t* br, int T, int H, int E,
+                                 int k, int tile_rows, const RouteClusterOut& o, cudaStream_t s);
 
 struct ExpertMlpBuffers {
   const uint8_t* xp;        // gate_up B rows [TK][H]

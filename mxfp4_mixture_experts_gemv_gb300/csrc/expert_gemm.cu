@@ -108,7 +108,8 @@ __device__ __forceinline__ TileRef tile_ref(int tile, int n_gu, const MlpParams&
 }
 
 // Where a bounded wait expired: role (1 producer/empty, 2 mma/accumulator, 3 mma/full,
-// 4 epilogue, 5 producer/dependency), tile and k-step, packed for the second status word.
+// 4 epilogue, 5 producer/dependency; 6 is the cluster routing kernel's copies), tile and
+// k-step, packed for the second status word.
 __device__ __forceinline__ uint32_t wait_site(uint32_t role, int tile, int kt) {
   return (role << 28) | ((uint32_t)min(tile, 0xFFFF) << 12) | (uint32_t)min(kt, 0xFFF);
 }

@@ -34,15 +34,16 @@ __device__ __forceinline__ void bf16x8(const uint4 v, float (&f)[8]) {
   }
 }
 
-// Quantise one 32-element block of a bf16 row to MXFP8: 32 codes into dst, returns the scale code.
-__device__ __forceinline__ uint8_t quant_block(const uint16_t* src, uint8_t* dst) {
+// Quantise one 32-element block of a bf16 row to MXFP8: the 32 codes in c, returns
+// the scale code.  src may point to global or shared memory (16-byte aligned).
+__device__ __forceinline__ uint8_t quant_block_regs(const uint16_t* src, uint4 (&c)[2]) {
   float f[32];
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
+  for (int q = 0; q < 4; ++q) {
     float g[8];
-    bf16x8(reinterpret_cast<const uint4*>(src)[c], g);
+    bf16x8(reinterpret_cast<const uint4*>(src)[q], g);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) f[8 * c + i] = g[i];
+    for (int i = 0; i < 8; ++i) f[8 * q + i] = g[i];
   }
   float amax = 0.f;
 #pragma unroll
@@ -56,9 +57,18 @@ __device__ __forceinline__ uint8_t quant_block(const uint16_t* src, uint8_t* dst
     const uint32_t hi = cvt_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv);
     pk[i] = lo | (hi << 16);
   }
-  reinterpret_cast<uint4*>(dst)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-  reinterpret_cast<uint4*>(dst)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  c[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  c[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
   return (uint8_t)(s + 127);
+}
+
+// The same, with the 32 codes stored to dst (16-byte aligned).
+__device__ __forceinline__ uint8_t quant_block(const uint16_t* src, uint8_t* dst) {
+  uint4 c[2];
+  const uint8_t sc = quant_block_regs(src, c);
+  reinterpret_cast<uint4*>(dst)[0] = c[0];
+  reinterpret_cast<uint4*>(dst)[1] = c[1];
+  return sc;
 }
 
 // Exclusive prefix sums over E <= 256 counts by one warp (lane l owns entries

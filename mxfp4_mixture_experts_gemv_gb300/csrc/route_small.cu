@@ -1,4 +1,4 @@
-// Routing for small token counts (decode) in one cooperative launch: router GEMV
+// Routing for small token counts (batched decode) in one cooperative launch: router GEMV
 // + bias, top-k + softmax, MXFP8 quantisation of x, the stable grouping by
 // expert with its tile list, and the gather of the quantised rows into grouped
 // order with their scale atoms.
@@ -11,13 +11,14 @@
 // which spares a second barrier; then each CTA quantises and places its share
 // of the grouped rows and writes its share of the tiles' scale atoms.
 //
-// Same arithmetic as router.cu / permute.cu: fp32 logits, top-k by (logit desc,
-// index asc), softmax over the selected, OCP-style MXFP8 (see quant.cuh).
+// Same arithmetic as the other routing kernels: fp32 logits, top-k by (logit
+// desc, index asc), softmax over the selected, OCP-style MXFP8 (quant.cuh).
 #include <algorithm>
 
 #include "common.cuh"
 #include "ptx.cuh"
 #include "quant.cuh"
+#include "routing.cuh"
 
 namespace moe {
 namespace {
@@ -47,7 +48,6 @@ struct RouteSmallArgs {
 };
 
 __global__ void __launch_bounds__(kThreads) route_small_kernel(const RouteSmallArgs a) {
-  __shared__ float s_part[kThreads / 32][kRouteSmallMaxT];
   __shared__ int s_ids[kRouteSmallMaxT * 8];
   __shared__ float s_w[kRouteSmallMaxT * 8];
   __shared__ int s_cnt[257], s_off[258], s_run[257], s_toff[258];
@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(kThreads) route_small_kernel(const RouteSmallA
   extern __shared__ uint4 s_dyn[];  // phase A: staged rows; phase B: logits [T][257]
   float* s_logit = reinterpret_cast<float*>(s_dyn);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int T = a.T, H = a.H, E = a.E, I = a.I, k = a.k;
+  const int T = a.T, H = a.H, E = a.E, k = a.k;
   // the expert kernel may start its prologue now; it waits for this grid's results
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int TK = T * k;
@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(kThreads) route_small_kernel(const RouteSmallA
     uint4* s_rows4 = s_dyn;  // [(T + 1) * H / 8]: row 0 = router row of e, rows 1.. = tokens
     const int e = blockIdx.x;
     const int hc = H / 8;
+    const float bias = __uint_as_float((uint32_t)a.br[e] << 16);
     {
       const uint4* wsrc = reinterpret_cast<const uint4*>(a.wr + (int64_t)e * H);
       const uint4* xsrc = reinterpret_cast<const uint4*>(a.x);
@@ -79,36 +80,34 @@ __global__ void __launch_bounds__(kThreads) route_small_kernel(const RouteSmallA
       asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
     }
     __syncthreads();
-    float part[kRouteSmallMaxT];
+    // warp w contracts the tokens t = w, w + 8, ...: no cross-warp reduction
+    constexpr int kTpw = kRouteSmallMaxT / (kThreads / 32);
+    float part[kTpw];
 #pragma unroll
-    for (int t = 0; t < kRouteSmallMaxT; ++t) part[t] = 0.f;
-    for (int c = tid; c < hc; c += kThreads) {
+    for (int m = 0; m < kTpw; ++m) part[m] = 0.f;
+    for (int c = lane; c < hc; c += 32) {
       float wv[8];
       bf16x8(s_rows4[c], wv);
 #pragma unroll
-      for (int t = 0; t < kRouteSmallMaxT; ++t) {
+      for (int m = 0; m < kTpw; ++m) {
+        const int t = warp + 8 * m;
         if (t < T) {
           float xv[8];
           bf16x8(s_rows4[(t + 1) * hc + c], xv);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) part[t] = fmaf(xv[i], wv[i], part[t]);
+          for (int i = 0; i < 8; ++i) part[m] = fmaf(xv[i], wv[i], part[m]);
         }
       }
     }
 #pragma unroll
-    for (int t = 0; t < kRouteSmallMaxT; ++t) {
+    for (int m = 0; m < kTpw; ++m) {
+      const int t = warp + 8 * m;
       if (t < T) {
-        float v = part[t];
+        float v = part[m];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) s_part[warp][t] = v;
+        if (lane == 0) a.logits[(int64_t)t * E + e] = v + bias;
       }
-    }
-    __syncthreads();
-    if (tid < T) {
-      float v = 0.f;
-      for (int wi = 0; wi < kThreads / 32; ++wi) v += s_part[wi][tid];
-      a.logits[(int64_t)tid * E + e] = v + __uint_as_float((uint32_t)a.br[e] << 16);
     }
   }
 
@@ -133,102 +132,32 @@ __global__ void __launch_bounds__(kThreads) route_small_kernel(const RouteSmallA
   __syncthreads();
 
   // ------------------------------------------------------------ phase B
-  for (int i = tid; i < T * E; i += kThreads) s_logit[(i / E) * 257 + i % E] = __ldcg(a.logits + i);
+  // every logit (8 independent loads in flight per thread and round)
+  for (int i0 = 0; i0 < T * E; i0 += 8 * kThreads) {
+    float v[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int i = i0 + r * kThreads + tid;
+      v[r] = i < T * E ? __ldcg(a.logits + i) : 0.f;
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int i = i0 + r * kThreads + tid;
+      if (i < T * E) s_logit[(i / E) * 257 + i % E] = v[r];
+    }
+  }
   for (int e = tid; e < E; e += kThreads) s_cnt[e] = 0;
   __syncthreads();
-  // top-k + softmax: warp per token
-  for (int t = warp; t < T; t += kThreads / 32) {
-    float v[8];
-    uint32_t taken = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      const float l = e < E ? s_logit[t * 257 + e] : -INFINITY;
-      v[i] = isnan(l) ? -INFINITY : l;
-    }
-    float l0 = 0.f, den = 0.f;
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int bi = 0x7FFFFFFF;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !(taken >> i & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-          bv = v[i];
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (j == 0) l0 = bv;
-      if (lane == 0) {
-        s_ids[t * k + j] = bi;
-        s_w[t * k + j] = bv;  // logit for now
-      }
-      den += expf(bv - l0);
-    }
-    __syncwarp();
-    if (lane < k) s_w[t * k + lane] = expf(s_w[t * k + lane] - l0) / den;
-  }
+  for (int t = warp; t < T; t += kThreads / 32) topk_softmax_warp(s_logit + t * 257, E, k, s_ids + t * k, s_w + t * k, lane);
   __syncthreads();
-  // grouping (stable counting sort of the T*k pairs by expert), warp 0
-  if (warp == 0) {
-    for (int f = lane; f < TK; f += 32) atomicAdd(&s_cnt[s_ids[f]], 1);
-    __syncwarp();
-    warp_expert_scan(s_cnt, E, __ffs(a.tile_rows) - 1, s_off, s_toff, s_tile_e, lane);
-    __syncwarp();
-    for (int e = lane; e < E; e += 32) s_run[e] = s_off[e];
-    __syncwarp();
-    const unsigned lt = (1u << lane) - 1u;
-    for (int base = 0; base < TK; base += 32) {
-      const int f = base + lane;
-      const int e = f < TK ? s_ids[f] : -1;
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
-      const int rank = __popc(peers & lt);
-      if (f < TK) {
-        const int pos = s_run[e] + rank;
-        s_sorted[pos] = f;
-        s_inv[f] = pos;
-      }
-      __syncwarp();
-      if (f < TK && rank == 0) s_run[e] += __popc(peers);
-      __syncwarp();
-    }
-  }
+  const int tshift = __ffs(a.tile_rows) - 1;
+  if (warp == 0) group_pairs_warp(s_ids, TK, E, tshift, s_cnt, s_off, s_toff, s_tile_e, s_run, s_sorted, s_inv, lane);
   __syncthreads();
-  const int n_tiles = s_toff[E];
-  // CTA 0 publishes the routing results
-  if (blockIdx.x == 0) {
-    for (int i = tid; i < TK; i += kThreads) {
-      a.ids[i] = s_ids[i];
-      a.w[i] = s_w[i];
-      a.sorted_rows[i] = s_sorted[i];
-      a.inv_pos[i] = s_inv[i];
-    }
-    for (int e = tid; e < E; e += kThreads) {
-      a.counts[e] = s_cnt[e];
-      a.offsets[e] = s_off[e];
-    }
-    for (int t = tid; t < n_tiles; t += kThreads) {
-      const int e = s_tile_e[t];
-      const int r0 = (t - s_toff[e]) * a.tile_rows;
-      reinterpret_cast<int4*>(a.tiles + 4)[t] = make_int4(e, s_off[e] + r0, min(a.tile_rows, s_cnt[e] - r0), 0);
-    }
-    if (tid == 0) {
-      a.offsets[E] = s_off[E];
-      a.tiles[0] = n_tiles;
-    }
-  }
+  if (blockIdx.x == 0)
+    publish_routing(s_ids, s_w, s_sorted, s_inv, s_cnt, s_off, s_toff, s_tile_e, TK, E, a.tile_rows, a.ids, a.w,
+                    a.sorted_rows, a.inv_pos, a.counts, a.offsets, a.tiles);
   // gather: grouped row p -> quantised x row of its token, plus its scale words
-  const int nbh = H / 32, kth = (H + kTileK - 1) / kTileK, kti = (I + kTileK - 1) / kTileK;
+  const int nbh = H / 32, kth = (H + kTileK - 1) / kTileK;
   for (int p = blockIdx.x; p < TK; p += gridDim.x) {
     const int f = s_sorted[p], t = f / k;
     // tile of p and its row inside the tile
@@ -237,12 +166,16 @@ __global__ void __launch_bounds__(kThreads) route_small_kernel(const RouteSmallA
     const int b = s_toff[e] + r_in_e / a.tile_rows;
     const int n = r_in_e % a.tile_rows;
     for (int blk = tid; blk < nbh; blk += kThreads) {
-      const uint8_t sc = quant_block(a.x + (int64_t)t * H + blk * 32, a.xp + (int64_t)p * H + blk * 32);
+      uint4 c[2];
+      const uint8_t sc = quant_block_regs(a.x + (int64_t)t * H + blk * 32, c);
+      uint4* dst = reinterpret_cast<uint4*>(a.xp + (int64_t)p * H + blk * 32);
+      dst[0] = c[0];
+      dst[1] = c[1];
       s_scale[blk] = sc;
       if (f % k == 0) {  // the token's first slot also publishes x's codes (stage output)
-        for (int i = 0; i < 32; i += 16)
-          *reinterpret_cast<uint4*>(a.xq + (int64_t)t * H + blk * 32 + i) =
-              *reinterpret_cast<const uint4*>(a.xp + (int64_t)p * H + blk * 32 + i);
+        uint4* q = reinterpret_cast<uint4*>(a.xq + (int64_t)t * H + blk * 32);
+        q[0] = c[0];
+        q[1] = c[1];
         a.xs[(int64_t)t * nbh + blk] = sc;
       }
     }

@@ -1,0 +1,141 @@
+// Warp-level steps shared by the small-batch routing kernels: the top-k +
+// softmax of one token's logits and the stable grouping of the T*k (token,
+// slot) pairs by expert, with the tile list the expert kernel walks.
+//
+// Routing rule: top-k experts by logit (descending, lower index first on ties),
+// then softmax over the k selected ("GPT-OSS-120B on DGX Spark: From MXFP4 to
+// NVFP4", section "GPT-OSS-120B Architecture": 128 experts, 4 active per token).
+#pragma once
+
+#include <stdint.h>
+
+#include "common.cuh"
+#include "quant.cuh"
+
+namespace moe {
+
+// Order-preserving map of a non-NaN fp32 onto uint32 (a larger float gives a larger
+// key; -0 and +0 must be merged by the caller).  Key 0 is never produced.
+__device__ __forceinline__ uint32_t f32_order_key(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float f32_from_order_key(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// One warp selects the k <= 8 largest of E <= 256 logits (a NaN ranks as -inf,
+// ties go to the lower expert index) and writes their ids and their softmax
+// weights, exp(l_j - l_0) / sum_i exp(l_i - l_0) with l_0 the largest.
+__device__ __forceinline__ void topk_softmax_warp(const float* logit, int E, int k, int32_t* ids, float* w,
+                                                  int lane) {
+  uint32_t key[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    float v = e < E ? logit[e] : 0.f;
+    if (isnan(v)) v = -INFINITY;
+    if (v == 0.f) v = 0.f;  // -0 ranks equal to +0
+    key[i] = e < E ? f32_order_key(v) : 0u;
+  }
+  float l0 = 0.f, den = 0.f, mine = 0.f;
+  int mine_id = 0;
+  for (int j = 0; j < k; ++j) {
+    uint32_t bk = 0u;
+    int bi = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (key[i] > bk) {  // strict: the lower index of this lane wins a tie
+        bk = key[i];
+        bi = i;
+      }
+    const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+    const int e = __reduce_min_sync(0xffffffffu, bk == mk ? lane + 32 * bi : 0x7FFFFFFF);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if ((e & 31) == lane && (e >> 5) == i) key[i] = 0u;
+    const float lv = f32_from_order_key(mk);
+    if (j == 0) l0 = lv;
+    den += expf(lv - l0);
+    if (lane == j) {
+      mine = lv;
+      mine_id = e;
+    }
+  }
+  if (lane < k) {
+    ids[lane] = mine_id;
+    w[lane] = expf(mine - l0) / den;
+  }
+}
+
+// Warp 0: stable counting sort of the TK pairs f = t*k + j by expert ids[f].
+// cnt must be zero on entry.  Produces the counts, the offsets off[0..E], the
+// tile offsets toff[0..E] (tiles of 2^tshift rows), the expert of every tile,
+// sorted[p] = pair at grouped row p and its inverse inv[f].
+__device__ __forceinline__ void group_pairs_warp(const int32_t* ids, int TK, int E, int tshift, int* cnt, int* off,
+                                                 int* toff, int* tile_e, int* run, int* sorted, int* inv, int lane) {
+  for (int f = lane; f < TK; f += 32) atomicAdd(&cnt[ids[f]], 1);
+  __syncwarp();
+  warp_expert_scan(cnt, E, tshift, off, toff, tile_e, lane);
+  __syncwarp();
+  for (int e = lane; e < E; e += 32) run[e] = off[e];
+  __syncwarp();
+  const unsigned lt = (1u << lane) - 1u;
+  for (int base = 0; base < TK; base += 32) {
+    const int f = base + lane;
+    const int e = f < TK ? ids[f] : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lt);
+    if (f < TK) {
+      const int pos = run[e] + rank;
+      sorted[pos] = f;
+      inv[f] = pos;
+    }
+    __syncwarp();
+    if (f < TK && rank == 0) run[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+// Block: write the routing results held in shared memory to global memory.
+__device__ __forceinline__ void publish_routing(const int* s_ids, const float* s_w, const int* s_sorted,
+                                                const int* s_inv, const int* s_cnt, const int* s_off,
+                                                const int* s_toff, const int* s_tile_e, int TK, int E,
+                                                int tile_rows, int32_t* ids, float* w, int32_t* sorted_rows,
+                                                int32_t* inv_pos, int32_t* counts, int32_t* offsets,
+                                                int32_t* tiles) {
+  const int n_tiles = s_toff[E];
+  for (int i = threadIdx.x; i < TK; i += blockDim.x) {
+    ids[i] = s_ids[i];
+    w[i] = s_w[i];
+    sorted_rows[i] = s_sorted[i];
+    inv_pos[i] = s_inv[i];
+  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    counts[e] = s_cnt[e];
+    offsets[e] = s_off[e];
+  }
+  for (int t = threadIdx.x; t < n_tiles; t += blockDim.x) {
+    const int e = s_tile_e[t];
+    const int r0 = (t - s_toff[e]) * tile_rows;
+    reinterpret_cast<int4*>(tiles + 4)[t] = make_int4(e, s_off[e] + r0, min(tile_rows, s_cnt[e] - r0), 0);
+  }
+  if (threadIdx.x == 0) {
+    offsets[E] = s_off[E];
+    tiles[0] = n_tiles;
+  }
+}
+
+// Byte offset of grouped row p's 32-bit scale word for atom column ka, in the
+// scale atoms of the tile list (tiles of 2^tshift rows, kt atoms per tile).
+__device__ __forceinline__ int64_t row_sf_word(int p, int ka, int kt, const int* s_ids, const int* s_sorted,
+                                               const int* s_off, const int* s_toff, int tshift) {
+  const int e = s_ids[s_sorted[p]];
+  const int r_in_e = p - s_off[e];
+  const int b = s_toff[e] + (r_in_e >> tshift);
+  const int n = r_in_e & ((1 << tshift) - 1);
+  return ((int64_t)b * kt + ka) * kAtomBytes + (n & 31) * 16 + (n >> 5) * 4;
+}
+
+}  // namespace moe

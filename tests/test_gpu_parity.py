@@ -20,6 +20,11 @@ SMALL_CASES = {
     "many_tiles_T300": (ms.LayerShape(T=300, H=256, I=128, E=8, k=2), 5),
     "tails_H288_I192": (ms.LayerShape(T=50, H=288, I=192, E=6, k=3), 6),
     "k8_E16": (ms.LayerShape(T=20, H=128, I=64, E=16, k=8), 7),
+    # a few tokens (cluster routing): experts not a multiple of the cluster, k = 8, E = 200
+    "cluster_E6_tails": (ms.LayerShape(T=5, H=288, I=192, E=6, k=3), 10),
+    "cluster_k8_E200": (ms.LayerShape(T=3, H=128, I=64, E=200, k=8), 11),
+    # batched decode (grid routing) with padded contraction tails
+    "grid_T12_tails": (ms.LayerShape(T=12, H=288, I=192, E=6, k=3), 12),
 }
 
 
@@ -112,8 +117,9 @@ def test_pack_is_a_bijection_with_deterministic_padding():
     np.testing.assert_array_equal(bias, inp.down_bias.float().numpy())
 
 
-def test_deterministic_and_independent_of_workspace_contents():
-    shape = ms.LayerShape(T=64, H=256, I=256, E=8, k=4)
+@pytest.mark.parametrize("T", [4, 20, 64], ids=["cluster_route", "grid_route", "tensor_core_route"])
+def test_deterministic_and_independent_of_workspace_contents(T):
+    shape = ms.LayerShape(T=T, H=256, I=256, E=8, k=4)
     inp = ms.make_layer(shape, seed=11).to("cuda")
     _, packed = mc.pack(inp)
     a = mc.run_gpu(inp, packed, poison=0x00)
@@ -121,7 +127,7 @@ def test_deterministic_and_independent_of_workspace_contents():
     c = mc.run_gpu(inp, packed, poison=0x7F)
     for r in (b, c):
         assert torch.equal(a.out.view(torch.int16), r.out.view(torch.int16))
-        for name, shp in [("topk_ids", (64 * 4,)), ("sorted_rows", (64 * 4,)), ("inv_pos", (64 * 4,))]:
+        for name, shp in [("topk_ids", (T * 4,)), ("sorted_rows", (T * 4,)), ("inv_pos", (T * 4,))]:
             assert torch.equal(a.section(name, shp, torch.int32), r.section(name, shp, torch.int32))
 
 
