@@ -85,7 +85,7 @@ typedef struct {
   size_t status;       /* uint32 [4]: device status words (0 = ok)                  */
   size_t done_gu;      /* int32 [max_tiles]: finished gate_up tiles per token tile  */
   size_t done_tok;     /* int32 [T, ceil(H/128)]: finished down slots per block     */
-  size_t grid_bar;     /* int32: arrival count of the small-batch routing kernel    */
+  size_t grid_bar;     /* int32[2]: grid routing arrivals, expert tiles claimed     */
   size_t zero_bytes;   /* bytes from offset 0 the forward zeroes before it starts   */
   size_t logits;       /* fp32 [T, E] router logits                                 */
   size_t topk_ids;     /* int32 [T, k]                                              */

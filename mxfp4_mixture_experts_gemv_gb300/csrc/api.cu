@@ -242,6 +242,7 @@ moe_status moe_forward(moe_dims d, const void* hidden, int32_t T, const void* ro
   b.topk_w = w;
   b.done_gu = reinterpret_cast<int32_t*>(at(L.done_gu));
   b.done_tok = reinterpret_cast<int32_t*>(at(L.done_tok));
+  b.sched = reinterpret_cast<int32_t*>(at(L.grid_bar)) + 1;  // word 0 is the grid routing barrier
   b.status = status;
   e = moe::launch_expert_mlp(h, pk, b, T, top_k, L.max_tiles, L.tile_rows, sms, s);
   if (e != cudaSuccess) return cuda_fail(e, "expert MLP kernel");

@@ -227,6 +227,7 @@ struct ExpertMlpBuffers {
   const float* topk_w;
   int32_t* done_gu;
   int32_t* done_tok;
+  int32_t* sched;  // tile claim counter, zero at launch
   uint32_t* status;
 };
 cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, const ExpertMlpBuffers& b, int T, int k,

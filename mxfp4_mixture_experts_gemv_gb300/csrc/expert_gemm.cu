@@ -48,6 +48,10 @@ namespace {
 // commit.  Fewer, larger copies per byte keep the single issuing lanes ahead of HBM.
 constexpr int kKS = 2;
 
+// Tiles are claimed from a global counter by the producer warp and handed to the
+// MMA and epilogue warps through a small queue in shared memory.
+constexpr int kTileQ = 4;
+
 template <int BN>
 struct GemmCfg {
   static constexpr uint32_t kA1 = kTileM * kTileK;      // 16 KB smem per weight k-tile (4-bit unpacked form)
@@ -63,7 +67,8 @@ struct GemmCfg {
   static constexpr uint32_t kSmem = 1024 + kStages * kStage + kBars + kXbuf;
   static_assert(kStages >= 2, "pipeline too shallow");
   static_assert(256 + 8 * kKS * kStages <= 512, "tmem columns");
-  static_assert((2 * kStages + 5) * 8 + 16 + 4 * (BN + 1) <= kBars, "barrier area");
+  // barriers (stages, accumulators, drain, tile queue), tmem slot, tile queue, combine list
+  static_assert((2 * kStages + 5 + 2 * kTileQ) * 8 + 16 + 16 * (kTileQ + 1) + 4 * (BN + 1) + 16 <= kBars, "barrier area");
 };
 
 struct MlpParams {
@@ -82,10 +87,12 @@ struct MlpParams {
   const float* topk_w;         // [T][k]
   int32_t* done_gu;          // [tiles] gate_up m-tiles finished per token tile
   int32_t* done_tok;         // [T][d_mtiles] down contributions finished per (token, feature block)
+  int32_t* sched;            // tiles claimed so far (zero at launch)
   uint32_t* status;
   int gu_mtiles, gu_ktiles, gu_rows_stored;
   int d_mtiles, d_ktiles, d_rows_stored;
   int I, H, k;
+  int weights_evict_first;  // weights are read once per forward: let them leave L2 first
 };
 
 struct TileRef {
@@ -108,8 +115,9 @@ __device__ __forceinline__ TileRef tile_ref(int tile, int n_gu, const MlpParams&
 }
 
 // Where a bounded wait expired: role (1 producer/empty, 2 mma/accumulator, 3 mma/full,
-// 4 epilogue, 5 producer/dependency; 6 is the cluster routing kernel's copies), tile and
-// k-step, packed for the second status word.
+// 4 epilogue, 5 producer/dependency, 6 producer/tile queue, 7 mma/tile queue; 8 is the
+// cluster routing kernel's copies), tile (or queue position) and k-step, packed for the
+// second status word.
 __device__ __forceinline__ uint32_t wait_site(uint32_t role, int tile, int kt) {
   return (role << 28) | ((uint32_t)min(tile, 0xFFFF) << 12) | (uint32_t)min(kt, 0xFFF);
 }
@@ -172,8 +180,12 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* tfull = empty + S;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  int* comb_list = reinterpret_cast<int*>(tmem_slot + 4);  // [BN + 1]: count, tokens to combine
+  uint64_t* q_full = drain + 1;  // [kTileQ] tile queue: entry written
+  uint64_t* q_empty = q_full + kTileQ;  // [kTileQ] entry read by the MMA warp and by the epilogue
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_empty + kTileQ);
+  int4* s_tq = reinterpret_cast<int4*>((reinterpret_cast<uintptr_t>(tmem_slot + 4) + 15) & ~uintptr_t(15));
+  int4* s_eq = s_tq + kTileQ;  // the epilogue's copy of its current entry
+  int* comb_list = reinterpret_cast<int*>(s_eq + 1);  // [BN + 1]: count, tokens to combine
   float* xbuf = reinterpret_cast<float*>(sSF + S * C::kSF + C::kBars);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -187,6 +199,10 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&tempty[a], 4);
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < kTileQ; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 2);
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -197,6 +213,17 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (warp == 0 && elect_one()) {
+    tma_prefetch_desc(&tmGu2);
+    tma_prefetch_desc(&tmGu);
+    tma_prefetch_desc(&tmGuT);
+    tma_prefetch_desc(&tmXp);
+    tma_prefetch_desc(&tmD2);
+    tma_prefetch_desc(&tmD);
+    tma_prefetch_desc(&tmDT);
+    tma_prefetch_desc(&tmHq);
+  }
+  __syncwarp();
   // Everything above overlaps the previous kernel (programmatic dependent
   // launch); the tile list and activations it produced are read only after this.
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -207,26 +234,41 @@ __global__ void __launch_bounds__(192, 1)
 
   if (warp == 0) {
     // -------------------------------------------------------------- producer
-    if (elect_one()) {
-      tma_prefetch_desc(&tmGu2);
-      tma_prefetch_desc(&tmGu);
-      tma_prefetch_desc(&tmXp);
-      tma_prefetch_desc(&tmD2);
-      tma_prefetch_desc(&tmD);
-      tma_prefetch_desc(&tmDT);
-      tma_prefetch_desc(&tmHq);
-    }
-    __syncwarp();
     int s = 0;
     uint32_t ph = 0;
     int64_t issued = 0;
     bool ok = true;
-    int4 td_next = blockIdx.x < total ? tl[tile_ref(blockIdx.x, n_gu, p).b] : make_int4(0, 0, 0, 0);
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      const TileRef r = tile_ref(tile, n_gu, p);
+    const uint64_t wpol = l2_policy(p.weights_evict_first != 0);
+    // Tiles are claimed in increasing order, so every gate_up tile a down tile
+    // depends on was claimed earlier by a running CTA.  The next claim is issued a
+    // few stages before the current tile's last loads, its descriptor fetched
+    // two stages later.
+    int claim = 0;
+    if (lane == 0) claim = atomicAdd(p.sched, 1);
+    int tile = __shfl_sync(0xffffffffu, claim, 0);
+    int4 td_next = tile < total ? tl[tile_ref(tile, n_gu, p).b] : make_int4(0, 0, 0, 0);
+    for (int i = 0; ok; ++i) {
       const int4 td = td_next;
-      if (tile + (int)gridDim.x < total) td_next = tl[tile_ref(tile + gridDim.x, n_gu, p).b];
+      // hand the tile (or the end, -1) to the MMA and epilogue warps
+      const int slot = i & (kTileQ - 1);
+      if (!mbar_wait_warp(&q_empty[slot], (uint32_t)((i / kTileQ) & 1) ^ 1u, kWaitLimitNs)) {
+        if (lane == 0) {
+          atomicOr(p.status, kStatusTimeoutProducer);
+          atomicCAS(p.status + 1, 0u, wait_site(6, i, 0));
+        }
+        break;
+      }
+      if (lane == 0) {
+        s_tq[slot] = make_int4(tile < total ? tile : -1, td.x, td.y, td.z);
+        mbar_arrive(&q_full[slot]);
+      }
+      __syncwarp();
+      if (tile >= total) break;
+      const TileRef r = tile_ref(tile, n_gu, p);
       const int k_tiles = r.gu ? p.gu_ktiles : p.d_ktiles;
+      const int n_st = (k_tiles + kKS - 1) / kKS;
+      const int claim_st = max(0, n_st - 4), fetch_st = max(0, n_st - 2);
+      int next = total;
       const int m_tiles = r.gu ? p.gu_mtiles : p.d_mtiles;
       const int rows_stored = r.gu ? p.gu_rows_stored : p.d_rows_stored;
       const uint8_t* sfa = (r.gu ? p.gu_sfa : p.d_sfa) + ((int64_t)td.x * m_tiles + r.m) * k_tiles * kAtomBytes;
@@ -247,6 +289,12 @@ __global__ void __launch_bounds__(192, 1)
       }
       for (int kt = 0; kt < k_tiles; kt += kKS) {
         const int nk = min(kKS, k_tiles - kt);
+        const int st = kt / kKS;
+        if (st == claim_st && lane == 0) claim = atomicAdd(p.sched, 1);
+        if (st == fetch_st) {
+          next = __shfl_sync(0xffffffffu, claim, 0);
+          if (next < total) td_next = tl[tile_ref(next, n_gu, p).b];
+        }
         if (!mbar_wait_warp(&empty[s], ph ^ 1u, kWaitLimitNs)) {
           if (lane == 0) {
             atomicOr(p.status, kStatusTimeoutProducer);
@@ -261,11 +309,12 @@ __global__ void __launch_bounds__(192, 1)
           const CUtensorMap* amap = r.gu ? (box_rows == 256 ? &tmGu2 : (box_rows == 128 ? &tmGu : &tmGuT))
                                          : (box_rows == 256 ? &tmD2 : (box_rows == 128 ? &tmD : &tmDT));
           mbar_arrive_expect_tx(&full[s], (uint32_t)(box_rows * kTileRowBytes + nk * (C::kB1 + 2 * kAtomBytes)));
-          tma_load_2d(sA + s * C::kA, amap, &full[s], 0, (int)tile_row0(td.x, r.m, kt, rows_stored, k_tiles));
+          tma_load_2d_hint(sA + s * C::kA, amap, &full[s], 0, (int)tile_row0(td.x, r.m, kt, rows_stored, k_tiles),
+                           wpol);
           for (int j = 0; j < nk; ++j)
             tma_load_2d(sB + s * C::kB + j * C::kB1, bmap, &full[s], (kt + j) * kTileK, td.y);
           uint8_t* sf = sSF + s * C::kSF;
-          bulk_g2s(sf, sfa + kt * kAtomBytes, nk * kAtomBytes, &full[s]);
+          bulk_g2s_hint(sf, sfa + kt * kAtomBytes, nk * kAtomBytes, &full[s], wpol);
           bulk_g2s(sf + kKS * kAtomBytes, sfb + kt * kAtomBytes, nk * kAtomBytes, &full[s]);
         }
         __syncwarp();
@@ -275,6 +324,7 @@ __global__ void __launch_bounds__(192, 1)
           ph ^= 1u;
         }
       }
+      tile = next;
     }
     // Let every copy this warp issued land before the CTA can exit.
     for (int st = 0; st < S && st < issued; ++st) {
@@ -287,11 +337,22 @@ __global__ void __launch_bounds__(192, 1)
     int s = 0, acc = 0;
     uint32_t ph = 0, aph = 0;
     bool ok = true;
-    int4 td_next = blockIdx.x < total ? tl[tile_ref(blockIdx.x, n_gu, p).b] : make_int4(0, 0, 0, 0);
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+    for (int i = 0; ok; ++i) {
+      const int slot = i & (kTileQ - 1);
+      if (!mbar_wait_warp(&q_full[slot], (uint32_t)((i / kTileQ) & 1), kWaitLimitNs)) {
+        if (lane == 0) {
+          atomicOr(p.status, kStatusTimeoutMma);
+          atomicCAS(p.status + 1, 0u, wait_site(7, i, 0));
+        }
+        break;
+      }
+      const int4 q = s_tq[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_empty[slot]);
+      if (q.x < 0) break;
+      const int tile = q.x;
       const TileRef r = tile_ref(tile, n_gu, p);
-      const int4 td = td_next;
-      if (tile + (int)gridDim.x < total) td_next = tl[tile_ref(tile + gridDim.x, n_gu, p).b];
+      const int4 td = make_int4(q.y, q.z, q.w, 0);
       const int k_tiles = r.gu ? p.gu_ktiles : p.d_ktiles;
       const int rows_m = min(kTileM, (r.gu ? p.gu_rows_stored : p.d_rows_stored) - r.m * kTileM);
       if (!mbar_wait_warp(&tempty[acc], aph ^ 1u, kWaitLimitNs)) {
@@ -361,28 +422,34 @@ __global__ void __launch_bounds__(192, 1)
     int acc = 0;
     uint32_t aph = 0;
     bool ok = true;
-    // the next tile's descriptor and bias are fetched while this one is processed
     auto bias_of = [&](const TileRef& rr, const int4& t4) -> float {
       if (rr.gu) return p.gu_bias[(int64_t)t4.x * 2 * p.I + rr.m * kTileM + row];
       const int o = rr.m * kTileM + row;
       return o < p.H ? p.d_bias[(int64_t)t4.x * p.H + o] : 0.0f;
     };
-    int4 td_next = make_int4(0, 0, 0, 0);
-    float bias_next = 0.f;
-    if (blockIdx.x < total) {
-      const TileRef r0 = tile_ref(blockIdx.x, n_gu, p);
-      td_next = tl[r0.b];
-      bias_next = bias_of(r0, td_next);
-    }
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const TileRef r = tile_ref(tile, n_gu, p);
-      const int4 td = td_next;
-      const float bias_v = bias_next;
-      if (tile + (int)gridDim.x < total) {
-        const TileRef rn = tile_ref(tile + gridDim.x, n_gu, p);
-        td_next = tl[rn.b];
-        bias_next = bias_of(rn, td_next);
+    for (int i = 0;; ++i) {
+      // one warp takes the next queue entry for all four, so that they agree on
+      // every tile (and on stopping) and meet at the same named barriers
+      const int slot = i & (kTileQ - 1);
+      if (warp == 2) {
+        const bool got = mbar_wait_warp(&q_full[slot], (uint32_t)((i / kTileQ) & 1), kWaitLimitNs);
+        if (lane == 0) {
+          *s_eq = got ? s_tq[slot] : make_int4(-2, 0, 0, 0);
+          if (got) {
+            mbar_arrive(&q_empty[slot]);
+          } else {
+            atomicOr(p.status, kStatusTimeoutEpilogue);
+            atomicCAS(p.status + 1, 0u, wait_site(4, i, 0xFFE));
+          }
+        }
       }
+      named_barrier_sync(1, 128);
+      const int4 qe = *s_eq;
+      if (qe.x < 0) break;
+      const int tile = qe.x;
+      const TileRef r = tile_ref(tile, n_gu, p);
+      const int4 td = make_int4(qe.y, qe.z, qe.w, 0);
+      const float bias_v = bias_of(r, td);
       const int rows = td.z;
       if (ok) {
         // all lanes take the same decision, so the warp-collective tcgen05.ld stays uniform
@@ -681,6 +748,7 @@ cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, cons
   p.topk_w = b.topk_w;
   p.done_gu = b.done_gu;
   p.done_tok = b.done_tok;
+  p.sched = b.sched;
   p.status = b.status;
   p.gu_mtiles = h.gu_mtiles;
   p.gu_ktiles = h.gu_ktiles;
@@ -691,6 +759,9 @@ cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, cons
   p.I = h.I;
   p.H = h.H;
   p.k = k;
+  // when the token rows of an expert fit one tile on average, each weight byte is
+  // read once per forward
+  p.weights_evict_first = (int64_t)T * k <= (int64_t)h.E * tile_rows;
   const int grid = (int)std::min<int64_t>(num_sms, (int64_t)max_tiles * (h.gu_mtiles + h.d_mtiles));
   switch (tile_rows) {
     case 16: return launch_bn<16>(m, p, grid, s);

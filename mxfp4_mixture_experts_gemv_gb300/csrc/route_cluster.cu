@@ -5,14 +5,15 @@
 //
 // The cluster's CTAs split the experts: each CTA copies its slice of router rows
 // and all T token rows into shared memory with two bulk copies, computes its
-// experts' logits, and after one cluster barrier reads every CTA's logits
-// through distributed shared memory.  The selection and the grouping are then
-// recomputed by every CTA (a few dozen pairs; deterministic, so identical
-// everywhere) and each CTA quantises its share of (token, 128-column) units
-// from the token rows it already holds, writing every slot the token goes to.
-// Nothing here goes through global memory twice and nothing waits on another
-// grid, so the chain from launch to the tile list is a single DRAM round trip
-// plus a cluster barrier.  The kernel also clears the counters the expert
+// experts' logits and stores them into every CTA's shared memory (distributed
+// shared memory) before one cluster barrier.  While the barrier completes, each
+// thread quantises its (token, 32-element block) unit of the token rows it
+// already holds.  The selection and the grouping (a few dozen pairs, ranked
+// inside one warp) are then recomputed by every CTA -- deterministic, so
+// identical everywhere -- and each thread writes its unit to every grouped row
+// of its token.  Nothing goes through global memory twice and nothing waits on
+// another grid: the chain from launch to the tile list is one DRAM round trip
+// plus one cluster barrier.  The kernel also clears the counters the expert
 // kernel uses, which the expert kernel reads only after this grid completes.
 //
 // Same arithmetic as the other routing kernels: fp32 logits, top-k by (logit
@@ -28,8 +29,7 @@
 namespace moe {
 namespace {
 
-constexpr int kRcThreads = 256;
-constexpr int kRcMaxT = kRouteClusterMaxT;
+constexpr int kRcThreads = 384;
 constexpr int kRcMaxEpc = 32;  // experts per CTA: E <= 256 over at least 8 CTAs
 
 struct RouteClusterArgs {
@@ -54,14 +54,44 @@ struct RouteClusterArgs {
   uint32_t* status;
 };
 
+// Sum-reduce N values held by every lane of a warp so that each lane ends up
+// with N / 32 complete sums: after the call lane l holds the sums of the values
+// with index l * (N / 32) + m in v[m].
+template <int N>
+__device__ __forceinline__ void warp_reduce_scatter(float (&v)[N], int lane) {
+  int n = N;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+      if (i < n / 2) {
+        const float lo = v[i], hi = v[i + n / 2];
+        const float got = __shfl_xor_sync(0xffffffffu, up ? lo : hi, o);
+        v[i] = (up ? hi : lo) + got;
+      }
+    }
+    n >>= 1;
+  }
+}
+
+__device__ __forceinline__ void st_dsmem_f32(const void* p, uint32_t cta, float v) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(cta));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(r), "f"(v) : "memory");
+}
+
+template <int TM>  // token capacity of this instance (4 or 8)
 __global__ void __launch_bounds__(kRcThreads, 1) route_cluster_kernel(const RouteClusterArgs a) {
+  constexpr int kG = 8;           // experts contracted together
+  constexpr int kN = kG * TM;     // partial sums per thread
   extern __shared__ __align__(128) uint8_t rc_dyn[];  // [epc][H] router rows, then [T][H] token rows (bf16)
-  __shared__ float s_mine[kRcMaxEpc][kRcMaxT];       // logits of this CTA's experts
-  __shared__ float s_log[kRcMaxT][257];              // every expert's logits
-  __shared__ int s_ids[kRcMaxT * 8], s_sorted[kRcMaxT * 8], s_inv[kRcMaxT * 8];
-  __shared__ float s_w[kRcMaxT * 8];
-  __shared__ int s_cnt[257], s_off[258], s_run[257], s_toff[258];
-  __shared__ int s_tile_e[kRcMaxT * 8 + 256];
+  __shared__ float s_log[TM][257];                    // every expert's logits (pushed by their CTAs)
+  __shared__ float s_red[kRcThreads / 32][kN];
+  __shared__ float s_bias[kRcMaxEpc];
+  __shared__ int s_ids[TM * 8], s_sorted[TM * 8], s_inv[TM * 8];
+  __shared__ float s_w[TM * 8];
+  __shared__ int s_off[256], s_toff[256];  // of the experts the pairs use
   __shared__ __align__(8) uint64_t s_bar;
   // the expert kernel may start its prologue now; it waits for this grid's results
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -79,117 +109,128 @@ __global__ void __launch_bounds__(kRcThreads, 1) route_cluster_kernel(const Rout
     mbar_arrive_expect_tx(&s_bar, bw + bx);
     if (bw) bulk_g2s(s_wr, a.wr + (int64_t)e0 * H, bw, &s_bar);
     bulk_g2s(s_x, a.x, bx, &s_bar);
+    // this forward's status words, cleared before the cluster barrier that orders
+    // them before any report
+    if (rank == 0) *reinterpret_cast<uint4*>(a.zero) = make_uint4(0u, 0u, 0u, 0u);
   }
-  // biases of this warp's experts (in flight with the copies)
-  float bias[kRcMaxEpc / 8];
-#pragma unroll
-  for (int m = 0; m < kRcMaxEpc / 8; ++m) {
-    const int j = warp + 8 * m;
-    bias[m] = j < ne ? __uint_as_float((uint32_t)a.br[e0 + j] << 16) : 0.f;
-  }
-  for (int i = rank + ncta * tid; i < a.zero_words; i += ncta * kRcThreads) a.zero[i] = 0u;
-  for (int e = tid; e < E; e += kRcThreads) s_cnt[e] = 0;
+  // biases of this CTA's experts (in flight with the copies)
+  if (tid < ne) s_bias[tid] = __uint_as_float((uint32_t)a.br[e0 + tid] << 16);
   __syncthreads();  // the barrier's initialisation is visible to every thread
   const bool staged = mbar_wait(&s_bar, 0, kWaitLimitNs);
 
-  // logits of this CTA's experts: warp per expert, lanes over 16-byte column chunks
+  // logits of this CTA's experts, kG at a time: thread = 16-byte column chunk(s),
+  // the token chunks stay in registers across the kG router rows
   const int hc = H / 8;
+  for (int g0 = 0; g0 < ne; g0 += kG) {
+    float acc[kN];
 #pragma unroll
-  for (int m = 0; m < kRcMaxEpc / 8; ++m) {
-    const int j = warp + 8 * m;
-    if (j < ne) {
-      float acc[kRcMaxT];
+    for (int i = 0; i < kN; ++i) acc[i] = 0.f;
+    for (int c = tid; c < hc; c += kRcThreads) {
+      float xv[TM][8];
 #pragma unroll
-      for (int t = 0; t < kRcMaxT; ++t) acc[t] = 0.f;
-      const uint4* w4 = reinterpret_cast<const uint4*>(s_wr + (size_t)j * H);
-      for (int c = lane; c < hc; c += 32) {
-        float wv[8];
-        bf16x8(w4[c], wv);
+      for (int t = 0; t < TM; ++t) {
+        if (t < T) bf16x8(reinterpret_cast<const uint4*>(s_x + (size_t)t * H)[c], xv[t]);
+        else
 #pragma unroll
-        for (int t = 0; t < kRcMaxT; ++t) {
-          if (t < T) {
-            float xv[8];
-            bf16x8(reinterpret_cast<const uint4*>(s_x + (size_t)t * H)[c], xv);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[t] = fmaf(xv[i], wv[i], acc[t]);
-          }
-        }
+          for (int i = 0; i < 8; ++i) xv[t][i] = 0.f;
       }
 #pragma unroll
-      for (int t = 0; t < kRcMaxT; ++t) {
-        if (t < T) {
-          float v = acc[t];
+      for (int j = 0; j < kG; ++j) {
+        if (g0 + j < ne) {
+          float wv[8];
+          bf16x8(reinterpret_cast<const uint4*>(s_wr + (size_t)(g0 + j) * H)[c], wv);
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-          v += bias[m];
-          if (lane == 0) {
-            s_mine[j][t] = v;
-            a.logits[(int64_t)t * E + e0 + j] = v;
-          }
+          for (int t = 0; t < TM; ++t)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[j * TM + t] = fmaf(xv[t][i], wv[i], acc[j * TM + t]);
         }
       }
     }
+    warp_reduce_scatter<kN>(acc, lane);
+#pragma unroll
+    for (int m = 0; m < kN / 32; ++m) s_red[warp][lane * (kN / 32) + m] = acc[m];
+    __syncthreads();
+    if (tid < kN) {
+      const int j = tid / TM, t = tid % TM;
+      float v = 0.f;
+#pragma unroll
+      for (int wi = 0; wi < kRcThreads / 32; ++wi) v += s_red[wi][tid];
+      if (g0 + j < ne && t < T) {
+        v += s_bias[g0 + j];
+        const int e = e0 + g0 + j;
+        for (int r = 0; r < ncta; ++r) st_dsmem_f32(&s_log[t][e], (uint32_t)r, v);
+      }
+    }
+    __syncthreads();
   }
   cluster_arrive();
-  cluster_wait();  // every CTA's logits (and every CTA's clearing) are done
+
+  // While the logits travel: this thread's quantisation unit (token t, 32-element
+  // block kb) into registers, the token's codes and scale (stage output), and the
+  // expert kernel's counters (read by it only after this grid completes).
+  const int nbh = H / 32, kth = (H + kTileK - 1) / kTileK;
+  const int u = rank + ncta * tid;
+  const bool has_u = u < T * nbh;
+  const int ut = has_u ? u / nbh : 0, ukb = has_u ? u - ut * nbh : 0;
+  uint4 qc[2];
+  uint8_t qs = 0;
+  if (has_u) {
+    qs = quant_block_regs(s_x + (size_t)ut * H + ukb * 32, qc);
+    uint4* q = reinterpret_cast<uint4*>(a.xq + (int64_t)ut * H + ukb * 32);
+    q[0] = qc[0];
+    q[1] = qc[1];
+    a.xs[(int64_t)ut * nbh + ukb] = qs;
+  }
+  for (int i = 4 + rank + ncta * tid; i < a.zero_words; i += ncta * kRcThreads) a.zero[i] = 0u;
+
+  cluster_wait();  // every CTA has every logit; no CTA touches another's shared memory after this
   if (!staged && tid == 0) {
     atomicOr(a.status, kStatusTimeoutProducer);
-    atomicCAS(a.status + 1, 0u, (6u << 28) | ((uint32_t)rank << 12));  // role 6: routing copies
+    atomicCAS(a.status + 1, 0u, (8u << 28) | ((uint32_t)rank << 12));  // role 8: routing copies
   }
-  for (int i = tid; i < T * E; i += kRcThreads) {
-    const int t = i / E, e = i - t * E;
-    s_log[t][e] = ld_dsmem_f32(&s_mine[e % epc][t], (uint32_t)(e / epc));
-  }
-  cluster_arrive();  // done reading the other CTAs' shared memory (matched by the wait at the end)
-  __syncthreads();
   for (int t = warp; t < T; t += kRcThreads / 32) topk_softmax_warp(s_log[t], E, k, s_ids + t * k, s_w + t * k, lane);
   __syncthreads();
-  if (warp == 0)
-    group_pairs_warp(s_ids, TK, E, a.tshift, s_cnt, s_off, s_toff, s_tile_e, s_run, s_sorted, s_inv, lane);
-  __syncthreads();
-  if (rank == 0)
-    publish_routing(s_ids, s_w, s_sorted, s_inv, s_cnt, s_off, s_toff, s_tile_e, TK, E, 1 << a.tshift, a.ids, a.w,
-                    a.sorted_rows, a.inv_pos, a.counts, a.offsets, a.tiles);
-
-  // quantise (token t, atom column ka) units: four 32-element blocks, written to
-  // every grouped row of the token with one scale word each
-  const int nbh = H / 32, kth = (H + kTileK - 1) / kTileK;
-  for (int u = rank + ncta * tid; u < T * kth; u += ncta * kRcThreads) {
-    const int t = u / kth, ka = u - t * kth;
-    uint4 c[4][2];
-    uint32_t word = 0;
-#pragma unroll
-    for (int jb = 0; jb < 4; ++jb) {
-      const int kb = 4 * ka + jb;
-      const uint8_t sc = kb < nbh ? quant_block_regs(s_x + (size_t)t * H + kb * 32, c[jb]) : (uint8_t)127;
-      word |= (uint32_t)sc << (8 * jb);
+  if (warp == 0) {
+    group_pairs_small_warp(s_ids, TK, a.tshift, s_off, s_toff, s_sorted, s_inv, rank == 0 ? a.tiles : nullptr, lane);
+  } else {
+    // meanwhile: this CTA's experts' logits, and (CTA 0) the selection and the
+    // per-expert counts and offsets (stage outputs)
+    const int v = tid - 32, nv = kRcThreads - 32;
+    for (int i = v; i < T * ne; i += nv) {
+      const int t = i / ne, e = e0 + i % ne;
+      a.logits[(int64_t)t * E + e] = s_log[t][e];
     }
-    for (int j = 0; j < k; ++j) {
-      const int f = t * k + j, p = s_inv[f];
-      uint4* dst = reinterpret_cast<uint4*>(a.xp + (int64_t)p * H + ka * kTileK);
-#pragma unroll
-      for (int jb = 0; jb < 4; ++jb) {
-        if (4 * ka + jb < nbh) {
-          dst[2 * jb] = c[jb][0];
-          dst[2 * jb + 1] = c[jb][1];
-        }
+    if (rank == 0) {
+      for (int i = v; i < TK; i += nv) {
+        a.ids[i] = s_ids[i];
+        a.w[i] = s_w[i];
       }
-      *reinterpret_cast<uint32_t*>(a.xp_sf + row_sf_word(p, ka, kth, s_ids, s_sorted, s_off, s_toff, a.tshift)) =
-          word;
-    }
-    // the token's codes and scales (stage output)
-    uint4* q = reinterpret_cast<uint4*>(a.xq + (int64_t)t * H + ka * kTileK);
-#pragma unroll
-    for (int jb = 0; jb < 4; ++jb) {
-      const int kb = 4 * ka + jb;
-      if (kb < nbh) {
-        q[2 * jb] = c[jb][0];
-        q[2 * jb + 1] = c[jb][1];
-        a.xs[(int64_t)t * nbh + kb] = (uint8_t)(word >> (8 * jb));
-      }
+      expert_counts_offsets(s_ids, TK, E, a.counts, a.offsets, v, nv);
     }
   }
-  cluster_wait();
+  __syncthreads();
+  if (rank == 0)
+    for (int i = tid; i < TK; i += kRcThreads) {
+      a.sorted_rows[i] = s_sorted[i];
+      a.inv_pos[i] = s_inv[i];
+    }
+  // the unit's codes go to every grouped row of its token, the scale byte to each
+  // row's atom word; the last real block also sets the padding bytes of its word
+  if (has_u) {
+    const int ka = ukb >> 2;
+    for (int j = 0; j < k; ++j) {
+      const int f = ut * k + j, p = s_inv[f], e = s_ids[f];
+      uint4* dst = reinterpret_cast<uint4*>(a.xp + (int64_t)p * H + ukb * 32);
+      dst[0] = qc[0];
+      dst[1] = qc[1];
+      const int r_in_e = p - s_off[e];
+      const int b = s_toff[e] + (r_in_e >> a.tshift), n = r_in_e & ((1 << a.tshift) - 1);
+      uint8_t* wd = a.xp_sf + ((int64_t)b * kth + ka) * kAtomBytes + (n & 31) * 16 + (n >> 5) * 4;
+      wd[ukb & 3] = qs;
+      if (ukb == nbh - 1)
+        for (int jj = (ukb & 3) + 1; jj < 4; ++jj) wd[jj] = 127;
+    }
+  }
 }
 
 int g_cluster_size[64];  // per device: 0 = not chosen yet
@@ -199,8 +240,9 @@ std::mutex g_cluster_mu;
 
 bool route_cluster_fits(int T, int E, int H) {
   const int epc = (E + 7) / 8;  // the smallest cluster this kernel runs on
-  return T >= 1 && T <= kRouteClusterMaxT && E <= 256 &&
-         (size_t)(epc + T) * H * 2 <= kRouteClusterMaxSmem;
+  // (T * k <= 64 pairs follows from T <= 8, k <= 8; one quantisation unit per thread)
+  return T >= 1 && T <= kRouteClusterMaxT && E <= 256 && (size_t)(epc + T) * H * 2 <= kRouteClusterMaxSmem &&
+         T * (H / 32) <= 8 * kRcThreads;
 }
 
 cudaError_t launch_route_cluster(const uint16_t* x, const uint16_t* wr, const uint16_t* br, int T, int H, int E,
@@ -214,10 +256,12 @@ cudaError_t launch_route_cluster(const uint16_t* x, const uint16_t* wr, const ui
     std::lock_guard<std::mutex> lk(g_cluster_mu);
     csize = g_cluster_size[dev];
     if (csize == 0) {
-      e = cudaFuncSetAttribute(route_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)kRouteClusterMaxSmem);
-      if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(route_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      for (auto fn : {route_cluster_kernel<4>, route_cluster_kernel<8>}) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRouteClusterMaxSmem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) break;
+      }
       // 16 CTAs when the device can place such a cluster with the largest shared
       // memory this kernel asks for, else the portable 8
       csize = 8;
@@ -234,7 +278,7 @@ cudaError_t launch_route_cluster(const uint16_t* x, const uint16_t* wr, const ui
         q.attrs = qa;
         q.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel, &q) == cudaSuccess && n >= 1) csize = 16;
+        if (cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<8>, &q) == cudaSuccess && n >= 1) csize = 16;
       }
       (void)cudaGetLastError();
       g_cluster_size[dev] = csize;
@@ -256,7 +300,7 @@ cudaError_t launch_route_cluster(const uint16_t* x, const uint16_t* wr, const ui
   attrs[0].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, route_cluster_kernel, a);
+  return T <= 4 ? cudaLaunchKernelEx(&cfg, route_cluster_kernel<4>, a) : cudaLaunchKernelEx(&cfg, route_cluster_kernel<8>, a);
 }
 
 }  // namespace moe

@@ -98,6 +98,88 @@ __device__ __forceinline__ void group_pairs_warp(const int32_t* ids, int TK, int
   }
 }
 
+// Warp: the same grouping for at most 64 pairs, by ranking instead of counting.
+// Pair f's key (expert << 6 | f) is unique, so its rank among all keys is its
+// grouped row (stable within an expert); the pairs of smaller experts give the
+// expert's offset, the pairs of the same expert its count, and the first pair of
+// every used expert places that expert's tiles after the tiles of the smaller
+// used experts.  Writes sorted[p], inv[f], and for every used expert e off[e] and
+// toff[e]; when `tiles` is given also the tile list ({expert, row0, rows, 0} at
+// tiles + 4 + 4i, the count in tiles[0]).  Nothing here touches experts no pair
+// uses.
+__device__ __forceinline__ void group_pairs_small_warp(const int32_t* ids, int TK, int tshift, int* off, int* toff,
+                                                       int* sorted, int* inv, int32_t* tiles, int lane) {
+  const int f0 = lane, f1 = lane + 32;
+  const int id0 = f0 < TK ? ids[f0] : 0x3FFFFFF, id1 = f1 < TK ? ids[f1] : 0x3FFFFFF;
+  const int key0 = f0 < TK ? (id0 << 6) | f0 : 0x7FFFFFFF, key1 = f1 < TK ? (id1 << 6) | f1 : 0x7FFFFFFF;
+  int rank0 = 0, rank1 = 0, less0 = 0, less1 = 0, same0 = 0, same1 = 0;
+  for (int g = 0; g < 32; ++g) {
+    const int ka = __shfl_sync(0xffffffffu, key0, g), kb = __shfl_sync(0xffffffffu, key1, g);
+    const int ia = ka >> 6, ib = kb >> 6;
+    rank0 += (ka < key0) + (kb < key0);
+    rank1 += (ka < key1) + (kb < key1);
+    less0 += (ia < id0) + (ib < id0);
+    less1 += (ia < id1) + (ib < id1);
+    same0 += (ia == id0) + (ib == id0);
+    same1 += (ia == id1) + (ib == id1);
+  }
+  const int tr = 1 << tshift;
+  // the first pair of each used expert carries its tile count
+  const bool first0 = f0 < TK && rank0 == less0, first1 = f1 < TK && rank1 == less1;
+  const int tc0 = first0 ? (same0 + tr - 1) >> tshift : 0, tc1 = first1 ? (same1 + tr - 1) >> tshift : 0;
+  int tpre0 = 0, tpre1 = 0;
+  for (int g = 0; g < 32; ++g) {
+    const int ia = __shfl_sync(0xffffffffu, id0, g), ib = __shfl_sync(0xffffffffu, id1, g);
+    const int ta = __shfl_sync(0xffffffffu, tc0, g), tb = __shfl_sync(0xffffffffu, tc1, g);
+    tpre0 += (ia < id0 ? ta : 0) + (ib < id0 ? tb : 0);
+    tpre1 += (ia < id1 ? ta : 0) + (ib < id1 ? tb : 0);
+  }
+  if (f0 < TK) {
+    sorted[rank0] = f0;
+    inv[f0] = rank0;
+  }
+  if (f1 < TK) {
+    sorted[rank1] = f1;
+    inv[f1] = rank1;
+  }
+  if (first0) {
+    off[id0] = less0;
+    toff[id0] = tpre0;
+    if (tiles)
+      for (int i = 0; i < tc0; ++i)
+        reinterpret_cast<int4*>(tiles + 4)[tpre0 + i] = make_int4(id0, less0 + i * tr, min(tr, same0 - i * tr), 0);
+  }
+  if (first1) {
+    off[id1] = less1;
+    toff[id1] = tpre1;
+    if (tiles)
+      for (int i = 0; i < tc1; ++i)
+        reinterpret_cast<int4*>(tiles + 4)[tpre1 + i] = make_int4(id1, less1 + i * tr, min(tr, same1 - i * tr), 0);
+  }
+  if (tiles) {
+    int n = tc0 + tc1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+    if (lane == 0) tiles[0] = n;
+  }
+}
+
+// Thread t of nt: counts[e] and offsets[e] of every expert e < E and offsets[E] =
+// TK, straight from the ids of the TK pairs.
+__device__ __forceinline__ void expert_counts_offsets(const int32_t* ids, int TK, int E, int32_t* counts,
+                                                      int32_t* offsets, int t, int nt) {
+  for (int e = t; e <= E; e += nt) {
+    int c = 0, o = 0;
+    for (int f = 0; f < TK; ++f) {
+      const int id = ids[f];
+      c += id == e;
+      o += id < e;
+    }
+    if (e < E) counts[e] = c;
+    offsets[e] = o;
+  }
+}
+
 // Block: write the routing results held in shared memory to global memory.
 __device__ __forceinline__ void publish_routing(const int* s_ids, const float* s_w, const int* s_sorted,
                                                 const int* s_inv, const int* s_cnt, const int* s_off,
