@@ -239,13 +239,13 @@ __global__ void __launch_bounds__(192, 1)
     int64_t issued = 0;
     bool ok = true;
     const uint64_t wpol = l2_policy(p.weights_evict_first != 0);
-    // Tiles are claimed in increasing order, so every gate_up tile a down tile
-    // depends on was claimed earlier by a running CTA.  The next claim is issued a
-    // few stages before the current tile's last loads, its descriptor fetched
-    // two stages later.
+    // CTA c starts with tile c; later tiles are claimed in increasing order from
+    // the counter, so every gate_up tile a down tile depends on was taken earlier
+    // by a running CTA.  A claim is issued several stages before the current
+    // tile's last loads and its descriptor fetched two stages before them, so
+    // neither round trip stalls the copies.
     int claim = 0;
-    if (lane == 0) claim = atomicAdd(p.sched, 1);
-    int tile = __shfl_sync(0xffffffffu, claim, 0);
+    int tile = blockIdx.x;
     int4 td_next = tile < total ? tl[tile_ref(tile, n_gu, p).b] : make_int4(0, 0, 0, 0);
     for (int i = 0; ok; ++i) {
       const int4 td = td_next;
@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(192, 1)
       const TileRef r = tile_ref(tile, n_gu, p);
       const int k_tiles = r.gu ? p.gu_ktiles : p.d_ktiles;
       const int n_st = (k_tiles + kKS - 1) / kKS;
-      const int claim_st = max(0, n_st - 4), fetch_st = max(0, n_st - 2);
+      const int claim_st = max(0, n_st - 6), fetch_st = max(0, n_st - 2);
       int next = total;
       const int m_tiles = r.gu ? p.gu_mtiles : p.d_mtiles;
       const int rows_stored = r.gu ? p.gu_rows_stored : p.d_rows_stored;
@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(192, 1)
       for (int kt = 0; kt < k_tiles; kt += kKS) {
         const int nk = min(kKS, k_tiles - kt);
         const int st = kt / kKS;
-        if (st == claim_st && lane == 0) claim = atomicAdd(p.sched, 1);
+        if (st == claim_st && lane == 0) claim = (int)gridDim.x + atomicAdd(p.sched, 1);
         if (st == fetch_st) {
           next = __shfl_sync(0xffffffffu, claim, 0);
           if (next < total) td_next = tl[tile_ref(next, n_gu, p).b];
