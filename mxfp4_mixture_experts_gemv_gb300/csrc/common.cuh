@@ -100,6 +100,7 @@ bool route_cluster_fits(int T, int E, int H);
 inline int tile_rows_for(int T, int k, int E) {
   (void)k;
   (void)E;
+  if (T <= 8) return 8;  // a token visits an expert at most once: at most T rows per tile
   if (T <= 16) return 16;
   if (T <= 32) return 32;
   if (T <= 64) return 64;

@@ -60,7 +60,10 @@ struct GemmCfg {
   static constexpr uint32_t kB = kKS * kB1;
   static constexpr uint32_t kSF = 2 * kKS * kAtomBytes;  // scale atoms of A (first half) and B
   static constexpr uint32_t kStage = kA + kB + kSF;
-  static constexpr uint32_t kXbuf = 128 * 33 * 4;   // gate_up: the accumulator chunk exchanged through smem
+  // gate_up epilogue: accumulator chunks of kCW token columns are transposed
+  // through shared memory (a token tile of at most 16 rows needs one 16-wide chunk)
+  static constexpr int kCW = BN >= 32 ? 32 : 16;
+  static constexpr uint32_t kXbuf = 128 * (kCW + 1) * 4;
   static constexpr uint32_t kBars = 1024;
   static constexpr uint32_t kBudget = 227 * 1024 - 1024 - kXbuf - kBars;
   static constexpr int kStages = (kBudget / kStage) > 8 ? 8 : (int)(kBudget / kStage);
@@ -161,13 +164,26 @@ __device__ __forceinline__ bool wait_counter_warp(const int32_t* ctr, int target
   return true;
 }
 
+// Activation tiles are fetched with the smallest of these box heights that covers
+// the unit's token rows (the MMA's N rounds rows up to 16; columns past the rows
+// are never read back), so a sparse token tile does not pull a full BN x 128 box.
+constexpr int kActBoxes = 5;  // 8, 16, 32, 64, 128 rows
+__host__ __device__ constexpr int act_box_rows(int i) { return 8 << i; }
+__device__ __forceinline__ int act_box_index(int rows) {
+  return rows <= 8 ? 0 : rows <= 16 ? 1 : rows <= 32 ? 2 : rows <= 64 ? 3 : 4;
+}
+
+// Tensor maps of one launch: weight boxes of 256, 128 and 64 rows (two k-tiles,
+// one k-tile, a 64-row tail tile), and the activation maps (grouped x for
+// gate_up, hq for down) for each box height.
+struct Maps {
+  CUtensorMap gu2, gu, gut, d2, d, dt;
+  CUtensorMap xp[kActBoxes], hq[kActBoxes];
+};
+
 template <int BN>
 __global__ void __launch_bounds__(192, 1)
-    expert_mlp_kernel(const __grid_constant__ CUtensorMap tmGu2, const __grid_constant__ CUtensorMap tmGu,
-                      const __grid_constant__ CUtensorMap tmGuT, const __grid_constant__ CUtensorMap tmXp,
-                      const __grid_constant__ CUtensorMap tmD2, const __grid_constant__ CUtensorMap tmD,
-                      const __grid_constant__ CUtensorMap tmDT, const __grid_constant__ CUtensorMap tmHq,
-                      const MlpParams p) {
+    expert_mlp_kernel(const __grid_constant__ Maps maps, const MlpParams p) {
   using C = GemmCfg<BN>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -214,14 +230,16 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   if (warp == 0 && elect_one()) {
-    tma_prefetch_desc(&tmGu2);
-    tma_prefetch_desc(&tmGu);
-    tma_prefetch_desc(&tmGuT);
-    tma_prefetch_desc(&tmXp);
-    tma_prefetch_desc(&tmD2);
-    tma_prefetch_desc(&tmD);
-    tma_prefetch_desc(&tmDT);
-    tma_prefetch_desc(&tmHq);
+    tma_prefetch_desc(&maps.gu2);
+    tma_prefetch_desc(&maps.gu);
+    tma_prefetch_desc(&maps.gut);
+    tma_prefetch_desc(&maps.d2);
+    tma_prefetch_desc(&maps.d);
+    tma_prefetch_desc(&maps.dt);
+    for (int i = 0; i < kActBoxes && act_box_rows(i) <= BN; ++i) {
+      tma_prefetch_desc(&maps.xp[i]);
+      tma_prefetch_desc(&maps.hq[i]);
+    }
   }
   __syncwarp();
   // Everything above overlaps the previous kernel (programmatic dependent
@@ -274,7 +292,9 @@ __global__ void __launch_bounds__(192, 1)
       const uint8_t* sfa = (r.gu ? p.gu_sfa : p.d_sfa) + ((int64_t)td.x * m_tiles + r.m) * k_tiles * kAtomBytes;
       const uint8_t* sfb = (r.gu ? p.xp_sf : p.hq_sf) + (int64_t)r.b * k_tiles * kAtomBytes;
       const int rows_m = min(kTileM, rows_stored - r.m * kTileM);  // 64 for a tail m-tile
-      const CUtensorMap* bmap = r.gu ? &tmXp : &tmHq;
+      const int bi = min(act_box_index(td.z), kActBoxes - 1);
+      const CUtensorMap* bmap = r.gu ? &maps.xp[bi] : &maps.hq[bi];
+      const uint32_t b_bytes = (uint32_t)act_box_rows(bi) * kTileK;
       if (!r.gu) {
         // the intermediate of this token tile must be complete (all gate_up m-tiles)
         if (!wait_counter_warp(p.done_gu + r.b, p.gu_mtiles, kWaitLimitNs)) {
@@ -306,9 +326,9 @@ __global__ void __launch_bounds__(192, 1)
         if (elect_one()) {
           // the nk weight tiles are rows_m * nk consecutive 64-byte rows: one box
           const int box_rows = rows_m * nk;
-          const CUtensorMap* amap = r.gu ? (box_rows == 256 ? &tmGu2 : (box_rows == 128 ? &tmGu : &tmGuT))
-                                         : (box_rows == 256 ? &tmD2 : (box_rows == 128 ? &tmD : &tmDT));
-          mbar_arrive_expect_tx(&full[s], (uint32_t)(box_rows * kTileRowBytes + nk * (C::kB1 + 2 * kAtomBytes)));
+          const CUtensorMap* amap = r.gu ? (box_rows == 256 ? &maps.gu2 : (box_rows == 128 ? &maps.gu : &maps.gut))
+                                         : (box_rows == 256 ? &maps.d2 : (box_rows == 128 ? &maps.d : &maps.dt));
+          mbar_arrive_expect_tx(&full[s], (uint32_t)(box_rows * kTileRowBytes + nk * (b_bytes + 2 * kAtomBytes)));
           tma_load_2d_hint(sA + s * C::kA, amap, &full[s], 0, (int)tile_row0(td.x, r.m, kt, rows_stored, k_tiles),
                            wpol);
           for (int j = 0; j < nk; ++j)
@@ -363,7 +383,9 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t n_mma = (uint32_t)min(BN, max(16, (td.z + 15) & ~15));
+      // N of the MMA: the unit's rows rounded up to 16 (the smallest N for M = 128);
+      // B rows past the unit's rows are never read back
+      const uint32_t n_mma = (uint32_t)max(16, min(BN, (td.z + 15) & ~15));
       const uint32_t d_tmem = tmem + (uint32_t)acc * 128u;
       const uint32_t idesc0 = idesc_mxf8f6f4(128, n_mma, 5 /*E2M1*/, 0 /*E4M3*/, 0, 0);
       for (int kt = 0; kt < k_tiles; kt += kKS) {
@@ -464,33 +486,36 @@ __global__ void __launch_bounds__(192, 1)
       if (r.gu) {
         // accumulator rows 0..63 = gate, 64..127 = up of intermediate columns 64m..64m+63
         // SwiGLU + MXFP8 of a 32-column chunk, transposed through shared memory:
-        // thread et takes token column j = (et >> 1) & 31 and 16 rows (half hh = et & 1)
-        // of MX block rb = et >> 6 (gate rows 32rb..32rb+31); the two halves of a block
-        // are neighbouring lanes and share their amax with one shuffle.
-        const int hh = et & 1, jt = (et >> 1) & 31, rb = et >> 6;
+        // thread et takes token column jt of the chunk and 16 rows (half hh = et & 1)
+        // of MX block rb (gate rows 32rb..32rb+31); the two halves of a block are
+        // neighbouring lanes and share their amax with one shuffle.  A 16-wide chunk
+        // needs the first 64 threads only.
+        constexpr int CW = C::kCW, XS = CW + 1;
+        const int hh = et & 1, jt = (et >> 1) & (CW - 1), rb = (et >> (CW == 32 ? 6 : 5)) & 1;
+        const bool active = et < 4 * CW;
         const int kb = 2 * r.m + rb;  // MX block of the intermediate
-        for (int c0 = 0; c0 < rows; c0 += 32) {
+        for (int c0 = 0; c0 < rows; c0 += CW) {
           uint32_t r0[16], r1[16];
           if (ok) {
             tmem_ld_32x32b_x16(tb + (uint32_t)c0, r0);
-            tmem_ld_32x32b_x16(tb + (uint32_t)c0 + 16u, r1);
+            if (CW == 32) tmem_ld_32x32b_x16(tb + (uint32_t)c0 + 16u, r1);
             tmem_ld_wait();
           } else {
 #pragma unroll
             for (int j = 0; j < 16; ++j) r0[j] = r1[j] = 0;
           }
 #pragma unroll
-          for (int j = 0; j < 32; ++j) xbuf[row * 33 + j] = __uint_as_float(j < 16 ? r0[j] : r1[j - 16]) + bias_v;
+          for (int j = 0; j < CW; ++j) xbuf[row * XS + j] = __uint_as_float(j < 16 ? r0[j] : r1[j - 16]) + bias_v;
           named_barrier_sync(1, 128);
           const int n = c0 + jt;
           float h[16];
           float amax = 0.f;
-          if (n < rows) {  // same for both lanes of a pair
+          if (active && n < rows) {  // same for both lanes of a pair
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int rr = 32 * rb + 16 * hh + i;
-              const float g = xbuf[rr * 33 + jt];
-              const float u = xbuf[(64 + rr) * 33 + jt];
+              const float g = xbuf[rr * XS + jt];
+              const float u = xbuf[(64 + rr) * XS + jt];
               h[i] = g / (1.0f + expf(-g)) * u;
               amax = fmaxf(amax, fabsf(h[i]));
             }
@@ -508,7 +533,7 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t hi = cvt_e4m3x2(h[4 * i + 2] * inv, h[4 * i + 3] * inv);
             pk[i] = lo | (hi << 16);
           }
-          if (ok && n < rows) {
+          if (ok && active && n < rows) {
             *reinterpret_cast<uint4*>(p.hq + (int64_t)(td.y + n) * p.I + r.m * 64 + 32 * rb + 16 * hh) =
                 make_uint4(pk[0], pk[1], pk[2], pk[3]);
             if (hh == 0) {
@@ -650,10 +675,6 @@ bool make_act_map(CUtensorMap* map, const uint8_t* base, int K, int rows, int bo
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-struct Maps {
-  CUtensorMap gu2, gu, gut, xp, d2, d, dt, hq;
-};
-
 template <int BN>
 cudaError_t launch_bn(const Maps& m, const MlpParams& p, int grid, cudaStream_t s) {
   using C = GemmCfg<BN>;
@@ -679,7 +700,7 @@ cudaError_t launch_bn(const Maps& m, const MlpParams& p, int grid, cudaStream_t 
   attrs[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, expert_mlp_kernel<BN>, m.gu2, m.gu, m.gut, m.xp, m.d2, m.d, m.dt, m.hq, p);
+  return cudaLaunchKernelEx(&cfg, expert_mlp_kernel<BN>, m, p);
 }
 
 }  // namespace
@@ -723,9 +744,14 @@ cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, cons
       !make_weight_map(&m.gut, packed + h.off_gu_data, gu_rows, 64) ||
       !make_weight_map(&m.d2, packed + h.off_d_data, d_rows, 2 * kTileM) ||
       !make_weight_map(&m.d, packed + h.off_d_data, d_rows, kTileM) ||
-      !make_weight_map(&m.dt, packed + h.off_d_data, d_rows, 64) ||
-      !make_act_map(&m.xp, b.xp, h.H, TK, tile_rows) || !make_act_map(&m.hq, b.hq, h.I, TK, tile_rows))
+      !make_weight_map(&m.dt, packed + h.off_d_data, d_rows, 64))
     return cudaErrorInvalidValue;
+  for (int i = 0; i < kActBoxes; ++i) {
+    // boxes taller than the token tile are never used; encode them at its height
+    const int rows = std::min(act_box_rows(i), tile_rows);
+    if (!make_act_map(&m.xp[i], b.xp, h.H, TK, rows) || !make_act_map(&m.hq[i], b.hq, h.I, TK, rows))
+      return cudaErrorInvalidValue;
+  }
     std::lock_guard<std::mutex> lk(mu);
     keys[next_slot] = key;
     cache[next_slot] = m;
@@ -764,6 +790,7 @@ cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, cons
   p.weights_evict_first = (int64_t)T * k <= (int64_t)h.E * tile_rows;
   const int grid = (int)std::min<int64_t>(num_sms, (int64_t)max_tiles * (h.gu_mtiles + h.d_mtiles));
   switch (tile_rows) {
+    case 8: return launch_bn<8>(m, p, grid, s);
     case 16: return launch_bn<16>(m, p, grid, s);
     case 32: return launch_bn<32>(m, p, grid, s);
     case 64: return launch_bn<64>(m, p, grid, s);

@@ -71,7 +71,7 @@ def test_workspace_layout_sections_are_disjoint_and_aligned():
         offs = [getattr(lay, n) for n in names]
         assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
         assert lay.total == moe.workspace_size(GPT, T, 4)
-        want = 16 if T <= 16 else 32 if T <= 32 else 64 if T <= 64 else 128
+        want = 8 if T <= 8 else 16 if T <= 16 else 32 if T <= 32 else 64 if T <= 64 else 128
         assert lay.tile_rows == want
         # enough tiles for any routing: every expert's partial tile plus full tiles
         assert lay.max_tiles >= T * 4 // lay.tile_rows + min(T * 4, 128)
