@@ -42,11 +42,15 @@
 namespace moe {
 namespace {
 
-// One pipeline stage covers kKS consecutive 128-element k-tiles: one TMA box for
-// the weights (their tiles are adjacent in the packed layout), one box per k-tile
-// for the activations, one bulk copy per operand for the scale atoms, and a single
-// commit.  Fewer, larger copies per byte keep the single issuing lanes ahead of HBM.
-constexpr int kKS = 2;
+// One pipeline stage covers kKS consecutive 128-element k-tiles: weight boxes of
+// up to 256 rows (the k-tiles of a weight tile are adjacent in the packed
+// layout), one box per k-tile for the activations, one bulk copy per operand for
+// the scale atoms, and a single commit.  Fewer, larger copies per byte stream
+// faster (measured with the same copies alone: three stages of four k-tiles
+// reach 6.8 TB/s where six stages of two reach 5.9 TB/s), so the smallest token
+// tile, whose activation slots are small, takes four k-tiles per stage.
+template <int BN>
+constexpr int stage_ktiles() { return BN == 8 ? 4 : 2; }
 
 // Tiles are claimed from a global counter by the producer warp and handed to the
 // MMA and epilogue warps through a small queue in shared memory.
@@ -54,6 +58,7 @@ constexpr int kTileQ = 4;
 
 template <int BN>
 struct GemmCfg {
+  static constexpr int kKS = stage_ktiles<BN>();
   static constexpr uint32_t kA1 = kTileM * kTileK;      // 16 KB smem per weight k-tile (4-bit unpacked form)
   static constexpr uint32_t kB1 = BN * kTileK;          // BN rows x 128 B of E4M3 per k-tile
   static constexpr uint32_t kA = kKS * kA1;
@@ -64,6 +69,7 @@ struct GemmCfg {
   // through shared memory (a token tile of at most 16 rows needs one 16-wide chunk)
   static constexpr int kCW = BN >= 32 ? 32 : 16;
   static constexpr uint32_t kXbuf = 128 * (kCW + 1) * 4;
+  static_assert(kXbuf >= BN * 16 * 4, "combine staging lives in the transpose buffer");
   static constexpr uint32_t kBars = 1024;
   static constexpr uint32_t kBudget = 227 * 1024 - 1024 - kXbuf - kBars;
   static constexpr int kStages = (kBudget / kStage) > 8 ? 8 : (int)(kBudget / kStage);
@@ -185,6 +191,7 @@ template <int BN>
 __global__ void __launch_bounds__(192, 1)
     expert_mlp_kernel(const __grid_constant__ Maps maps, const MlpParams p) {
   using C = GemmCfg<BN>;
+  constexpr int kKS = C::kKS;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -324,13 +331,18 @@ __global__ void __launch_bounds__(192, 1)
           break;
         }
         if (elect_one()) {
-          // the nk weight tiles are rows_m * nk consecutive 64-byte rows: one box
-          const int box_rows = rows_m * nk;
-          const CUtensorMap* amap = r.gu ? (box_rows == 256 ? &maps.gu2 : (box_rows == 128 ? &maps.gu : &maps.gut))
-                                         : (box_rows == 256 ? &maps.d2 : (box_rows == 128 ? &maps.d : &maps.dt));
-          mbar_arrive_expect_tx(&full[s], (uint32_t)(box_rows * kTileRowBytes + nk * (b_bytes + 2 * kAtomBytes)));
-          tma_load_2d_hint(sA + s * C::kA, amap, &full[s], 0, (int)tile_row0(td.x, r.m, kt, rows_stored, k_tiles),
-                           wpol);
+          // the nk weight tiles are rows_m * nk consecutive 64-byte rows (128 bytes
+          // each in shared memory): boxes of 256, 128 or 64 rows
+          const int a_rows = rows_m * nk;
+          mbar_arrive_expect_tx(&full[s], (uint32_t)(a_rows * kTileRowBytes + nk * (b_bytes + 2 * kAtomBytes)));
+          const int row0 = (int)tile_row0(td.x, r.m, kt, rows_stored, k_tiles);
+          for (int off = 0; off < a_rows;) {
+            const int c = a_rows - off >= 256 ? 256 : a_rows - off >= 128 ? 128 : 64;
+            const CUtensorMap* amap = r.gu ? (c == 256 ? &maps.gu2 : (c == 128 ? &maps.gu : &maps.gut))
+                                           : (c == 256 ? &maps.d2 : (c == 128 ? &maps.d : &maps.dt));
+            tma_load_2d_hint(sA + s * C::kA + off * kTileK, amap, &full[s], 0, row0 + off, wpol);
+            off += c;
+          }
           for (int j = 0; j < nk; ++j)
             tma_load_2d(sB + s * C::kB + j * C::kB1, bmap, &full[s], (kt + j) * kTileK, td.y);
           uint8_t* sf = sSF + s * C::kSF;
@@ -516,7 +528,7 @@ __global__ void __launch_bounds__(192, 1)
               const int rr = 32 * rb + 16 * hh + i;
               const float g = xbuf[rr * XS + jt];
               const float u = xbuf[(64 + rr) * XS + jt];
-              h[i] = g / (1.0f + expf(-g)) * u;
+              h[i] = __fdividef(g, 1.0f + __expf(-g)) * u;  // rel. error ~1e-6, far below an E4M3 step
               amax = fmaxf(amax, fabsf(h[i]));
             }
           } else {
@@ -575,7 +587,13 @@ __global__ void __launch_bounds__(192, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
         // combine: each token of the tile has one more of its k contributions to
-        // feature block m; the epilogue that completes the k-th sums them (slot order)
+        // feature block m; the epilogue that completes the k-th sums them (slot order).
+        // The completing thread stages the token's slot positions and weights in
+        // shared memory (the transpose buffer is free here); then every epilogue
+        // thread takes one feature column of all completed tokens, four tokens'
+        // loads in flight at a time.
+        int* cpos = reinterpret_cast<int*>(xbuf);    // [BN][8] grouped positions of the slots
+        float* cwt = xbuf + BN * 8;                  // [BN][8] routing weights
         if (et == 0) comb_list[0] = 0;
         named_barrier_sync(1, 128);
         if (et < rows && ok) {
@@ -584,40 +602,36 @@ __global__ void __launch_bounds__(192, 1)
           // y of this tile is stored (barrier above); release it, and acquire the
           // other slots' rows if this is the last of the k contributions
           const int prev = atom_add_acq_rel_gpu(p.done_tok + (int64_t)t * p.d_mtiles + r.m, 1);
-          if (prev == p.k - 1) comb_list[1 + atomicAdd(comb_list, 1)] = t;
+          if (prev == p.k - 1) {
+            const int c = atomicAdd(comb_list, 1);
+            comb_list[1 + c] = t;
+            for (int j = 0; j < p.k; ++j) {
+              cpos[c * 8 + j] = p.inv_pos[(int64_t)t * p.k + j];
+              cwt[c * 8 + j] = p.topk_w[(int64_t)t * p.k + j];
+            }
+          }
         }
         named_barrier_sync(1, 128);
         const int ncomb = comb_list[0];
-        for (int i = warp - 2; i < ncomb; i += 4) {
-          const int t = comb_list[1 + i];
-          const int f = r.m * kTileM + 4 * lane;
-          if (f < p.H) {
-            // every slot's row is fetched before the sum (all loads in flight)
-            float4 v[8];
-            float wj[8];
+        const int f = r.m * kTileM + et;
+        if (f < p.H) {
+          for (int i0 = 0; i0 < ncomb; i0 += 4) {
+            float v[4][8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if (j < p.k) {
-                wj[j] = p.topk_w[(int64_t)t * p.k + j];
-                const int64_t pos = p.inv_pos[(int64_t)t * p.k + j];
-                v[j] = __ldcg(reinterpret_cast<const float4*>(p.y + pos * p.H + f));
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                v[u][j] = (i0 + u < ncomb && j < p.k) ? __ldcg(p.y + (int64_t)cpos[(i0 + u) * 8 + j] * p.H + f) : 0.f;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              if (i0 + u < ncomb) {
+                float a = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  if (j < p.k) a = fmaf(cwt[(i0 + u) * 8 + j], v[u][j], a);
+                p.out[(int64_t)comb_list[1 + i0 + u] * p.H + f] = __bfloat16_as_ushort(__float2bfloat16_rn(a));
               }
             }
-            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if (j < p.k) {
-                a.x = fmaf(wj[j], v[j].x, a.x);
-                a.y = fmaf(wj[j], v[j].y, a.y);
-                a.z = fmaf(wj[j], v[j].z, a.z);
-                a.w = fmaf(wj[j], v[j].w, a.w);
-              }
-            }
-            const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a.x)) |
-                                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a.y)) << 16);
-            const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a.z)) |
-                                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a.w)) << 16);
-            *reinterpret_cast<uint2*>(p.out + (int64_t)t * p.H + f) = make_uint2(lo, hi);
           }
         }
         named_barrier_sync(1, 128);
@@ -647,7 +661,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Weights: the tile-contiguous layout seen as a 2-D array of 128-element (64-byte)
-// rows of 4-bit codes; one box is kKS adjacent tiles or fewer (256, 128 or 64 rows),
+// rows of 4-bit codes; a box is 256, 128 or 64 rows (whole adjacent k-tiles),
 // unpacked by TMA into the 16-byte-aligned smem form the MMA reads (16 codes in
 // each 16-byte chunk, 8 bytes used).
 bool make_weight_map(CUtensorMap* map, const uint8_t* base, int64_t total_rows, int box_rows) {
