@@ -50,7 +50,7 @@ namespace {
 // reach 6.8 TB/s where six stages of two reach 5.9 TB/s), so the smallest token
 // tile, whose activation slots are small, takes four k-tiles per stage.
 template <int BN>
-constexpr int stage_ktiles() { return BN == 8 ? 4 : 2; }
+constexpr int stage_ktiles() { return BN == 8 ? 4 : (BN <= 32 ? 3 : 2); }
 
 // Tiles are claimed from a global counter by the producer warp and handed to the
 // MMA and epilogue warps through a small queue in shared memory.
