@@ -244,8 +244,16 @@ moe_status moe_forward(moe_dims d, const void* hidden, int32_t T, const void* ro
   b.done_tok = reinterpret_cast<int32_t*>(at(L.done_tok));
   b.sched = reinterpret_cast<int32_t*>(at(L.grid_bar)) + 1;  // word 0 is the grid routing barrier
   b.status = status;
+  // A few tokens: the down epilogue combines (no extra launch on the decode path).
+  // Many tokens: a streaming pass after the expert kernel, which would otherwise
+  // stall on the slot loads of every completed token.
+  b.fused_combine = L.tile_rows <= 32;
   e = moe::launch_expert_mlp(h, pk, b, T, top_k, L.max_tiles, L.tile_rows, sms, s);
   if (e != cudaSuccess) return cuda_fail(e, "expert MLP kernel");
+  if (!b.fused_combine) {
+    e = moe::launch_combine(b.y, inv_pos, w, T, top_k, d.H, static_cast<uint16_t*>(out), s);
+    if (e != cudaSuccess) return cuda_fail(e, "combine kernel");
+  }
   mark(2);
   return MOE_OK;
 }

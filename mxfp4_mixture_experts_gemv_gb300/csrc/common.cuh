@@ -230,7 +230,11 @@ struct ExpertMlpBuffers {
   int32_t* done_tok;
   int32_t* sched;  // tile claim counter, zero at launch
   uint32_t* status;
+  bool fused_combine;  // false: launch_combine sums the slots after the expert kernel
 };
+// out[t] = bf16(sum_j w[t][j] * y[inv_pos[t][j]]), slots in order, fp32 sums.
+cudaError_t launch_combine(const float* y, const int32_t* inv_pos, const float* topk_w, int T, int k, int H,
+                           uint16_t* out, cudaStream_t s);
 cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, const ExpertMlpBuffers& b, int T, int k,
                               int max_tiles, int tile_rows, int num_sms, cudaStream_t s);
 

@@ -102,6 +102,7 @@ struct MlpParams {
   int d_mtiles, d_ktiles, d_rows_stored;
   int I, H, k;
   int weights_evict_first;  // weights are read once per forward: let them leave L2 first
+  int fused_combine;  // the down epilogue also combines the k slots of completed tokens
 };
 
 struct TileRef {
@@ -586,6 +587,7 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
+        if (p.fused_combine) {
         // combine: each token of the tile has one more of its k contributions to
         // feature block m; the epilogue that completes the k-th sums them (slot order).
         // The completing thread stages the token's slot positions and weights in
@@ -635,6 +637,7 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
         named_barrier_sync(1, 128);
+        }  // fused_combine (otherwise a separate streaming pass combines y)
       }
       acc ^= 1;
       if (acc == 0) aph ^= 1u;
@@ -802,6 +805,7 @@ cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, cons
   // when the token rows of an expert fit one tile on average, each weight byte is
   // read once per forward
   p.weights_evict_first = (int64_t)T * k <= (int64_t)h.E * tile_rows;
+  p.fused_combine = b.fused_combine ? 1 : 0;
   const int grid = (int)std::min<int64_t>(num_sms, (int64_t)max_tiles * (h.gu_mtiles + h.d_mtiles));
   switch (tile_rows) {
     case 8: return launch_bn<8>(m, p, grid, s);

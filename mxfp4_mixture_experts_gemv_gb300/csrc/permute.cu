@@ -5,6 +5,8 @@
 // The grouping is deterministic: counts are order-free and every pair's
 // position is its rank among equal experts in ascending flat index t*k+j,
 // decided with warp match/popcount, never by atomics racing for slots.
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 #include "quant.cuh"
 
@@ -129,7 +131,51 @@ __global__ void __launch_bounds__(512) gather_quant_kernel(const uint16_t* __res
   }
 }
 
+// Routing-weighted combine of the down projection's slot rows, one CTA per token:
+// each thread sums four consecutive features over the k slots (fixed slot order,
+// fp32) and rounds once to bf16.  A streaming pass over y, used when many tokens
+// finish in each down tile and summing inside the expert kernel would stall it.
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ inv_pos,
+                                                      const float* __restrict__ topk_w, int k, int H,
+                                                      uint16_t* __restrict__ out) {
+  const int t = blockIdx.x;
+  __shared__ int s_pos[8];
+  __shared__ float s_w[8];
+  if (threadIdx.x < k) {
+    s_pos[threadIdx.x] = inv_pos[(int64_t)t * k + threadIdx.x];
+    s_w[threadIdx.x] = topk_w[(int64_t)t * k + threadIdx.x];
+  }
+  __syncthreads();
+  for (int f = 4 * threadIdx.x; f < H; f += 4 * blockDim.x) {
+    float4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < k) v[j] = __ldcs(reinterpret_cast<const float4*>(y + (int64_t)s_pos[j] * H + f));
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < k) {
+        a.x = fmaf(s_w[j], v[j].x, a.x);
+        a.y = fmaf(s_w[j], v[j].y, a.y);
+        a.z = fmaf(s_w[j], v[j].z, a.z);
+        a.w = fmaf(s_w[j], v[j].w, a.w);
+      }
+    }
+    const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a.x)) |
+                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a.y)) << 16);
+    const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a.z)) |
+                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a.w)) << 16);
+    *reinterpret_cast<uint2*>(out + (int64_t)t * H + f) = make_uint2(lo, hi);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_combine(const float* y, const int32_t* inv_pos, const float* topk_w, int T, int k, int H,
+                           uint16_t* out, cudaStream_t s) {
+  combine_kernel<<<T, 256, 0, s>>>(y, inv_pos, topk_w, k, H, out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_permute(const int32_t* ids, int TK, int k, int E, int tile_rows, int max_tiles,
                            int32_t* counts, int32_t* offsets, int32_t* sorted_rows, int32_t* inv_pos,
