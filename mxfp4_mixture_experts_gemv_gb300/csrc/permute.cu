@@ -30,8 +30,20 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(
   const int chunk = (TK + kPermWarps - 1) / kPermWarps;
   const int start = min(TK, warp * chunk), end = min(TK, start + chunk);
   // ids come from the top-k kernel and are always in [0, E); the clamp only keeps
-  // shared-memory indexing safe whatever the input
-  for (int i = start + lane; i < end; i += 32) atomicAdd(&hist[warp][min(max(ids[i], 0), E - 1)], 1);
+  // shared-memory indexing safe whatever the input.  Each lane loads its ids in
+  // batches of kBatch independent loads.
+  constexpr int kBatch = 16;
+  for (int b0 = start; b0 < end; b0 += 32 * kBatch) {
+    int e[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = b0 + 32 * u + lane;
+      e[u] = i < end ? min(max(ids[i], 0), E - 1) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+      if (e[u] >= 0) atomicAdd(&hist[warp][e[u]], 1);
+  }
   __syncthreads();
   __shared__ int s_cnt[257];
   if (threadIdx.x < E) {
@@ -66,20 +78,29 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(
   }
   __syncthreads();
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int base = start; base < end; base += 32) {
-    const int i = base + lane;
-    const bool valid = i < end;
-    const int e = valid ? min(max(ids[i], 0), E - 1) : -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(peers & lt_mask);
-    if (valid) {
-      const int pos = hist[warp][e] + rank;
-      sorted_rows[pos] = i;
-      inv_pos[i] = pos;
+  for (int b0 = start; b0 < end; b0 += 32 * kBatch) {
+    int eb[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = b0 + 32 * u + lane;
+      eb[u] = i < end ? min(max(ids[i], 0), E - 1) : -1;
     }
-    __syncwarp();
-    if (valid && rank == 0) hist[warp][e] += __popc(peers);
-    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (b0 + 32 * u >= end) break;  // warp-uniform
+      const int i = b0 + 32 * u + lane;
+      const int e = eb[u];
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int rank = __popc(peers & lt_mask);
+      if (e >= 0) {
+        const int pos = hist[warp][e] + rank;
+        sorted_rows[pos] = i;
+        inv_pos[i] = pos;
+      }
+      __syncwarp();
+      if (e >= 0 && rank == 0) hist[warp][e] += __popc(peers);
+      __syncwarp();
+    }
   }
 }
 
@@ -107,14 +128,34 @@ __global__ void __launch_bounds__(512) gather_quant_kernel(const uint16_t* __res
   for (int r = warp; r < rows; r += 16) {
     const int f = sorted_rows[row0 + r], t = f / k;
     const bool first = (f % k) == 0;
-    for (int blk = lane; blk < nbh; blk += 32) {
-      uint8_t* dst = xp + (int64_t)(row0 + r) * H + blk * 32;
-      const uint8_t sc = quant_block(x + (int64_t)t * H + blk * 32, dst);
-      s_scale[warp][blk] = sc;
-      if (first) {
-        reinterpret_cast<uint4*>(xq + (int64_t)t * H + blk * 32)[0] = reinterpret_cast<const uint4*>(dst)[0];
-        reinterpret_cast<uint4*>(xq + (int64_t)t * H + blk * 32)[1] = reinterpret_cast<const uint4*>(dst)[1];
-        xs[(int64_t)t * nbh + blk] = sc;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)t * H);
+    // up to four blocks per lane per round, every load of the round in flight
+    for (int b0 = 0; b0 < nbh; b0 += 128) {
+      uint4 v[4][4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int blk = b0 + 32 * u + lane;
+        if (blk < nbh)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) v[u][q] = __ldg(xr + blk * 4 + q);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int blk = b0 + 32 * u + lane;
+        if (blk < nbh) {
+          uint4 c[2];
+          const uint8_t sc = quant_block_vals(v[u], c);
+          uint4* dst = reinterpret_cast<uint4*>(xp + (int64_t)(row0 + r) * H + blk * 32);
+          dst[0] = c[0];
+          dst[1] = c[1];
+          s_scale[warp][blk] = sc;
+          if (first) {
+            uint4* q = reinterpret_cast<uint4*>(xq + (int64_t)t * H + blk * 32);
+            q[0] = c[0];
+            q[1] = c[1];
+            xs[(int64_t)t * nbh + blk] = sc;
+          }
+        }
       }
     }
     __syncwarp();

@@ -34,14 +34,14 @@ __device__ __forceinline__ void bf16x8(const uint4 v, float (&f)[8]) {
   }
 }
 
-// Quantise one 32-element block of a bf16 row to MXFP8: the 32 codes in c, returns
-// the scale code.  src may point to global or shared memory (16-byte aligned).
-__device__ __forceinline__ uint8_t quant_block_regs(const uint16_t* src, uint4 (&c)[2]) {
+// Quantise one 32-element block of bf16 (four 16-byte words, already loaded) to
+// MXFP8: the 32 codes in c, returns the scale code.
+__device__ __forceinline__ uint8_t quant_block_vals(const uint4 (&v)[4], uint4 (&c)[2]) {
   float f[32];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     float g[8];
-    bf16x8(reinterpret_cast<const uint4*>(src)[q], g);
+    bf16x8(v[q], g);
 #pragma unroll
     for (int i = 0; i < 8; ++i) f[8 * q + i] = g[i];
   }
@@ -60,6 +60,14 @@ __device__ __forceinline__ uint8_t quant_block_regs(const uint16_t* src, uint4 (
   c[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
   c[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
   return (uint8_t)(s + 127);
+}
+
+// The same from a block in global or shared memory (16-byte aligned).
+__device__ __forceinline__ uint8_t quant_block_regs(const uint16_t* src, uint4 (&c)[2]) {
+  uint4 v[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) v[q] = reinterpret_cast<const uint4*>(src)[q];
+  return quant_block_vals(v, c);
 }
 
 // The same, with the 32 codes stored to dst (16-byte aligned).
