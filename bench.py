@@ -160,6 +160,30 @@ def _oracle_tokens_per_s(T_sample: int, budget_s: float, seed: int = 0):
     return done / el, done, el
 
 
+def _oracle_tokens_per_s_all_cores(budget_s: float, seed: int = 0):
+    """The same oracle, one token per task on every host core (it holds no global
+    state, and its calls release the interpreter lock)."""
+    import concurrent.futures as cf
+    import oracle
+    n = os.cpu_count() or 1
+    T_sample = 2 * n
+    x = ms.make_tokens(seed, T_sample, H)
+    rw, rb = ms.make_router(seed, H, E)
+    _, ids, _ = oracle.route(x, rw, rb, K_TOP)
+    need = sorted(set(ids.reshape(-1).tolist()))
+    w = ms.make_expert_weights(seed, H, I, E, experts=need)
+    full = []
+    for t_sub in w:
+        z = torch.zeros((E,) + tuple(t_sub.shape[1:]), dtype=t_sub.dtype)
+        z[need] = t_sub
+        full.append(z)
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=n) as ex:
+        list(ex.map(lambda t: oracle.moe_forward(x[t:t + 1], rw, rb, *full, k=K_TOP), range(T_sample)))
+    el = time.perf_counter() - t0
+    return T_sample / el, T_sample, el, n
+
+
 def run_reference(args):
     dist, rank, world, _ = _dist()
     if rank != 0:
@@ -273,6 +297,16 @@ def _workload(layers: Layers, T: int, hot: int, hot_bias: float, steps: int, war
         torch.cuda.synchronize()
     _barrier(dist)
     ms_total = e0.elapsed_time(e1)
+    # per-step distribution (outside the timed region): each replay between its own events
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)]
+    ev[0].record(stream)
+    for i, g in enumerate(graphs):
+        g.replay()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per = sorted(ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(len(graphs)))
+    step_us = {"median": statistics.median(per), "min": per[0], "max": per[-1], "n": len(per),
+               "note": "each replay between its own events, after the timed region"}
     del graphs
     # The per-stage split comes from a second set of graphs whose captures each
     # take one profiling slot (the stage events become graph nodes, so these
@@ -300,7 +334,8 @@ def _workload(layers: Layers, T: int, hot: int, hot_bias: float, steps: int, war
     return dict(T=T, ms_per_step=ms_step, tokens_per_s=T / (ms_step * 1e-3), active_experts=n_act,
                 step_bytes=step_bytes, gu_bytes=gu_bytes, d_bytes=d_bytes, flop=flop,
                 gbs=step_bytes / (ms_step * 1e-3) / 1e9, tflops=flop / (ms_step * 1e-3) / 1e12,
-                stage_ms=stage_avg, clocks=clocks.summary(), xs=xs, routers=routers, out=out, ws=ws)
+                stage_ms=stage_avg, clocks=clocks.summary(), xs=xs, routers=routers, out=out, ws=ws,
+                step_us=step_us)
 
 
 def _stack(layers: Layers, n_layers: int, T: int, steps: int, warmup: int, device, dist, graph: bool):
@@ -479,8 +514,13 @@ def run_ours(args):
         extra["stack36_decode_t4"] = dec
 
     cpu_v, cpu_n, cpu_s = (None, 0, 0.0)
+    cpu_all = None
     if rank == 0 and not args.no_cpu:
         cpu_v, cpu_n, cpu_s = _oracle_tokens_per_s(64, args.cpu_budget)
+        av, an, asec, acores = _oracle_tokens_per_s_all_cores(args.cpu_budget)
+        cpu_all = {"value": av, "unit": "tokens/s", "cores": acores, "kind": "oracle",
+                   "sample": f"{an} tokens of the decode workload, one per task on {acores} threads "
+                             f"({asec:.1f} s, fp64)"}
 
     mlp_ms = main["stage_ms"].get("expert_mlp", 0.0)
     mlp_bytes = main["gu_bytes"] + main["d_bytes"]
@@ -513,6 +553,8 @@ def run_ours(args):
         "cpu_baseline": ({"value": cpu_v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                           "sample": f"{cpu_n} tokens of the decode workload ({cpu_s:.1f} s, single-threaded fp64)"}
                          if cpu_v else None),
+        "cpu_baseline_all_cores": cpu_all,
+        "step_us_distribution": main["step_us"],
         "workloads": extra,
         "peaks": {"hbm_gbs": hbm_peak, "fp8_tflops": fp8_peak, "source": peak_src},
         "setup_s": t_gen,
