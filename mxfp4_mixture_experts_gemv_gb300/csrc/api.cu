@@ -221,11 +221,13 @@ moe_status moe_forward(moe_dims d, const void* hidden, int32_t T, const void* ro
                               static_cast<const uint16_t*>(router_b), T, d.H, d.E, top_k,
                               reinterpret_cast<float*>(at(L.logits)), ids, w, status, s);
     if (e != cudaSuccess) return cuda_fail(e, "router kernel");
+    // the grouping's per-chunk counts live at the start of y, which is written only later
     e = moe::launch_permute(ids, TK, top_k, d.E, L.tile_rows, L.max_tiles, reinterpret_cast<int32_t*>(at(L.counts)),
-                            reinterpret_cast<int32_t*>(at(L.offsets)), sorted_rows, inv_pos, tiles, s);
+                            reinterpret_cast<int32_t*>(at(L.offsets)), sorted_rows, inv_pos, tiles,
+                            reinterpret_cast<int32_t*>(at(L.y)), s);
     if (e != cudaSuccess) return cuda_fail(e, "grouping kernel");
-    e = moe::launch_gather_quant(static_cast<const uint16_t*>(hidden), sorted_rows, tiles, L.max_tiles, top_k, d.H,
-                                 d.I, at(L.xq), at(L.xs), at(L.xp), at(L.xp_sf), at(L.hq_sf), s);
+    e = moe::launch_gather_quant(static_cast<const uint16_t*>(hidden), inv_pos, tiles, L.max_tiles, T, top_k, d.H,
+                                 at(L.xq), at(L.xs), at(L.xp), at(L.xp_sf), s);
     if (e != cudaSuccess) return cuda_fail(e, "gather kernel");
   }
   mark(1);

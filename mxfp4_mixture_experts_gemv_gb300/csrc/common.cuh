@@ -165,12 +165,13 @@ cudaError_t launch_pack(const moe_dims& d, const PackedHeader& h, const moe_mxfp
                         uint8_t* packed, cudaStream_t s);
 cudaError_t launch_router_tc(const uint16_t* x, const uint16_t* wr, const uint16_t* br, int T, int H, int E, int k,
                              float* logits, int32_t* ids, float* w, uint32_t* status, cudaStream_t s);
+// Grouping in two passes over chunks of pairs; `scratch` holds one count per
+// (chunk, expert): ceil(TK / 2048) * E ints.
 cudaError_t launch_permute(const int32_t* ids, int TK, int k, int E, int tile_rows, int max_tiles,
-                           int32_t* counts, int32_t* offsets, int32_t* sorted_rows,
-                           int32_t* inv_pos, int32_t* tiles, cudaStream_t s);
-cudaError_t launch_gather_quant(const uint16_t* x, const int32_t* sorted_rows, const int32_t* tiles, int max_tiles,
-                                int k, int H, int I, uint8_t* xq, uint8_t* xs, uint8_t* xp, uint8_t* xp_sf,
-                                uint8_t* hq_sf, cudaStream_t s);
+                           int32_t* counts, int32_t* offsets, int32_t* sorted_rows, int32_t* inv_pos,
+                           int32_t* tiles, int32_t* scratch, cudaStream_t s);
+cudaError_t launch_gather_quant(const uint16_t* x, const int32_t* inv_pos, const int32_t* tiles, int max_tiles, int T,
+                                int k, int H, uint8_t* xq, uint8_t* xs, uint8_t* xp, uint8_t* xp_sf, cudaStream_t s);
 
 cudaError_t launch_residual_rmsnorm(float* x_res, const uint16_t* layer_out, int T, int H, float eps,
                                     uint16_t* hidden, cudaStream_t s);

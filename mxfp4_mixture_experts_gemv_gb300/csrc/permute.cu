@@ -13,162 +13,189 @@
 namespace moe {
 namespace {
 
-constexpr int kPermThreads = 1024;
+constexpr int kPermThreads = 256;
 constexpr int kPermWarps = kPermThreads / 32;
+constexpr int kPermChunk = 2048;          // pairs per CTA
+constexpr int kPermPerLane = kPermChunk / kPermThreads;  // 8 pairs per thread
 
-__global__ void __launch_bounds__(kPermThreads) permute_kernel(
-    const int32_t* __restrict__ ids, int TK, int E, int tile_rows, int max_tiles, int32_t* __restrict__ counts,
-    int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_rows, int32_t* __restrict__ inv_pos,
-    int32_t* __restrict__ tiles) {
+// Pass 1: expert counts of each CTA's chunk of pairs, to part[blk][E].
+__global__ void __launch_bounds__(kPermThreads) perm_count_kernel(const int32_t* __restrict__ ids, int TK, int E,
+                                                                  int32_t* __restrict__ part) {
+  __shared__ int h[256];
+  for (int e = threadIdx.x; e < E; e += kPermThreads) h[e] = 0;
+  __syncthreads();
+  const int base = blockIdx.x * kPermChunk;
+  int e[kPermPerLane];
+#pragma unroll
+  for (int u = 0; u < kPermPerLane; ++u) {
+    const int i = base + u * kPermThreads + threadIdx.x;
+    // ids come from the top-k kernel and are always in [0, E); the clamp only keeps
+    // shared-memory indexing safe whatever the input
+    e[u] = i < TK ? min(max(ids[i], 0), E - 1) : -1;
+  }
+#pragma unroll
+  for (int u = 0; u < kPermPerLane; ++u)
+    if (e[u] >= 0) atomicAdd(&h[e[u]], 1);
+  __syncthreads();
+  for (int x = threadIdx.x; x < E; x += kPermThreads) part[(int64_t)blockIdx.x * E + x] = h[x];
+}
+
+// Pass 2: every CTA takes the totals and the counts of the CTAs before it, so the
+// first grouped row of (its chunk, expert e) is off[e] + the earlier chunks' count;
+// inside the chunk each warp owns a contiguous run of pairs and ranks them with
+// match/popcount, so every pair's row is its rank among equal experts in
+// ascending flat index.  CTA 0 also writes the counts, offsets and tile list.
+__global__ void __launch_bounds__(kPermThreads) perm_scatter_kernel(
+    const int32_t* __restrict__ ids, int TK, int E, int tile_rows, int max_tiles, const int32_t* __restrict__ part,
+    int nb, int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_rows,
+    int32_t* __restrict__ inv_pos, int32_t* __restrict__ tiles) {
   __shared__ int hist[kPermWarps][257];
-  __shared__ int s_off[258];
-  __shared__ int s_tile_off[258];
+  __shared__ int s_tot[257], s_off[258], s_tile_off[258], s_pre[257];
   extern __shared__ int s_tile_e[];  // [max_tiles]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int blk = blockIdx.x;
+  for (int e = threadIdx.x; e < E; e += kPermThreads) {
+    int tot = 0, pre = 0;
+    for (int b = 0; b < nb; ++b) {
+      const int c = part[(int64_t)b * E + e];
+      tot += c;
+      pre += b < blk ? c : 0;
+    }
+    s_tot[e] = tot;
+    s_pre[e] = pre;
+  }
   for (int i = threadIdx.x; i < kPermWarps * 257; i += kPermThreads) (&hist[0][0])[i] = 0;
   __syncthreads();
-  const int chunk = (TK + kPermWarps - 1) / kPermWarps;
-  const int start = min(TK, warp * chunk), end = min(TK, start + chunk);
-  // ids come from the top-k kernel and are always in [0, E); the clamp only keeps
-  // shared-memory indexing safe whatever the input.  Each lane loads its ids in
-  // batches of kBatch independent loads.
-  constexpr int kBatch = 16;
-  for (int b0 = start; b0 < end; b0 += 32 * kBatch) {
-    int e[kBatch];
+  if (warp == 0) warp_expert_scan(s_tot, E, __ffs(tile_rows) - 1, s_off, s_tile_off, s_tile_e, lane);
+  // this warp's run of pairs: ids in registers
+  const int per_warp = kPermChunk / kPermWarps;  // 256
+  const int start = min(TK, blk * kPermChunk + warp * per_warp), end = min(TK, start + per_warp);
+  int ev[per_warp / 32];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int i = b0 + 32 * u + lane;
-      e[u] = i < end ? min(max(ids[i], 0), E - 1) : -1;
-    }
+  for (int u = 0; u < per_warp / 32; ++u) {
+    const int i = start + 32 * u + lane;
+    ev[u] = i < end ? min(max(ids[i], 0), E - 1) : -1;
+  }
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u)
-      if (e[u] >= 0) atomicAdd(&hist[warp][e[u]], 1);
-  }
+  for (int u = 0; u < per_warp / 32; ++u)
+    if (ev[u] >= 0) atomicAdd(&hist[warp][ev[u]], 1);
   __syncthreads();
-  __shared__ int s_cnt[257];
-  if (threadIdx.x < E) {
-    int c = 0;
-    for (int w = 0; w < kPermWarps; ++w) c += hist[w][threadIdx.x];
-    counts[threadIdx.x] = c;
-    s_cnt[threadIdx.x] = c;
-  }
-  __syncthreads();
-  if (warp == 0) warp_expert_scan(s_cnt, E, __ffs(tile_rows) - 1, s_off, s_tile_off, s_tile_e, lane);
-  __syncthreads();
-  if (threadIdx.x < E) {
-    const int e = threadIdx.x;
-    int run = s_off[e];
+  // hist[w][e] becomes the first grouped row of warp w's pairs of expert e
+  for (int e = threadIdx.x; e < E; e += kPermThreads) {
+    int run = s_off[e] + s_pre[e];
     for (int w = 0; w < kPermWarps; ++w) {
       const int c = hist[w][e];
       hist[w][e] = run;
       run += c;
     }
-    offsets[e] = s_off[e];
-    // tile list entries of expert e
-    const int cnt = s_off[e + 1] - s_off[e];
-    int t = s_tile_off[e];
-    for (int r0 = 0; r0 < cnt && t < max_tiles; r0 += tile_rows, ++t) {
-      int4 td = make_int4(e, s_off[e] + r0, min(tile_rows, cnt - r0), 0);
-      reinterpret_cast<int4*>(tiles + 4)[t] = td;
-    }
   }
-  if (threadIdx.x == 0) {
-    offsets[E] = s_off[E];
-    tiles[0] = min(s_tile_off[E], max_tiles);
+  if (blk == 0) {
+    for (int e = threadIdx.x; e < E; e += kPermThreads) {
+      counts[e] = s_tot[e];
+      offsets[e] = s_off[e];
+      const int cnt = s_tot[e];
+      int t = s_tile_off[e];
+      for (int r0 = 0; r0 < cnt && t < max_tiles; r0 += tile_rows, ++t)
+        reinterpret_cast<int4*>(tiles + 4)[t] = make_int4(e, s_off[e] + r0, min(tile_rows, cnt - r0), 0);
+    }
+    if (threadIdx.x == 0) {
+      offsets[E] = s_off[E];
+      tiles[0] = min(s_tile_off[E], max_tiles);
+    }
   }
   __syncthreads();
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int b0 = start; b0 < end; b0 += 32 * kBatch) {
-    int eb[kBatch];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int i = b0 + 32 * u + lane;
-      eb[u] = i < end ? min(max(ids[i], 0), E - 1) : -1;
+  for (int u = 0; u < per_warp / 32; ++u) {
+    if (start + 32 * u >= end) break;  // warp-uniform
+    const int i = start + 32 * u + lane;
+    const int e = ev[u];
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lt_mask);
+    if (e >= 0) {
+      const int pos = hist[warp][e] + rank;
+      sorted_rows[pos] = i;
+      inv_pos[i] = pos;
     }
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      if (b0 + 32 * u >= end) break;  // warp-uniform
-      const int i = b0 + 32 * u + lane;
-      const int e = eb[u];
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
-      const int rank = __popc(peers & lt_mask);
-      if (e >= 0) {
-        const int pos = hist[warp][e] + rank;
-        sorted_rows[pos] = i;
-        inv_pos[i] = pos;
-      }
-      __syncwarp();
-      if (e >= 0 && rank == 0) hist[warp][e] += __popc(peers);
-      __syncwarp();
-    }
+    __syncwarp();
+    if (e >= 0 && rank == 0) hist[warp][e] += __popc(peers);
+    __syncwarp();
   }
 }
 
-// One CTA per tile: quantise the tile's token rows to MXFP8 straight into grouped
-// order (x -> Xp rows and their scale atoms); the row of a token's first slot also
-// publishes the token's codes (xq, xs).  Atom words of rows past the tile's rows
-// are left as they are: they only feed accumulator columns that are discarded.
-__global__ void __launch_bounds__(512) gather_quant_kernel(const uint16_t* __restrict__ x,
-                                                           const int32_t* __restrict__ sorted_rows,
-                                                           const int32_t* __restrict__ tiles, int k, int H, int I,
-                                                           uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
-                                                           uint8_t* __restrict__ xp, uint8_t* __restrict__ xp_sf,
-                                                           uint8_t* __restrict__ hq_sf) {
+// Quantise-on-gather, one warp per token: the token's row is quantised to MXFP8
+// once and its codes go to each of its k grouped rows, with one scale byte per
+// block in each row's atom word (a row's tile and place in it are found by binary
+// search over the tile list, staged in shared memory).  The token's codes and
+// scales are also published (xq, xs).  Atom words of rows past a tile's rows are
+// left as they are: they only feed accumulator columns that are discarded.
+constexpr int kGatherWarps = 8;
+
+__global__ void __launch_bounds__(32 * kGatherWarps) gather_tok_kernel(
+    const uint16_t* __restrict__ x, const int32_t* __restrict__ inv_pos, const int32_t* __restrict__ tiles,
+    int max_tiles, int T, int k, int H, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs, uint8_t* __restrict__ xp,
+    uint8_t* __restrict__ xp_sf) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int b = blockIdx.x;
-  if (b >= tiles[0]) return;
-  const int4 td = reinterpret_cast<const int4*>(tiles + 4)[b];
-  const int row0 = td.y, rows = td.z;
+  extern __shared__ int2 s_tl[];  // [max_tiles]: {row0, rows}
+  const int n_tiles = min(tiles[0], max_tiles);
+  for (int i = threadIdx.x; i < n_tiles; i += blockDim.x) {
+    const int4 td = reinterpret_cast<const int4*>(tiles + 4)[i];
+    s_tl[i] = make_int2(td.y, td.z);
+  }
+  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nbh = H / 32;
-  const int kth = (H + kTileK - 1) / kTileK;
-  (void)I;
-  (void)hq_sf;
-  __shared__ uint8_t s_scale[16][kRouteSmallMaxH / 32];
-  for (int r = warp; r < rows; r += 16) {
-    const int f = sorted_rows[row0 + r], t = f / k;
-    const bool first = (f % k) == 0;
-    const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)t * H);
-    // up to four blocks per lane per round, every load of the round in flight
-    for (int b0 = 0; b0 < nbh; b0 += 128) {
-      uint4 v[4][4];
+  const int t = blockIdx.x * kGatherWarps + warp;
+  if (t >= T) return;  // whole warp
+  const int nbh = H / 32, kth = (H + kTileK - 1) / kTileK;
+  // lanes j < k: grouped row p of slot j, its tile b and row n in the tile
+  int p = 0, b = 0, n = 0;
+  if (lane < k) {
+    p = inv_pos[(int64_t)t * k + lane];
+    int lo = 0, hi = n_tiles - 1;
+    while (lo < hi) {  // last tile whose first row is <= p (tiles are in row order)
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_tl[mid].x <= p) lo = mid;
+      else hi = mid - 1;
+    }
+    b = lo;
+    n = p - s_tl[lo].x;
+  }
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)t * H);
+  for (int b0 = 0; b0 < nbh; b0 += 128) {
+    uint4 v[4][4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int blk = b0 + 32 * u + lane;
-        if (blk < nbh)
+    for (int u = 0; u < 4; ++u) {
+      const int blk = b0 + 32 * u + lane;
+      if (blk < nbh)
 #pragma unroll
-          for (int q = 0; q < 4; ++q) v[u][q] = __ldg(xr + blk * 4 + q);
+        for (int q = 0; q < 4; ++q) v[u][q] = __ldg(xr + blk * 4 + q);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int blk = b0 + 32 * u + lane;
+      uint4 c[2];
+      uint8_t sc = 0;
+      if (blk < nbh) {
+        sc = quant_block_vals(v[u], c);
+        uint4* q = reinterpret_cast<uint4*>(xq + (int64_t)t * H + blk * 32);
+        q[0] = c[0];
+        q[1] = c[1];
+        xs[(int64_t)t * nbh + blk] = sc;
       }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int blk = b0 + 32 * u + lane;
+      for (int j = 0; j < k; ++j) {
+        const int pj = __shfl_sync(0xffffffffu, p, j), bj = __shfl_sync(0xffffffffu, b, j),
+                  nj = __shfl_sync(0xffffffffu, n, j);
         if (blk < nbh) {
-          uint4 c[2];
-          const uint8_t sc = quant_block_vals(v[u], c);
-          uint4* dst = reinterpret_cast<uint4*>(xp + (int64_t)(row0 + r) * H + blk * 32);
+          uint4* dst = reinterpret_cast<uint4*>(xp + (int64_t)pj * H + blk * 32);
           dst[0] = c[0];
           dst[1] = c[1];
-          s_scale[warp][blk] = sc;
-          if (first) {
-            uint4* q = reinterpret_cast<uint4*>(xq + (int64_t)t * H + blk * 32);
-            q[0] = c[0];
-            q[1] = c[1];
-            xs[(int64_t)t * nbh + blk] = sc;
-          }
+          uint8_t* wd = xp_sf + ((int64_t)bj * kth + (blk >> 2)) * kAtomBytes + (nj & 31) * 16 + (nj >> 5) * 4;
+          wd[blk & 3] = sc;
+          if (blk == nbh - 1)  // the last real block also sets the padding bytes of its word
+            for (int jj = (blk & 3) + 1; jj < 4; ++jj) wd[jj] = 127;
         }
       }
     }
-    __syncwarp();
-    for (int ka = lane; ka < kth; ka += 32) {
-      uint32_t wv = 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int kb = 4 * ka + j;
-        wv |= (uint32_t)(kb < nbh ? s_scale[warp][kb] : 127) << (8 * j);
-      }
-      *reinterpret_cast<uint32_t*>(xp_sf + ((int64_t)b * kth + ka) * kAtomBytes + (r & 31) * 16 + (r >> 5) * 4) = wv;
-    }
-    __syncwarp();
   }
 }
 
@@ -220,17 +247,26 @@ cudaError_t launch_combine(const float* y, const int32_t* inv_pos, const float* 
 
 cudaError_t launch_permute(const int32_t* ids, int TK, int k, int E, int tile_rows, int max_tiles,
                            int32_t* counts, int32_t* offsets, int32_t* sorted_rows, int32_t* inv_pos,
-                           int32_t* tiles, cudaStream_t s) {
+                           int32_t* tiles, int32_t* scratch, cudaStream_t s) {
   (void)k;
-  permute_kernel<<<1, kPermThreads, (size_t)max_tiles * sizeof(int), s>>>(ids, TK, E, tile_rows, max_tiles, counts,
-                                                                           offsets, sorted_rows, inv_pos, tiles);
+  const int nb = (TK + kPermChunk - 1) / kPermChunk;
+  perm_count_kernel<<<nb, kPermThreads, 0, s>>>(ids, TK, E, scratch);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  perm_scatter_kernel<<<nb, kPermThreads, (size_t)max_tiles * sizeof(int), s>>>(
+      ids, TK, E, tile_rows, max_tiles, scratch, nb, counts, offsets, sorted_rows, inv_pos, tiles);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather_quant(const uint16_t* x, const int32_t* sorted_rows, const int32_t* tiles, int max_tiles,
-                                int k, int H, int I, uint8_t* xq, uint8_t* xs, uint8_t* xp, uint8_t* xp_sf,
-                                uint8_t* hq_sf, cudaStream_t s) {
-  gather_quant_kernel<<<max_tiles, 512, 0, s>>>(x, sorted_rows, tiles, k, H, I, xq, xs, xp, xp_sf, hq_sf);
+cudaError_t launch_gather_quant(const uint16_t* x, const int32_t* inv_pos, const int32_t* tiles, int max_tiles, int T,
+                                int k, int H, uint8_t* xq, uint8_t* xs, uint8_t* xp, uint8_t* xp_sf, cudaStream_t s) {
+  const size_t smem = (size_t)max_tiles * sizeof(int2);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(gather_tok_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  gather_tok_kernel<<<(T + kGatherWarps - 1) / kGatherWarps, 32 * kGatherWarps, smem, s>>>(
+      x, inv_pos, tiles, max_tiles, T, k, H, xq, xs, xp, xp_sf);
   return cudaGetLastError();
 }
 
