@@ -102,6 +102,29 @@ __device__ __forceinline__ float ld_dsmem_f32(const void* p, uint32_t cta) {
   return v;
 }
 
+// Address in the shared memory of CTA `cta` of this cluster at the offset that
+// `p` has in this CTA's shared memory.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t cta) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(cta));
+  return r;
+}
+
+// Generic-proxy writes to this CTA's shared memory, before an async-proxy
+// (bulk copy) read of them.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Bulk copy from this CTA's shared memory to the shared memory of a CTA of the
+// cluster (`dst`, `bar`: cluster addresses); completes on that CTA's mbarrier.
+// Addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "r"(smem_u32(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // ----------------------------------------------------------------- TMA / bulk copies
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -25,6 +25,11 @@ SMALL_CASES = {
     "cluster_k8_E200": (ms.LayerShape(T=3, H=128, I=64, E=200, k=8), 11),
     # batched decode (grid routing) with padded contraction tails
     "grid_T12_tails": (ms.LayerShape(T=12, H=288, I=192, E=6, k=3), 12),
+    # tensor-core router split along H (4 and 3 CTAs per token tile), one and two tiles
+    "router_split_T40_H1024": (ms.LayerShape(T=40, H=1024, I=128, E=8, k=2), 13),
+    "router_split_T150_E24": (ms.LayerShape(T=150, H=768, I=64, E=24, k=3), 14),
+    # tensor-core router with more than 128 experts (MMA N = 256), k = 8
+    "router_E200_k8": (ms.LayerShape(T=40, H=256, I=64, E=200, k=8), 15),
 }
 
 
