@@ -173,15 +173,20 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_tok_kernel(
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int blk = b0 + 32 * u + lane;
+      if (b0 + 32 * u >= nbh) break;  // whole warp
       uint4 c[2];
-      uint8_t sc = 0;
+      uint32_t sc = 127u;  // padding blocks past H carry the neutral scale
       if (blk < nbh) {
         sc = quant_block_vals(v[u], c);
         uint4* q = reinterpret_cast<uint4*>(xq + (int64_t)t * H + blk * 32);
         q[0] = c[0];
         q[1] = c[1];
-        xs[(int64_t)t * nbh + blk] = sc;
+        xs[(int64_t)t * nbh + blk] = (uint8_t)sc;
       }
+      // the scales of the four blocks of a 128-element k-tile form one word of the
+      // row's atom entry: lanes 4i..4i+3 hold them, lane 4i stores the word
+      const uint32_t word = sc | (__shfl_down_sync(0xffffffffu, sc, 1) << 8) |
+                            (__shfl_down_sync(0xffffffffu, sc, 2) << 16) | (__shfl_down_sync(0xffffffffu, sc, 3) << 24);
       for (int j = 0; j < k; ++j) {
         const int pj = __shfl_sync(0xffffffffu, p, j), bj = __shfl_sync(0xffffffffu, b, j),
                   nj = __shfl_sync(0xffffffffu, n, j);
@@ -189,10 +194,9 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_tok_kernel(
           uint4* dst = reinterpret_cast<uint4*>(xp + (int64_t)pj * H + blk * 32);
           dst[0] = c[0];
           dst[1] = c[1];
-          uint8_t* wd = xp_sf + ((int64_t)bj * kth + (blk >> 2)) * kAtomBytes + (nj & 31) * 16 + (nj >> 5) * 4;
-          wd[blk & 3] = sc;
-          if (blk == nbh - 1)  // the last real block also sets the padding bytes of its word
-            for (int jj = (blk & 3) + 1; jj < 4; ++jj) wd[jj] = 127;
+          if ((lane & 3) == 0)
+            *reinterpret_cast<uint32_t*>(xp_sf + ((int64_t)bj * kth + (blk >> 2)) * kAtomBytes + (nj & 31) * 16 +
+                                         (nj >> 5) * 4) = word;
         }
       }
     }
