@@ -30,6 +30,12 @@ SMALL_CASES = {
     "router_split_T150_E24": (ms.LayerShape(T=150, H=768, I=64, E=24, k=3), 14),
     # tensor-core router with more than 128 experts (MMA N = 256), k = 8
     "router_E200_k8": (ms.LayerShape(T=40, H=256, I=64, E=200, k=8), 15),
+    # degenerate routing: one expert (every weight is 1), and k = E (every token takes
+    # every expert), on the small-batch, cluster and tensor-core routing paths
+    "single_expert_T20": (ms.LayerShape(T=20, H=128, I=64, E=1, k=1), 16),
+    "single_expert_T40": (ms.LayerShape(T=40, H=256, I=64, E=1, k=1), 17),
+    "k_equals_E_T6": (ms.LayerShape(T=6, H=128, I=64, E=2, k=2), 18),
+    "k_equals_E_T70": (ms.LayerShape(T=70, H=256, I=128, E=2, k=2), 19),
 }
 
 
