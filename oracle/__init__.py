@@ -48,6 +48,12 @@ def lib():
             L.oracle_e4m3_value.argtypes = [ctypes.c_int]
             L.oracle_e4m3_encode.restype = ctypes.c_int
             L.oracle_e4m3_encode.argtypes = [d]
+            L.oracle_e2m1_encode.restype = ctypes.c_int
+            L.oracle_e2m1_encode.argtypes = [d]
+            L.oracle_mxfp4_quantize.restype = None
+            L.oracle_mxfp4_quantize.argtypes = [p, i64, p, p]
+            L.oracle_expert_mlp_fmt.restype = None
+            L.oracle_expert_mlp_fmt.argtypes = [p, p, i64, i64, p, p, p, p, p, p, p, p, p, p, p, i32]
             L.oracle_bf16_value.restype = d
             L.oracle_bf16_value.argtypes = [ctypes.c_uint16]
             L.oracle_bf16_round.restype = ctypes.c_uint16
@@ -67,6 +73,9 @@ def lib():
             L.oracle_moe_forward.restype = None
             L.oracle_moe_forward.argtypes = [p, i64, i64, i64, i64, i32, p, p, p, p, p, p, p, p,
                                              p, p, p, p, p, p, p, p, p]
+            L.oracle_moe_forward_fmt.restype = None
+            L.oracle_moe_forward_fmt.argtypes = [p, i64, i64, i64, i64, i32, p, p, p, p, p, p, p, p,
+                                             p, p, p, p, p, p, p, p, p, i32]
             L.oracle_rmsnorm_bf16.restype = None
             L.oracle_rmsnorm_bf16.argtypes = [p, i64, i64, d, p]
             _lib = L
@@ -111,6 +120,10 @@ def e4m3_encode(v: float) -> int:
     return lib().oracle_e4m3_encode(float(v))
 
 
+def e2m1_encode(v: float) -> int:
+    return lib().oracle_e2m1_encode(float(v))
+
+
 def bf16_value(bits: int) -> float:
     return lib().oracle_bf16_value(bits)
 
@@ -143,6 +156,18 @@ def mxfp8_quantize(v):
     return q, s
 
 
+def mxfp4_quantize(v):
+    """fp64 values (last dim a multiple of 32) -> (e2m1 codes uint8, one per byte; e8m0 scale codes uint8)."""
+    a = _np(v, np.float64)
+    q = np.empty(a.shape, np.uint8)
+    s = np.empty(a.shape[:-1] + (a.shape[-1] // 32,), np.uint8)
+    lib().oracle_mxfp4_quantize(_ptr(a), a.size, _ptr(q), _ptr(s))
+    return q, s
+
+
+_ACT = {"mxfp8": 0, "mxfp4": 1}
+
+
 def route(x, router_w, router_b, k: int):
     """-> (logits fp64 [T,E], ids int32 [T,k], w fp64 [T,k])."""
     xx = _np(x, np.uint16)
@@ -169,8 +194,8 @@ def permute(ids, E: int):
     return cnt, off, sr, inv
 
 
-def expert_mlp(xq, xs, gu_blocks, gu_scales, gu_bias, d_blocks, d_scales, d_bias):
-    """One expert on one quantised row -> dict(g, h, hq, hs, y)."""
+def expert_mlp(xq, xs, gu_blocks, gu_scales, gu_bias, d_blocks, d_scales, d_bias, act_format: str = "mxfp8"):
+    """One expert on one quantised row -> dict(g, h, hq, hs, y); act_format "mxfp8" or "mxfp4"."""
     xq = _np(xq, np.uint8)
     xs = _np(xs, np.uint8)
     gub, gus, gubias = _np(gu_blocks, np.uint8), _np(gu_scales, np.uint8), _np(gu_bias, np.uint16)
@@ -182,15 +207,18 @@ def expert_mlp(xq, xs, gu_blocks, gu_scales, gu_bias, d_blocks, d_scales, d_bias
     hq = np.empty(I, np.uint8)
     hs = np.empty(I // 32, np.uint8)
     y = np.empty(H, np.float64)
-    lib().oracle_expert_mlp(_ptr(xq), _ptr(xs), H, I, _ptr(gub), _ptr(gus), _ptr(gubias),
-                            _ptr(db), _ptr(ds), _ptr(dbias), _ptr(g), _ptr(h), _ptr(hq), _ptr(hs),
-                            _ptr(y))
+    lib().oracle_expert_mlp_fmt(_ptr(xq), _ptr(xs), H, I, _ptr(gub), _ptr(gus), _ptr(gubias),
+                                _ptr(db), _ptr(ds), _ptr(dbias), _ptr(g), _ptr(h), _ptr(hq), _ptr(hs),
+                                _ptr(y), _ACT[act_format])
     return dict(g=g, h=h, hq=hq, hs=hs, y=y)
 
 
 def moe_forward(x, router_w, router_b, gu_blocks, gu_scales, gu_bias, d_blocks, d_scales, d_bias,
-                k: int, intermediates: bool = False):
-    """The whole layer -> dict(out fp64 [T,H], logits, ids, w, xq, xs[, h, hq, hs])."""
+                k: int, intermediates: bool = False, act_format: str = "mxfp8"):
+    """The whole layer -> dict(out fp64 [T,H], logits, ids, w, xq, xs[, h, hq, hs]).
+
+    act_format "mxfp8" (the layer as built) or "mxfp4" (activations x and h
+    quantised to MXFP4, the FP4 x FP4 variant)."""
     xx = _np(x, np.uint16)
     wr, br = _np(router_w, np.uint16), _np(router_b, np.uint16)
     gub, gus, gubias = _np(gu_blocks, np.uint8), _np(gu_scales, np.uint8), _np(gu_bias, np.uint16)
@@ -209,10 +237,10 @@ def moe_forward(x, router_w, router_b, gu_blocks, gu_scales, gu_bias, d_blocks, 
         h = np.empty((T, k, I), np.float64)
         hq = np.empty((T, k, I), np.uint8)
         hs = np.empty((T, k, I // 32), np.uint8)
-    lib().oracle_moe_forward(_ptr(xx), T, H, I, E, k, _ptr(wr), _ptr(br), _ptr(gub), _ptr(gus),
-                             _ptr(gubias), _ptr(db), _ptr(ds), _ptr(dbias), _ptr(out),
-                             _ptr(logits), _ptr(ids), _ptr(w), _ptr(xq), _ptr(xs), _ptr(h),
-                             _ptr(hq), _ptr(hs))
+    lib().oracle_moe_forward_fmt(_ptr(xx), T, H, I, E, k, _ptr(wr), _ptr(br), _ptr(gub), _ptr(gus),
+                                 _ptr(gubias), _ptr(db), _ptr(ds), _ptr(dbias), _ptr(out),
+                                 _ptr(logits), _ptr(ids), _ptr(w), _ptr(xq), _ptr(xs), _ptr(h),
+                                 _ptr(hq), _ptr(hs), _ACT[act_format])
     r = dict(out=out, logits=logits, ids=ids, w=w, xq=xq, xs=xs)
     if intermediates:
         r.update(h=h, hq=hq, hs=hs)

@@ -17,6 +17,10 @@
 //  * "GPT-OSS-120B with MXFP4 on DGX Spark (SM121/GB10)", "What's Included":
 //    the MoE layer is an FP8-activation x FP4-weight grouped GEMM;
 //    "Numerical Accuracy": full-scale (block-scaled) activation quantisation.
+//  * "GPT-OSS-120B with MXFP4 on DGX Spark (SM121/GB10)", "Performance
+//    Optimizations": native FP4 x FP4 block-scaled MMA as the next step, for
+//    which the layer can also quantise its activations to MXFP4 (the
+//    `act_fp4` variant below).
 //  The layer definition the pages leave open (routing rule, SwiGLU, MXFP8
 //  scale rule, nibble order, gate/up row order) follows the readings listed
 //  in the design notes; each function below states the one it uses.
@@ -117,6 +121,40 @@ int mxfp8_block(const double* v, uint8_t* q) {
   return sexp;
 }
 
+// E2M1 encoding: the nearest magnitude of the value set, ties to the even
+// mantissa (code bit 0 clear), magnitudes above 6 saturating to 6.  The sign
+// is kept, so a negative value that rounds to zero gives code 8 (-0).
+int e2m1_encode(double v) {
+  if (std::isnan(v)) return 7;  // never produced by these inputs
+  const int sign = std::signbit(v) ? 8 : 0;
+  const double a = std::fabs(v);
+  if (a >= 6.0) return sign | 7;  // (far out, the distances to 4 and 6 round equal)
+  int best = 0;
+  for (int c = 1; c < 8; ++c) {
+    const double d = std::fabs(a - kE2M1Magnitude[c]), db = std::fabs(a - kE2M1Magnitude[best]);
+    if (d < db || (d == db && (c & 1) == 0)) best = c;
+  }
+  return sign | best;
+}
+
+// MXFP4 quantisation of one 32-element block of activations (reading: the
+// same OCP-MX shared-exponent rule as MXFP8, floor(log2(amax)) - 2, 2 being
+// E2M1's largest exponent; scale code = that exponent + 127).  Codes are one
+// E2M1 code per byte.  Returns the scale exponent.
+int mxfp4_block(const double* v, uint8_t* q) {
+  double amax = 0.0;
+  for (int i = 0; i < 32; ++i) amax = std::max(amax, std::fabs(v[i]));
+  int sexp = -127;
+  if (amax > 0.0) {
+    int ex;
+    std::frexp(amax, &ex);
+    sexp = std::max(ex - 1 - 2, -127);
+    sexp = std::min(sexp, 127);
+  }
+  for (int i = 0; i < 32; ++i) q[i] = static_cast<uint8_t>(e2m1_encode(std::ldexp(v[i], -sexp)));
+  return sexp;
+}
+
 // One MXFP4 weight W[r][c] of a [rows, K] matrix stored as blocks [rows, K/32, 16]
 // and scales [rows, K/32].  Reading: the low nibble of a byte holds the even
 // element of the pair.
@@ -138,6 +176,7 @@ double oracle_e2m1_value(int code) { return e2m1(code & 15); }
 double oracle_e8m0_value(int code) { return e8m0(code & 255); }
 double oracle_e4m3_value(int code) { return e4m3(code & 255); }
 int oracle_e4m3_encode(double v) { return e4m3_encode(v); }
+int oracle_e2m1_encode(double v) { return e2m1_encode(v); }
 double oracle_bf16_value(uint16_t b) { return bf16_to_double(b); }
 uint16_t oracle_bf16_round(double v) { return double_to_bf16(v); }
 double oracle_silu(double z) { return silu(z); }
@@ -152,6 +191,12 @@ void oracle_dequant_mxfp4(const uint8_t* blocks, const uint8_t* scales, int64_t 
 // MXFP8-quantise n values (n a multiple of 32): codes q[n], scale codes s[n/32].
 void oracle_mxfp8_quantize(const double* v, int64_t n, uint8_t* q, uint8_t* s) {
   for (int64_t b = 0; b < n / 32; ++b) s[b] = static_cast<uint8_t>(mxfp8_block(v + 32 * b, q + 32 * b) + 127);
+}
+
+// MXFP4-quantise n values (n a multiple of 32): E2M1 codes q[n] (one per byte),
+// scale codes s[n/32].
+void oracle_mxfp4_quantize(const double* v, int64_t n, uint8_t* q, uint8_t* s) {
+  for (int64_t b = 0; b < n / 32; ++b) s[b] = static_cast<uint8_t>(mxfp4_block(v + 32 * b, q + 32 * b) + 127);
 }
 
 // Router: logits l[t][e] = sum_h x[t][h] * Wr[e][h] + br[e] (bf16 inputs widened
@@ -199,28 +244,35 @@ void oracle_permute(const int32_t* ids, int64_t T, int32_t k, int32_t E, int32_t
   }
 }
 
-// One expert's MLP on one MXFP8-quantised row.
-//   xq, xs : the row's E4M3 codes [H] and E8M0 scale codes [H/32]
+// One expert's MLP on one quantised row; act_fp4 = 0 for MXFP8 activations
+// (E4M3 codes), 1 for MXFP4 activations (E2M1 codes, one per byte) -- both x
+// and the intermediate h use that format.
+//   xq, xs : the row's codes [H] and E8M0 scale codes [H/32]
 //   g      : gate_up pre-activation [2I] = xq . Wgu^T + bgu   (rows [0,I) gate, [I,2I) up)
 //   h      : silu(g[i]) * g[I+i] [I], rounded to fp32 (the precision the kernel
 //            quantises from), then MXFP8-quantised to hq [I] / hs [I/32]
 //   y      : down output [H] = hq . Wd^T + bd
 // Any of g / h / hq / hs may be NULL.
-void oracle_expert_mlp(const uint8_t* xq, const uint8_t* xs, int64_t H, int64_t I,
-                       const uint8_t* gu_blocks, const uint8_t* gu_scales, const uint16_t* gu_bias,
-                       const uint8_t* d_blocks, const uint8_t* d_scales, const uint16_t* d_bias,
-                       double* g_out, double* h_out, uint8_t* hq_out, uint8_t* hs_out, double* y) {
+void oracle_expert_mlp_fmt(const uint8_t* xq, const uint8_t* xs, int64_t H, int64_t I,
+                           const uint8_t* gu_blocks, const uint8_t* gu_scales, const uint16_t* gu_bias,
+                           const uint8_t* d_blocks, const uint8_t* d_scales, const uint16_t* d_bias,
+                           double* g_out, double* h_out, uint8_t* hq_out, uint8_t* hs_out, double* y,
+                           int32_t act_fp4) {
   std::vector<double> xv(H), g(2 * I), h(I), hv(I);
   std::vector<uint8_t> hq(I), hs(I / 32);
-  for (int64_t c = 0; c < H; ++c) xv[c] = e4m3(xq[c]) * e8m0(xs[c / 32]);
+  auto act = [&](uint8_t code) { return act_fp4 ? e2m1(code) : e4m3(code); };
+  for (int64_t c = 0; c < H; ++c) xv[c] = act(xq[c]) * e8m0(xs[c / 32]);
   for (int64_t r = 0; r < 2 * I; ++r) {
     double acc = 0.0;
     for (int64_t c = 0; c < H; ++c) acc += xv[c] * mxfp4_weight(gu_blocks, gu_scales, H, r, c);
     g[r] = acc + bf16_to_double(gu_bias[r]);
   }
   for (int64_t i = 0; i < I; ++i) h[i] = static_cast<double>(static_cast<float>(silu(g[i]) * g[I + i]));
-  oracle_mxfp8_quantize(h.data(), I, hq.data(), hs.data());
-  for (int64_t i = 0; i < I; ++i) hv[i] = e4m3(hq[i]) * e8m0(hs[i / 32]);
+  if (act_fp4)
+    oracle_mxfp4_quantize(h.data(), I, hq.data(), hs.data());
+  else
+    oracle_mxfp8_quantize(h.data(), I, hq.data(), hs.data());
+  for (int64_t i = 0; i < I; ++i) hv[i] = act(hq[i]) * e8m0(hs[i / 32]);
   for (int64_t c = 0; c < H; ++c) {
     double acc = 0.0;
     for (int64_t i = 0; i < I; ++i) acc += hv[i] * mxfp4_weight(d_blocks, d_scales, I, c, i);
@@ -232,6 +284,14 @@ void oracle_expert_mlp(const uint8_t* xq, const uint8_t* xs, int64_t H, int64_t 
   if (hs_out) std::copy(hs.begin(), hs.end(), hs_out);
 }
 
+void oracle_expert_mlp(const uint8_t* xq, const uint8_t* xs, int64_t H, int64_t I,
+                       const uint8_t* gu_blocks, const uint8_t* gu_scales, const uint16_t* gu_bias,
+                       const uint8_t* d_blocks, const uint8_t* d_scales, const uint16_t* d_bias,
+                       double* g_out, double* h_out, uint8_t* hq_out, uint8_t* hs_out, double* y) {
+  oracle_expert_mlp_fmt(xq, xs, H, I, gu_blocks, gu_scales, gu_bias, d_blocks, d_scales, d_bias, g_out, h_out,
+                        hq_out, hs_out, y, 0);
+}
+
 // The whole layer for T tokens.
 //   x [T,H] bf16; router_w [E,H] bf16; router_b [E] bf16
 //   expert weights in the checkpoint layout, all E experts:
@@ -240,13 +300,14 @@ void oracle_expert_mlp(const uint8_t* xq, const uint8_t* xs, int64_t H, int64_t 
 //   out [T,H] fp64: sum_j w[t][j] * y(t, ids[t][j]), accumulated in slot order.
 //   Optional (may be NULL): logits [T,E], ids [T,k], w [T,k], xq [T,H], xs [T,H/32],
 //   and the intermediate of every (token, slot): h [T,k,I], hq [T,k,I], hs [T,k,I/32].
-void oracle_moe_forward(const uint16_t* x, int64_t T, int64_t H, int64_t I, int64_t E, int32_t k,
-                        const uint16_t* router_w, const uint16_t* router_b,
-                        const uint8_t* gu_blocks, const uint8_t* gu_scales, const uint16_t* gu_bias,
-                        const uint8_t* d_blocks, const uint8_t* d_scales, const uint16_t* d_bias,
-                        double* out, double* logits_out, int32_t* ids_out, double* w_out,
-                        uint8_t* xq_out, uint8_t* xs_out, double* h_out, uint8_t* hq_out,
-                        uint8_t* hs_out) {
+//   act_fp4 selects MXFP4 instead of MXFP8 for the activations (x and h).
+void oracle_moe_forward_fmt(const uint16_t* x, int64_t T, int64_t H, int64_t I, int64_t E, int32_t k,
+                            const uint16_t* router_w, const uint16_t* router_b,
+                            const uint8_t* gu_blocks, const uint8_t* gu_scales, const uint16_t* gu_bias,
+                            const uint8_t* d_blocks, const uint8_t* d_scales, const uint16_t* d_bias,
+                            double* out, double* logits_out, int32_t* ids_out, double* w_out,
+                            uint8_t* xq_out, uint8_t* xs_out, double* h_out, uint8_t* hq_out,
+                            uint8_t* hs_out, int32_t act_fp4) {
   std::vector<double> logits(T * E), w(T * k), xrow(H), y(H);
   std::vector<int32_t> ids(T * k);
   std::vector<uint8_t> xq(H), xs(H / 32);
@@ -254,25 +315,39 @@ void oracle_moe_forward(const uint16_t* x, int64_t T, int64_t H, int64_t I, int6
   const int64_t gu_rows = 2 * I, nbh = H / 32, nbi = I / 32;
   for (int64_t t = 0; t < T; ++t) {
     for (int64_t c = 0; c < H; ++c) xrow[c] = bf16_to_double(x[t * H + c]);
-    oracle_mxfp8_quantize(xrow.data(), H, xq.data(), xs.data());
+    if (act_fp4)
+      oracle_mxfp4_quantize(xrow.data(), H, xq.data(), xs.data());
+    else
+      oracle_mxfp8_quantize(xrow.data(), H, xq.data(), xs.data());
     if (xq_out) std::copy(xq.begin(), xq.end(), xq_out + t * H);
     if (xs_out) std::copy(xs.begin(), xs.end(), xs_out + t * nbh);
     for (int64_t c = 0; c < H; ++c) out[t * H + c] = 0.0;
     for (int32_t j = 0; j < k; ++j) {
       const int64_t e = ids[t * k + j];
       const int64_t tj = t * k + j;
-      oracle_expert_mlp(xq.data(), xs.data(), H, I,
-                        gu_blocks + e * gu_rows * nbh * 16, gu_scales + e * gu_rows * nbh,
-                        gu_bias + e * gu_rows,
-                        d_blocks + e * H * nbi * 16, d_scales + e * H * nbi, d_bias + e * H,
-                        nullptr, h_out ? h_out + tj * I : nullptr, hq_out ? hq_out + tj * I : nullptr,
-                        hs_out ? hs_out + tj * nbi : nullptr, y.data());
+      oracle_expert_mlp_fmt(xq.data(), xs.data(), H, I,
+                            gu_blocks + e * gu_rows * nbh * 16, gu_scales + e * gu_rows * nbh,
+                            gu_bias + e * gu_rows,
+                            d_blocks + e * H * nbi * 16, d_scales + e * H * nbi, d_bias + e * H,
+                            nullptr, h_out ? h_out + tj * I : nullptr, hq_out ? hq_out + tj * I : nullptr,
+                            hs_out ? hs_out + tj * nbi : nullptr, y.data(), act_fp4);
       for (int64_t c = 0; c < H; ++c) out[t * H + c] += w[t * k + j] * y[c];
     }
   }
   if (logits_out) std::copy(logits.begin(), logits.end(), logits_out);
   if (ids_out) std::copy(ids.begin(), ids.end(), ids_out);
   if (w_out) std::copy(w.begin(), w.end(), w_out);
+}
+
+void oracle_moe_forward(const uint16_t* x, int64_t T, int64_t H, int64_t I, int64_t E, int32_t k,
+                        const uint16_t* router_w, const uint16_t* router_b,
+                        const uint8_t* gu_blocks, const uint8_t* gu_scales, const uint16_t* gu_bias,
+                        const uint8_t* d_blocks, const uint8_t* d_scales, const uint16_t* d_bias,
+                        double* out, double* logits_out, int32_t* ids_out, double* w_out,
+                        uint8_t* xq_out, uint8_t* xs_out, double* h_out, uint8_t* hq_out,
+                        uint8_t* hs_out) {
+  oracle_moe_forward_fmt(x, T, H, I, E, k, router_w, router_b, gu_blocks, gu_scales, gu_bias, d_blocks, d_scales,
+                         d_bias, out, logits_out, ids_out, w_out, xq_out, xs_out, h_out, hq_out, hs_out, 0);
 }
 
 // RMSNorm with unit gain: x / sqrt(mean(x^2) + eps), rounded to bf16 (RNE).

@@ -165,6 +165,114 @@ def test_mxfp8_elements_match_torch_cast_and_are_idempotent():
     np.testing.assert_array_equal(s2, s)
 
 
+# --- MXFP4 activations (the FP4 x FP4 variant) ----------------------------------------------
+def test_e2m1_encode_round_trips_the_page_value_set():
+    for code, value in _golden("e2m1_values.txt"):
+        assert oracle.e2m1_encode(value) == code
+
+
+def test_e2m1_encode_midpoints_tie_to_even_mantissa_and_saturate():
+    # midpoints between neighbouring magnitudes go to the code whose mantissa bit
+    # (bit 0) is clear: 0 (0), 1.0 (2), 2.0 (4), 4.0 (6)
+    for v, code in [(0.25, 0), (0.75, 2), (1.25, 2), (1.75, 4), (2.5, 4), (3.5, 6), (5.0, 6)]:
+        assert oracle.e2m1_encode(v) == code, v
+        assert oracle.e2m1_encode(-v) == code | 8, -v
+    # just off a midpoint: the nearer magnitude
+    for v, code in [(0.26, 1), (0.74, 1), (1.26, 3), (2.51, 5), (5.01, 7), (4.99, 6)]:
+        assert oracle.e2m1_encode(v) == code, v
+    # beyond the largest magnitude: saturate to 6; a tiny negative keeps its sign
+    for v in (6.0, 6.5, 7.99, 1e30, math.inf):
+        assert oracle.e2m1_encode(v) == 7 and oracle.e2m1_encode(-v) == 15
+    assert oracle.e2m1_encode(-1e-30) == 8
+
+
+def test_e2m1_encode_is_the_nearest_page_value_off_midpoints():
+    mags = np.array(sorted({abs(v) for _, v in _golden("e2m1_values.txt")}))
+    codes = {abs(v): c for c, v in _golden("e2m1_values.txt") if c < 8}
+    rng = np.random.default_rng(11)
+    v = rng.uniform(-7.5, 7.5, 4000)
+    mids = (mags[1:] + mags[:-1]) / 2
+    v = v[np.abs(np.abs(v)[:, None] - mids[None, :]).min(axis=1) > 1e-6]
+    for x in v:
+        m = mags[np.abs(mags - min(abs(x), 6.0)).argmin()]
+        assert oracle.e2m1_encode(x) == codes[m] | (8 if x < 0 else 0), x
+
+
+def _mx4_values(q, s):
+    e2 = np.array([oracle.e2m1_value(c) for c in range(16)])
+    return e2[q] * np.ldexp(1.0, s.astype(np.int64) - 127).repeat(32, axis=-1)
+
+
+def test_mxfp4_hand_examples():
+    # amax 6 = 1.5 * 2^2 -> shared exponent 2 - 2 = 0 (code 127); 6 -> code 7, -1.5 -> 11
+    v = np.zeros(32)
+    v[0], v[1] = 6.0, -1.5
+    q, s = oracle.mxfp4_quantize(v)
+    assert s[0] == 127 and q[0] == 7 and q[1] == 11 and (q[2:] == 0).all()
+    # amax 12 -> exponent 3 - 2 = 1 (code 128): 12 / 2 = 6 -> 7; 5 / 2 = 2.5 ties to 2.0 -> 4
+    v[0], v[1] = 12.0, 5.0
+    q, s = oracle.mxfp4_quantize(v)
+    assert s[0] == 128 and q[0] == 7 and q[1] == 4
+    # amax 0.75 -> exponent -1 - 2 = -3 (code 124): 0.75 * 8 = 6 -> 7
+    q, s = oracle.mxfp4_quantize(np.full(32, 0.75))
+    assert s[0] == 124 and (q == 7).all()
+    # amax 7 -> exponent 0: 7 exceeds 6 and saturates (the clamp case)
+    q, s = oracle.mxfp4_quantize(np.full(32, 7.0))
+    assert s[0] == 127 and (q == 7).all()
+    # all-zero block -> smallest scale code, zero codes
+    q, s = oracle.mxfp4_quantize(np.zeros(32))
+    assert s[0] == 0 and (q == 0).all()
+
+
+def test_mxfp4_block_lands_in_the_top_binade_and_is_idempotent():
+    rng = np.random.default_rng(12)
+    v = rng.standard_normal((64, 32)) * np.exp(rng.uniform(-6, 6, (64, 1)))
+    q, s = oracle.mxfp4_quantize(v)
+    scale = np.ldexp(1.0, s.astype(np.int64) - 127)
+    amax = np.abs(v).max(axis=1)
+    assert ((amax / scale[:, 0] >= 4) & (amax / scale[:, 0] < 8)).all()
+    # so the block's largest code is 4 or 6
+    top = np.abs(_mx4_values(q, s) / scale.repeat(32, axis=1)).max(axis=1)
+    assert set(np.unique(top)) <= {4.0, 6.0}
+    q2, s2 = oracle.mxfp4_quantize(_mx4_values(q, s))
+    np.testing.assert_array_equal(q2, q)
+    np.testing.assert_array_equal(s2, s)
+
+
+def test_fp4_activation_layer_matches_dequantised_dense_path():
+    """The layer with x and h quantised to MXFP4, against numpy matmuls on the
+    pinned dequantiser, the pinned MXFP4 quantiser and the pinned router."""
+    rng = np.random.default_rng(13)
+    T, H, I, E, k = 5, 64, 64, 4, 2
+    x, wr, br = _tiny_router(T, H, E, seed=14)
+    ex = [_rand_expert(H, I, rng) for _ in range(E)]
+    gub, gus, gubias, db, ds, dbias = (np.stack([e[i] for e in ex]) for i in range(6))
+    r = oracle.moe_forward(x, wr, br, gub, gus, gubias, db, ds, dbias, k=k, intermediates=True,
+                           act_format="mxfp4")
+    _, ids, w = oracle.route(x, wr, br, k)
+    np.testing.assert_array_equal(r["ids"], ids)
+    xq, xs = oracle.mxfp4_quantize(_widen(x))
+    np.testing.assert_array_equal(r["xq"], xq)
+    np.testing.assert_array_equal(r["xs"], xs)
+    out = np.zeros((T, H))
+    for t in range(T):
+        for j in range(k):
+            e = ids[t, j]
+            g = oracle.dequant_mxfp4(gub[e], gus[e]) @ _mx4_values(xq[t], xs[t]) + _widen(gubias[e])
+            h = (g[:I] * scipy.special.expit(g[:I]) * g[I:]).astype(np.float32).astype(np.float64)
+            np.testing.assert_allclose(r["h"][t, j], h, rtol=1e-6, atol=1e-30)
+            hq, hs = oracle.mxfp4_quantize(r["h"][t, j])
+            np.testing.assert_array_equal(r["hq"][t, j], hq)
+            y = oracle.dequant_mxfp4(db[e], ds[e]) @ _mx4_values(hq, hs) + _widen(dbias[e])
+            out[t] += w[t, j] * y
+    np.testing.assert_allclose(r["out"], out, rtol=1e-12, atol=1e-12 * np.abs(out).max())
+    # and the MXFP8 layer is unchanged by the format switch
+    r8 = oracle.moe_forward(x, wr, br, gub, gus, gubias, db, ds, dbias, k=k)
+    r8b = oracle.moe_forward(x, wr, br, gub, gus, gubias, db, ds, dbias, k=k, act_format="mxfp8")
+    np.testing.assert_array_equal(r8["out"], r8b["out"])
+    assert np.abs(r8["out"] - r["out"]).max() > 0
+
+
 # --- routing -------------------------------------------------------------------------------
 def _tiny_router(T=16, H=64, E=8, seed=5):
     rng = np.random.default_rng(seed)
