@@ -28,7 +28,7 @@
  *    never allocates or frees device memory and keeps no pointer after return.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
  *    enqueued asynchronously; no entry point synchronises the host except
- *    moe_get_device_status.
+ *    moe_get_device_status, moe_static_scratch_status and moe_profile_end.
  *  - Argument errors are detected on the host before anything is enqueued and
  *    return a non-zero moe_status; moe_last_error() gives the message.
  *  - bf16 values are passed as uint16_t bit patterns.
@@ -108,13 +108,17 @@ typedef struct {
 } moe_workspace_layout;
 
 /* Bytes of the packed (repacked) weight buffer for these dims; 0 if the
- * dims are unsupported. */
+ * dims are unsupported.  (The packed form has no counterpart on the pages; it
+ * holds the tensors of "MXFP4 Tensor Structure" rearranged, see below.) */
 size_t moe_packed_size(moe_dims d);
 
 /*
- * Repack checkpoint-layout MXFP4 expert weights into the layout the forward
- * kernels stream: rows padded along the contraction axis to a multiple of
- * 128 elements, gate and up rows interleaved per 128-row tile, E8M0 scales
+ * Repack checkpoint-layout MXFP4 expert weights ("GPT-OSS-120B on DGX Spark:
+ * From MXFP4 to NVFP4", section "MXFP4 Tensor Structure": *_blocks
+ * [E, out, in/32, 16] packed E2M1, *_scales [E, out, in/32] E8M0, *_bias bf16)
+ * into the layout the forward kernels stream: rows padded along the
+ * contraction axis to a multiple of 128 elements, gate and up rows interleaved
+ * per 128-row tile, E8M0 scales
  * rearranged into the tensor-core scale-factor atoms, biases widened to fp32.
  * The source tensors are only read.  `packed` (device, 256-byte aligned,
  * >= moe_packed_size(d) bytes) is fully written, header included.
@@ -123,7 +127,10 @@ size_t moe_packed_size(moe_dims d);
 moe_status moe_pack_weights(moe_dims d, const moe_mxfp4_weights *src, void *packed,
                             size_t packed_bytes, void *stream);
 
-/* Workspace bytes moe_forward needs for up to T tokens with top_k. */
+/* Workspace bytes moe_forward needs for up to T tokens with top_k (0 for
+ * unsupported dims or arguments).  The workspace has no counterpart on the
+ * pages: it holds this library's intermediates (logits, grouping, quantised
+ * activations, the expert outputs before the combine). */
 size_t moe_workspace_size(moe_dims d, int32_t T, int32_t top_k);
 
 /* Offsets of the intermediates for T tokens (same layout moe_forward uses). */
@@ -131,7 +138,13 @@ moe_status moe_workspace_layout_get(moe_dims d, int32_t T, int32_t top_k,
                                     moe_workspace_layout *out);
 
 /*
- * One MoE layer forward for T tokens.
+ * One MoE layer forward for T tokens: the layer defined at the top of this
+ * file.  Passages: "GPT-OSS-120B on DGX Spark: From MXFP4 to NVFP4", section
+ * "GPT-OSS-120B Architecture" (128 experts, top-4 routing, hidden 2880, router
+ * weights in BF16) and section "MXFP4 Tensor Structure" (E2M1 values, E8M0
+ * scales with bias 127); "GPT-OSS-120B with MXFP4 on DGX Spark (SM121/GB10)",
+ * section "What's Included" (the MoE layer as an FP8 x FP4 grouped GEMM) and
+ * section "Numerical Accuracy" (full-scale block activation quantisation).
  *   hidden    bf16 [T, H]            (16-byte aligned)
  *   router_w  bf16 [E, H]            (16-byte aligned)
  *   router_b  bf16 [E]
@@ -176,13 +189,60 @@ moe_status moe_forward_static_scratch(moe_dims d, const void *hidden, int32_t T,
                                       const void *router_b, const void *packed, int32_t top_k, void *out,
                                       void *stream);
 
-/* Synchronise `stream`, then read the workspace status words: MOE_OK, or
- * MOE_ERR_TIMEOUT if a kernel of the last forward gave up on a wait. */
+/* Failure detection (no counterpart on the pages).  Synchronise `stream`, then
+ * read the workspace status words: MOE_OK, or MOE_ERR_TIMEOUT if a kernel of
+ * the last forward that used `workspace` gave up on a bounded wait (its output
+ * is then not valid).  `workspace` is the device workspace passed to that
+ * forward; NULL is MOE_ERR_INVALID_ARG.  Takes a workspace, unlike a global
+ * status query, because concurrent forwards on different workspaces report
+ * separately. */
 moe_status moe_get_device_status(const void *workspace, void *stream);
+
+/* The same for the allocation-free entry point: synchronise `stream`, then read
+ * the status words at the start of the library's static scratch array on the
+ * current device (the last moe_forward_static_scratch call on it). */
+moe_status moe_static_scratch_status(void *stream);
+
+/* Size of the static scratch array (MOE_STATIC_SCRATCH_BYTES of the library as
+ * built), for callers that load the library without this header. */
+size_t moe_static_scratch_bytes(void);
+
+/*
+ * Failure detection (no counterpart on the pages): the limit, in nanoseconds,
+ * of every bounded device-side wait (pipeline barriers, the expert kernel's
+ * dependency counters, the small-batch routing grid's barrier) in kernels
+ * launched after the call.  0 restores the default of 2 s; other values must lie
+ * in [1 us, 60 s], else MOE_ERR_INVALID_ARG.  A healthy wait lasts microseconds,
+ * so a limit of a millisecond or more never fires in a correct run.  Process-wide;
+ * forwards already enqueued (or captured in a graph) keep the limit they were
+ * launched with.
+ */
+moe_status moe_set_wait_limit_ns(uint64_t ns);
+uint64_t moe_get_wait_limit_ns(void);
+
+/*
+ * Test hook for failure detection (no counterpart on the pages).  `which` is a
+ * mask of the waits that later forwards make unreachable, so that they always
+ * expire:
+ *   MOE_DEBUG_HOLD_DOWN_UNITS       the expert kernel's down units wait for one
+ *                                   more gate_up completion than exists;
+ *   MOE_DEBUG_HOLD_ROUTING_BARRIER  the small-batch routing grid (8 < T <= 32)
+ *                                   waits at its grid barrier for one more CTA
+ *                                   than it has.
+ * Such a forward reports MOE_ERR_TIMEOUT through moe_get_device_status after a
+ * few wait limits (pair the hook with a short moe_set_wait_limit_ns), its output
+ * is not valid, and the device stays usable.  0 restores normal forwards.
+ * Process-wide.
+ */
+#define MOE_DEBUG_HOLD_DOWN_UNITS 1
+#define MOE_DEBUG_HOLD_ROUTING_BARRIER 2
+moe_status moe_debug_hold_waits(int32_t which);
 
 /*
  * Residual stream of a stack of MoE layers, x <- x + moe(rmsnorm(x)) (the
- * stacked-layer workload; RMSNorm with unit gain): if layer_out (bf16 [T, H],
+ * stacked-layer workload; RMSNorm with unit gain; 36 MoE layers per model,
+ * "GPT-OSS-120B on DGX Spark: From MXFP4 to NVFP4", section "GPT-OSS-120B
+ * Architecture", which names the layernorms without their form): if layer_out (bf16 [T, H],
  * the previous layer's moe_forward output) is not NULL, x_res (fp32 [T, H]) +=
  * layer_out; then hidden (bf16 [T, H]) = bf16(x_res / sqrt(mean(x_res^2) + eps))
  * per token, ready to be the next layer's input.  H a multiple of 4.
@@ -191,7 +251,8 @@ moe_status moe_residual_rmsnorm(float *x_res, const void *layer_out, int32_t T, 
                                 void *hidden, void *stream);
 
 /*
- * Optional per-stage timing of moe_forward with CUDA events (host-side event
+ * Optional per-stage timing of moe_forward with CUDA events (measurement; no
+ * counterpart on the pages) (host-side event
  * objects only; no device memory).  moe_profile_begin(n) arms event recording
  * for the next n forward calls (three events each: start, expert-kernel start,
  * end; inside a stream capture they become timestamping graph nodes);

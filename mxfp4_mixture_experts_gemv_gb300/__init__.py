@@ -25,8 +25,9 @@ STATUS_NAMES = {
 
 # Every symbol the C ABI exports (include/moe.h).
 EXPORTED = ["moe_packed_size", "moe_pack_weights", "moe_workspace_size", "moe_workspace_layout_get",
-            "moe_forward", "moe_forward_static_scratch", "moe_get_device_status", "moe_profile_begin",
-            "moe_profile_end", "moe_residual_rmsnorm",
+            "moe_forward", "moe_forward_static_scratch", "moe_static_scratch_status", "moe_static_scratch_bytes",
+            "moe_get_device_status", "moe_set_wait_limit_ns", "moe_get_wait_limit_ns",
+            "moe_debug_hold_waits", "moe_profile_begin", "moe_profile_end", "moe_residual_rmsnorm",
             "moe_last_error", "moe_version"]
 STAGES = ["routing", "expert_mlp"]
 
@@ -77,8 +78,18 @@ def lib() -> ctypes.CDLL:
         L.moe_forward.argtypes = [Dims, vp, i32, vp, vp, vp, i32, vp, vp, sz, vp]
         L.moe_forward_static_scratch.restype = st
         L.moe_forward_static_scratch.argtypes = [Dims, vp, i32, vp, vp, vp, i32, vp, vp]
+        L.moe_static_scratch_status.restype = st
+        L.moe_static_scratch_status.argtypes = [vp]
+        L.moe_static_scratch_bytes.restype = sz
+        L.moe_static_scratch_bytes.argtypes = []
         L.moe_get_device_status.restype = st
         L.moe_get_device_status.argtypes = [vp, vp]
+        L.moe_set_wait_limit_ns.restype = st
+        L.moe_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        L.moe_get_wait_limit_ns.restype = ctypes.c_uint64
+        L.moe_get_wait_limit_ns.argtypes = []
+        L.moe_debug_hold_waits.restype = st
+        L.moe_debug_hold_waits.argtypes = [i32]
         L.moe_residual_rmsnorm.restype = st
         L.moe_residual_rmsnorm.argtypes = [vp, vp, i32, i32, ctypes.c_float, vp, vp]
         L.moe_profile_begin.restype = st
@@ -186,7 +197,9 @@ def forward(dims: LayerDims, hidden: torch.Tensor, router_w: torch.Tensor, route
     return out
 
 
-STATIC_SCRATCH_BYTES = 8 << 20
+def static_scratch_bytes() -> int:
+    """Size of the library's static scratch array (MOE_STATIC_SCRATCH_BYTES as built)."""
+    return lib().moe_static_scratch_bytes()
 
 
 def forward_static_scratch(dims: LayerDims, hidden: torch.Tensor, router_w: torch.Tensor,
@@ -229,6 +242,30 @@ def profile_end() -> tuple[dict, int]:
 def device_status(workspace: torch.Tensor, stream=None) -> int:
     """Synchronise and return the status of the last forward that used ``workspace``."""
     return lib().moe_get_device_status(_dev_ptr(workspace, "workspace"), _stream(stream))
+
+
+def static_scratch_status(stream=None) -> int:
+    """Synchronise and return the status of the last allocation-free forward on this device."""
+    return lib().moe_static_scratch_status(_stream(stream))
+
+
+def set_wait_limit_ns(ns: int):
+    """Limit of every bounded device-side wait in later launches (0 = the 2 s default)."""
+    _check(lib().moe_set_wait_limit_ns(ns))
+
+
+def wait_limit_ns() -> int:
+    return lib().moe_get_wait_limit_ns()
+
+
+HOLD_DOWN_UNITS = 1
+HOLD_ROUTING_BARRIER = 2
+
+
+def debug_hold_waits(which: int):
+    """Failure-detection test hook: make the masked waits of later forwards unreachable
+    (HOLD_DOWN_UNITS, HOLD_ROUTING_BARRIER); 0 restores normal forwards."""
+    _check(lib().moe_debug_hold_waits(which))
 
 
 def view(workspace: torch.Tensor, offset: int, shape, dtype) -> torch.Tensor:

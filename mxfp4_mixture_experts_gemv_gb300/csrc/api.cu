@@ -1,6 +1,7 @@
 // C ABI of the MXFP4 MoE layer: argument validation, workspace carving and the
 // launch sequence  router -> top-k/quant -> grouping -> gather -> gate_up GEMM
 // -> down GEMM -> combine, all on the caller's stream.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -40,6 +41,9 @@ moe_status check_dims(const moe_dims& d) {
 
 constexpr int kStages = 2;  // routing (all routing kernels), expert MLP
 
+std::atomic<uint64_t> g_wait_limit_ns{moe::kWaitLimitNsDefault};
+std::atomic<int> g_hold_waits{0};
+
 // Per-stage CUDA events of profiled forward calls.
 struct Profiler {
   bool armed = false;
@@ -71,6 +75,36 @@ moe_status report_error(moe_status st, const char* fmt, ...) {
   va_end(ap);
   g_last_error = buf;
   return st;
+}
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+int debug_hold_waits() { return g_hold_waits.load(std::memory_order_relaxed); }
+
+moe_status check_forward_args(const moe_dims& d, const void* hidden, int32_t T, const void* router_w,
+                              const void* router_b, const void* packed, int32_t top_k, const void* out) {
+  moe_status st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T=%d < 0", T);
+  if (top_k < 1 || top_k > 8 || top_k > d.E) return fail(MOE_ERR_INVALID_ARG, "top_k=%d outside [1, min(E, 8)]", top_k);
+  if (T == 0) return MOE_OK;
+  if ((int64_t)T * top_k * (int64_t)(d.H > d.I ? d.H : d.I) >= (int64_t)1 << 31)
+    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "T*top_k*max(H,I) must stay below 2^31");
+  if (!hidden || !router_w || !router_b || !packed || !out) return fail(MOE_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(hidden, 16) || !aligned(router_w, 16) || !aligned(out, 16))
+    return fail(MOE_ERR_ALIGNMENT, "hidden, router_w and out must be 16-byte aligned");
+  if (!aligned(packed, 256)) return fail(MOE_ERR_ALIGNMENT, "packed must be 256-byte aligned");
+  return MOE_OK;
+}
+
+moe_status read_status_words(const void* status_words, void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  uint32_t st[4] = {0, 0, 0, 0};
+  e = cudaMemcpy(st, status_words, sizeof(st), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (st[0] != 0)
+    return fail(MOE_ERR_TIMEOUT, "device wait expired (status bits 0x%x, first expired wait 0x%08x)", st[0], st[1]);
+  return MOE_OK;
 }
 }  // namespace moe
 
@@ -125,19 +159,10 @@ moe_status moe_workspace_layout_get(moe_dims d, int32_t T, int32_t top_k, moe_wo
 moe_status moe_forward(moe_dims d, const void* hidden, int32_t T, const void* router_w, const void* router_b,
                        const void* packed, int32_t top_k, void* out, void* workspace, size_t workspace_bytes,
                        void* stream) {
-  moe_status st = check_dims(d);
-  if (st != MOE_OK) return st;
-  if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T=%d < 0", T);
-  if (top_k < 1 || top_k > 8 || top_k > d.E) return fail(MOE_ERR_INVALID_ARG, "top_k=%d outside [1, min(E, 8)]", top_k);
-  if (T == 0) return MOE_OK;
-  if ((int64_t)T * top_k * (int64_t)(d.H > d.I ? d.H : d.I) >= (int64_t)1 << 31)
-    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "T*top_k*max(H,I) must stay below 2^31");
-  if (!hidden || !router_w || !router_b || !packed || !out || !workspace)
-    return fail(MOE_ERR_INVALID_ARG, "null pointer argument");
-  if (!aligned(hidden, 16) || !aligned(router_w, 16) || !aligned(out, 16))
-    return fail(MOE_ERR_ALIGNMENT, "hidden, router_w and out must be 16-byte aligned");
-  if (!aligned(packed, 256) || !aligned(workspace, 256))
-    return fail(MOE_ERR_ALIGNMENT, "packed and workspace must be 256-byte aligned");
+  moe_status st = moe::check_forward_args(d, hidden, T, router_w, router_b, packed, top_k, out);
+  if (st != MOE_OK || T == 0) return st;
+  if (!workspace) return fail(MOE_ERR_INVALID_ARG, "null workspace");
+  if (!aligned(workspace, 256)) return fail(MOE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
   moe_workspace_layout L;
   moe::workspace_layout(d, T, top_k, &L);
   if (workspace_bytes < L.total)
@@ -310,13 +335,23 @@ moe_status moe_profile_end(double* stage_ms, int32_t* calls) {
 
 moe_status moe_get_device_status(const void* workspace, void* stream) {
   if (!workspace) return fail(MOE_ERR_INVALID_ARG, "null workspace");
-  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
-  uint32_t st[4] = {0, 0, 0, 0};
-  e = cudaMemcpy(st, workspace, sizeof(st), cudaMemcpyDeviceToHost);
-  if (e != cudaSuccess) return cuda_fail(e, "status read");
-  if (st[0] != 0)
-    return fail(MOE_ERR_TIMEOUT, "device wait expired (status bits 0x%x, first expired wait 0x%08x)", st[0], st[1]);
+  return moe::read_status_words(workspace, stream);
+}
+
+moe_status moe_set_wait_limit_ns(uint64_t ns) {
+  if (ns == 0) ns = moe::kWaitLimitNsDefault;
+  if (ns < 1000ull || ns > 60000000000ull)
+    return fail(MOE_ERR_INVALID_ARG, "wait limit %llu ns outside [1 us, 60 s]", (unsigned long long)ns);
+  g_wait_limit_ns.store(ns, std::memory_order_relaxed);
+  return MOE_OK;
+}
+
+uint64_t moe_get_wait_limit_ns(void) { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
+moe_status moe_debug_hold_waits(int32_t which) {
+  if (which & ~(MOE_DEBUG_HOLD_DOWN_UNITS | MOE_DEBUG_HOLD_ROUTING_BARRIER))
+    return fail(MOE_ERR_INVALID_ARG, "unknown wait mask 0x%x", which);
+  g_hold_waits.store(which, std::memory_order_relaxed);
   return MOE_OK;
 }
 

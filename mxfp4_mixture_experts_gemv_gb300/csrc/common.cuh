@@ -151,11 +151,27 @@ enum : uint32_t {
   kStatusTimeoutMma = 1u << 1,
   kStatusTimeoutEpilogue = 1u << 2,
   kStatusTimeoutDrain = 1u << 3,
+  kStatusTimeoutRouting = 1u << 4,  // the small-batch routing grid's barrier
 };
 
-// Bounded waits give up after this many nanoseconds (a healthy wait lasts
-// microseconds).
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Bounded waits give up after this many nanoseconds unless the host sets
+// another limit (a healthy wait lasts microseconds).
+constexpr uint64_t kWaitLimitNsDefault = 2000000000ull;
+// Drains (waiting for copies and MMAs already issued, which always complete)
+// are bounded separately.
+constexpr uint64_t kDrainLimitNs = 200000000ull;
+
+// The limit every kernel launched from now on passes to its bounded waits
+// (moe_set_wait_limit_ns), and the failure-detection hook's mask of waits made
+// unreachable (moe_debug_hold_waits).  Both are process-wide host settings.
+uint64_t wait_limit_ns();
+int debug_hold_waits();
+
+// moe_forward's argument checks (everything but the workspace), in its order.
+moe_status check_forward_args(const moe_dims& d, const void* hidden, int32_t T, const void* router_w,
+                              const void* router_b, const void* packed, int32_t top_k, const void* out);
+// Synchronise `stream`, then read four status words at a device address.
+moe_status read_status_words(const void* status_words, void* stream);
 
 // Record a status and its message for moe_last_error (defined with the C ABI).
 moe_status report_error(moe_status st, const char* fmt, ...);

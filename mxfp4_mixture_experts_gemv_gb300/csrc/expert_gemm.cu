@@ -18,9 +18,12 @@
 // tile.  A down tile needs the whole intermediate of its token rows, i.e. all
 // gate_up m-tiles of the same token tile; their epilogues count themselves in a
 // per-token-tile counter that the down tile's producer waits on (acquire) before
-// it streams hq.  Every CTA is resident (one per SM at most), each walks its
-// tiles in increasing order and finishes every gate_up tile it owns before its
-// first down tile, so every wait is on work that is already in progress.
+// it streams hq.  Its weights do not depend on hq, so the producer issues the
+// weight copies of its first stages before that wait.  Every unit is taken by a
+// running CTA from one claim counter, in increasing order: the first down unit
+// is claimed only after every gate_up unit has been claimed, so every unit a
+// down unit waits for is owned by a CTA that is already running and never waits
+// itself (whether or not all CTAs of the grid are resident at once).
 //
 // Warp roles (192 threads, one CTA per SM):
 //   warp 0      TMA producer (whole warp walks the schedule, one elected lane issues)
@@ -98,6 +101,8 @@ struct MlpParams {
   int32_t* done_tok;         // [T][d_mtiles] down contributions finished per (token, feature block)
   int32_t* sched;            // tiles claimed so far (zero at launch)
   uint32_t* status;
+  uint64_t wait_ns;          // limit of every bounded wait
+  int dep_extra;             // failure-detection hook: down units wait for this many extra gate_up tiles
   int gu_mtiles, gu_ktiles, gu_rows_stored;
   int d_mtiles, d_ktiles, d_rows_stored;
   int I, H, k;
@@ -265,19 +270,19 @@ __global__ void __launch_bounds__(192, 1)
     int64_t issued = 0;
     bool ok = true;
     const uint64_t wpol = l2_policy(p.weights_evict_first != 0);
-    // CTA c starts with tile c; later tiles are claimed in increasing order from
-    // the counter, so every gate_up tile a down tile depends on was taken earlier
-    // by a running CTA.  A claim is issued several stages before the current
-    // tile's last loads and its descriptor fetched two stages before them, so
+    // Units are claimed from the counter in increasing order, the first one at
+    // the start; later claims are issued several stages before the current
+    // unit's last loads and their descriptor fetched two stages before them, so
     // neither round trip stalls the copies.
     int claim = 0;
-    int tile = blockIdx.x;
+    if (lane == 0) claim = atomicAdd(p.sched, 1);
+    int tile = __shfl_sync(0xffffffffu, claim, 0);
     int4 td_next = tile < total ? tl[tile_ref(tile, n_gu, p).b] : make_int4(0, 0, 0, 0);
     for (int i = 0; ok; ++i) {
       const int4 td = td_next;
       // hand the tile (or the end, -1) to the MMA and epilogue warps
       const int slot = i & (kTileQ - 1);
-      if (!mbar_wait_warp(&q_empty[slot], (uint32_t)((i / kTileQ) & 1) ^ 1u, kWaitLimitNs)) {
+      if (!mbar_wait_warp(&q_empty[slot], (uint32_t)((i / kTileQ) & 1) ^ 1u, p.wait_ns)) {
         if (lane == 0) {
           atomicOr(p.status, kStatusTimeoutProducer);
           atomicCAS(p.status + 1, 0u, wait_site(6, i, 0));
@@ -303,31 +308,48 @@ __global__ void __launch_bounds__(192, 1)
       const int bi = min(act_box_index(td.z), kActBoxes - 1);
       const CUtensorMap* bmap = r.gu ? &maps.xp[bi] : &maps.hq[bi];
       const uint32_t b_bytes = (uint32_t)act_box_rows(bi) * kTileK;
-      if (!r.gu) {
-        // the intermediate of this token tile must be complete (all gate_up m-tiles)
-        if (!wait_counter_warp(p.done_gu + r.b, p.gu_mtiles, kWaitLimitNs)) {
-          if (lane == 0) {
-            atomicOr(p.status, kStatusTimeoutProducer);
-            atomicCAS(p.status + 1, 0u, wait_site(5, tile, 0));
-          }
-          ok = false;
-          break;
-        }
-        fence_proxy_async_global();  // hq was written by generic stores; TMA reads it
-      }
+      const int row0_unit = (int)tile_row0(td.x, r.m, 0, rows_stored, k_tiles);
+      // activation (B) copies of stage slot `ss` covering k-tiles kt..kt+nk-1
+      auto issue_b = [&](int ss, int kt, int nk) {
+        for (int j = 0; j < nk; ++j)
+          tma_load_2d(sB + ss * C::kB + j * C::kB1, bmap, &full[ss], (kt + j) * kTileK, td.y);
+        bulk_g2s(sSF + ss * C::kSF + kKS * kAtomBytes, sfb + kt * kAtomBytes, nk * kAtomBytes, &full[ss]);
+      };
+      // A down unit's hq is ready once all gate_up m-tiles of its token tile are
+      // counted; until then its stages get their weight copies only, and the
+      // activation copies of those stages follow the (bounded) wait.
+      bool dep_ok = r.gu;
+      bool dep_timeout = false;
+      const int dep_target = p.gu_mtiles + p.dep_extra;
+      int pend_s = 0, pend_kt = 0, pend_n = 0;  // stages waiting for their activation copies
       for (int kt = 0; kt < k_tiles; kt += kKS) {
         const int nk = min(kKS, k_tiles - kt);
         const int st = kt / kKS;
-        if (st == claim_st && lane == 0) claim = (int)gridDim.x + atomicAdd(p.sched, 1);
+        if (st == claim_st && lane == 0) claim = atomicAdd(p.sched, 1);
         if (st == fetch_st) {
           next = __shfl_sync(0xffffffffu, claim, 0);
           if (next < total) td_next = tl[tile_ref(next, n_gu, p).b];
         }
-        if (!mbar_wait_warp(&empty[s], ph ^ 1u, kWaitLimitNs)) {
+        // activation copies of the stages that wait for them (none after this)
+        auto flush_pending = [&]() {
+          // hq was written by generic stores; TMA reads it.  After an expired wait the
+          // copies still go out (they read in-bounds workspace bytes), so that every
+          // stage's phase completes before the roles wind down.
+          fence_proxy_async_global();
+          if (elect_one())
+            for (int j = 0; j < pend_n; ++j) {
+              const int kk = pend_kt + j * kKS;
+              issue_b((pend_s + j) % S, kk, min(kKS, k_tiles - kk));
+            }
+          __syncwarp();
+          pend_n = 0;
+        };
+        if (!mbar_wait_warp(&empty[s], ph ^ 1u, p.wait_ns)) {
           if (lane == 0) {
             atomicOr(p.status, kStatusTimeoutProducer);
             atomicCAS(p.status + 1, 0u, wait_site(1, tile, kt));
           }
+          flush_pending();
           ok = false;
           break;
         }
@@ -336,7 +358,7 @@ __global__ void __launch_bounds__(192, 1)
           // each in shared memory): boxes of 256, 128 or 64 rows
           const int a_rows = rows_m * nk;
           mbar_arrive_expect_tx(&full[s], (uint32_t)(a_rows * kTileRowBytes + nk * (b_bytes + 2 * kAtomBytes)));
-          const int row0 = (int)tile_row0(td.x, r.m, kt, rows_stored, k_tiles);
+          const int row0 = row0_unit + kt * rows_m;
           for (int off = 0; off < a_rows;) {
             const int c = a_rows - off >= 256 ? 256 : a_rows - off >= 128 ? 128 : 64;
             const CUtensorMap* amap = r.gu ? (c == 256 ? &maps.gu2 : (c == 128 ? &maps.gu : &maps.gut))
@@ -344,17 +366,41 @@ __global__ void __launch_bounds__(192, 1)
             tma_load_2d_hint(sA + s * C::kA + off * kTileK, amap, &full[s], 0, row0 + off, wpol);
             off += c;
           }
-          for (int j = 0; j < nk; ++j)
-            tma_load_2d(sB + s * C::kB + j * C::kB1, bmap, &full[s], (kt + j) * kTileK, td.y);
-          uint8_t* sf = sSF + s * C::kSF;
-          bulk_g2s_hint(sf, sfa + kt * kAtomBytes, nk * kAtomBytes, &full[s], wpol);
-          bulk_g2s(sf + kKS * kAtomBytes, sfb + kt * kAtomBytes, nk * kAtomBytes, &full[s]);
+          bulk_g2s_hint(sSF + s * C::kSF, sfa + kt * kAtomBytes, nk * kAtomBytes, &full[s], wpol);
         }
         __syncwarp();
+        if (dep_ok) {
+          if (elect_one()) issue_b(s, kt, nk);
+          __syncwarp();
+        } else {
+          if (pend_n == 0) {
+            pend_s = s;
+            pend_kt = kt;
+          }
+          ++pend_n;
+          dep_ok = __all_sync(0xffffffffu, ld_acquire_gpu(p.done_gu + r.b) >= dep_target);
+          // keep streaming weights while the intermediate is not ready, until every
+          // stage slot is taken or this is the unit's last stage
+          if (!dep_ok && (pend_n >= S || kt + kKS >= k_tiles)) {
+            if (!wait_counter_warp(p.done_gu + r.b, dep_target, p.wait_ns)) {
+              if (lane == 0) {
+                atomicOr(p.status, kStatusTimeoutProducer);
+                atomicCAS(p.status + 1, 0u, wait_site(5, tile, kt));
+              }
+              dep_timeout = true;
+            }
+            dep_ok = true;
+          }
+          if (dep_ok) flush_pending();
+        }
         ++issued;
         if (++s == S) {
           s = 0;
           ph ^= 1u;
+        }
+        if (dep_timeout) {
+          ok = false;
+          break;
         }
       }
       tile = next;
@@ -362,7 +408,7 @@ __global__ void __launch_bounds__(192, 1)
     // Let every copy this warp issued land before the CTA can exit.
     for (int st = 0; st < S && st < issued; ++st) {
       const int64_t last = ((issued - 1 - st) / S) * S + st;
-      if (!mbar_wait_warp(&full[st], (uint32_t)((last / S) & 1), 200000000ull) && lane == 0)
+      if (!mbar_wait_warp(&full[st], (uint32_t)((last / S) & 1), kDrainLimitNs) && lane == 0)
         atomicOr(p.status, kStatusTimeoutDrain);
     }
   } else if (warp == 1) {
@@ -372,7 +418,7 @@ __global__ void __launch_bounds__(192, 1)
     bool ok = true;
     for (int i = 0; ok; ++i) {
       const int slot = i & (kTileQ - 1);
-      if (!mbar_wait_warp(&q_full[slot], (uint32_t)((i / kTileQ) & 1), kWaitLimitNs)) {
+      if (!mbar_wait_warp(&q_full[slot], (uint32_t)((i / kTileQ) & 1), p.wait_ns)) {
         if (lane == 0) {
           atomicOr(p.status, kStatusTimeoutMma);
           atomicCAS(p.status + 1, 0u, wait_site(7, i, 0));
@@ -388,7 +434,7 @@ __global__ void __launch_bounds__(192, 1)
       const int4 td = make_int4(q.y, q.z, q.w, 0);
       const int k_tiles = r.gu ? p.gu_ktiles : p.d_ktiles;
       const int rows_m = min(kTileM, (r.gu ? p.gu_rows_stored : p.d_rows_stored) - r.m * kTileM);
-      if (!mbar_wait_warp(&tempty[acc], aph ^ 1u, kWaitLimitNs)) {
+      if (!mbar_wait_warp(&tempty[acc], aph ^ 1u, p.wait_ns)) {
         if (lane == 0) {
           atomicOr(p.status, kStatusTimeoutMma);
           atomicCAS(p.status + 1, 0u, wait_site(2, tile, 0xFFF));
@@ -403,7 +449,7 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t idesc0 = idesc_mxf8f6f4(128, n_mma, 5 /*E2M1*/, 0 /*E4M3*/, 0, 0);
       for (int kt = 0; kt < k_tiles; kt += kKS) {
         const int nk = min(kKS, k_tiles - kt);
-        if (!mbar_wait_warp(&full[s], ph, kWaitLimitNs)) {
+        if (!mbar_wait_warp(&full[s], ph, p.wait_ns)) {
           if (lane == 0) {
             atomicOr(p.status, kStatusTimeoutMma);
             atomicCAS(p.status + 1, 0u, wait_site(3, tile, kt));
@@ -448,7 +494,7 @@ __global__ void __launch_bounds__(192, 1)
     // No MMA may still be running when the tensor memory is released.
     if (elect_one()) umma_commit(drain);
     __syncwarp();
-    if (!mbar_wait_warp(drain, 0, 200000000ull) && lane == 0) atomicOr(p.status, kStatusTimeoutDrain);
+    if (!mbar_wait_warp(drain, 0, kDrainLimitNs) && lane == 0) atomicOr(p.status, kStatusTimeoutDrain);
   } else {
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;              // tmem lane quadrant this warp may read
@@ -467,7 +513,7 @@ __global__ void __launch_bounds__(192, 1)
       // every tile (and on stopping) and meet at the same named barriers
       const int slot = i & (kTileQ - 1);
       if (warp == 2) {
-        const bool got = mbar_wait_warp(&q_full[slot], (uint32_t)((i / kTileQ) & 1), kWaitLimitNs);
+        const bool got = mbar_wait_warp(&q_full[slot], (uint32_t)((i / kTileQ) & 1), p.wait_ns);
         if (lane == 0) {
           *s_eq = got ? s_tq[slot] : make_int4(-2, 0, 0, 0);
           if (got) {
@@ -488,7 +534,7 @@ __global__ void __launch_bounds__(192, 1)
       const int rows = td.z;
       if (ok) {
         // all lanes take the same decision, so the warp-collective tcgen05.ld stays uniform
-        ok = mbar_wait_warp(&tfull[acc], aph, kWaitLimitNs);
+        ok = mbar_wait_warp(&tfull[acc], aph, p.wait_ns);
         if (!ok && lane == 0) {
           atomicOr(p.status, kStatusTimeoutEpilogue);
           atomicCAS(p.status + 1, 0u, wait_site(4, tile, 0));
@@ -709,9 +755,9 @@ cudaError_t launch_bn(const Maps& m, const MlpParams& p, int grid, cudaStream_t 
   cfg.stream = s;
   // Programmatic dependent launch: the CTAs start (barrier init, TMEM allocation,
   // descriptor prefetch) while the routing kernel finishes.  The grid is at most
-  // one CTA per SM and each CTA needs most of an SM's shared memory, so every CTA
-  // becomes resident once the previous kernel's CTAs leave; the tile dependencies
-  // only ever wait on resident CTAs' work (and are bounded regardless).
+  // one CTA per SM.  Units are claimed at run time by the CTAs that are running,
+  // so the dependencies between units hold even when only part of the grid is
+  // resident (another kernel holding SMs); every wait is bounded regardless.
   cudaLaunchAttribute attrs[1];
   attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attrs[0].val.programmaticStreamSerializationAllowed = 1;
@@ -793,6 +839,8 @@ cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, cons
   p.done_tok = b.done_tok;
   p.sched = b.sched;
   p.status = b.status;
+  p.wait_ns = wait_limit_ns();
+  p.dep_extra = (debug_hold_waits() & MOE_DEBUG_HOLD_DOWN_UNITS) ? 1 : 0;
   p.gu_mtiles = h.gu_mtiles;
   p.gu_ktiles = h.gu_ktiles;
   p.gu_rows_stored = h.gu_rows_stored;

@@ -52,6 +52,7 @@ struct RouteClusterArgs {
   uint32_t* zero;  // words cleared for this forward (status and the expert kernel's counters)
   int zero_words;
   uint32_t* status;
+  uint64_t wait_ns;
 };
 
 // Sum-reduce N values held by every lane of a warp so that each lane ends up
@@ -116,7 +117,7 @@ __global__ void __launch_bounds__(kRcThreads, 1) route_cluster_kernel(const Rout
   // biases of this CTA's experts (in flight with the copies)
   if (tid < ne) s_bias[tid] = __uint_as_float((uint32_t)a.br[e0 + tid] << 16);
   __syncthreads();  // the barrier's initialisation is visible to every thread
-  const bool staged = mbar_wait(&s_bar, 0, kWaitLimitNs);
+  const bool staged = mbar_wait(&s_bar, 0, a.wait_ns);
 
   // logits of this CTA's experts, kG at a time: thread = 16-byte column chunk(s),
   // the token chunks stay in registers across the kG router rows
@@ -287,7 +288,7 @@ cudaError_t launch_route_cluster(const uint16_t* x, const uint16_t* wr, const ui
   const int epc = (E + csize - 1) / csize;
   RouteClusterArgs a{x, wr, br, T, H, E, k, __builtin_ctz((unsigned)tile_rows), o.logits, o.ids, o.w, o.xq, o.xs,
                      o.counts, o.offsets, o.sorted_rows, o.inv_pos, o.tiles, o.xp, o.xp_sf, o.zero,
-                     o.zero_words, o.status};
+                     o.zero_words, o.status, wait_limit_ns()};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(csize);
   cfg.blockDim = dim3(kRcThreads);

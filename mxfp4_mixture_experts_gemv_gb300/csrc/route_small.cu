@@ -45,6 +45,8 @@ struct RouteSmallArgs {
   uint8_t* hq_sf;
   int32_t* grid_bar;
   uint32_t* status;
+  uint64_t wait_ns;
+  int bar_extra;  // failure-detection hook: wait for this many CTAs more than the grid has
 };
 
 __global__ void __launch_bounds__(kThreads) route_small_kernel(const RouteSmallArgs a) {
@@ -112,24 +114,36 @@ __global__ void __launch_bounds__(kThreads) route_small_kernel(const RouteSmallA
   }
 
   // ------------------------------------------------------------ grid barrier (bounded)
+  __shared__ int s_barrier_ok;
   __syncthreads();
   if (tid == 0) {
     __threadfence();
     atomicAdd(a.grid_bar, 1);
     const uint64_t t0 = global_timer_ns();
+    int ok = 1;
     while (true) {
       int v;
       asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a.grid_bar) : "memory");
-      if (v >= (int)gridDim.x) break;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        atomicOr(a.status, kStatusTimeoutDrain);
+      if (v >= (int)gridDim.x + a.bar_extra) break;
+      if (global_timer_ns() - t0 > a.wait_ns) {
+        // some logits may be missing: report it (role 9: routing grid barrier) and
+        // publish nothing computed from them
+        atomicOr(a.status, kStatusTimeoutRouting);
+        atomicCAS(a.status + 1, 0u, (9u << 28) | ((uint32_t)blockIdx.x << 12));
+        ok = 0;
         break;
       }
       __nanosleep(32);
     }
     __threadfence();
+    s_barrier_ok = ok;
   }
   __syncthreads();
+  if (!s_barrier_ok) {
+    // an empty tile list: the expert kernel then has no work and writes no output
+    if (blockIdx.x == 0 && tid == 0) a.tiles[0] = 0;
+    return;
+  }
 
   // ------------------------------------------------------------ phase B
   // every logit (8 independent loads in flight per thread and round)
@@ -198,7 +212,8 @@ __global__ void __launch_bounds__(kThreads) route_small_kernel(const RouteSmallA
 cudaError_t launch_route_small(const uint16_t* x, const uint16_t* wr, const uint16_t* br, int T, int H, int E, int I,
                                int k, int tile_rows, int max_tiles, const RouteSmallOut& o, cudaStream_t s) {
   RouteSmallArgs a{x, wr, br, T, H, E, I, k, tile_rows, max_tiles, o.logits, o.ids, o.w, o.xq, o.xs, o.counts,
-                   o.offsets, o.sorted_rows, o.inv_pos, o.tiles, o.xp, o.xp_sf, o.hq_sf, o.grid_bar, o.status};
+                   o.offsets, o.sorted_rows, o.inv_pos, o.tiles, o.xp, o.xp_sf, o.hq_sf, o.grid_bar, o.status,
+                   wait_limit_ns(), (debug_hold_waits() & MOE_DEBUG_HOLD_ROUTING_BARRIER) ? 1 : 0};
   const size_t smem = std::max((size_t)(T + 1) * H * 2, (size_t)T * 257 * 4);  // staged rows, later the logits
   static bool attr = false;
   if (!attr) {

@@ -42,6 +42,7 @@ struct RouterArgs {
   uint32_t* status;
   int T, H, E, k, n_pad;  // n_pad: E rounded up to 16 (MMA N)
   int splits, slices;     // CTAs per tile (the cluster), k-slices per CTA
+  uint64_t wait_ns;       // limit of every bounded wait
 };
 
 // Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulator, both K-major.
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
     uint32_t ph = 0;
     int issued = 0;
     for (int kk = k0; kk < k1; ++kk) {
-      if (!mbar_wait_warp(&empty[s], ph ^ 1u, kWaitLimitNs)) {
+      if (!mbar_wait_warp(&empty[s], ph ^ 1u, a.wait_ns)) {
         if (lane == 0) atomicOr(a.status, kStatusTimeoutProducer);
         break;
       }
@@ -192,7 +193,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
     }
     for (int st = 0; st < kRStages && st < issued; ++st) {
       const int last = ((issued - 1 - st) / kRStages) * kRStages + st;
-      if (!mbar_wait_warp(&full[st], (uint32_t)((last / kRStages) & 1), 200000000ull) && lane == 0)
+      if (!mbar_wait_warp(&full[st], (uint32_t)((last / kRStages) & 1), kDrainLimitNs) && lane == 0)
         atomicOr(a.status, kStatusTimeoutDrain);
     }
   } else if (warp == 1) {
@@ -200,7 +201,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
     uint32_t ph = 0;
     const uint32_t idesc = idesc_bf16(kRTileM, NPAD);
     for (int kk = k0; kk < k1; ++kk) {
-      if (!mbar_wait_warp(&full[s], ph, kWaitLimitNs)) {
+      if (!mbar_wait_warp(&full[s], ph, a.wait_ns)) {
         if (lane == 0) atomicOr(a.status, kStatusTimeoutMma);
         break;
       }
@@ -224,7 +225,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
   } else if (warp < 6) {
     // epilogue: thread = token row of the tile (tmem lane quarter warp % 4)
     const int q = warp & 3, row = 32 * q + lane, t = t0 + row;
-    const bool ok = mbar_wait_warp(done, 0, kWaitLimitNs);
+    const bool ok = mbar_wait_warp(done, 0, a.wait_ns);
     if (!ok && lane == 0) atomicOr(a.status, kStatusTimeoutEpilogue);
     tc_fence_after();
     const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16);
@@ -291,7 +292,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
                        cluster_addr(inbox_full, (uint32_t)q));
       }
     }
-    const bool got = __all_sync(0xffffffffu, mbar_wait(inbox_full, 0, kWaitLimitNs));  // warp-uniform
+    const bool got = __all_sync(0xffffffffu, mbar_wait(inbox_full, 0, a.wait_ns));  // warp-uniform
     if (!got && lane == 0) atomicOr(a.status, kStatusTimeoutEpilogue);
     const int n = min(rows_mine, a.T - t0 - r0);  // tokens this CTA finishes
     for (int lr = warp; got && lr < n; lr += kRWarps) {
@@ -481,7 +482,7 @@ cudaError_t launch_router_tc(const uint16_t* x, const uint16_t* wr, const uint16
   const int np = n_pad <= 64 ? 64 : (n_pad <= 128 ? 128 : 256);
   CUtensorMap mx, mw;
   if (!make_bf16_map(&mx, x, H, T, kRTileM) || !make_bf16_map(&mw, wr, H, E, np)) return cudaErrorInvalidValue;
-  RouterArgs a{br, logits, ids, w, status, T, H, E, k, np, 1, 0};
+  RouterArgs a{br, logits, ids, w, status, T, H, E, k, np, 1, 0, wait_limit_ns()};
   switch (np) {
     case 64: return launch_np<64>(mx, mw, a, s);
     case 128: return launch_np<128>(mx, mw, a, s);

@@ -130,3 +130,13 @@ def test_residual_rmsnorm_rejects_bad_arguments_on_host(L):
     assert L.moe_residual_rmsnorm(0, None, 4, 2880, 1e-5, FAKE, None) == 1       # null residual
     assert L.moe_residual_rmsnorm(FAKE + 8, None, 4, 2880, 1e-5, FAKE, None) == 3
     assert L.moe_residual_rmsnorm(FAKE, None, 0, 2880, 1e-5, FAKE, None) == 0    # T = 0: no-op
+
+
+def test_wait_limit_and_hold_mask_are_checked_on_host(L):
+    assert L.moe_set_wait_limit_ns(10) == 1             # below 1 us
+    assert L.moe_set_wait_limit_ns(61_000_000_000) == 1  # above 60 s
+    assert L.moe_set_wait_limit_ns(5_000_000) == 0 and L.moe_get_wait_limit_ns() == 5_000_000
+    assert L.moe_set_wait_limit_ns(0) == 0 and L.moe_get_wait_limit_ns() == 2_000_000_000
+    assert L.moe_debug_hold_waits(8) == 1
+    assert L.moe_debug_hold_waits(moe.HOLD_DOWN_UNITS | moe.HOLD_ROUTING_BARRIER) == 0
+    assert L.moe_debug_hold_waits(0) == 0

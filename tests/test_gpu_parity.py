@@ -48,6 +48,7 @@ def _full_check(inp_cpu, run, strict=True):
     assert not ties, f"near-tie tokens {sorted(ties)}"
     mc.check_quantised_x(run, ref["xq"], ref["xs"])
     cnt, off, sr, inv = mc.check_grouping(run, s.T)
+    mc.check_gathered(run, s.T, sr, ref["xq"], ref["xs"])
     allow, flips = mc.check_intermediate(run, ref, inp_cpu, inv)
     got = mc.bf16_to_f64(run.out)
     mc.compare_out(got, ref["out"], "out", allow=allow, bf16_rounding=not strict)

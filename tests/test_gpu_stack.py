@@ -1,5 +1,18 @@
-"""The stacked-layer workload, x <- x + moe(rmsnorm(x)): the residual/RMSNorm
-kernel, and a chain of gpt-oss-shaped layers against the oracle's own chain."""
+"""The stacked-layer workload, x <- x + moe(rmsnorm(x)) over the 36 MoE layers of
+a gpt-oss-120b-shaped model ("GPT-OSS-120B on DGX Spark: From MXFP4 to NVFP4",
+"GPT-OSS-120B Architecture"): the residual/RMSNorm kernel, and the whole stack
+checked layer by layer against the oracle, teacher-forced.
+
+Chained layers amplify rounding: a later layer's input already differs from an
+untouched oracle chain by the earlier layers' bf16 and MXFP8 rounding, and the
+router turns those differences into genuine selection changes.  So every layer
+is checked on the input the GPU actually gave it: the oracle recomputes that
+layer from the GPU's bf16 hidden (itself checked against the oracle's RMSNorm of
+the GPU's residual), and the layer must meet the layer tolerance there.  The
+drift of an untouched oracle chain is printed, not gated."""
+import concurrent.futures as cf
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -11,8 +24,10 @@ from tests import moe_cases as mc
 
 pytestmark = pytest.mark.gpu
 
-# Bound on the relative Frobenius drift of chained layers (layer 0 uses the layer tolerance).
-DRIFT_REL = 5e-2
+N_LAYERS = ms.STACK_LAYERS  # 36
+H = I = 2880
+E, K = 128, 4
+WORKERS = max(1, os.cpu_count() or 1)
 
 
 def _bits(t):
@@ -46,50 +61,134 @@ def test_residual_rmsnorm_matches_oracle():
     assert np.abs(_widen(_bits(hidden)) - want_h).max() <= 2.0 ** -7 * np.abs(want_h).max()
 
 
-def test_three_layer_stack_matches_oracle_chain():
-    H = I = 2880
-    E, k, T, n_layers = 128, 4, 3, 3
+def _oracle_route_all(x_bits, rw, rb, pool):
+    """The oracle's fp64 logits of every token, sharded over host threads (each call
+    is the single-threaded oracle on a slice of tokens; its calls release the
+    interpreter lock)."""
+    T = x_bits.shape[0]
+    n = min(T, 4 * WORKERS)
+    cuts = np.linspace(0, T, n + 1).astype(int)
+    parts = list(pool.map(lambda ab: oracle.route(x_bits[ab[0]:ab[1]], rw, rb, K)[0], zip(cuts[:-1], cuts[1:])))
+    return np.concatenate(parts, axis=0)
+
+
+def _oracle_tokens(rows_bits, rw, rb, w_cpu, pool):
+    """The oracle layer on each given token (one call per token, in parallel)."""
+    refs = list(pool.map(lambda i: oracle.moe_forward(rows_bits[i:i + 1], rw, rb, *w_cpu, k=K, intermediates=True),
+                         range(rows_bits.shape[0])))
+    out = {key: np.concatenate([r[key] for r in refs], axis=0) for key in refs[0]}
+    return out
+
+
+def _sample(T, cnt, off, sr, ties):
+    """16 tokens spread over the batch, plus the tokens of the last rows of the most
+    loaded expert (its ragged last tile), minus accepted near-tie tokens."""
+    if T <= 32:
+        return sorted(set(range(T)) - ties)
+    e_max = int(np.argmax(cnt))
+    last = [int(sr[p]) // K for p in range(max(off[e_max], off[e_max + 1] - 4), off[e_max + 1])]
+    spread = np.linspace(0, T - 1, 16).astype(int).tolist()
+    return sorted(set(spread + last) - ties)
+
+
+def _teacher_forced_stack(T):
     dims = moe.LayerDims(E, H, I)
     x0 = ms.make_tokens(0, T, H)
-    # GPU chain
     xr = x0.float().cuda()
     hidden = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
-    outs, cpu_layers = [], []
-    out = None
-    for l in range(n_layers):
-        w = ms.make_expert_weights(0, H, I, E, layer=l, device="cuda")
-        packed = moe.pack_weights(dims, *w)
-        rw, rb = ms.make_router(0, H, E, layer=l)
-        cpu_layers.append((rw, rb, [t.cpu() for t in w]))
-        moe.residual_rmsnorm(xr, out, hidden)
-        out = moe.forward(dims, hidden, rw.cuda(), rb.cuda(), packed, k)
-        outs.append(out.clone())
-        torch.cuda.synchronize()
-        del w, packed
-    moe.residual_rmsnorm(xr, out, hidden)
-    torch.cuda.synchronize()
-    # oracle chain: the same recurrence with each layer's output rounded to bf16,
-    # the layer's output format
+    out = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    ws = moe.alloc_workspace(dims, T, K)
+    layout = moe.workspace_layout(dims, T, K)
+    prev = None
+    xr_prev = None
+    out_prev = None
+    worst = (0.0, 0.0)
+    n_ties = 0
+    hidden_log = []
+    with cf.ThreadPoolExecutor(max_workers=WORKERS) as pool:
+        for l in range(N_LAYERS):
+            w = ms.make_expert_weights(0, H, I, E, layer=l, device="cuda")
+            packed = moe.pack_weights(dims, *w)
+            rw, rb = ms.make_router(0, H, E, layer=l)
+            moe.residual_rmsnorm(xr, prev, hidden)
+            moe.forward(dims, hidden, rw.cuda(), rb.cuda(), packed, K, out=out, workspace=ws)
+            st = moe.device_status(ws)
+            assert st == moe.MOE_OK, f"layer {l}: {moe.STATUS_NAMES.get(st, st)}"
+            prev = out
+            xr_cpu = xr.cpu().double().numpy()
+            hid_bits = _bits(hidden)
+            w_cpu = [t.cpu() for t in w]
+            del w, packed
+            # the residual step: x_l = x_(l-1) + out_(l-1), one fp32 rounding
+            if l == 0:
+                np.testing.assert_array_equal(xr_cpu, _widen(_bits(x0)))
+            else:
+                want_x = xr_prev + _widen(out_prev)
+                assert (np.abs(xr_cpu - want_x) <= 2.0 ** -24 * np.abs(want_x)).all(), f"layer {l}: residual"
+            # the layer's input: RMSNorm of the GPU's residual, the same bf16 grid (one step
+            # apart only where the fp32 and fp64 norms round differently)
+            want_h = _widen(oracle.rmsnorm_bf16(xr_cpu, 1e-5))
+            got_h = _widen(hid_bits)
+            dh = np.abs(got_h - want_h)
+            assert (dh <= 2.0 ** -7 * np.abs(want_h)).all() and (dh > 0).mean() < 0.01, f"layer {l}: rmsnorm"
+            # routing and grouping of every token, on the GPU's own input
+            x_t = torch.from_numpy(hid_bits.view(np.int16)).view(torch.bfloat16)
+            logits = _oracle_route_all(hid_bits, rw, rb, pool)
+            run = mc.GpuRun(dims, K, out, ws, layout)
+            ties = mc.check_routing(run, x_t, rw, rb, logits)
+            n_ties += len(ties)
+            cnt, off, sr, inv = mc.check_grouping(run, T)
+            # the layer's output on the sampled tokens
+            sample = _sample(T, cnt, off, sr, ties)
+            ref = _oracle_tokens(hid_bits[sample], rw, rb, w_cpu, pool)
+            inp_cpu = ms.LayerInputs(ms.LayerShape(T=len(sample), H=H, I=I, E=E, k=K), x_t[sample], rw, rb, *w_cpu)
+            allow, _ = mc.check_intermediate(run, ref, inp_cpu, inv.reshape(T, K)[sample])
+            got = mc.bf16_to_f64(out)[sample]
+            m, rel = mc.compare_out(got, ref["out"], f"layer {l}", allow=allow)
+            worst = (max(worst[0], m), max(worst[1], rel))
+            xr_prev, out_prev = xr_cpu, _bits(out)
+            if T <= 32:
+                hidden_log.append(hid_bits)
+    print(f"T={T}: {N_LAYERS} layers teacher-forced; worst max|d|/rms {worst[0]:.3g}, worst rel Frobenius "
+          f"{worst[1]:.3g}, accepted near-tie tokens {n_ties}")
+    return x0, hidden_log
+
+
+def _untouched_drift(x0, hidden_log):
+    """Relative difference between the GPU's layer inputs and an untouched oracle
+    chain (the oracle's own outputs fed forward), per layer: printed only."""
+    T = x0.shape[0]
     xo = _widen(_bits(x0))
     prev = None
-    for l, (rw, rb, w) in enumerate(cpu_layers):
-        if prev is not None:
-            xo = xo + _widen(prev)
-        h_bits = oracle.rmsnorm_bf16(xo, 1e-5)
-        r = oracle.moe_forward(h_bits.view(np.uint16), rw, rb, *w, k=k)
-        prev = oracle.bf16_round_array(r["out"])
-        got = mc.bf16_to_f64(outs[l])
-        if l == 0:
-            # the first layer sees identical inputs: the layer tolerance holds
-            mc.compare_out(got, r["out"], "layer 0", bf16_rounding=True)
-        else:
-            # later layers see inputs that already differ by the earlier layers' rounding
-            # (about a quarter of the bf16 inputs one step apart), which the MXFP8
-            # re-quantisation of x turns into code changes: only a bounded drift holds
-            rel = np.linalg.norm(got - r["out"]) / np.linalg.norm(r["out"])
-            print(f"layer {l}: relative drift {rel:.3g}")
-            assert np.isfinite(got).all() and rel <= DRIFT_REL, f"layer {l}: drift {rel:.3g}"
-    xo = xo + _widen(prev)
-    rel = np.linalg.norm(xr.cpu().double().numpy() - xo) / np.linalg.norm(xo)
-    print(f"residual after {n_layers} layers: relative drift {rel:.3g}")
-    assert rel <= DRIFT_REL
+    drift = []
+    with cf.ThreadPoolExecutor(max_workers=WORKERS) as pool:
+        for l in range(N_LAYERS):
+            if prev is not None:
+                xo = xo + _widen(prev)
+            h_bits = oracle.rmsnorm_bf16(xo, 1e-5)
+            g = _widen(hidden_log[l])
+            o = _widen(h_bits)
+            drift.append(float(np.linalg.norm(g - o) / np.linalg.norm(o)))
+            rw, rb = ms.make_router(0, H, E, layer=l)
+            rows = [i for i in range(T)]
+            _, ids, _ = oracle.route(h_bits, rw, rb, K)
+            need = sorted(set(ids.reshape(-1).tolist()))
+            sub = ms.make_expert_weights(0, H, I, E, layer=l, experts=need)
+            full = []
+            for t_sub in sub:
+                z = torch.zeros((E,) + tuple(t_sub.shape[1:]), dtype=t_sub.dtype)
+                z[need] = t_sub
+                full.append(z)
+            outs = list(pool.map(lambda i: oracle.moe_forward(h_bits[i:i + 1], rw, rb, *full, k=K)["out"], rows))
+            prev = oracle.bf16_round_array(np.concatenate(outs, axis=0))
+    print("untouched oracle chain: relative drift of the layer inputs by layer " +
+          " ".join(f"{d:.2g}" for d in drift))
+
+
+def test_stack36_teacher_forced_T4():
+    x0, hidden_log = _teacher_forced_stack(4)
+    _untouched_drift(x0, hidden_log)
+
+
+def test_stack36_teacher_forced_T8192():
+    _teacher_forced_stack(8192)
