@@ -247,7 +247,7 @@ def _active_bytes(moe, ws, layout, n_active_out):
 
 
 def _workload(layers: Layers, T: int, hot: int, hot_bias: float, steps: int, warmup: int, device, dist,
-              profile=True, seed=0):
+              profile=True, seed=0, act_format="mxfp8"):
     """Time `steps` forwards of T tokens rotating over the layers; returns a stats dict."""
     moe = layers.moe
     routers = layers.routers(hot, hot_bias, device, seed)
@@ -258,7 +258,8 @@ def _workload(layers: Layers, T: int, hot: int, hot_bias: float, steps: int, war
     # routing statistics per layer (active experts -> algorithmic bytes)
     act = []
     for l in range(layers.n):
-        moe.forward(layers.dims, xs[l], routers[l][0], routers[l][1], layers.packed[l], K_TOP, out=out, workspace=ws)
+        moe.forward(layers.dims, xs[l], routers[l][0], routers[l][1], layers.packed[l], K_TOP, out=out, workspace=ws,
+                    act_format=act_format)
         _active_bytes(moe, ws, layout, act)
     st = moe.device_status(ws)
     if st != moe.MOE_OK:
@@ -267,7 +268,8 @@ def _workload(layers: Layers, T: int, hot: int, hot_bias: float, steps: int, war
     # loop runs it).
     for i in range(warmup):
         l = i % layers.n
-        moe.forward(layers.dims, xs[l], routers[l][0], routers[l][1], layers.packed[l], K_TOP, out=out, workspace=ws)
+        moe.forward(layers.dims, xs[l], routers[l][0], routers[l][1], layers.packed[l], K_TOP, out=out, workspace=ws,
+                    act_format=act_format)
     torch.cuda.synchronize()
 
     def capture():
@@ -277,7 +279,7 @@ def _workload(layers: Layers, T: int, hot: int, hot_bias: float, steps: int, war
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 moe.forward(layers.dims, xs[l], routers[l][0], routers[l][1], layers.packed[l], K_TOP, out=out,
-                            workspace=ws)
+                            workspace=ws, act_format=act_format)
             graphs.append(g)
         for i in range(min(warmup, steps)):
             graphs[i].replay()
@@ -338,7 +340,8 @@ def _workload(layers: Layers, T: int, hot: int, hot_bias: float, steps: int, war
                 step_us=step_us)
 
 
-def _stack(layers: Layers, n_layers: int, T: int, steps: int, warmup: int, device, dist, graph: bool):
+def _stack(layers: Layers, n_layers: int, T: int, steps: int, warmup: int, device, dist, graph: bool,
+           act_format="mxfp8"):
     """x <- x + moe(rmsnorm(x)) over n_layers independently seeded layers (all resident)."""
     moe = layers.moe
     while len(layers.packed) < n_layers:
@@ -360,7 +363,7 @@ def _stack(layers: Layers, n_layers: int, T: int, steps: int, warmup: int, devic
         for l in range(n_layers):
             moe.residual_rmsnorm(x_res, prev, hidden)
             moe.forward(layers.dims, hidden, routers[l][0], routers[l][1], layers.packed[l], K_TOP, out=out,
-                        workspace=ws)
+                        workspace=ws, act_format=act_format)
             if count is not None:
                 count.append(int((moe.view(ws, lay.counts, (E,), torch.int32) > 0).sum().item()))
             prev = out
@@ -516,6 +519,7 @@ def run_ours(args):
     moe.lib()
     hbm_peak, bf16_peak, bf16_sust, peak_src = _peaks()
     fp8_peak = 2 * bf16_peak  # kind::mxf8f6f4 runs at the fp8 rate: 2x the bf16 dense rate (nominal ratio)
+    fp4_peak = 6 * bf16_peak  # kind::mxf4: the dense fp4 rate, 13.5 / 2.25 times the bf16 rate (nominal ratio)
     t_gen = time.perf_counter()
     layers = Layers(args.layers, device)
     t_gen = time.perf_counter() - t_gen
@@ -540,6 +544,23 @@ def run_ours(args):
                 "stage_ms": w["stage_ms"], "clocks": w["clocks"]}
             del w
 
+    if not args.no_extra:
+        # the FP4 x FP4 variant (activations in MXFP4, tcgen05 kind::mxf4)
+        for name, T, n in (("mxfp4act_decode_t4", 4, args.steps), ("mxfp4act_prefill_t2048", 2048, max(10, args.steps // 5))):
+            w = _workload(layers, T, 0, 0.0, n, min(args.warmup, 3), device, dist, act_format="mxfp4")
+            mlp_ms = w["stage_ms"].get("expert_mlp", 0) or float("nan")
+            expert_flop = T * K_TOP * FLOP_PER_ROW
+            extra[name] = {
+                "T": T, "act_format": "mxfp4", "tokens_per_s": _replica_tokens_per_s(world, T, w["ms_per_step"]),
+                "ms_per_step": w["ms_per_step"], "active_experts": w["active_experts"],
+                "algorithmic_bytes": w["step_bytes"], "gbs": w["gbs"], "hbm_frac": w["gbs"] / hbm_peak,
+                "tflops": w["tflops"],
+                "expert_mlp_gbs": (w["gu_bytes"] + w["d_bytes"]) / (mlp_ms * 1e-3) / 1e9,
+                "expert_mlp_tflops": expert_flop / (mlp_ms * 1e-3) / 1e12,
+                "expert_mlp_tflops_frac_of_fp4_peak": expert_flop / (mlp_ms * 1e-3) / 1e12 / fp4_peak,
+                "stage_ms": w["stage_ms"], "clocks": w["clocks"]}
+            del w
+
     if not args.no_extra and not args.no_stack:
         n_l = 36
         pre = _stack(layers, n_l, 8192, 2, 1, device, dist, graph=False)
@@ -548,6 +569,11 @@ def run_ours(args):
         dec = _stack(layers, n_l, 4, max(5, args.steps // 5), 2, device, dist, graph=True)
         dec["hbm_frac"] = dec["gbs"] / hbm_peak
         extra["stack36_decode_t4"] = dec
+        pre4 = _stack(layers, n_l, 8192, 2, 1, device, dist, graph=False, act_format="mxfp4")
+        pre4["tflops_frac_of_fp4_peak"] = pre4["tflops"] / fp4_peak
+        pre4["tflops_frac_of_fp8_peak"] = pre4["tflops"] / fp8_peak
+        pre4["act_format"] = "mxfp4"
+        extra["mxfp4act_stack36_prefill_t8192"] = pre4
 
     cpu_v, cpu_n, cpu_s = (None, 0, 0.0)
     cpu_all = None
@@ -592,7 +618,7 @@ def run_ours(args):
         "cpu_baseline_all_cores": cpu_all,
         "step_us_distribution": main["step_us"],
         "workloads": extra,
-        "peaks": {"hbm_gbs": hbm_peak, "fp8_tflops": fp8_peak, "source": peak_src},
+        "peaks": {"hbm_gbs": hbm_peak, "fp8_tflops": fp8_peak, "fp4_tflops": fp4_peak, "source": peak_src},
         "setup_s": t_gen,
     }
     if rank == 0:
@@ -625,6 +651,80 @@ def run_case(T: int, calls: int):
         raise SystemExit(1)
 
 
+SWEEP_T = (1, 2, 4, 8, 12, 16, 24, 32, 48, 64, 96, 128, 256, 512, 1024, 2048, 4096, 8192)
+
+
+def _plans_for(T: int):
+    """Candidate (tile_rows, routing path) pairs for T tokens: every tile height the
+    kernels have, every routing path whose capacity covers T."""
+    routes = (["cluster"] if T <= 8 else []) + (["grid"] if T <= 32 else []) + ["tensor_core"]
+    rows = (8, 16, 32, 64, 128) if T <= 256 else (32, 64, 128)
+    return [(r, rt) for r in rows for rt in routes]
+
+
+def run_sweep(args):
+    """Plan sweep: for each T, the median step time of every candidate plan
+    (moe_set_plan) on the gpt-oss-shaped layer, layers rotated so that weights
+    stream from HBM; one JSON line per (T, plan), then the table of the fastest."""
+    import mxfp4_mixture_experts_gemv_gb300 as moe
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    if not os.path.exists(moe.LIB_PATH):
+        from mxfp4_mixture_experts_gemv_gb300 import build as b
+        b.build()
+    layers = Layers(args.layers, device)
+    routers = layers.routers(device=device)
+    best = {}
+    for T in SWEEP_T:
+        xs = [ms.make_tokens(0, T, H, layer=l).to(device) for l in range(layers.n)]
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        rows = []
+        for tr, rt in _plans_for(T):
+            moe.set_plan(tr, rt)
+            try:
+                ws = moe.alloc_workspace(layers.dims, T, K_TOP, device)
+                for l in range(layers.n):  # warm-up, and the plan must run
+                    moe.forward(layers.dims, xs[l], routers[l][0], routers[l][1], layers.packed[l], K_TOP, out=out,
+                                workspace=ws)
+                st = moe.device_status(ws)
+                if st != moe.MOE_OK:
+                    raise RuntimeError(f"device status {st}")
+                graphs = []
+                for i in range(args.steps):
+                    l = i % layers.n
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g):
+                        moe.forward(layers.dims, xs[l], routers[l][0], routers[l][1], layers.packed[l], K_TOP,
+                                    out=out, workspace=ws)
+                    graphs.append(g)
+                for g in graphs[:args.warmup]:
+                    g.replay()
+                torch.cuda.synchronize()
+                stream = torch.cuda.current_stream()
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)]
+                ev[0].record(stream)
+                for i, g in enumerate(graphs):
+                    g.replay()
+                    ev[i + 1].record(stream)
+                torch.cuda.synchronize()
+                us = statistics.median(ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(len(graphs)))
+                del graphs, ws
+            finally:
+                moe.set_plan(0, "auto")
+            line = {"sweep": "plan", "T": T, "tile_rows": tr, "route": rt, "step_us": us,
+                    "tokens_per_s": T / (us * 1e-6)}
+            rows.append(line)
+            print(json.dumps(line), flush=True)
+        # the automatic plan, for comparison
+        ws = moe.alloc_workspace(layers.dims, T, K_TOP, device)
+        lay = moe.workspace_layout(layers.dims, T, K_TOP)
+        fastest = min(rows, key=lambda r: r["step_us"])
+        best[T] = {"fastest": (fastest["tile_rows"], fastest["route"], round(fastest["step_us"], 1)),
+                   "auto_tile_rows": lay.tile_rows}
+        del ws
+    print(json.dumps({"sweep": "summary", "best": best}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -636,6 +736,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-stack", action="store_true", help="skip the 36-layer stack workloads")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of CPU oracle work")
+    ap.add_argument("--sweep", action="store_true",
+                    help="plan sweep: median step time of every tile-height and routing-path candidate per T")
     ap.add_argument("--case", type=int, default=None, metavar="T",
                     help="profiling run: one gpt-oss-shaped layer at T tokens, warmup + steps plain "
                          "forward calls, no timing and no JSON line (T=32 uses the skewed router)")
@@ -644,6 +746,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.case is not None:
         run_case(args.case, args.warmup + args.steps)
+    elif args.sweep:
+        run_sweep(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -163,6 +163,28 @@ moe_status moe_forward(moe_dims d, const void *hidden, int32_t T, const void *ro
                        void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * The layer with a choice of activation format (act_format):
+ *   MOE_ACT_MXFP8  x and h quantised to MXFP8 (E4M3, one E8M0 scale per 32): the
+ *                  FP8-activation x FP4-weight layer, identical to moe_forward;
+ *   MOE_ACT_MXFP4  x and h quantised to MXFP4 (E2M1 with the same OCP-style
+ *                  shared exponent, floor(log2 amax) - 2, round-to-nearest-even,
+ *                  saturating at +-6), run on the tensor cores as FP4 x FP4
+ *                  (tcgen05 kind::mxf4) with both operands packed.
+ * Passage: "GPT-OSS-120B with MXFP4 on DGX Spark (SM121/GB10)", section
+ * "Performance Optimizations" (native FP4 x FP4 block-scale MMA as the next
+ * step after FP8 x FP4); the activation rule is this library's reading of
+ * "Numerical Accuracy" (full-scale block activation quantisation), the same as
+ * for MXFP8.  Same arguments, weights, workspace and errors as moe_forward (an
+ * unknown act_format is MOE_ERR_INVALID_ARG); in the MXFP4 format the workspace's
+ * xq, xp and hq sections hold two codes per byte (rows of H/2 and I/2 bytes).
+ */
+#define MOE_ACT_MXFP8 0
+#define MOE_ACT_MXFP4 1
+moe_status moe_forward_act(moe_dims d, int32_t act_format, const void *hidden, int32_t T,
+                           const void *router_w, const void *router_b, const void *packed, int32_t top_k,
+                           void *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Allocation-free forward.  This entry point has no counterpart in the pages
  * the layer follows; it exists for callers that cannot allocate device memory
  * themselves: code whose device memory is owned by a host runtime that forbids
@@ -249,6 +271,24 @@ moe_status moe_debug_hold_waits(int32_t which);
  */
 moe_status moe_residual_rmsnorm(float *x_res, const void *layer_out, int32_t T, int32_t H, float eps,
                                 void *hidden, void *stream);
+
+/*
+ * Measurement hook for the tile and schedule selection (the pages' planned
+ * autotuner and small-tile variants: "GPT-OSS-120B with MXFP4 on DGX Spark
+ * (SM121/GB10)", "Performance Optimizations").  Forces the token rows per expert
+ * tile of the grouped GEMM (8, 16, 32, 64 or 128; 0 = the measured default for
+ * T) and the routing path (MOE_ROUTE_AUTO = the measured default; _CLUSTER needs
+ * T <= 8, _GRID T <= 32, _TENSOR_CORE any T).  Process-wide.  moe_workspace_size
+ * and moe_workspace_layout_get follow the tile override, so size workspaces
+ * after setting it.  A forced routing path that does not fit the call's T makes
+ * that forward return MOE_ERR_UNSUPPORTED_SHAPE.  Results do not depend on the
+ * plan; only the launch shapes do.  Invalid values are MOE_ERR_INVALID_ARG.
+ */
+#define MOE_ROUTE_AUTO 0
+#define MOE_ROUTE_CLUSTER 1
+#define MOE_ROUTE_GRID 2
+#define MOE_ROUTE_TENSOR_CORE 3
+moe_status moe_set_plan(int32_t tile_rows, int32_t route);
 
 /*
  * Optional per-stage timing of moe_forward with CUDA events (measurement; no

@@ -25,9 +25,9 @@ STATUS_NAMES = {
 
 # Every symbol the C ABI exports (include/moe.h).
 EXPORTED = ["moe_packed_size", "moe_pack_weights", "moe_workspace_size", "moe_workspace_layout_get",
-            "moe_forward", "moe_forward_static_scratch", "moe_static_scratch_status", "moe_static_scratch_bytes",
+            "moe_forward", "moe_forward_act", "moe_forward_static_scratch", "moe_static_scratch_status", "moe_static_scratch_bytes",
             "moe_get_device_status", "moe_set_wait_limit_ns", "moe_get_wait_limit_ns",
-            "moe_debug_hold_waits", "moe_profile_begin", "moe_profile_end", "moe_residual_rmsnorm",
+            "moe_debug_hold_waits", "moe_set_plan", "moe_profile_begin", "moe_profile_end", "moe_residual_rmsnorm",
             "moe_last_error", "moe_version"]
 STAGES = ["routing", "expert_mlp"]
 
@@ -76,6 +76,8 @@ def lib() -> ctypes.CDLL:
         L.moe_workspace_layout_get.argtypes = [Dims, i32, i32, ctypes.POINTER(WorkspaceLayout)]
         L.moe_forward.restype = st
         L.moe_forward.argtypes = [Dims, vp, i32, vp, vp, vp, i32, vp, vp, sz, vp]
+        L.moe_forward_act.restype = st
+        L.moe_forward_act.argtypes = [Dims, i32, vp, i32, vp, vp, vp, i32, vp, vp, sz, vp]
         L.moe_forward_static_scratch.restype = st
         L.moe_forward_static_scratch.argtypes = [Dims, vp, i32, vp, vp, vp, i32, vp, vp]
         L.moe_static_scratch_status.restype = st
@@ -88,6 +90,8 @@ def lib() -> ctypes.CDLL:
         L.moe_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
         L.moe_get_wait_limit_ns.restype = ctypes.c_uint64
         L.moe_get_wait_limit_ns.argtypes = []
+        L.moe_set_plan.restype = st
+        L.moe_set_plan.argtypes = [i32, i32]
         L.moe_debug_hold_waits.restype = st
         L.moe_debug_hold_waits.argtypes = [i32]
         L.moe_residual_rmsnorm.restype = st
@@ -179,21 +183,28 @@ def alloc_workspace(dims: LayerDims, T: int, top_k: int, device="cuda") -> torch
     return _alloc_aligned(max(workspace_size(dims, T, top_k), 256), device)
 
 
+ACT_FORMATS = {"mxfp8": 0, "mxfp4": 1}
+
+
 def forward(dims: LayerDims, hidden: torch.Tensor, router_w: torch.Tensor, router_b: torch.Tensor,
             packed: torch.Tensor, top_k: int, out: torch.Tensor | None = None,
-            workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """One MoE layer: bf16 hidden [T, H] -> bf16 out [T, H]."""
+            workspace: torch.Tensor | None = None, stream=None, act_format: str = "mxfp8") -> torch.Tensor:
+    """One MoE layer: bf16 hidden [T, H] -> bf16 out [T, H].
+
+    act_format "mxfp8" (moe_forward) or "mxfp4" (moe_forward_act, FP4 x FP4)."""
     T = hidden.shape[0]
     if out is None:
         out = torch.empty_like(hidden)
     if workspace is None:
         workspace = alloc_workspace(dims, T, top_k, hidden.device)
-    _check(lib().moe_forward(dims.c(), _dev_ptr(hidden, "hidden", torch.bfloat16), T,
-                             _dev_ptr(router_w, "router_w", torch.bfloat16),
-                             _dev_ptr(router_b, "router_b", torch.bfloat16),
-                             _dev_ptr(packed, "packed"), top_k, _dev_ptr(out, "out", torch.bfloat16),
-                             _dev_ptr(workspace, "workspace"),
-                             workspace.numel() * workspace.element_size(), _stream(stream)))
+    args = (_dev_ptr(hidden, "hidden", torch.bfloat16), T, _dev_ptr(router_w, "router_w", torch.bfloat16),
+            _dev_ptr(router_b, "router_b", torch.bfloat16), _dev_ptr(packed, "packed"), top_k,
+            _dev_ptr(out, "out", torch.bfloat16), _dev_ptr(workspace, "workspace"),
+            workspace.numel() * workspace.element_size(), _stream(stream))
+    if act_format == "mxfp8":
+        _check(lib().moe_forward(dims.c(), *args))
+    else:
+        _check(lib().moe_forward_act(dims.c(), ACT_FORMATS[act_format], *args))
     return out
 
 
@@ -256,6 +267,15 @@ def set_wait_limit_ns(ns: int):
 
 def wait_limit_ns() -> int:
     return lib().moe_get_wait_limit_ns()
+
+
+ROUTES = {"auto": 0, "cluster": 1, "grid": 2, "tensor_core": 3}
+
+
+def set_plan(tile_rows: int = 0, route: str = "auto"):
+    """Force the token rows per expert tile (0 = default) and the routing path
+    ("auto", "cluster", "grid", "tensor_core") of later forwards (measurement hook)."""
+    _check(lib().moe_set_plan(tile_rows, ROUTES[route]))
 
 
 HOLD_DOWN_UNITS = 1

@@ -43,6 +43,8 @@ constexpr int kStages = 2;  // routing (all routing kernels), expert MLP
 
 std::atomic<uint64_t> g_wait_limit_ns{moe::kWaitLimitNsDefault};
 std::atomic<int> g_hold_waits{0};
+std::atomic<int> g_plan_tile_rows{0};
+std::atomic<int> g_plan_route{0};
 
 // Per-stage CUDA events of profiled forward calls.
 struct Profiler {
@@ -79,6 +81,8 @@ moe_status report_error(moe_status st, const char* fmt, ...) {
 
 uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 int debug_hold_waits() { return g_hold_waits.load(std::memory_order_relaxed); }
+int plan_tile_rows() { return g_plan_tile_rows.load(std::memory_order_relaxed); }
+int plan_route() { return g_plan_route.load(std::memory_order_relaxed); }
 
 moe_status check_forward_args(const moe_dims& d, const void* hidden, int32_t T, const void* router_w,
                               const void* router_b, const void* packed, int32_t top_k, const void* out) {
@@ -156,9 +160,14 @@ moe_status moe_workspace_layout_get(moe_dims d, int32_t T, int32_t top_k, moe_wo
   return MOE_OK;
 }
 
-moe_status moe_forward(moe_dims d, const void* hidden, int32_t T, const void* router_w, const void* router_b,
-                       const void* packed, int32_t top_k, void* out, void* workspace, size_t workspace_bytes,
-                       void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The forward for either activation format (MXFP8, or MXFP4 with fp4).
+moe_status forward_impl(moe_dims d, bool fp4, const void* hidden, int32_t T, const void* router_w,
+                        const void* router_b, const void* packed, int32_t top_k, void* out, void* workspace,
+                        size_t workspace_bytes, void* stream) {
   moe_status st = moe::check_forward_args(d, hidden, T, router_w, router_b, packed, top_k, out);
   if (st != MOE_OK || T == 0) return st;
   if (!workspace) return fail(MOE_ERR_INVALID_ARG, "null workspace");
@@ -183,9 +192,18 @@ moe_status moe_forward(moe_dims d, const void* hidden, int32_t T, const void* ro
   int32_t* sorted_rows = reinterpret_cast<int32_t*>(at(L.sorted_rows));
   const int sms = num_sms();
 
+  // routing path: a few tokens in one cluster, batched decode in one cooperative
+  // grid, else the tensor-core router with separate grouping and gather passes
+  const int forced = moe::plan_route();
+  const bool cluster_fits = moe::route_cluster_fits(T, d.E, d.H), grid_fits = moe::route_small_fits(T, d.H);
+  const int route = forced != moe::kRouteAuto
+                        ? forced
+                        : (cluster_fits ? moe::kRouteCluster : (grid_fits ? moe::kRouteGrid : moe::kRouteTensorCore));
+  if ((route == moe::kRouteCluster && !cluster_fits) || (route == moe::kRouteGrid && !grid_fits))
+    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "the forced routing path %d does not fit T=%d", route, T);
   // The cluster routing kernel clears the status words and counters itself; the
   // other paths start from a memset.
-  const bool cluster_route = moe::route_cluster_fits(T, d.E, d.H);
+  const bool cluster_route = route == moe::kRouteCluster;
   cudaError_t e = cudaSuccess;
   if (!cluster_route) {
     e = cudaMemsetAsync(ws, 0, L.zero_bytes, s);
@@ -216,9 +234,9 @@ moe_status moe_forward(moe_dims d, const void* hidden, int32_t T, const void* ro
     o.zero_words = (int)(L.zero_bytes / 4);
     o.status = status;
     e = moe::launch_route_cluster(static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(router_w),
-                                  static_cast<const uint16_t*>(router_b), T, d.H, d.E, top_k, L.tile_rows, o, s);
+                                  static_cast<const uint16_t*>(router_b), T, d.H, d.E, top_k, L.tile_rows, fp4, o, s);
     if (e != cudaSuccess) return cuda_fail(e, "cluster routing kernel");
-  } else if (moe::route_small_fits(T, d.H)) {
+  } else if (route == moe::kRouteGrid) {
     // decode: routing, quantisation, grouping and gather in one launch
     moe::RouteSmallOut o;
     o.logits = reinterpret_cast<float*>(at(L.logits));
@@ -238,7 +256,7 @@ moe_status moe_forward(moe_dims d, const void* hidden, int32_t T, const void* ro
     o.status = status;
     e = moe::launch_route_small(static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(router_w),
                                 static_cast<const uint16_t*>(router_b), T, d.H, d.E, d.I, top_k, L.tile_rows,
-                                L.max_tiles, o, s);
+                                L.max_tiles, fp4, o, s);
     if (e != cudaSuccess) return cuda_fail(e, "small-batch routing kernel");
   } else {
     // larger T: tensor-core router with top-k in its epilogue, grouping, quantise-on-gather
@@ -252,7 +270,7 @@ moe_status moe_forward(moe_dims d, const void* hidden, int32_t T, const void* ro
                             reinterpret_cast<int32_t*>(at(L.y)), s);
     if (e != cudaSuccess) return cuda_fail(e, "grouping kernel");
     e = moe::launch_gather_quant(static_cast<const uint16_t*>(hidden), inv_pos, tiles, L.max_tiles, T, top_k, d.H,
-                                 at(L.xq), at(L.xs), at(L.xp), at(L.xp_sf), s);
+                                 fp4, at(L.xq), at(L.xs), at(L.xp), at(L.xp_sf), s);
     if (e != cudaSuccess) return cuda_fail(e, "gather kernel");
   }
   mark(1);
@@ -275,7 +293,7 @@ moe_status moe_forward(moe_dims d, const void* hidden, int32_t T, const void* ro
   // Many tokens: a streaming pass after the expert kernel, which would otherwise
   // stall on the slot loads of every completed token.
   b.fused_combine = L.tile_rows <= 32;
-  e = moe::launch_expert_mlp(h, pk, b, T, top_k, L.max_tiles, L.tile_rows, sms, s);
+  e = moe::launch_expert_mlp(h, pk, b, T, top_k, L.max_tiles, L.tile_rows, sms, fp4, s);
   if (e != cudaSuccess) return cuda_fail(e, "expert MLP kernel");
   if (!b.fused_combine) {
     e = moe::launch_combine(b.y, inv_pos, w, T, top_k, d.H, static_cast<uint16_t*>(out), s);
@@ -283,6 +301,26 @@ moe_status moe_forward(moe_dims d, const void* hidden, int32_t T, const void* ro
   }
   mark(2);
   return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_forward(moe_dims d, const void* hidden, int32_t T, const void* router_w, const void* router_b,
+                       const void* packed, int32_t top_k, void* out, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  return forward_impl(d, false, hidden, T, router_w, router_b, packed, top_k, out, workspace, workspace_bytes,
+                      stream);
+}
+
+moe_status moe_forward_act(moe_dims d, int32_t act_format, const void* hidden, int32_t T, const void* router_w,
+                           const void* router_b, const void* packed, int32_t top_k, void* out, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  if (act_format != MOE_ACT_MXFP8 && act_format != MOE_ACT_MXFP4)
+    return fail(MOE_ERR_INVALID_ARG, "unknown activation format %d", act_format);
+  return forward_impl(d, act_format == MOE_ACT_MXFP4, hidden, T, router_w, router_b, packed, top_k, out, workspace,
+                      workspace_bytes, stream);
 }
 
 moe_status moe_residual_rmsnorm(float* x_res, const void* layer_out, int32_t T, int32_t H, float eps, void* hidden,
@@ -347,6 +385,15 @@ moe_status moe_set_wait_limit_ns(uint64_t ns) {
 }
 
 uint64_t moe_get_wait_limit_ns(void) { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
+moe_status moe_set_plan(int32_t tile_rows, int32_t route) {
+  if (tile_rows != 0 && tile_rows != 8 && tile_rows != 16 && tile_rows != 32 && tile_rows != 64 && tile_rows != 128)
+    return fail(MOE_ERR_INVALID_ARG, "tile_rows=%d is not 0, 8, 16, 32, 64 or 128", tile_rows);
+  if (route < MOE_ROUTE_AUTO || route > MOE_ROUTE_TENSOR_CORE) return fail(MOE_ERR_INVALID_ARG, "route=%d", route);
+  g_plan_tile_rows.store(tile_rows, std::memory_order_relaxed);
+  g_plan_route.store(route, std::memory_order_relaxed);
+  return MOE_OK;
+}
 
 moe_status moe_debug_hold_waits(int32_t which) {
   if (which & ~(MOE_DEBUG_HOLD_DOWN_UNITS | MOE_DEBUG_HOLD_ROUTING_BARRIER))

@@ -93,6 +93,12 @@ constexpr int kRouteClusterMaxT = 8;
 constexpr size_t kRouteClusterMaxSmem = 200 * 1024;
 bool route_cluster_fits(int T, int E, int H);
 
+// Measurement overrides of the plan (moe_set_plan), process-wide: token rows per
+// tile (0 = automatic) and the routing path (kRouteAuto = automatic).
+enum : int { kRouteAuto = 0, kRouteCluster = 1, kRouteGrid = 2, kRouteTensorCore = 3 };
+int plan_tile_rows();
+int plan_route();
+
 // Token rows per tile of the grouped GEMM (MMA N upper bound): a token visits an
 // expert at most once, so up to 64 tokens one tile of the next size covers any
 // expert; beyond that 128 (measured: smaller tiles re-read the weights of
@@ -100,6 +106,7 @@ bool route_cluster_fits(int T, int E, int H);
 inline int tile_rows_for(int T, int k, int E) {
   (void)k;
   (void)E;
+  if (const int forced = plan_tile_rows()) return forced;
   if (T <= 8) return 8;  // a token visits an expert at most once: at most T rows per tile
   if (T <= 16) return 16;
   if (T <= 32) return 32;
@@ -186,8 +193,11 @@ cudaError_t launch_router_tc(const uint16_t* x, const uint16_t* wr, const uint16
 cudaError_t launch_permute(const int32_t* ids, int TK, int k, int E, int tile_rows, int max_tiles,
                            int32_t* counts, int32_t* offsets, int32_t* sorted_rows, int32_t* inv_pos,
                            int32_t* tiles, int32_t* scratch, cudaStream_t s);
+// Activations are quantised to MXFP8 (fp4 false: one E4M3 code byte per element)
+// or MXFP4 (fp4 true: two E2M1 codes per byte), one E8M0 scale per 32 elements.
 cudaError_t launch_gather_quant(const uint16_t* x, const int32_t* inv_pos, const int32_t* tiles, int max_tiles, int T,
-                                int k, int H, uint8_t* xq, uint8_t* xs, uint8_t* xp, uint8_t* xp_sf, cudaStream_t s);
+                                int k, int H, bool fp4, uint8_t* xq, uint8_t* xs, uint8_t* xp, uint8_t* xp_sf,
+                                cudaStream_t s);
 
 cudaError_t launch_residual_rmsnorm(float* x_res, const uint16_t* layer_out, int T, int H, float eps,
                                     uint16_t* hidden, cudaStream_t s);
@@ -210,7 +220,7 @@ struct RouteSmallOut {
   uint32_t* status;
 };
 cudaError_t launch_route_small(const uint16_t* x, const uint16_t* wr, const uint16_t* br, int T, int H, int E, int I,
-                               int k, int tile_rows, int max_tiles, const RouteSmallOut& o, cudaStream_t s);
+                               int k, int tile_rows, int max_tiles, bool fp4, const RouteSmallOut& o, cudaStream_t s);
 
 struct RouteClusterOut {
   float* logits;
@@ -230,7 +240,7 @@ struct RouteClusterOut {
   uint32_t* status;
 };
 cudaError_t launch_route_cluster(const uint16_t* x, const uint16_t* wr, const uint16_t* br, int T, int H, int E,
-                                 int k, int tile_rows, const RouteClusterOut& o, cudaStream_t s);
+                                 int k, int tile_rows, bool fp4, const RouteClusterOut& o, cudaStream_t s);
 
 struct ExpertMlpBuffers {
   const uint8_t* xp;        // gate_up B rows [TK][H]
@@ -252,7 +262,9 @@ struct ExpertMlpBuffers {
 // out[t] = bf16(sum_j w[t][j] * y[inv_pos[t][j]]), slots in order, fp32 sums.
 cudaError_t launch_combine(const float* y, const int32_t* inv_pos, const float* topk_w, int T, int k, int H,
                            uint16_t* out, cudaStream_t s);
+// fp4: activations (xp, hq) in MXFP4 and the tcgen05 kind::mxf4 MMA; else MXFP8
+// and kind::mxf8f6f4.
 cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, const ExpertMlpBuffers& b, int T, int k,
-                              int max_tiles, int tile_rows, int num_sms, cudaStream_t s);
+                              int max_tiles, int tile_rows, int num_sms, bool fp4, cudaStream_t s);
 
 }  // namespace moe

@@ -2,6 +2,10 @@
 // (kind::mxf8f6f4 block-scaled MMA): E2M1 weights (A, 128 rows per tile) x E4M3
 // activations (B, up to BN token rows per tile), one E8M0 scale per 32
 // contraction elements on both sides, fp32 accumulation in tensor memory.
+// The FP4 x FP4 variant (FP4 = true) quantises the activations to MXFP4 as well
+// and runs kind::mxf4 on packed E2M1 operands ("GPT-OSS-120B with MXFP4 on DGX
+// Spark (SM121/GB10)", "Performance Optimizations": native FP4 x FP4
+// block-scale MMA); both operands then stay packed in shared memory.
 //
 //   gate_up tiles: g = Xp . Wgu[e]^T + bgu[e]; epilogue h = silu(gate) * up, MXFP8(h)
 //   down tiles:    y = hq . Wd[e]^T + bd[e];   epilogue writes y, then the
@@ -55,15 +59,22 @@ namespace {
 template <int BN>
 constexpr int stage_ktiles() { return BN == 8 ? 4 : (BN <= 32 ? 3 : 2); }
 
+// Shared-memory bytes of one 128-element k-tile row of an operand: 128 for E4M3
+// and for E2M1 weights unpacked by TMA for kind::mxf8f6f4 (16 codes per 16-byte
+// chunk), 64 for packed E2M1 (kind::mxf4).
+template <bool FP4>
+constexpr uint32_t smem_row_bytes() { return FP4 ? 64u : 128u; }
+
 // Tiles are claimed from a global counter by the producer warp and handed to the
 // MMA and epilogue warps through a small queue in shared memory.
 constexpr int kTileQ = 4;
 
-template <int BN>
+template <int BN, bool FP4>
 struct GemmCfg {
   static constexpr int kKS = stage_ktiles<BN>();
-  static constexpr uint32_t kA1 = kTileM * kTileK;      // 16 KB smem per weight k-tile (4-bit unpacked form)
-  static constexpr uint32_t kB1 = BN * kTileK;          // BN rows x 128 B of E4M3 per k-tile
+  static constexpr uint32_t kRow = smem_row_bytes<FP4>();
+  static constexpr uint32_t kA1 = kTileM * kRow;        // smem per weight k-tile (16 KB unpacked, 8 KB packed)
+  static constexpr uint32_t kB1 = BN * kRow;            // BN activation rows per k-tile
   static constexpr uint32_t kA = kKS * kA1;
   static constexpr uint32_t kB = kKS * kB1;
   static constexpr uint32_t kSF = 2 * kKS * kAtomBytes;  // scale atoms of A (first half) and B
@@ -193,10 +204,10 @@ struct Maps {
   CUtensorMap xp[kActBoxes], hq[kActBoxes];
 };
 
-template <int BN>
+template <int BN, bool FP4>
 __global__ void __launch_bounds__(192, 1)
     expert_mlp_kernel(const __grid_constant__ Maps maps, const MlpParams p) {
-  using C = GemmCfg<BN>;
+  using C = GemmCfg<BN, FP4>;
   constexpr int kKS = C::kKS;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -307,21 +318,53 @@ __global__ void __launch_bounds__(192, 1)
       const int rows_m = min(kTileM, rows_stored - r.m * kTileM);  // 64 for a tail m-tile
       const int bi = min(act_box_index(td.z), kActBoxes - 1);
       const CUtensorMap* bmap = r.gu ? &maps.xp[bi] : &maps.hq[bi];
-      const uint32_t b_bytes = (uint32_t)act_box_rows(bi) * kTileK;
+      const uint32_t b_bytes = (uint32_t)act_box_rows(bi) * C::kRow;
       const int row0_unit = (int)tile_row0(td.x, r.m, 0, rows_stored, k_tiles);
+      // weight (A) copies of stage slot `ss`: the nk weight tiles are rows_m * nk
+      // consecutive 64-byte rows (128 bytes each in shared memory when unpacked),
+      // boxes of 256, 128 or 64 rows, then their scale atoms
+      auto issue_a = [&](int ss, int kt, int nk) {
+        const int a_rows = rows_m * nk;
+        const int row0 = row0_unit + kt * rows_m;
+        for (int off = 0; off < a_rows;) {
+          const int c = a_rows - off >= 256 ? 256 : a_rows - off >= 128 ? 128 : 64;
+          const CUtensorMap* amap = r.gu ? (c == 256 ? &maps.gu2 : (c == 128 ? &maps.gu : &maps.gut))
+                                         : (c == 256 ? &maps.d2 : (c == 128 ? &maps.d : &maps.dt));
+          tma_load_2d_hint(sA + ss * C::kA + off * C::kRow, amap, &full[ss], 0, row0 + off, wpol);
+          off += c;
+        }
+      };
       // activation (B) copies of stage slot `ss` covering k-tiles kt..kt+nk-1
       auto issue_b = [&](int ss, int kt, int nk) {
         for (int j = 0; j < nk; ++j)
-          tma_load_2d(sB + ss * C::kB + j * C::kB1, bmap, &full[ss], (kt + j) * kTileK, td.y);
-        bulk_g2s(sSF + ss * C::kSF + kKS * kAtomBytes, sfb + kt * kAtomBytes, nk * kAtomBytes, &full[ss]);
+          tma_load_2d(sB + ss * C::kB + j * C::kB1, bmap, &full[ss], (kt + j) * (int)C::kRow, td.y);
+      };
+      auto stage_bytes = [&](int nk) {
+        return (uint32_t)(rows_m * nk * kTileRowBytes + nk * (b_bytes + 2 * kAtomBytes));
       };
       // A down unit's hq is ready once all gate_up m-tiles of its token tile are
-      // counted; until then its stages get their weight copies only, and the
-      // activation copies of those stages follow the (bounded) wait.
-      bool dep_ok = r.gu;
-      bool dep_timeout = false;
+      // counted.  If it is not ready yet, the unit's first stages get their weight
+      // copies only, and the activation copies of those stages follow the
+      // (bounded) wait.
       const int dep_target = p.gu_mtiles + p.dep_extra;
+      bool dep_ok = r.gu || __all_sync(0xffffffffu, ld_acquire_gpu(p.done_gu + r.b) >= dep_target);
+      if (!r.gu && dep_ok) fence_proxy_async_global();  // hq was written by generic stores; TMA reads it
+      bool dep_timeout = false;
       int pend_s = 0, pend_kt = 0, pend_n = 0;  // stages waiting for their activation copies
+      // activation copies of the stages that wait for them.  After an expired wait
+      // the copies still go out (they read in-bounds workspace bytes), so that every
+      // stage's phase completes before the roles wind down.
+      auto flush_pending = [&]() {
+        fence_proxy_async_global();
+        if (elect_one())
+          for (int j = 0; j < pend_n; ++j) {
+            const int kk = pend_kt + j * kKS, nn = min(kKS, k_tiles - kk), ss = (pend_s + j) % S;
+            issue_b(ss, kk, nn);
+            bulk_g2s(sSF + ss * C::kSF + kKS * kAtomBytes, sfb + kk * kAtomBytes, nn * kAtomBytes, &full[ss]);
+          }
+        __syncwarp();
+        pend_n = 0;
+      };
       for (int kt = 0; kt < k_tiles; kt += kKS) {
         const int nk = min(kKS, k_tiles - kt);
         const int st = kt / kKS;
@@ -330,20 +373,6 @@ __global__ void __launch_bounds__(192, 1)
           next = __shfl_sync(0xffffffffu, claim, 0);
           if (next < total) td_next = tl[tile_ref(next, n_gu, p).b];
         }
-        // activation copies of the stages that wait for them (none after this)
-        auto flush_pending = [&]() {
-          // hq was written by generic stores; TMA reads it.  After an expired wait the
-          // copies still go out (they read in-bounds workspace bytes), so that every
-          // stage's phase completes before the roles wind down.
-          fence_proxy_async_global();
-          if (elect_one())
-            for (int j = 0; j < pend_n; ++j) {
-              const int kk = pend_kt + j * kKS;
-              issue_b((pend_s + j) % S, kk, min(kKS, k_tiles - kk));
-            }
-          __syncwarp();
-          pend_n = 0;
-        };
         if (!mbar_wait_warp(&empty[s], ph ^ 1u, p.wait_ns)) {
           if (lane == 0) {
             atomicOr(p.status, kStatusTimeoutProducer);
@@ -353,26 +382,23 @@ __global__ void __launch_bounds__(192, 1)
           ok = false;
           break;
         }
-        if (elect_one()) {
-          // the nk weight tiles are rows_m * nk consecutive 64-byte rows (128 bytes
-          // each in shared memory): boxes of 256, 128 or 64 rows
-          const int a_rows = rows_m * nk;
-          mbar_arrive_expect_tx(&full[s], (uint32_t)(a_rows * kTileRowBytes + nk * (b_bytes + 2 * kAtomBytes)));
-          const int row0 = row0_unit + kt * rows_m;
-          for (int off = 0; off < a_rows;) {
-            const int c = a_rows - off >= 256 ? 256 : a_rows - off >= 128 ? 128 : 64;
-            const CUtensorMap* amap = r.gu ? (c == 256 ? &maps.gu2 : (c == 128 ? &maps.gu : &maps.gut))
-                                           : (c == 256 ? &maps.d2 : (c == 128 ? &maps.d : &maps.dt));
-            tma_load_2d_hint(sA + s * C::kA + off * kTileK, amap, &full[s], 0, row0 + off, wpol);
-            off += c;
-          }
-          bulk_g2s_hint(sSF + s * C::kSF, sfa + kt * kAtomBytes, nk * kAtomBytes, &full[s], wpol);
-        }
-        __syncwarp();
         if (dep_ok) {
-          if (elect_one()) issue_b(s, kt, nk);
+          if (elect_one()) {
+            mbar_arrive_expect_tx(&full[s], stage_bytes(nk));
+            issue_a(s, kt, nk);
+            issue_b(s, kt, nk);
+            uint8_t* sf = sSF + s * C::kSF;
+            bulk_g2s_hint(sf, sfa + kt * kAtomBytes, nk * kAtomBytes, &full[s], wpol);
+            bulk_g2s(sf + kKS * kAtomBytes, sfb + kt * kAtomBytes, nk * kAtomBytes, &full[s]);
+          }
           __syncwarp();
         } else {
+          if (elect_one()) {
+            mbar_arrive_expect_tx(&full[s], stage_bytes(nk));
+            issue_a(s, kt, nk);
+            bulk_g2s_hint(sSF + s * C::kSF, sfa + kt * kAtomBytes, nk * kAtomBytes, &full[s], wpol);
+          }
+          __syncwarp();
           if (pend_n == 0) {
             pend_s = s;
             pend_kt = kt;
@@ -446,7 +472,8 @@ __global__ void __launch_bounds__(192, 1)
       // B rows past the unit's rows are never read back
       const uint32_t n_mma = (uint32_t)max(16, min(BN, (td.z + 15) & ~15));
       const uint32_t d_tmem = tmem + (uint32_t)acc * 128u;
-      const uint32_t idesc0 = idesc_mxf8f6f4(128, n_mma, 5 /*E2M1*/, 0 /*E4M3*/, 0, 0);
+      const uint32_t idesc0 = FP4 ? idesc_mxf8f6f4(128, n_mma, 1 /*E2M1*/, 1 /*E2M1*/, 0, 0)
+                                  : idesc_mxf8f6f4(128, n_mma, 5 /*E2M1*/, 0 /*E4M3*/, 0, 0);
       for (int kt = 0; kt < k_tiles; kt += kKS) {
         const int nk = min(kKS, k_tiles - kt);
         if (!mbar_wait_warp(&full[s], ph, p.wait_ns)) {
@@ -467,14 +494,25 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t sfa_t = sf_t + 8u * j, sfb_t = sfa_t + 4u;
             tmem_cp_32x128b_x4(sfa_t, sdesc_sf_atom(sf_s + j * kAtomBytes));
             tmem_cp_32x128b_x4(sfb_t, sdesc_sf_atom(sf_s + (kKS + j) * kAtomBytes));
-            // weight k-tile j starts rows_m rows into the stage (8 or 16 KB, a swizzle-atom multiple)
-            const uint64_t ad = sdesc_sw128(a_s + (uint32_t)(j * rows_m * kTileK));
-            const uint64_t bd = sdesc_sw128(b_s + j * C::kB1);
+            // weight k-tile j starts rows_m rows into the stage (a swizzle-atom multiple)
+            const uint32_t a_j = a_s + (uint32_t)(j * rows_m) * C::kRow, b_j = b_s + j * C::kB1;
+            if constexpr (FP4) {
+              // two MMAs of K = 64 (32 bytes of each 64-byte row); each takes two of the
+              // row's four block scales, starting at byte 2kk
+              const uint64_t ad = sdesc_sw64(a_j), bd = sdesc_sw64(b_j);
 #pragma unroll
-            for (uint32_t kk = 0; kk < 4; ++kk) {
-              // block-scale ids pick byte kk of the scale columns (bits 4-5 for B, 29-30 for A)
-              const uint32_t idesc = idesc0 | (kk << 4) | (kk << 29);
-              umma_mxf8f6f4(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, sfa_t, sfb_t, (kt + j + (int)kk) != 0);
+              for (uint32_t kk = 0; kk < 2; ++kk) {
+                const uint32_t idesc = idesc0 | ((2u * kk) << 4) | ((2u * kk) << 29);
+                umma_mxf4(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, sfa_t, sfb_t, (kt + j + (int)kk) != 0);
+              }
+            } else {
+              const uint64_t ad = sdesc_sw128(a_j), bd = sdesc_sw128(b_j);
+#pragma unroll
+              for (uint32_t kk = 0; kk < 4; ++kk) {
+                // block-scale ids pick byte kk of the scale columns (bits 4-5 for B, 29-30 for A)
+                const uint32_t idesc = idesc0 | (kk << 4) | (kk << 29);
+                umma_mxf8f6f4(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, sfa_t, sfb_t, (kt + j + (int)kk) != 0);
+              }
             }
           }
           umma_commit(&empty[s]);
@@ -583,18 +621,28 @@ __global__ void __launch_bounds__(192, 1)
             for (int i = 0; i < 16; ++i) h[i] = 0.f;
           }
           amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-          const int sx = mx_scale_exp(amax);
+          const int sx = FP4 ? mx_scale_exp<2>(amax) : mx_scale_exp<8>(amax);
           const float inv = mx_pow2_neg(sx);
           uint32_t pk[4];
+          if constexpr (FP4) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t lo = cvt_e4m3x2(h[4 * i] * inv, h[4 * i + 1] * inv);
-            const uint32_t hi = cvt_e4m3x2(h[4 * i + 2] * inv, h[4 * i + 3] * inv);
-            pk[i] = lo | (hi << 16);
+            for (int i = 0; i < 16; ++i) h[i] *= inv;
+            pk[0] = cvt_e2m1x8(h);
+            pk[1] = cvt_e2m1x8(h + 8);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t lo = cvt_e4m3x2(h[4 * i] * inv, h[4 * i + 1] * inv);
+              const uint32_t hi = cvt_e4m3x2(h[4 * i + 2] * inv, h[4 * i + 3] * inv);
+              pk[i] = lo | (hi << 16);
+            }
           }
           if (ok && active && n < rows) {
-            *reinterpret_cast<uint4*>(p.hq + (int64_t)(td.y + n) * p.I + r.m * 64 + 32 * rb + 16 * hh) =
-                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            const int64_t col = r.m * 64 + 32 * rb + 16 * hh;  // first intermediate of this half block
+            if constexpr (FP4)
+              *reinterpret_cast<uint2*>(p.hq + (int64_t)(td.y + n) * (p.I / 2) + col / 2) = make_uint2(pk[0], pk[1]);
+            else
+              *reinterpret_cast<uint4*>(p.hq + (int64_t)(td.y + n) * p.I + col) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             if (hh == 0) {
               uint8_t* wd = p.hq_sf + ((int64_t)r.b * p.d_ktiles + (kb >> 2)) * kAtomBytes + (n & 31) * 16 + (n >> 5) * 4;
               wd[kb & 3] = (uint8_t)(sx + 127);
@@ -725,26 +773,41 @@ bool make_weight_map(CUtensorMap* map, const uint8_t* base, int64_t total_rows, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Activations: 2-D [rows][K] bytes (E4M3 codes), rows of the grouped order.
-bool make_act_map(CUtensorMap* map, const uint8_t* base, int K, int rows, int box_rows) {
+// The same layout seen as packed bytes (kind::mxf4 reads E2M1 two per byte): 64-byte
+// rows, 64-byte swizzle.
+bool make_weight_map_packed(CUtensorMap* map, const uint8_t* base, int64_t total_rows, int box_rows) {
   auto enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)K};
-  cuuint32_t box[2] = {kTileK, (cuuint32_t)box_rows};
+  cuuint64_t dims[2] = {(cuuint64_t)kTileRowBytes, (cuuint64_t)total_rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kTileRowBytes};
+  cuuint32_t box[2] = {(cuuint32_t)kTileRowBytes, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN>
+// Activations: 2-D [rows][row_bytes] (E4M3 codes, or E2M1 codes two per byte),
+// rows of the grouped order; a box covers one 128-element k-tile.
+bool make_act_map(CUtensorMap* map, const uint8_t* base, int row_bytes, int rows, int box_rows, bool fp4) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {fp4 ? (cuuint32_t)kTileRowBytes : (cuuint32_t)kTileK, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, fp4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, bool FP4>
 cudaError_t launch_bn(const Maps& m, const MlpParams& p, int grid, cudaStream_t s) {
-  using C = GemmCfg<BN>;
+  using C = GemmCfg<BN, FP4>;
   static bool attr = false;
   if (!attr) {
     cudaError_t e =
-        cudaFuncSetAttribute(expert_mlp_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+        cudaFuncSetAttribute(expert_mlp_kernel<BN, FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
@@ -763,7 +826,7 @@ cudaError_t launch_bn(const Maps& m, const MlpParams& p, int grid, cudaStream_t 
   attrs[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, expert_mlp_kernel<BN>, m, p);
+  return cudaLaunchKernelEx(&cfg, expert_mlp_kernel<BN, FP4>, m, p);
 }
 
 }  // namespace
@@ -774,20 +837,21 @@ struct MapKey {
   const uint8_t* xp;
   const uint8_t* hq;
   int E, H, I, TK, tile_rows;
+  bool fp4;
   bool operator==(const MapKey& o) const {
     return packed == o.packed && xp == o.xp && hq == o.hq && E == o.E && H == o.H && I == o.I && TK == o.TK &&
-           tile_rows == o.tile_rows;
+           tile_rows == o.tile_rows && fp4 == o.fp4;
   }
 };
 
 cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, const ExpertMlpBuffers& b, int T, int k,
-                              int max_tiles, int tile_rows, int num_sms, cudaStream_t s) {
+                              int max_tiles, int tile_rows, int num_sms, bool fp4, cudaStream_t s) {
   const int TK = T * k;
   static std::mutex mu;
   static MapKey keys[32];
   static Maps cache[32];
   static int n_cached = 0, next_slot = 0;
-  const MapKey key{packed, b.xp, b.hq, h.E, h.H, h.I, TK, tile_rows};
+  const MapKey key{packed, b.xp, b.hq, h.E, h.H, h.I, TK, tile_rows, fp4};
   Maps m;
   bool hit = false;
   {
@@ -802,17 +866,17 @@ cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, cons
   if (!hit) {
   const int64_t gu_rows = (int64_t)h.E * h.gu_rows_stored * h.gu_ktiles;
   const int64_t d_rows = (int64_t)h.E * h.d_rows_stored * h.d_ktiles;
-  if (!make_weight_map(&m.gu2, packed + h.off_gu_data, gu_rows, 2 * kTileM) ||
-      !make_weight_map(&m.gu, packed + h.off_gu_data, gu_rows, kTileM) ||
-      !make_weight_map(&m.gut, packed + h.off_gu_data, gu_rows, 64) ||
-      !make_weight_map(&m.d2, packed + h.off_d_data, d_rows, 2 * kTileM) ||
-      !make_weight_map(&m.d, packed + h.off_d_data, d_rows, kTileM) ||
-      !make_weight_map(&m.dt, packed + h.off_d_data, d_rows, 64))
+  auto wmap = fp4 ? make_weight_map_packed : make_weight_map;
+  if (!wmap(&m.gu2, packed + h.off_gu_data, gu_rows, 2 * kTileM) ||
+      !wmap(&m.gu, packed + h.off_gu_data, gu_rows, kTileM) || !wmap(&m.gut, packed + h.off_gu_data, gu_rows, 64) ||
+      !wmap(&m.d2, packed + h.off_d_data, d_rows, 2 * kTileM) || !wmap(&m.d, packed + h.off_d_data, d_rows, kTileM) ||
+      !wmap(&m.dt, packed + h.off_d_data, d_rows, 64))
     return cudaErrorInvalidValue;
   for (int i = 0; i < kActBoxes; ++i) {
     // boxes taller than the token tile are never used; encode them at its height
     const int rows = std::min(act_box_rows(i), tile_rows);
-    if (!make_act_map(&m.xp[i], b.xp, h.H, TK, rows) || !make_act_map(&m.hq[i], b.hq, h.I, TK, rows))
+    if (!make_act_map(&m.xp[i], b.xp, fp4 ? h.H / 2 : h.H, TK, rows, fp4) ||
+        !make_act_map(&m.hq[i], b.hq, fp4 ? h.I / 2 : h.I, TK, rows, fp4))
       return cudaErrorInvalidValue;
   }
     std::lock_guard<std::mutex> lk(mu);
@@ -856,11 +920,11 @@ cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, cons
   p.fused_combine = b.fused_combine ? 1 : 0;
   const int grid = (int)std::min<int64_t>(num_sms, (int64_t)max_tiles * (h.gu_mtiles + h.d_mtiles));
   switch (tile_rows) {
-    case 8: return launch_bn<8>(m, p, grid, s);
-    case 16: return launch_bn<16>(m, p, grid, s);
-    case 32: return launch_bn<32>(m, p, grid, s);
-    case 64: return launch_bn<64>(m, p, grid, s);
-    case 128: return launch_bn<128>(m, p, grid, s);
+    case 8: return fp4 ? launch_bn<8, true>(m, p, grid, s) : launch_bn<8, false>(m, p, grid, s);
+    case 16: return fp4 ? launch_bn<16, true>(m, p, grid, s) : launch_bn<16, false>(m, p, grid, s);
+    case 32: return fp4 ? launch_bn<32, true>(m, p, grid, s) : launch_bn<32, false>(m, p, grid, s);
+    case 64: return fp4 ? launch_bn<64, true>(m, p, grid, s) : launch_bn<64, false>(m, p, grid, s);
+    case 128: return fp4 ? launch_bn<128, true>(m, p, grid, s) : launch_bn<128, false>(m, p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

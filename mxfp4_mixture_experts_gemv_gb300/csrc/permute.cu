@@ -133,8 +133,8 @@ constexpr int kGatherWarps = 8;
 
 __global__ void __launch_bounds__(32 * kGatherWarps) gather_tok_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ inv_pos, const int32_t* __restrict__ tiles,
-    int max_tiles, int T, int k, int H, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs, uint8_t* __restrict__ xp,
-    uint8_t* __restrict__ xp_sf) {
+    int max_tiles, int T, int k, int H, int fp4, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
+    uint8_t* __restrict__ xp, uint8_t* __restrict__ xp_sf) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ int2 s_tl[];  // [max_tiles]: {row0, rows}
   const int n_tiles = min(tiles[0], max_tiles);
@@ -177,10 +177,8 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_tok_kernel(
       uint4 c[2];
       uint32_t sc = 127u;  // padding blocks past H carry the neutral scale
       if (blk < nbh) {
-        sc = quant_block_vals(v[u], c);
-        uint4* q = reinterpret_cast<uint4*>(xq + (int64_t)t * H + blk * 32);
-        q[0] = c[0];
-        q[1] = c[1];
+        sc = quant_block_act(v[u], c, fp4);
+        store_block_codes(xq + (int64_t)t * (H >> fp4) + blk * (32 >> fp4), c, fp4);
         xs[(int64_t)t * nbh + blk] = (uint8_t)sc;
       }
       // the scales of the four blocks of a 128-element k-tile form one word of the
@@ -191,9 +189,7 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_tok_kernel(
         const int pj = __shfl_sync(0xffffffffu, p, j), bj = __shfl_sync(0xffffffffu, b, j),
                   nj = __shfl_sync(0xffffffffu, n, j);
         if (blk < nbh) {
-          uint4* dst = reinterpret_cast<uint4*>(xp + (int64_t)pj * H + blk * 32);
-          dst[0] = c[0];
-          dst[1] = c[1];
+          store_block_codes(xp + (int64_t)pj * (H >> fp4) + blk * (32 >> fp4), c, fp4);
           if ((lane & 3) == 0)
             *reinterpret_cast<uint32_t*>(xp_sf + ((int64_t)bj * kth + (blk >> 2)) * kAtomBytes + (nj & 31) * 16 +
                                          (nj >> 5) * 4) = word;
@@ -263,14 +259,15 @@ cudaError_t launch_permute(const int32_t* ids, int TK, int k, int E, int tile_ro
 }
 
 cudaError_t launch_gather_quant(const uint16_t* x, const int32_t* inv_pos, const int32_t* tiles, int max_tiles, int T,
-                                int k, int H, uint8_t* xq, uint8_t* xs, uint8_t* xp, uint8_t* xp_sf, cudaStream_t s) {
+                                int k, int H, bool fp4, uint8_t* xq, uint8_t* xs, uint8_t* xp, uint8_t* xp_sf,
+                                cudaStream_t s) {
   const size_t smem = (size_t)max_tiles * sizeof(int2);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(gather_tok_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
   gather_tok_kernel<<<(T + kGatherWarps - 1) / kGatherWarps, 32 * kGatherWarps, smem, s>>>(
-      x, inv_pos, tiles, max_tiles, T, k, H, xq, xs, xp, xp_sf);
+      x, inv_pos, tiles, max_tiles, T, k, H, fp4 ? 1 : 0, xq, xs, xp, xp_sf);
   return cudaGetLastError();
 }
 

@@ -217,6 +217,19 @@ __device__ __forceinline__ void umma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, u
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, both packed E2M1 (K = 64 per instruction), with
+// two E8M0 block scales per row per instruction (32-element blocks) from tmem.
+__device__ __forceinline__ void umma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on an mbarrier once all previously issued tcgen05 async ops of this thread complete.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -253,6 +266,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   return d;
 }
 
+// The same for an operand staged with 64-byte swizzle (64-byte rows of packed
+// E2M1, 128 elements): 8-row x 64-byte swizzle atoms stacked every 512 bytes.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;              // leading byte offset (unused with swizzling)
+  d |= (uint64_t)(512 >> 4) << 32;     // stride byte offset: next 8-row group
+  d |= (uint64_t)1 << 46;              // descriptor version for tcgen05
+  d |= (uint64_t)4 << 61;              // SWIZZLE_64B
+  return d;
+}
+
 // Descriptor of a 32-row x 16-byte scale-factor atom (no swizzle; 8-row core
 // matrices of 128 contiguous bytes).
 __device__ __forceinline__ uint64_t sdesc_sf_atom(uint32_t saddr) {
@@ -263,8 +288,8 @@ __device__ __forceinline__ uint64_t sdesc_sf_atom(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor of kind::mxf8f6f4 with block scaling (E8M0 scales),
-// A and B K-major.  Formats: 0 = E4M3, 5 = E2M1.
+// Instruction descriptor of the block-scaled kinds with E8M0 scales, A and B
+// K-major.  Formats for kind::mxf8f6f4: 0 = E4M3, 5 = E2M1; for kind::mxf4: 1 = E2M1.
 __host__ __device__ constexpr uint32_t idesc_mxf8f6f4(uint32_t M, uint32_t N, uint32_t a_fmt, uint32_t b_fmt,
                                                       uint32_t sfa_id, uint32_t sfb_id) {
   return (sfb_id << 4) | (a_fmt << 7) | (b_fmt << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) |
@@ -273,6 +298,21 @@ __host__ __device__ constexpr uint32_t idesc_mxf8f6f4(uint32_t M, uint32_t N, ui
 
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Eight fp32 -> eight E2M1 codes (round to nearest even, saturate to +-6), two per
+// byte with the lower-index element in the low nibble, in one 32-bit word.
+__device__ __forceinline__ uint32_t cvt_e2m1x8(const float* f) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(f[0]), "f"(f[1]), "f"(f[2]), "f"(f[3]), "f"(f[4]), "f"(f[5]), "f"(f[6]), "f"(f[7]));
+  return r;
 }
 
 // Two fp32 -> two E4M3 codes (round to nearest even, saturate to +-448); `lo` in the low byte.

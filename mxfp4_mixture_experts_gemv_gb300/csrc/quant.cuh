@@ -14,11 +14,14 @@
 
 namespace moe {
 
-// floor(log2(amax)) - 8, at least -127.  amax >= 0 (fp32 bit pattern ordering).
+// floor(log2(amax)) - emax, at least -127.  amax >= 0 (fp32 bit pattern ordering);
+// emax is the element format's largest exponent: 8 for E4M3 (448 = 1.75 * 2^8),
+// 2 for E2M1 (6 = 1.5 * 2^2).
+template <int EMAX = 8>
 __device__ __forceinline__ int mx_scale_exp(float amax) {
   const int biased = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
   if (biased == 0) return -127;  // zero or subnormal: floor(log2) <= -127
-  return max(biased - 127 - 8, -127);
+  return max(biased - 127 - EMAX, -127);
 }
 
 // 2^-s as an fp32 (exact for s in [-127, 126]).
@@ -60,6 +63,52 @@ __device__ __forceinline__ uint8_t quant_block_vals(const uint4 (&v)[4], uint4 (
   c[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
   c[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
   return (uint8_t)(s + 127);
+}
+
+// Quantise one 32-element block of bf16 to MXFP4 (the FP4-activation variant):
+// shared exponent floor(log2(amax)) - 2, elements E2M1 with round-to-nearest-even
+// and saturation to +-6, the same reading of the OCP microscaling rule as MXFP8.
+// The 32 codes, two per byte (lower-index element in the low nibble), in c[0];
+// returns the scale code.
+__device__ __forceinline__ uint8_t quant_block_vals_fp4(const uint4 (&v)[4], uint4 (&c)[2]) {
+  float f[32];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float g[8];
+    bf16x8(v[q], g);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[8 * q + i] = g[i];
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  const int s = mx_scale_exp<2>(amax);
+  const float inv = mx_pow2_neg(s);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) f[i] *= inv;
+  c[0] = make_uint4(cvt_e2m1x8(f), cvt_e2m1x8(f + 8), cvt_e2m1x8(f + 16), cvt_e2m1x8(f + 24));
+  c[1] = make_uint4(0u, 0u, 0u, 0u);
+  return (uint8_t)(s + 127);
+}
+
+// Either activation format: MXFP8 (fp4 false; 32 code bytes in c[0..1]) or
+// MXFP4 (fp4 true; 16 code bytes in c[0]).
+__device__ __forceinline__ uint8_t quant_block_act(const uint4 (&v)[4], uint4 (&c)[2], bool fp4) {
+  return fp4 ? quant_block_vals_fp4(v, c) : quant_block_vals(v, c);
+}
+
+// Store one block's codes at dst (16-byte aligned): 32 bytes (MXFP8) or 16 (MXFP4).
+__device__ __forceinline__ void store_block_codes(uint8_t* dst, const uint4 (&c)[2], bool fp4) {
+  reinterpret_cast<uint4*>(dst)[0] = c[0];
+  if (!fp4) reinterpret_cast<uint4*>(dst)[1] = c[1];
+}
+
+// The same from a block in global or shared memory (16-byte aligned).
+__device__ __forceinline__ uint8_t quant_block_regs_act(const uint16_t* src, uint4 (&c)[2], bool fp4) {
+  uint4 v[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) v[q] = reinterpret_cast<const uint4*>(src)[q];
+  return quant_block_act(v, c, fp4);
 }
 
 // The same from a block in global or shared memory (16-byte aligned).

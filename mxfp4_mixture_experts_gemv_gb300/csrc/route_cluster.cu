@@ -53,6 +53,7 @@ struct RouteClusterArgs {
   int zero_words;
   uint32_t* status;
   uint64_t wait_ns;
+  int fp4;  // activation format: 0 MXFP8 (32 code bytes per block), 1 MXFP4 (16)
 };
 
 // Sum-reduce N values held by every lane of a warp so that each lane ends up
@@ -176,10 +177,8 @@ __global__ void __launch_bounds__(kRcThreads, 1) route_cluster_kernel(const Rout
   uint4 qc[2];
   uint8_t qs = 0;
   if (has_u) {
-    qs = quant_block_regs(s_x + (size_t)ut * H + ukb * 32, qc);
-    uint4* q = reinterpret_cast<uint4*>(a.xq + (int64_t)ut * H + ukb * 32);
-    q[0] = qc[0];
-    q[1] = qc[1];
+    qs = quant_block_regs_act(s_x + (size_t)ut * H + ukb * 32, qc, a.fp4);
+    store_block_codes(a.xq + (int64_t)ut * (H >> a.fp4) + ukb * (32 >> a.fp4), qc, a.fp4);
     a.xs[(int64_t)ut * nbh + ukb] = qs;
   }
   for (int i = 4 + rank + ncta * tid; i < a.zero_words; i += ncta * kRcThreads) a.zero[i] = 0u;
@@ -221,9 +220,7 @@ __global__ void __launch_bounds__(kRcThreads, 1) route_cluster_kernel(const Rout
     const int ka = ukb >> 2;
     for (int j = 0; j < k; ++j) {
       const int f = ut * k + j, p = s_inv[f], e = s_ids[f];
-      uint4* dst = reinterpret_cast<uint4*>(a.xp + (int64_t)p * H + ukb * 32);
-      dst[0] = qc[0];
-      dst[1] = qc[1];
+      store_block_codes(a.xp + (int64_t)p * (H >> a.fp4) + ukb * (32 >> a.fp4), qc, a.fp4);
       const int r_in_e = p - s_off[e];
       const int b = s_toff[e] + (r_in_e >> a.tshift), n = r_in_e & ((1 << a.tshift) - 1);
       uint8_t* wd = a.xp_sf + ((int64_t)b * kth + ka) * kAtomBytes + (n & 31) * 16 + (n >> 5) * 4;
@@ -247,7 +244,7 @@ bool route_cluster_fits(int T, int E, int H) {
 }
 
 cudaError_t launch_route_cluster(const uint16_t* x, const uint16_t* wr, const uint16_t* br, int T, int H, int E,
-                                 int k, int tile_rows, const RouteClusterOut& o, cudaStream_t s) {
+                                 int k, int tile_rows, bool fp4, const RouteClusterOut& o, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -288,7 +285,7 @@ cudaError_t launch_route_cluster(const uint16_t* x, const uint16_t* wr, const ui
   const int epc = (E + csize - 1) / csize;
   RouteClusterArgs a{x, wr, br, T, H, E, k, __builtin_ctz((unsigned)tile_rows), o.logits, o.ids, o.w, o.xq, o.xs,
                      o.counts, o.offsets, o.sorted_rows, o.inv_pos, o.tiles, o.xp, o.xp_sf, o.zero,
-                     o.zero_words, o.status, wait_limit_ns()};
+                     o.zero_words, o.status, wait_limit_ns(), fp4 ? 1 : 0};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(csize);
   cfg.blockDim = dim3(kRcThreads);

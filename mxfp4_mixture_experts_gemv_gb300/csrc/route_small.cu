@@ -47,6 +47,7 @@ struct RouteSmallArgs {
   uint32_t* status;
   uint64_t wait_ns;
   int bar_extra;  // failure-detection hook: wait for this many CTAs more than the grid has
+  int fp4;        // activation format: 0 MXFP8 (32 code bytes per block), 1 MXFP4 (16)
 };
 
 __global__ void __launch_bounds__(kThreads) route_small_kernel(const RouteSmallArgs a) {
@@ -181,15 +182,11 @@ __global__ void __launch_bounds__(kThreads) route_small_kernel(const RouteSmallA
     const int n = r_in_e % a.tile_rows;
     for (int blk = tid; blk < nbh; blk += kThreads) {
       uint4 c[2];
-      const uint8_t sc = quant_block_regs(a.x + (int64_t)t * H + blk * 32, c);
-      uint4* dst = reinterpret_cast<uint4*>(a.xp + (int64_t)p * H + blk * 32);
-      dst[0] = c[0];
-      dst[1] = c[1];
+      const uint8_t sc = quant_block_regs_act(a.x + (int64_t)t * H + blk * 32, c, a.fp4);
+      store_block_codes(a.xp + (int64_t)p * (H >> a.fp4) + blk * (32 >> a.fp4), c, a.fp4);
       s_scale[blk] = sc;
       if (f % k == 0) {  // the token's first slot also publishes x's codes (stage output)
-        uint4* q = reinterpret_cast<uint4*>(a.xq + (int64_t)t * H + blk * 32);
-        q[0] = c[0];
-        q[1] = c[1];
+        store_block_codes(a.xq + (int64_t)t * (H >> a.fp4) + blk * (32 >> a.fp4), c, a.fp4);
         a.xs[(int64_t)t * nbh + blk] = sc;
       }
     }
@@ -210,10 +207,10 @@ __global__ void __launch_bounds__(kThreads) route_small_kernel(const RouteSmallA
 }  // namespace
 
 cudaError_t launch_route_small(const uint16_t* x, const uint16_t* wr, const uint16_t* br, int T, int H, int E, int I,
-                               int k, int tile_rows, int max_tiles, const RouteSmallOut& o, cudaStream_t s) {
+                               int k, int tile_rows, int max_tiles, bool fp4, const RouteSmallOut& o, cudaStream_t s) {
   RouteSmallArgs a{x, wr, br, T, H, E, I, k, tile_rows, max_tiles, o.logits, o.ids, o.w, o.xq, o.xs, o.counts,
                    o.offsets, o.sorted_rows, o.inv_pos, o.tiles, o.xp, o.xp_sf, o.hq_sf, o.grid_bar, o.status,
-                   wait_limit_ns(), (debug_hold_waits() & MOE_DEBUG_HOLD_ROUTING_BARRIER) ? 1 : 0};
+                   wait_limit_ns(), (debug_hold_waits() & MOE_DEBUG_HOLD_ROUTING_BARRIER) ? 1 : 0, fp4 ? 1 : 0};
   const size_t smem = std::max((size_t)(T + 1) * H * 2, (size_t)T * 257 * 4);  // staged rows, later the logits
   static bool attr = false;
   if (!attr) {

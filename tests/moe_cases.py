@@ -2,8 +2,10 @@
 oracle, and compare stage by stage."""
 from __future__ import annotations
 
+import concurrent.futures as cf
 import dataclasses
 import math
+import os
 
 import numpy as np
 import torch
@@ -26,6 +28,18 @@ class GpuRun:
     out: torch.Tensor
     ws: torch.Tensor
     layout: moe.WorkspaceLayout
+    act_format: str = "mxfp8"
+
+    @property
+    def fp4(self) -> bool:
+        return self.act_format == "mxfp4"
+
+    def codes(self, name, rows, cols):
+        """Activation codes of a workspace section, one code per element: E4M3 bytes,
+        or E2M1 nibbles unpacked (two per byte, the even element in the low nibble)."""
+        if not self.fp4:
+            return self.section(name, (rows, cols), torch.uint8).numpy()
+        return unpack_e2m1(self.section(name, (rows, cols // 2), torch.uint8).numpy())
 
     def section(self, name, shape, dtype):
         return moe.view(self.ws, getattr(self.layout, name), shape, dtype).cpu()
@@ -39,7 +53,22 @@ def pack(inp: ms.LayerInputs):
     return dims, packed
 
 
-def run_gpu(inp: ms.LayerInputs, packed, x=None, poison: int | None = None) -> GpuRun:
+def unpack_e2m1(a: np.ndarray) -> np.ndarray:
+    out = np.empty(a.shape[:-1] + (2 * a.shape[-1],), np.uint8)
+    out[..., 0::2] = a & 0xF
+    out[..., 1::2] = a >> 4
+    return out
+
+
+def zero_codes_equal(codes: np.ndarray, fp4: bool) -> np.ndarray:
+    """The negative-zero code read as the positive one: both encode zero, and which
+    of the two a rounding of a tiny negative value gives is not part of the format."""
+    c = codes.copy()
+    c[c == (0x8 if fp4 else 0x80)] = 0
+    return c
+
+
+def run_gpu(inp: ms.LayerInputs, packed, x=None, poison: int | None = None, act_format: str = "mxfp8") -> GpuRun:
     s = inp.shape
     dims = moe.LayerDims(s.E, s.H, s.I)
     x = inp.x if x is None else x
@@ -48,10 +77,10 @@ def run_gpu(inp: ms.LayerInputs, packed, x=None, poison: int | None = None) -> G
     if poison is not None:
         ws.fill_(poison)
     out = torch.full_like(x, float("nan"))
-    moe.forward(dims, x, inp.router_w, inp.router_b, packed, s.k, out=out, workspace=ws)
+    moe.forward(dims, x, inp.router_w, inp.router_b, packed, s.k, out=out, workspace=ws, act_format=act_format)
     st = moe.device_status(ws)
     assert st == moe.MOE_OK, moe.STATUS_NAMES.get(st, st)
-    return GpuRun(dims, s.k, out, ws, moe.workspace_layout(dims, T, s.k))
+    return GpuRun(dims, s.k, out, ws, moe.workspace_layout(dims, T, s.k), act_format)
 
 
 def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
@@ -112,9 +141,9 @@ def H_gamma(n: int) -> float:
 
 def check_quantised_x(run: GpuRun, xq_ref, xs_ref):
     T, H = xq_ref.shape
-    xq = run.section("xq", (T, H), torch.uint8).numpy()
+    xq = run.codes("xq", T, H)
     xs = run.section("xs", (T, H // 32), torch.uint8).numpy()
-    np.testing.assert_array_equal(xq, xq_ref)
+    np.testing.assert_array_equal(zero_codes_equal(xq, run.fp4), zero_codes_equal(xq_ref, run.fp4))
     np.testing.assert_array_equal(xs, xs_ref)
 
 
@@ -125,8 +154,8 @@ def check_gathered(run: GpuRun, T: int, sr: np.ndarray, xq_ref: np.ndarray, xs_r
     H, k = run.dims.H, run.k
     L = run.layout
     TK = T * k
-    xp = run.section("xp", (TK, H), torch.uint8).numpy()
-    np.testing.assert_array_equal(xp, xq_ref[sr // k])
+    xp = run.codes("xp", TK, H)
+    np.testing.assert_array_equal(zero_codes_equal(xp, run.fp4), zero_codes_equal(xq_ref[sr // k], run.fp4))
     kth = (H + 127) // 128
     xp_sf = run.section("xp_sf", (L.max_tiles, kth, 512), torch.uint8).numpy()
     tiles = run.section("tiles", (4 + 4 * L.max_tiles,), torch.int32).numpy()
@@ -193,14 +222,15 @@ def compare_out(got: np.ndarray, want: np.ndarray, what="", allow=None, bf16_rou
     return float(per_tok.max()) / rms, rel
 
 
-_E4M3 = None
+_TABLES = {}
 
 
-def _e4m3_table():
-    global _E4M3
-    if _E4M3 is None:
-        _E4M3 = np.array([oracle.e4m3_value(c) for c in range(256)])
-    return _E4M3
+def _code_table(fp4: bool):
+    """Value of every activation code from the oracle's decoders (E2M1 or E4M3)."""
+    if fp4 not in _TABLES:
+        n, f = (16, oracle.e2m1_value) if fp4 else (256, oracle.e4m3_value)
+        _TABLES[fp4] = np.array([f(c) for c in range(n)])
+    return _TABLES[fp4]
 
 
 def gpu_hq(run: GpuRun, T: int, inv: np.ndarray):
@@ -208,7 +238,7 @@ def gpu_hq(run: GpuRun, T: int, inv: np.ndarray):
     I, k = run.dims.I, run.k
     L = run.layout
     TK = run.out.shape[0] * k
-    hq = run.section("hq", (TK, I), torch.uint8).numpy()
+    hq = run.codes("hq", TK, I)
     kti = (I + 127) // 128
     hq_sf = run.section("hq_sf", (L.max_tiles, kti, 512), torch.uint8).numpy()
     tiles = run.section("tiles", (4 + 4 * L.max_tiles,), torch.int32).numpy()
@@ -225,14 +255,16 @@ def check_intermediate(run: GpuRun, ref: dict, inp_cpu: ms.LayerInputs, inv: np.
                        rel_mid=2e-4):
     """Compare the GPU's MXFP8 intermediate with the oracle's for every (token, slot).
 
-    Codes may differ only where the oracle's h (fp32) lies within ``rel_mid`` of the
-    rounding midpoint between the two codes (or the block amax within ``rel_mid`` of
-    the power of two where the shared exponent changes): both codes are then
-    correct results of the same quantisation, taken from sums accumulated in a
-    different order.  Returns the per-token bound such flips put on the output
-    (sum over slots of w * sum |delta hq_i| * max_c |Wd[c][i]|) and the flip count."""
+    Codes may differ only where the two codes are neighbours in the format's value
+    grid and the oracle's h (fp32) lies within ``rel_mid`` of the rounding midpoint
+    between them (or the block amax within ``rel_mid`` of the power of two where
+    the shared exponent changes): both codes are then correct results of the same
+    quantisation, taken from sums accumulated in a different order.  Returns the
+    per-token bound such flips put on the output (sum over slots of
+    w * sum |delta hq_i| * max_c |Wd[c][i]|) and the flip count."""
     T, k, I = ref["hq"].shape
-    e4 = _e4m3_table()
+    e4 = _code_table(run.fp4)
+    mag = 0x7 if run.fp4 else 0x7F
     gq, gs = gpu_hq(run, T, inv)
     rq, rs = ref["hq"], ref["hs"]
     gv = e4[gq] * np.ldexp(1.0, np.repeat(gs.astype(np.int64), 32, axis=-1) - 127)
@@ -253,8 +285,10 @@ def check_intermediate(run: GpuRun, ref: dict, inp_cpu: ms.LayerInputs, inv: np.
             else:
                 for i in bad[(bad >= 32 * blk) & (bad < 32 * blk + 32)]:
                     mid = 0.5 * (gv[t, j, i] + rv[t, j, i])
-                    step = abs(gv[t, j, i] - rv[t, j, i])
-                    assert step <= abs(rv[t, j, i]) / 4 + 2.0 ** (int(rs[t, j, blk]) - 127 - 9) * 2, \
+                    a, b = int(gq[t, j, i]), int(rq[t, j, i])
+                    # neighbours: magnitudes one code apart with the same sign, or either side of zero
+                    same_sign = (a & ~mag) == (b & ~mag) or (a & mag) == 0 or (b & mag) == 0
+                    assert same_sign and abs((a & mag) - (b & mag)) == 1, \
                         f"pair {(t, j)} elem {i}: codes not adjacent ({gv[t, j, i]} vs {rv[t, j, i]})"
                     assert abs(h[t, j, i] - mid) <= rel_mid * abs(h[t, j, i]), \
                         f"pair {(t, j)} elem {i}: h={h[t, j, i]!r} not at the midpoint {mid!r}"
@@ -265,3 +299,19 @@ def check_intermediate(run: GpuRun, ref: dict, inp_cpu: ms.LayerInputs, inv: np.
     total = T * k * I
     assert flips <= max(4, 0.002 * total), f"intermediate flips {flips}/{total}"
     return allow, flips
+
+
+def oracle_tokens_parallel(inp: ms.LayerInputs, tokens, act_format: str = "mxfp8"):
+    """The oracle layer on the listed tokens, one single-threaded oracle call per
+    token on every host core (its calls release the interpreter lock); the
+    results stacked as one call would return them (with intermediates)."""
+    w = (inp.gate_up_blocks, inp.gate_up_scales, inp.gate_up_bias, inp.down_blocks, inp.down_scales,
+         inp.down_bias)
+
+    def one(t):
+        return oracle.moe_forward(inp.x[t:t + 1], inp.router_w, inp.router_b, *w, k=inp.shape.k,
+                                  intermediates=True, act_format=act_format)
+
+    with cf.ThreadPoolExecutor(max_workers=max(1, os.cpu_count() or 1)) as ex:
+        refs = list(ex.map(one, tokens))
+    return {key: np.concatenate([r[key] for r in refs], axis=0) for key in refs[0]}

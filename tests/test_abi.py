@@ -140,3 +140,23 @@ def test_wait_limit_and_hold_mask_are_checked_on_host(L):
     assert L.moe_debug_hold_waits(8) == 1
     assert L.moe_debug_hold_waits(moe.HOLD_DOWN_UNITS | moe.HOLD_ROUTING_BARRIER) == 0
     assert L.moe_debug_hold_waits(0) == 0
+
+
+def test_plan_override_is_checked_and_sizes_follow_it(L):
+    assert L.moe_set_plan(12, 0) == 1           # not a tile height the kernels have
+    assert L.moe_set_plan(0, 7) == 1            # unknown routing path
+    base = moe.workspace_layout(GPT, 64, 4)
+    assert base.tile_rows == 64
+    try:
+        moe.set_plan(8, "tensor_core")
+        lay = moe.workspace_layout(GPT, 64, 4)
+        assert lay.tile_rows == 8 and lay.max_tiles > base.max_tiles
+        assert moe.workspace_size(GPT, 64, 4) == lay.total
+    finally:
+        moe.set_plan(0, "auto")
+    assert moe.workspace_layout(GPT, 64, 4).tile_rows == 64
+
+
+def test_forward_act_rejects_unknown_formats(L):
+    assert L.moe_forward_act(GPT.c(), 2, FAKE, 4, FAKE, FAKE, FAKE, 4, FAKE, FAKE, 1 << 40, None) == 1
+    assert b"activation format" in L.moe_last_error()

@@ -43,7 +43,8 @@ def _full_check(inp_cpu, run, strict=True):
     s = inp_cpu.shape
     ref = oracle.moe_forward(inp_cpu.x, inp_cpu.router_w, inp_cpu.router_b, inp_cpu.gate_up_blocks,
                              inp_cpu.gate_up_scales, inp_cpu.gate_up_bias, inp_cpu.down_blocks,
-                             inp_cpu.down_scales, inp_cpu.down_bias, k=s.k, intermediates=True)
+                             inp_cpu.down_scales, inp_cpu.down_bias, k=s.k, intermediates=True,
+                             act_format=run.act_format)
     ties = mc.check_routing(run, inp_cpu.x, inp_cpu.router_w, inp_cpu.router_b, ref["logits"])
     assert not ties, f"near-tie tokens {sorted(ties)}"
     mc.check_quantised_x(run, ref["xq"], ref["xs"])
@@ -55,13 +56,14 @@ def _full_check(inp_cpu, run, strict=True):
     return ref
 
 
+@pytest.mark.parametrize("act_format", ["mxfp8", "mxfp4"])
 @pytest.mark.parametrize("name", list(SMALL_CASES))
-def test_small_layer_parity(name):
+def test_small_layer_parity(name, act_format):
     shape, seed = SMALL_CASES[name]
     inp = ms.make_layer(shape, seed=seed)
     dev = inp.to("cuda")
     _, packed = mc.pack(dev)
-    run = mc.run_gpu(dev, packed)
+    run = mc.run_gpu(dev, packed, act_format=act_format)
     _full_check(inp, run, strict=False)
 
 
@@ -175,19 +177,21 @@ def _gpt_inputs(gpt_layer, T, hot=0, hot_bias=0.0):
     return cpu_inp, dev_inp, packed
 
 
+@pytest.mark.parametrize("act_format", ["mxfp8", "mxfp4"])
 @pytest.mark.parametrize("T,hot", [(4, 0), (32, 16)], ids=["decode_t4", "decode_t32_skewed"])
-def test_gpt_oss_decode_parity(gpt_layer, T, hot):
+def test_gpt_oss_decode_parity(gpt_layer, T, hot, act_format):
     cpu_inp, dev_inp, packed = _gpt_inputs(gpt_layer, T, hot, 1.0 if hot else 0.0)
-    run = mc.run_gpu(dev_inp, packed)
+    run = mc.run_gpu(dev_inp, packed, act_format=act_format)
     _full_check(cpu_inp, run)
 
 
-def test_gpt_oss_prefill_sampled_parity(gpt_layer):
+@pytest.mark.parametrize("act_format", ["mxfp8", "mxfp4"])
+def test_gpt_oss_prefill_sampled_parity(gpt_layer, act_format):
     """T = 2048 with the launch configuration of the benchmark; all ids and the
     whole grouping are checked, the output on a sample of tokens."""
     T = 2048
     cpu_inp, dev_inp, packed = _gpt_inputs(gpt_layer, T)
-    run = mc.run_gpu(dev_inp, packed)
+    run = mc.run_gpu(dev_inp, packed, act_format=act_format)
     logits, ids_ref, _ = oracle.route(cpu_inp.x, cpu_inp.router_w, cpu_inp.router_b, 4)
     ties = mc.check_routing(run, cpu_inp.x, cpu_inp.router_w, cpu_inp.router_b, logits)
     cnt, off, sr, inv = mc.check_grouping(run, T)
@@ -197,7 +201,7 @@ def test_gpt_oss_prefill_sampled_parity(gpt_layer):
     sample = sorted(set(list(range(0, T, 257)) + last + [T - 1]) - ties)
     sub = cpu_inp.x[sample]
     ref = oracle.moe_forward(sub, cpu_inp.router_w, cpu_inp.router_b, *cpu_inp_weights(cpu_inp), k=4,
-                             intermediates=True)
+                             intermediates=True, act_format=act_format)
     allow, _ = mc.check_intermediate(run, ref, cpu_inp, inv.reshape(T, 4)[sample])
     got = mc.bf16_to_f64(run.out)[sample]
     mc.compare_out(got, ref["out"], "prefill sample", allow=allow)
@@ -205,3 +209,54 @@ def test_gpt_oss_prefill_sampled_parity(gpt_layer):
 
 def cpu_inp_weights(c):
     return (c.gate_up_blocks, c.gate_up_scales, c.gate_up_bias, c.down_blocks, c.down_scales, c.down_bias)
+
+
+# ----------------------------------------------------------------------- plans
+@pytest.mark.parametrize("T,tile_rows,route", [
+    (6, 8, "cluster"), (6, 32, "cluster"), (6, 16, "grid"), (6, 64, "tensor_core"),
+    (20, 8, "grid"), (20, 64, "grid"), (20, 16, "tensor_core"), (20, 128, "tensor_core"),
+    (70, 32, "tensor_core"), (70, 8, "tensor_core"),
+])
+def test_forced_plans_meet_the_oracle(T, tile_rows, route):
+    """Every tile height on every routing path that fits: the plan changes launch
+    shapes only, never the result beyond the layer tolerance."""
+    shape = ms.LayerShape(T=T, H=256, I=128, E=8, k=4)
+    inp = ms.make_layer(shape, seed=50 + T)
+    dev = inp.to("cuda")
+    _, packed = mc.pack(dev)
+    moe.set_plan(tile_rows, route)
+    try:
+        run = mc.run_gpu(dev, packed)
+        assert run.layout.tile_rows == tile_rows
+        _full_check(inp, run, strict=False)
+    finally:
+        moe.set_plan(0, "auto")
+
+
+def test_forced_route_that_does_not_fit_is_refused():
+    shape = ms.LayerShape(T=40, H=256, I=128, E=8, k=4)
+    dev = ms.make_layer(shape, seed=1).to("cuda")
+    dims, packed = mc.pack(dev)
+    moe.set_plan(0, "grid")  # the grid routing kernel holds at most 32 tokens
+    try:
+        with pytest.raises(moe.MoeError, match="UNSUPPORTED_SHAPE"):
+            moe.forward(dims, dev.x, dev.router_w, dev.router_b, packed, 4)
+    finally:
+        moe.set_plan(0, "auto")
+
+
+@pytest.mark.parametrize("T", [8, 9, 32, 33, 64, 65])
+def test_gpt_oss_parity_at_the_plan_cutoffs(gpt_layer, T):
+    """Either side of every automatic cutoff (cluster / grid routing at 8, grid /
+    tensor-core routing at 32, 64- / 128-row tiles at 64), all tokens checked,
+    with the oracle run one token per host thread."""
+    cpu_inp, dev_inp, packed = _gpt_inputs(gpt_layer, T)
+    run = mc.run_gpu(dev_inp, packed)
+    ref = mc.oracle_tokens_parallel(cpu_inp, list(range(T)))
+    ties = mc.check_routing(run, cpu_inp.x, cpu_inp.router_w, cpu_inp.router_b, ref["logits"])
+    assert not ties
+    mc.check_quantised_x(run, ref["xq"], ref["xs"])
+    cnt, off, sr, inv = mc.check_grouping(run, T)
+    mc.check_gathered(run, T, sr, ref["xq"], ref["xs"])
+    allow, _ = mc.check_intermediate(run, ref, cpu_inp, inv)
+    mc.compare_out(mc.bf16_to_f64(run.out), ref["out"], f"T={T}", allow=allow)
