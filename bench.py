@@ -655,11 +655,17 @@ SWEEP_T = (1, 2, 4, 8, 12, 16, 24, 32, 48, 64, 96, 128, 256, 512, 1024, 2048, 40
 
 
 def _plans_for(T: int):
-    """Candidate (tile_rows, routing path) pairs for T tokens: every tile height the
-    kernels have, every routing path whose capacity covers T."""
+    """Candidate (tile_rows, routing path, expert kernel) for T tokens: every tile
+    height the kernels have, every routing path whose capacity covers T, and both
+    expert kernels on 128-row tiles."""
     routes = (["cluster"] if T <= 8 else []) + (["grid"] if T <= 32 else []) + ["tensor_core"]
     rows = (8, 16, 32, 64, 128) if T <= 256 else (32, 64, 128)
-    return [(r, rt) for r in rows for rt in routes]
+    out = []
+    for r in rows:
+        for rt in routes:
+            for ex in (("weights_m", "tokens_m") if r == 128 else ("auto",)):
+                out.append((r, rt, ex))
+    return out
 
 
 def run_sweep(args):
@@ -675,12 +681,12 @@ def run_sweep(args):
     layers = Layers(args.layers, device)
     routers = layers.routers(device=device)
     best = {}
-    for T in SWEEP_T:
+    for T in (args.sweep_t or SWEEP_T):
         xs = [ms.make_tokens(0, T, H, layer=l).to(device) for l in range(layers.n)]
         out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
         rows = []
-        for tr, rt in _plans_for(T):
-            moe.set_plan(tr, rt)
+        for tr, rt, ex in _plans_for(T):
+            moe.set_plan(tr, rt, ex)
             try:
                 ws = moe.alloc_workspace(layers.dims, T, K_TOP, device)
                 for l in range(layers.n):  # warm-up, and the plan must run
@@ -711,7 +717,7 @@ def run_sweep(args):
                 del graphs, ws
             finally:
                 moe.set_plan(0, "auto")
-            line = {"sweep": "plan", "T": T, "tile_rows": tr, "route": rt, "step_us": us,
+            line = {"sweep": "plan", "T": T, "tile_rows": tr, "route": rt, "expert": ex, "step_us": us,
                     "tokens_per_s": T / (us * 1e-6)}
             rows.append(line)
             print(json.dumps(line), flush=True)
@@ -719,7 +725,7 @@ def run_sweep(args):
         ws = moe.alloc_workspace(layers.dims, T, K_TOP, device)
         lay = moe.workspace_layout(layers.dims, T, K_TOP)
         fastest = min(rows, key=lambda r: r["step_us"])
-        best[T] = {"fastest": (fastest["tile_rows"], fastest["route"], round(fastest["step_us"], 1)),
+        best[T] = {"fastest": (fastest["tile_rows"], fastest["route"], fastest["expert"], round(fastest["step_us"], 1)),
                    "auto_tile_rows": lay.tile_rows}
         del ws
     print(json.dumps({"sweep": "summary", "best": best}), flush=True)
@@ -738,6 +744,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of CPU oracle work")
     ap.add_argument("--sweep", action="store_true",
                     help="plan sweep: median step time of every tile-height and routing-path candidate per T")
+    ap.add_argument("--sweep-t", type=int, nargs="*", default=None, help="token counts of the plan sweep")
     ap.add_argument("--case", type=int, default=None, metavar="T",
                     help="profiling run: one gpt-oss-shaped layer at T tokens, warmup + steps plain "
                          "forward calls, no timing and no JSON line (T=32 uses the skewed router)")

@@ -194,7 +194,7 @@ moe_status moe_forward_act(moe_dims d, int32_t act_format, const void *hidden, i
  * the same arguments minus the workspace: its scratch is a file-scope device
  * array of MOE_STATIC_SCRATCH_BYTES inside this library (held by every GPU that
  * loads the library until the process exits; enough for a gpt-oss-sized layer
- * up to T = 64 with top_k = 4).
+ * up to T = 128 with top_k = 4).
  *  - A call whose scratch need (moe_workspace_size) exceeds that size returns
  *    MOE_ERR_WORKSPACE_TOO_SMALL with a message; nothing is enqueued.
  *  - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
@@ -206,7 +206,7 @@ moe_status moe_forward_act(moe_dims d, int32_t act_format, const void *hidden, i
  *    overlap on the GPU (concurrent streams or host threads) race on it:
  *    serialise them.
  */
-#define MOE_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
+#define MOE_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
 moe_status moe_forward_static_scratch(moe_dims d, const void *hidden, int32_t T, const void *router_w,
                                       const void *router_b, const void *packed, int32_t top_k, void *out,
                                       void *stream);
@@ -277,18 +277,25 @@ moe_status moe_residual_rmsnorm(float *x_res, const void *layer_out, int32_t T, 
  * autotuner and small-tile variants: "GPT-OSS-120B with MXFP4 on DGX Spark
  * (SM121/GB10)", "Performance Optimizations").  Forces the token rows per expert
  * tile of the grouped GEMM (8, 16, 32, 64 or 128; 0 = the measured default for
- * T) and the routing path (MOE_ROUTE_AUTO = the measured default; _CLUSTER needs
- * T <= 8, _GRID T <= 32, _TENSOR_CORE any T).  Process-wide.  moe_workspace_size
+ * T), the routing path (MOE_ROUTE_AUTO = the measured default; _CLUSTER needs
+ * T <= 8, _GRID T <= 32, _TENSOR_CORE any T) and the expert kernel
+ * (MOE_EXPERT_AUTO = the measured default; _WEIGHTS_M = weight rows in the MMA's
+ * M slot and token rows in N, any tile height; _TOKENS_M = 128 token rows in M and
+ * two 128-row weight tiles in N, 128-row tiles and MXFP8 activations only).
+ * Process-wide.  moe_workspace_size
  * and moe_workspace_layout_get follow the tile override, so size workspaces
- * after setting it.  A forced routing path that does not fit the call's T makes
- * that forward return MOE_ERR_UNSUPPORTED_SHAPE.  Results do not depend on the
+ * after setting it.  A forced routing path or expert kernel that does not fit
+ * the call makes that forward return MOE_ERR_UNSUPPORTED_SHAPE.  Results do not depend on the
  * plan; only the launch shapes do.  Invalid values are MOE_ERR_INVALID_ARG.
  */
 #define MOE_ROUTE_AUTO 0
 #define MOE_ROUTE_CLUSTER 1
 #define MOE_ROUTE_GRID 2
 #define MOE_ROUTE_TENSOR_CORE 3
-moe_status moe_set_plan(int32_t tile_rows, int32_t route);
+#define MOE_EXPERT_AUTO 0
+#define MOE_EXPERT_WEIGHTS_M 1
+#define MOE_EXPERT_TOKENS_M 2
+moe_status moe_set_plan(int32_t tile_rows, int32_t route, int32_t expert_kernel);
 
 /*
  * Optional per-stage timing of moe_forward with CUDA events (measurement; no

@@ -91,7 +91,7 @@ def lib() -> ctypes.CDLL:
         L.moe_get_wait_limit_ns.restype = ctypes.c_uint64
         L.moe_get_wait_limit_ns.argtypes = []
         L.moe_set_plan.restype = st
-        L.moe_set_plan.argtypes = [i32, i32]
+        L.moe_set_plan.argtypes = [i32, i32, i32]
         L.moe_debug_hold_waits.restype = st
         L.moe_debug_hold_waits.argtypes = [i32]
         L.moe_residual_rmsnorm.restype = st
@@ -270,12 +270,14 @@ def wait_limit_ns() -> int:
 
 
 ROUTES = {"auto": 0, "cluster": 1, "grid": 2, "tensor_core": 3}
+EXPERT_KERNELS = {"auto": 0, "weights_m": 1, "tokens_m": 2}
 
 
-def set_plan(tile_rows: int = 0, route: str = "auto"):
-    """Force the token rows per expert tile (0 = default) and the routing path
-    ("auto", "cluster", "grid", "tensor_core") of later forwards (measurement hook)."""
-    _check(lib().moe_set_plan(tile_rows, ROUTES[route]))
+def set_plan(tile_rows: int = 0, route: str = "auto", expert: str = "auto"):
+    """Force the token rows per expert tile (0 = default), the routing path ("auto",
+    "cluster", "grid", "tensor_core") and the expert kernel ("auto", "weights_m",
+    "tokens_m") of later forwards (measurement hook)."""
+    _check(lib().moe_set_plan(tile_rows, ROUTES[route], EXPERT_KERNELS[expert]))
 
 
 HOLD_DOWN_UNITS = 1

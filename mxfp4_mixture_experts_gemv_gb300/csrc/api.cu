@@ -45,6 +45,7 @@ std::atomic<uint64_t> g_wait_limit_ns{moe::kWaitLimitNsDefault};
 std::atomic<int> g_hold_waits{0};
 std::atomic<int> g_plan_tile_rows{0};
 std::atomic<int> g_plan_route{0};
+std::atomic<int> g_plan_expert{0};
 
 // Per-stage CUDA events of profiled forward calls.
 struct Profiler {
@@ -83,6 +84,7 @@ uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed
 int debug_hold_waits() { return g_hold_waits.load(std::memory_order_relaxed); }
 int plan_tile_rows() { return g_plan_tile_rows.load(std::memory_order_relaxed); }
 int plan_route() { return g_plan_route.load(std::memory_order_relaxed); }
+int plan_expert() { return g_plan_expert.load(std::memory_order_relaxed); }
 
 moe_status check_forward_args(const moe_dims& d, const void* hidden, int32_t T, const void* router_w,
                               const void* router_b, const void* packed, int32_t top_k, const void* out) {
@@ -293,7 +295,18 @@ moe_status forward_impl(moe_dims d, bool fp4, const void* hidden, int32_t T, con
   // Many tokens: a streaming pass after the expert kernel, which would otherwise
   // stall on the slot loads of every completed token.
   b.fused_combine = L.tile_rows <= 32;
-  e = moe::launch_expert_mlp(h, pk, b, T, top_k, L.max_tiles, L.tile_rows, sms, fp4, s);
+  // expert kernel: full 128-row token tiles take the tokens-on-M kernel (two
+  // weight tiles per MMA), smaller tiles the weights-on-M kernel
+  const int forced_expert = moe::plan_expert();
+  const bool tokens_m = !fp4 && L.tile_rows == 128 &&
+                        (forced_expert == moe::kExpertAuto || forced_expert == moe::kExpertTokensM) &&
+                        forced_expert != moe::kExpertWeightsM;
+  if (forced_expert == moe::kExpertTokensM && !tokens_m)
+    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "the tokens-on-M expert kernel needs 128-row tiles and MXFP8 activations");
+  if (tokens_m)
+    e = moe::launch_expert_swap(h, pk, b, T, top_k, L.max_tiles, sms, s);
+  else
+    e = moe::launch_expert_mlp(h, pk, b, T, top_k, L.max_tiles, L.tile_rows, sms, fp4, s);
   if (e != cudaSuccess) return cuda_fail(e, "expert MLP kernel");
   if (!b.fused_combine) {
     e = moe::launch_combine(b.y, inv_pos, w, T, top_k, d.H, static_cast<uint16_t*>(out), s);
@@ -386,12 +399,15 @@ moe_status moe_set_wait_limit_ns(uint64_t ns) {
 
 uint64_t moe_get_wait_limit_ns(void) { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
-moe_status moe_set_plan(int32_t tile_rows, int32_t route) {
+moe_status moe_set_plan(int32_t tile_rows, int32_t route, int32_t expert_kernel) {
   if (tile_rows != 0 && tile_rows != 8 && tile_rows != 16 && tile_rows != 32 && tile_rows != 64 && tile_rows != 128)
     return fail(MOE_ERR_INVALID_ARG, "tile_rows=%d is not 0, 8, 16, 32, 64 or 128", tile_rows);
   if (route < MOE_ROUTE_AUTO || route > MOE_ROUTE_TENSOR_CORE) return fail(MOE_ERR_INVALID_ARG, "route=%d", route);
+  if (expert_kernel < MOE_EXPERT_AUTO || expert_kernel > MOE_EXPERT_TOKENS_M)
+    return fail(MOE_ERR_INVALID_ARG, "expert_kernel=%d", expert_kernel);
   g_plan_tile_rows.store(tile_rows, std::memory_order_relaxed);
   g_plan_route.store(route, std::memory_order_relaxed);
+  g_plan_expert.store(expert_kernel, std::memory_order_relaxed);
   return MOE_OK;
 }
 

@@ -96,22 +96,24 @@ bool route_cluster_fits(int T, int E, int H);
 // Measurement overrides of the plan (moe_set_plan), process-wide: token rows per
 // tile (0 = automatic) and the routing path (kRouteAuto = automatic).
 enum : int { kRouteAuto = 0, kRouteCluster = 1, kRouteGrid = 2, kRouteTensorCore = 3 };
+enum : int { kExpertAuto = 0, kExpertWeightsM = 1, kExpertTokensM = 2 };
 int plan_tile_rows();
 int plan_route();
+int plan_expert();
 
-// Token rows per tile of the grouped GEMM (MMA N upper bound): a token visits an
-// expert at most once, so up to 64 tokens one tile of the next size covers any
-// expert; beyond that 128 (measured: smaller tiles re-read the weights of
-// experts with more rows than the tile and lose more than they gain).
+// Token rows per tile of the grouped GEMM, from the measured plan sweep on the
+// gpt-oss-shaped layer (E = 128, top-4): twice the average rows per expert,
+// rounded up to a power of two, within [8, 128].  Small tiles take the pipeline
+// shape that streams weights fastest (four k-tiles per stage) and most experts
+// still fit one tile, so each weight byte is read once; the fastest tile height
+// in the sweep was 8 rows up to T = 128 (2 to 4 rows per expert on average),
+// then 16, 32, 64 at T = 256, 512, 1024 and 128 from T = 2048.
 inline int tile_rows_for(int T, int k, int E) {
-  (void)k;
-  (void)E;
   if (const int forced = plan_tile_rows()) return forced;
-  if (T <= 8) return 8;  // a token visits an expert at most once: at most T rows per tile
-  if (T <= 16) return 16;
-  if (T <= 32) return 32;
-  if (T <= 64) return 64;
-  return 128;
+  const int64_t avg = ((int64_t)T * k + E - 1) / E;  // average token rows per expert
+  int tr = 8;
+  while (tr < 128 && tr < 2 * avg) tr *= 2;
+  return tr;
 }
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -266,5 +268,9 @@ cudaError_t launch_combine(const float* y, const int32_t* inv_pos, const float* 
 // and kind::mxf8f6f4.
 cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, const ExpertMlpBuffers& b, int T, int k,
                               int max_tiles, int tile_rows, int num_sms, bool fp4, cudaStream_t s);
+// The same layer for 128-row token tiles with the tokens in the MMA M slot and two
+// weight tiles in N (MXFP8 activations); y is combined by launch_combine.
+cudaError_t launch_expert_swap(const PackedHeader& h, const uint8_t* packed, const ExpertMlpBuffers& b, int T, int k,
+                               int max_tiles, int num_sms, cudaStream_t s);
 
 }  // namespace moe

@@ -43,6 +43,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "expert_common.cuh"
 #include "ptx.cuh"
 #include "quant.cuh"
 
@@ -139,70 +140,6 @@ __device__ __forceinline__ TileRef tile_ref(int tile, int n_gu, const MlpParams&
   }
   return r;
 }
-
-// Where a bounded wait expired: role (1 producer/empty, 2 mma/accumulator, 3 mma/full,
-// 4 epilogue, 5 producer/dependency, 6 producer/tile queue, 7 mma/tile queue; 8 is the
-// cluster routing kernel's copies), tile (or queue position) and k-step, packed for the
-// second status word.
-__device__ __forceinline__ uint32_t wait_site(uint32_t role, int tile, int kt) {
-  return (role << 28) | ((uint32_t)min(tile, 0xFFFF) << 12) | (uint32_t)min(kt, 0xFFF);
-}
-
-__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Release increment: every write that happens-before it (this CTA's, ordered by
-// the preceding barrier) is visible to whoever acquires the counter.
-__device__ __forceinline__ void red_add_release_gpu(int32_t* p, int v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Increment with acquire and release: returns the previous value; the caller sees
-// every write published by earlier increments.
-__device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t* p, int v) {
-  int old;
-  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-// Bounded wait (all lanes of the warp) until *ctr >= target.
-__device__ __forceinline__ bool wait_counter_warp(const int32_t* ctr, int target, uint64_t limit_ns) {
-  bool ok = ld_acquire_gpu(ctr) >= target;
-  if (!__all_sync(0xffffffffu, ok)) {
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-      ok = ld_acquire_gpu(ctr) >= target;
-      if (__all_sync(0xffffffffu, ok)) break;
-      if (global_timer_ns() - t0 > limit_ns) return false;
-      __nanosleep(64);
-    }
-  }
-  return true;
-}
-
-// Activation tiles are fetched with the smallest of these box heights that covers
-// the unit's token rows (the MMA's N rounds rows up to 16; columns past the rows
-// are never read back), so a sparse token tile does not pull a full BN x 128 box.
-constexpr int kActBoxes = 5;  // 8, 16, 32, 64, 128 rows
-__host__ __device__ constexpr int act_box_rows(int i) { return 8 << i; }
-__device__ __forceinline__ int act_box_index(int rows) {
-  return rows <= 8 ? 0 : rows <= 16 ? 1 : rows <= 32 ? 2 : rows <= 64 ? 3 : 4;
-}
-
-// Tensor maps of one launch: weight boxes of 256, 128 and 64 rows (two k-tiles,
-// one k-tile, a 64-row tail tile), and the activation maps (grouped x for
-// gate_up, hq for down) for each box height.
-struct Maps {
-  CUtensorMap gu2, gu, gut, d2, d, dt;
-  CUtensorMap xp[kActBoxes], hq[kActBoxes];
-};
 
 template <int BN, bool FP4>
 __global__ void __launch_bounds__(192, 1)
@@ -745,6 +682,36 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
+template <int BN, bool FP4>
+cudaError_t launch_bn(const Maps& m, const MlpParams& p, int grid, cudaStream_t s) {
+  using C = GemmCfg<BN, FP4>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e =
+        cudaFuncSetAttribute(expert_mlp_kernel<BN, FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = s;
+  // Programmatic dependent launch: the CTAs start (barrier init, TMEM allocation,
+  // descriptor prefetch) while the routing kernel finishes.  The grid is at most
+  // one CTA per SM.  Units are claimed at run time by the CTAs that are running,
+  // so the dependencies between units hold even when only part of the grid is
+  // resident (another kernel holding SMs); every wait is bounded regardless.
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, expert_mlp_kernel<BN, FP4>, m, p);
+}
+
+}  // namespace
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -800,36 +767,6 @@ bool make_act_map(CUtensorMap* map, const uint8_t* base, int row_bytes, int rows
              CU_TENSOR_MAP_INTERLEAVE_NONE, fp4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-template <int BN, bool FP4>
-cudaError_t launch_bn(const Maps& m, const MlpParams& p, int grid, cudaStream_t s) {
-  using C = GemmCfg<BN, FP4>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e =
-        cudaFuncSetAttribute(expert_mlp_kernel<BN, FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(192);
-  cfg.dynamicSmemBytes = C::kSmem;
-  cfg.stream = s;
-  // Programmatic dependent launch: the CTAs start (barrier init, TMEM allocation,
-  // descriptor prefetch) while the routing kernel finishes.  The grid is at most
-  // one CTA per SM.  Units are claimed at run time by the CTAs that are running,
-  // so the dependencies between units hold even when only part of the grid is
-  // resident (another kernel holding SMs); every wait is bounded regardless.
-  cudaLaunchAttribute attrs[1];
-  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attrs[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attrs;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, expert_mlp_kernel<BN, FP4>, m, p);
-}
-
-}  // namespace
 
 // Encoded descriptors depend only on these values, so they are reused across calls.
 struct MapKey {

@@ -64,14 +64,15 @@ def test_packed_size_layout():
 
 
 def test_workspace_layout_sections_are_disjoint_and_aligned():
-    for T in (1, 4, 32, 2048, 8192):
+    for T in (1, 4, 32, 128, 129, 256, 512, 1000, 1024, 2048, 8192):
         lay = moe.workspace_layout(GPT, T, 4)
         names = [f[0] for f in moe.WorkspaceLayout._fields_[:-3] if f[0] != "zero_bytes"]
         assert lay.zero_bytes == lay.logits  # status and counters lead the workspace
         offs = [getattr(lay, n) for n in names]
         assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
         assert lay.total == moe.workspace_size(GPT, T, 4)
-        want = 8 if T <= 8 else 16 if T <= 16 else 32 if T <= 32 else 64 if T <= 64 else 128
+        # the measured table: 8 rows up to T = 128, then 16, 32, 64, and 128 from 2048
+        want = 8 if T <= 128 else 16 if T <= 256 else 32 if T <= 512 else 64 if T <= 1024 else 128
         assert lay.tile_rows == want
         # enough tiles for any routing: every expert's partial tile plus full tiles
         assert lay.max_tiles >= T * 4 // lay.tile_rows + min(T * 4, 128)
@@ -143,18 +144,19 @@ def test_wait_limit_and_hold_mask_are_checked_on_host(L):
 
 
 def test_plan_override_is_checked_and_sizes_follow_it(L):
-    assert L.moe_set_plan(12, 0) == 1           # not a tile height the kernels have
-    assert L.moe_set_plan(0, 7) == 1            # unknown routing path
-    base = moe.workspace_layout(GPT, 64, 4)
+    assert L.moe_set_plan(12, 0, 0) == 1           # not a tile height the kernels have
+    assert L.moe_set_plan(0, 7, 0) == 1            # unknown routing path
+    assert L.moe_set_plan(0, 0, 3) == 1            # unknown expert kernel
+    base = moe.workspace_layout(GPT, 1024, 4)
     assert base.tile_rows == 64
     try:
         moe.set_plan(8, "tensor_core")
-        lay = moe.workspace_layout(GPT, 64, 4)
+        lay = moe.workspace_layout(GPT, 1024, 4)
         assert lay.tile_rows == 8 and lay.max_tiles > base.max_tiles
-        assert moe.workspace_size(GPT, 64, 4) == lay.total
+        assert moe.workspace_size(GPT, 1024, 4) == lay.total
     finally:
         moe.set_plan(0, "auto")
-    assert moe.workspace_layout(GPT, 64, 4).tile_rows == 64
+    assert moe.workspace_layout(GPT, 1024, 4).tile_rows == 64
 
 
 def test_forward_act_rejects_unknown_formats(L):

@@ -212,22 +212,41 @@ def cpu_inp_weights(c):
 
 
 # ----------------------------------------------------------------------- plans
-@pytest.mark.parametrize("T,tile_rows,route", [
-    (6, 8, "cluster"), (6, 32, "cluster"), (6, 16, "grid"), (6, 64, "tensor_core"),
-    (20, 8, "grid"), (20, 64, "grid"), (20, 16, "tensor_core"), (20, 128, "tensor_core"),
-    (70, 32, "tensor_core"), (70, 8, "tensor_core"),
+@pytest.mark.parametrize("T,tile_rows,route,expert", [
+    (6, 8, "cluster", "auto"), (6, 32, "cluster", "auto"), (6, 16, "grid", "auto"), (6, 64, "tensor_core", "auto"),
+    (20, 8, "grid", "auto"), (20, 64, "grid", "auto"), (20, 16, "tensor_core", "auto"),
+    (20, 128, "tensor_core", "weights_m"), (20, 128, "grid", "tokens_m"),
+    (70, 32, "tensor_core", "auto"), (70, 8, "tensor_core", "auto"),
+    (300, 128, "auto", "weights_m"), (300, 128, "auto", "tokens_m"),
 ])
-def test_forced_plans_meet_the_oracle(T, tile_rows, route):
-    """Every tile height on every routing path that fits: the plan changes launch
-    shapes only, never the result beyond the layer tolerance."""
+def test_forced_plans_meet_the_oracle(T, tile_rows, route, expert):
+    """Every tile height on every routing path that fits, and both expert kernels
+    on 128-row tiles: the plan changes launch shapes only, never the result beyond
+    the layer tolerance."""
     shape = ms.LayerShape(T=T, H=256, I=128, E=8, k=4)
     inp = ms.make_layer(shape, seed=50 + T)
     dev = inp.to("cuda")
     _, packed = mc.pack(dev)
-    moe.set_plan(tile_rows, route)
+    moe.set_plan(tile_rows, route, expert)
     try:
         run = mc.run_gpu(dev, packed)
         assert run.layout.tile_rows == tile_rows
+        _full_check(inp, run, strict=False)
+    finally:
+        moe.set_plan(0, "auto")
+
+
+@pytest.mark.parametrize("expert", ["weights_m", "tokens_m"])
+def test_both_expert_kernels_on_ragged_tails(expert):
+    """H = 288 (a 64-row down tail tile), I = 192 (three gate_up tiles: one pair and
+    a single), 128-row token tiles with a ragged last tile."""
+    shape = ms.LayerShape(T=90, H=288, I=192, E=6, k=3)
+    inp = ms.make_layer(shape, seed=61)
+    dev = inp.to("cuda")
+    _, packed = mc.pack(dev)
+    moe.set_plan(128, "auto", expert)
+    try:
+        run = mc.run_gpu(dev, packed)
         _full_check(inp, run, strict=False)
     finally:
         moe.set_plan(0, "auto")
@@ -245,18 +264,25 @@ def test_forced_route_that_does_not_fit_is_refused():
         moe.set_plan(0, "auto")
 
 
-@pytest.mark.parametrize("T", [8, 9, 32, 33, 64, 65])
+@pytest.mark.parametrize("T", [8, 9, 32, 33, 128, 129, 256, 257, 512, 513, 1024, 1025, 2048])
 def test_gpt_oss_parity_at_the_plan_cutoffs(gpt_layer, T):
-    """Either side of every automatic cutoff (cluster / grid routing at 8, grid /
-    tensor-core routing at 32, 64- / 128-row tiles at 64), all tokens checked,
-    with the oracle run one token per host thread."""
+    """Either side of every automatic cutoff: cluster / grid routing at 8, grid /
+    tensor-core routing at 32, and the token-tile heights 8 / 16 / 32 / 64 / 128
+    at 128, 256, 512 and 1024 (128-row tiles take the tokens-on-M expert kernel).
+    Routing, grouping and the gathered rows are checked for every token, the
+    output on up to 24 tokens (the oracle runs one token per host thread)."""
     cpu_inp, dev_inp, packed = _gpt_inputs(gpt_layer, T)
     run = mc.run_gpu(dev_inp, packed)
-    ref = mc.oracle_tokens_parallel(cpu_inp, list(range(T)))
-    ties = mc.check_routing(run, cpu_inp.x, cpu_inp.router_w, cpu_inp.router_b, ref["logits"])
-    assert not ties
-    mc.check_quantised_x(run, ref["xq"], ref["xs"])
+    logits, _, _ = oracle.route(cpu_inp.x, cpu_inp.router_w, cpu_inp.router_b, 4)
+    ties = mc.check_routing(run, cpu_inp.x, cpu_inp.router_w, cpu_inp.router_b, logits)
+    xq, xs = oracle.mxfp8_quantize(mc.bf16_to_f64(cpu_inp.x))
+    mc.check_quantised_x(run, xq, xs)
     cnt, off, sr, inv = mc.check_grouping(run, T)
-    mc.check_gathered(run, T, sr, ref["xq"], ref["xs"])
-    allow, _ = mc.check_intermediate(run, ref, cpu_inp, inv)
-    mc.compare_out(mc.bf16_to_f64(run.out), ref["out"], f"T={T}", allow=allow)
+    mc.check_gathered(run, T, sr, xq, xs)
+    e_max = int(np.argmax(cnt))
+    last = [int(sr[p]) // 4 for p in range(max(off[e_max], off[e_max + 1] - 4), off[e_max + 1])]
+    spread = np.linspace(0, T - 1, min(T, 20)).astype(int).tolist()
+    sample = sorted(set(spread + last) - ties)
+    ref = mc.oracle_tokens_parallel(cpu_inp, sample)
+    allow, _ = mc.check_intermediate(run, ref, cpu_inp, inv.reshape(T, 4)[sample])
+    mc.compare_out(mc.bf16_to_f64(run.out)[sample], ref["out"], f"T={T}", allow=allow)

@@ -46,8 +46,8 @@ def test_static_scratch_rejects_calls_larger_than_the_array():
     assert moe.workspace_size(dims, T, 4) > moe.static_scratch_bytes()
     st = L.moe_forward_static_scratch(dims.c(), FAKE, T, FAKE, FAKE, FAKE, 4, FAKE, None)
     assert st == 4 and b"static scratch" in L.moe_last_error()
-    # the largest documented call fits: gpt-oss shapes at T = 64, top-4
-    assert moe.workspace_size(dims, 64, 4) <= moe.static_scratch_bytes()
+    # the largest documented call fits: gpt-oss shapes at T = 128, top-4
+    assert moe.workspace_size(dims, 128, 4) <= moe.static_scratch_bytes()
 
 
 @pytest.mark.parametrize("dims,T,k,want", [
@@ -100,6 +100,6 @@ def test_static_scratch_matches_workspace_forward_twice(shape):
 @pytest.mark.gpu
 def test_static_scratch_switches_routing_paths_on_the_shared_array():
     """gpt-oss shapes: T = 32 (grid routing, cleared by a memset), T = 4 (cluster
-    routing, which clears its own counters), T = 64 (tensor-core routing, the
+    routing, which clears its own counters), T = 128 (tensor-core routing, the
     documented maximum), then T = 32 again, on the array the previous call left."""
-    _check_twice(ms.LayerShape(T=64, H=2880, I=2880, E=128, k=4), [32, 4, 64, 32])
+    _check_twice(ms.LayerShape(T=128, H=2880, I=2880, E=128, k=4), [32, 4, 128, 32])
