@@ -76,6 +76,20 @@ def lib():
             L.oracle_moe_forward_fmt.restype = None
             L.oracle_moe_forward_fmt.argtypes = [p, i64, i64, i64, i64, i32, p, p, p, p, p, p, p, p,
                                              p, p, p, p, p, p, p, p, p, i32]
+            L.oracle_pack_e2m1.restype = None
+            L.oracle_pack_e2m1.argtypes = [p, i64, i64, p]
+            L.oracle_quantize_mxfp4_weights.restype = None
+            L.oracle_quantize_mxfp4_weights.argtypes = [p, i64, i64, p, p]
+            L.oracle_dense_linear.restype = None
+            L.oracle_dense_linear.argtypes = [p, i64, i64, i64, p, p, p, p, i32]
+            L.oracle_nvfp4_global_scale.restype = d
+            L.oracle_nvfp4_global_scale.argtypes = [d]
+            L.oracle_nvfp4_quantize.restype = None
+            L.oracle_nvfp4_quantize.argtypes = [p, i64, d, p, p]
+            L.oracle_nvfp4_value.restype = d
+            L.oracle_nvfp4_value.argtypes = [ctypes.c_int, ctypes.c_int, d]
+            L.oracle_expert_mlp_nvfp4.restype = None
+            L.oracle_expert_mlp_nvfp4.argtypes = [p, p, i64, i64, p, p, d, p, p, p, d, p, p, p, p, p]
             L.oracle_rmsnorm_bf16.restype = None
             L.oracle_rmsnorm_bf16.argtypes = [p, i64, i64, d, p]
             _lib = L
@@ -261,3 +275,80 @@ def rmsnorm_bf16(x, eps: float = 1e-5) -> np.ndarray:
     out = np.empty((T, H), np.uint16)
     lib().oracle_rmsnorm_bf16(_ptr(a), T, H, eps, _ptr(out))
     return out
+
+
+# --- dense MXFP4 linears -------------------------------------------------------------
+def pack_e2m1(codes) -> np.ndarray:
+    """E2M1 codes one per byte [rows, K] -> checkpoint blocks [rows, K/32, 16]."""
+    c = _np(codes, np.uint8)
+    rows, K = c.shape
+    out = np.empty((rows, K // 32, 16), np.uint8)
+    lib().oracle_pack_e2m1(_ptr(c), rows, K, _ptr(out))
+    return out
+
+
+def quantize_mxfp4_weights(w):
+    """fp64 [rows, K] -> (blocks [rows, K/32, 16], scales [rows, K/32]) in the checkpoint layout."""
+    a = _np(w, np.float64)
+    rows, K = a.shape
+    blocks = np.empty((rows, K // 32, 16), np.uint8)
+    scales = np.empty((rows, K // 32), np.uint8)
+    lib().oracle_quantize_mxfp4_weights(_ptr(a), rows, K, _ptr(blocks), _ptr(scales))
+    return blocks, scales
+
+
+def dense_linear(x, blocks, scales, bias=None, act_format: str = "mxfp8") -> np.ndarray:
+    """bf16 x [T, K] against MXFP4 W [N, K] (+ bf16 bias [N]) -> fp64 [T, N]."""
+    xx = _np(x, np.uint16)
+    b = _np(blocks, np.uint8)
+    sc = _np(scales, np.uint8)
+    bb = None if bias is None else _np(bias, np.uint16)
+    T, K = xx.shape
+    N = sc.shape[0]
+    out = np.empty((T, N), np.float64)
+    lib().oracle_dense_linear(_ptr(xx), T, K, N, _ptr(b), _ptr(sc), _ptr(bb), _ptr(out), _ACT[act_format])
+    return out
+
+
+# --- NVFP4 -----------------------------------------------------------------------------
+def nvfp4_global_scale(amax: float) -> float:
+    return lib().oracle_nvfp4_global_scale(float(amax))
+
+
+def nvfp4_quantize(v, gs: float = 1.0):
+    """fp64 values (last dim a multiple of 16) -> (E2M1 codes one per byte, E4M3 scale codes per 16)."""
+    a = _np(v, np.float64)
+    q = np.empty(a.shape, np.uint8)
+    s = np.empty(a.shape[:-1] + (a.shape[-1] // 16,), np.uint8)
+    lib().oracle_nvfp4_quantize(_ptr(a), a.size, float(gs), _ptr(q), _ptr(s))
+    return q, s
+
+
+def nvfp4_value(code: int, scale_code: int, gs: float = 1.0) -> float:
+    return lib().oracle_nvfp4_value(code, scale_code, float(gs))
+
+
+def nvfp4_dequant(codes, scale_codes, gs: float) -> np.ndarray:
+    """codes [..., K] (one per byte) and scale codes [..., K/16] -> fp64 values."""
+    c = _np(codes, np.uint8)
+    s = _np(scale_codes, np.uint8)
+    e2 = np.array([e2m1_value(i) for i in range(16)])
+    e4 = np.array([e4m3_value(i) for i in range(256)])
+    return e2[c] * np.repeat(e4[s], 16, axis=-1) * gs
+
+
+def expert_mlp_nvfp4(xq, xs, gu_codes, gu_sc, gu_gs, gu_bias, d_codes, d_sc, d_gs, d_bias):
+    """One expert on one NVFP4 activation row with NVFP4 weights -> dict(h, hq, hs, y)."""
+    xq = _np(xq, np.uint8)
+    xs = _np(xs, np.uint8)
+    guc, gus, gub = _np(gu_codes, np.uint8), _np(gu_sc, np.uint8), _np(gu_bias, np.uint16)
+    dc, ds, db = _np(d_codes, np.uint8), _np(d_sc, np.uint8), _np(d_bias, np.uint16)
+    H = xq.shape[-1]
+    I = guc.shape[0] // 2
+    h = np.empty(I, np.float64)
+    hq = np.empty(I, np.uint8)
+    hs = np.empty(I // 16, np.uint8)
+    y = np.empty(H, np.float64)
+    lib().oracle_expert_mlp_nvfp4(_ptr(xq), _ptr(xs), H, I, _ptr(guc), _ptr(gus), float(gu_gs), _ptr(gub),
+                                  _ptr(dc), _ptr(ds), float(d_gs), _ptr(db), _ptr(h), _ptr(hq), _ptr(hs), _ptr(y))
+    return dict(h=h, hq=hq, hs=hs, y=y)

@@ -21,6 +21,14 @@
 //    Optimizations": native FP4 x FP4 block-scaled MMA as the next step, for
 //    which the layer can also quantise its activations to MXFP4 (the
 //    `act_fp4` variant below).
+//  * "GPT-OSS-120B with MXFP4 on DGX Spark (SM121/GB10)", "What's Included",
+//    "Full MXFP4 Quantization Stack": the dense projections (QKV, O, LM head)
+//    in MXFP4 as well (oracle_dense_linear, oracle_quantize_mxfp4_weights).
+//  * "GPT-OSS-120B on DGX Spark: From MXFP4 to NVFP4", "The MXFP4 -> NVFP4
+//    Conversion": NVFP4 = E2M1 data in 16-element blocks with an E4M3 scale per
+//    block and a global scale; "Conversion Methodology": dequantise MXFP4, then
+//    per 16-element block take the amax, choose the E4M3 scale, quantise the
+//    elements to E2M1 (oracle_nvfp4_*).
 //  The layer definition the pages leave open (routing rule, SwiGLU, MXFP8
 //  scale rule, nibble order, gate/up row order) follows the readings listed
 //  in the design notes; each function below states the one it uses.
@@ -348,6 +356,116 @@ void oracle_moe_forward(const uint16_t* x, int64_t T, int64_t H, int64_t I, int6
                         uint8_t* hs_out) {
   oracle_moe_forward_fmt(x, T, H, I, E, k, router_w, router_b, gu_blocks, gu_scales, gu_bias, d_blocks, d_scales,
                          d_bias, out, logits_out, ids_out, w_out, xq_out, xs_out, h_out, hq_out, hs_out, 0);
+}
+
+// ---------------------------------------------------------------- dense MXFP4 linears
+// Pack E2M1 codes (one per byte, [rows, K]) into the checkpoint block layout
+// [rows, K/32, 16]: two codes per byte, the even element in the low nibble.
+void oracle_pack_e2m1(const uint8_t* codes, int64_t rows, int64_t K, uint8_t* blocks) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < K; c += 2)
+      blocks[(r * K + c) / 2] = static_cast<uint8_t>((codes[r * K + c] & 0xF) | ((codes[r * K + c + 1] & 0xF) << 4));
+}
+
+// Quantise a [rows, K] weight matrix (fp64 values, e.g. widened bf16) to MXFP4 in the
+// checkpoint layout: per 32-element block the same shared-exponent rule as the
+// MXFP4 activations (floor(log2 amax) - 2; E2M1 round-to-nearest-even, saturating
+// at 6).  blocks [rows, K/32, 16], scales [rows, K/32].
+void oracle_quantize_mxfp4_weights(const double* w, int64_t rows, int64_t K, uint8_t* blocks, uint8_t* scales) {
+  std::vector<uint8_t> q(K);
+  for (int64_t r = 0; r < rows; ++r) {
+    oracle_mxfp4_quantize(w + r * K, K, q.data(), scales + r * (K / 32));
+    oracle_pack_e2m1(q.data(), 1, K, blocks + r * (K / 2));
+  }
+}
+
+// A dense MXFP4 linear: out[t][n] = sum_k xq[t][k] * W[n][k] + b[n], with x (bf16
+// [T, K]) quantised per row to MXFP8 (act_fp4 = 0) or MXFP4 (1) as in the expert
+// MLP, W [N, K] MXFP4 in the checkpoint layout, b bf16 [N] (may be NULL).  fp64
+// sums; out [T, N] fp64.
+void oracle_dense_linear(const uint16_t* x, int64_t T, int64_t K, int64_t N, const uint8_t* blocks,
+                         const uint8_t* scales, const uint16_t* bias, double* out, int32_t act_fp4) {
+  std::vector<double> xr(K), xv(K);
+  std::vector<uint8_t> xq(K), xs(K / 32);
+  for (int64_t t = 0; t < T; ++t) {
+    for (int64_t c = 0; c < K; ++c) xr[c] = bf16_to_double(x[t * K + c]);
+    if (act_fp4)
+      oracle_mxfp4_quantize(xr.data(), K, xq.data(), xs.data());
+    else
+      oracle_mxfp8_quantize(xr.data(), K, xq.data(), xs.data());
+    for (int64_t c = 0; c < K; ++c) xv[c] = (act_fp4 ? e2m1(xq[c]) : e4m3(xq[c])) * e8m0(xs[c / 32]);
+    for (int64_t n = 0; n < N; ++n) {
+      double acc = 0.0;
+      for (int64_t c = 0; c < K; ++c) acc += xv[c] * mxfp4_weight(blocks, scales, K, n, c);
+      out[t * N + n] = acc + (bias ? bf16_to_double(bias[n]) : 0.0);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- NVFP4
+// Global scale of a tensor whose largest magnitude is amax: amax / (6 * 448), so
+// that the largest block scale is E4M3's largest value (reading: the page's
+// conversion returns "a global scale factor" without its rule; this is the
+// plainest one that lets the E4M3 block scales span the tensor).  fp32, the
+// precision the scale is stored in; 1 for an all-zero tensor.
+double oracle_nvfp4_global_scale(double amax) {
+  if (!(amax > 0.0)) return 1.0;
+  return static_cast<double>(static_cast<float>(amax) / 2688.0f);
+}
+
+// NVFP4 quantisation of n values (n a multiple of 16) with global scale gs:
+// per 16-element block, scale code = E4M3(amax / (6 gs)) (round-to-nearest-even,
+// saturating at 448); element codes = E2M1(v / (scale * gs)) (ties to even,
+// saturating at 6), all-zero codes where the block scale is zero.  The divisions
+// that decide codes are taken in fp32, the precision a GPU quantiser computes
+// in.  codes q[n] one per byte, scale codes s[n/16].
+void oracle_nvfp4_quantize(const double* v, int64_t n, double gs, uint8_t* q, uint8_t* s) {
+  const float g = static_cast<float>(gs);
+  for (int64_t b = 0; b < n / 16; ++b) {
+    double amax = 0.0;
+    for (int i = 0; i < 16; ++i) amax = std::max(amax, std::fabs(v[16 * b + i]));
+    const float t = static_cast<float>(amax) / (6.0f * g);
+    const int sc = e4m3_encode(static_cast<double>(t));
+    s[b] = static_cast<uint8_t>(sc);
+    const float sv = static_cast<float>(e4m3(sc)) * g;
+    for (int i = 0; i < 16; ++i) {
+      const int64_t k = 16 * b + i;
+      q[k] = sv == 0.0f ? 0 : static_cast<uint8_t>(e2m1_encode(static_cast<double>(static_cast<float>(v[k]) / sv)));
+    }
+  }
+}
+
+// Value of NVFP4 element k of a row: e2m1(code) * e4m3(scale of its block) * gs.
+double oracle_nvfp4_value(int code, int scale_code, double gs) { return e2m1(code & 15) * e4m3(scale_code & 255) * gs; }
+
+// One expert's MLP with NVFP4 weights and NVFP4 activations (unit global scale
+// for the activations): x codes xq [H] (one per byte) with scales xs [H/16];
+// weights as codes [rows, K] (one per byte) with scale codes [rows, K/16] and a
+// global scale per projection.  h (rounded to fp32) is NVFP4-quantised the same
+// way.  Outputs as in oracle_expert_mlp_fmt.
+void oracle_expert_mlp_nvfp4(const uint8_t* xq, const uint8_t* xs, int64_t H, int64_t I, const uint8_t* gu_codes,
+                             const uint8_t* gu_sc, double gu_gs, const uint16_t* gu_bias, const uint8_t* d_codes,
+                             const uint8_t* d_sc, double d_gs, const uint16_t* d_bias, double* h_out, uint8_t* hq_out,
+                             uint8_t* hs_out, double* y) {
+  std::vector<double> xv(H), g(2 * I), h(I), hv(I);
+  std::vector<uint8_t> hq(I), hs(I / 16);
+  for (int64_t c = 0; c < H; ++c) xv[c] = oracle_nvfp4_value(xq[c], xs[c / 16], 1.0);
+  for (int64_t r = 0; r < 2 * I; ++r) {
+    double acc = 0.0;
+    for (int64_t c = 0; c < H; ++c) acc += xv[c] * oracle_nvfp4_value(gu_codes[r * H + c], gu_sc[r * (H / 16) + c / 16], gu_gs);
+    g[r] = acc + bf16_to_double(gu_bias[r]);
+  }
+  for (int64_t i = 0; i < I; ++i) h[i] = static_cast<double>(static_cast<float>(silu(g[i]) * g[I + i]));
+  oracle_nvfp4_quantize(h.data(), I, 1.0, hq.data(), hs.data());
+  for (int64_t i = 0; i < I; ++i) hv[i] = oracle_nvfp4_value(hq[i], hs[i / 16], 1.0);
+  for (int64_t c = 0; c < H; ++c) {
+    double acc = 0.0;
+    for (int64_t i = 0; i < I; ++i) acc += hv[i] * oracle_nvfp4_value(d_codes[c * I + i], d_sc[c * (I / 16) + i / 16], d_gs);
+    y[c] = acc + bf16_to_double(d_bias[c]);
+  }
+  if (h_out) std::copy(h.begin(), h.end(), h_out);
+  if (hq_out) std::copy(hq.begin(), hq.end(), hq_out);
+  if (hs_out) std::copy(hs.begin(), hs.end(), hs_out);
 }
 
 // RMSNorm with unit gain: x / sqrt(mean(x^2) + eps), rounded to bf16 (RNE).

@@ -452,3 +452,136 @@ def test_rmsnorm_closed_form():
     for t, c in enumerate([3.0, -0.5]):
         want = oracle.bf16_round(c / math.sqrt(c * c + 1e-5))
         assert (out[t] == want).all()
+
+
+# ----------------------------------------------------------------------- dense MXFP4 linears
+def _e2m1_table():
+    return np.array([v for _, v in sorted(_golden("e2m1_values.txt"))])
+
+
+def test_pack_e2m1_round_trips_through_the_dequantiser():
+    """Codes packed into the checkpoint blocks decode (by the pinned dequantiser) to the
+    page's value of each code times its block scale, element by element."""
+    rng = np.random.default_rng(5)
+    rows, K = 6, 96
+    codes = rng.integers(0, 16, (rows, K)).astype(np.uint8)
+    scales = rng.integers(118, 131, (rows, K // 32)).astype(np.uint8)
+    W = oracle.dequant_mxfp4(oracle.pack_e2m1(codes), scales)
+    want = _e2m1_table()[codes] * np.exp2(np.repeat(scales.astype(np.int64), 32, axis=1) - 127.0)
+    np.testing.assert_array_equal(W, want)
+
+
+def test_quantize_mxfp4_weights_hand_block_and_idempotence():
+    """A hand-worked block (amax 6 -> shared exponent 0, codes from the page's table),
+    idempotence on values the format holds, and the error bound of the top binade:
+    at most 2^(s+1) per element (the 4..6 gap halved, or saturation from below 8)."""
+    blk = np.zeros((1, 32))
+    blk[0, :6] = [6.0, 3.0, -1.5, 0.5, 0.25, 0.75]
+    b, s = oracle.quantize_mxfp4_weights(blk)
+    assert s[0, 0] == 127
+    by = b[0, 0]
+    lo = by[0] & 0xF, by[0] >> 4, by[1] & 0xF, by[1] >> 4, by[2] & 0xF, by[2] >> 4
+    assert lo == (7, 5, 11, 1, 0, 2)  # 0.25 and 0.75 are midpoints: ties go to the even code
+    rng = np.random.default_rng(6)
+    W = rng.normal(0, 0.3, (8, 128))
+    b1, s1 = oracle.quantize_mxfp4_weights(W)
+    W1 = oracle.dequant_mxfp4(b1, s1)
+    b2, s2 = oracle.quantize_mxfp4_weights(W1)
+    np.testing.assert_array_equal(b1, b2)
+    np.testing.assert_array_equal(s1, s2)
+    step = np.exp2(np.repeat(s1.astype(np.int64), 32, axis=1) - 127.0 + 1)
+    assert (np.abs(W - W1) <= step).all()
+
+
+@pytest.mark.parametrize("act_format", ["mxfp8", "mxfp4"])
+def test_dense_linear_matches_dequantised_matmul(act_format):
+    """The dense linear against numpy: the pinned activation quantiser and weight
+    dequantiser, then a library matmul and the bias."""
+    rng = np.random.default_rng(7)
+    T, K, N = 3, 96, 40
+    x = torch.from_numpy(rng.normal(0, 1, (T, K))).to(torch.bfloat16)
+    b, s = oracle.quantize_mxfp4_weights(rng.normal(0, 0.2, (N, K)))
+    bias = torch.from_numpy(rng.normal(0, 0.1, N)).to(torch.bfloat16)
+    got = oracle.dense_linear(x, b, s, bias, act_format=act_format)
+    xf = x.float().double().numpy()
+    if act_format == "mxfp8":
+        q, qs = oracle.mxfp8_quantize(xf)
+        xv = np.array([oracle.e4m3_value(c) for c in range(256)])[q]
+    else:
+        q, qs = oracle.mxfp4_quantize(xf)
+        xv = _e2m1_table()[q]
+    xv = xv * np.exp2(np.repeat(qs.astype(np.int64), 32, axis=1) - 127.0)
+    want = xv @ oracle.dequant_mxfp4(b, s).T + bias.float().double().numpy()
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+    assert np.allclose(oracle.dense_linear(x, b, s, None, act_format=act_format), want - bias.float().double().numpy(),
+                       rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------------------------------- NVFP4
+def test_nvfp4_global_scale_closed_form():
+    # amax / (6 * 448): a tensor whose amax is 6 * 448 needs no global scaling
+    assert oracle.nvfp4_global_scale(2688.0) == 1.0
+    assert oracle.nvfp4_global_scale(5376.0) == 2.0
+    assert oracle.nvfp4_global_scale(0.0) == 1.0
+    assert oracle.nvfp4_global_scale(1.0) == float(np.float32(1.0) / np.float32(2688.0))
+
+
+def test_nvfp4_hand_blocks():
+    """Scale = E4M3(amax / 6); elements E2M1(v / scale), ties to even, saturating at 6."""
+    v = np.zeros(16)
+    v[:7] = [6.0, -3.0, 1.5, 0.25, 0.75, 2.5, 5.0]
+    q, s = oracle.nvfp4_quantize(v)
+    assert s[0] == 0x38  # E4M3 1.0
+    assert tuple(q[:7]) == (7, 13, 3, 0, 2, 4, 6)  # 0.25->0, 0.75->1.0, 2.5->2, 5->4 (ties to even)
+    v2 = np.zeros(16)
+    v2[0] = 7.0  # 7/6 = 1.1667 rounds to E4M3 1.125; 7/1.125 = 6.2 saturates to 6
+    q, s = oracle.nvfp4_quantize(v2)
+    assert oracle.e4m3_value(int(s[0])) == 1.125 and q[0] == 7
+    q, s = oracle.nvfp4_quantize(np.zeros(16))  # an all-zero block: zero scale, zero codes
+    assert s[0] == 0 and (q == 0).all()
+    # a global scale divides the block scale's argument
+    q, s = oracle.nvfp4_quantize(v * 4.0, gs=4.0)
+    assert s[0] == 0x38 and tuple(q[:7]) == (7, 13, 3, 0, 2, 4, 6)
+
+
+def test_nvfp4_scale_matches_torch_cast_and_error_bound():
+    """The block scale code is torch's float8_e4m3fn cast of the fp32 amax / (6 gs)
+    (a library routine), and every element lies within one scale unit of its value
+    (the largest E2M1 gap, 4..6, halved; or saturation from at most 6 (1 + 1/16))."""
+    rng = np.random.default_rng(8)
+    v = rng.normal(0, 2.0, (32, 64)) * np.exp2(rng.integers(-6, 6, (32, 1)))
+    gs = oracle.nvfp4_global_scale(np.abs(v).max())
+    q, s = oracle.nvfp4_quantize(v, gs)
+    amax = np.abs(v).reshape(32, 4, 16).max(axis=2)
+    t = torch.from_numpy(amax.astype(np.float32)) / torch.tensor(6.0 * np.float32(gs), dtype=torch.float32)
+    want = t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(s, want)
+    deq = oracle.nvfp4_dequant(q, s, gs)
+    sv = np.repeat(np.array([oracle.e4m3_value(c) for c in range(256)])[s], 16, axis=1) * gs
+    assert (np.abs(v - deq) <= sv * (1 + 1e-12)).all()
+
+
+def test_expert_mlp_nvfp4_matches_dequantised_dense_path():
+    """One expert with NVFP4 weights and activations against numpy: dequantised
+    operands, library matmuls, scipy's expit for the SiLU; the intermediate is
+    quantised by the pinned NVFP4 quantiser."""
+    rng = np.random.default_rng(9)
+    H, I = 64, 32
+    x = rng.normal(0, 1, H)
+    xq, xs = oracle.nvfp4_quantize(x)
+    wgu = rng.normal(0, 0.2, (2 * I, H))
+    wd = rng.normal(0, 0.2, (H, I))
+    gsg = oracle.nvfp4_global_scale(np.abs(wgu).max())
+    gsd = oracle.nvfp4_global_scale(np.abs(wd).max())
+    guq, gus = oracle.nvfp4_quantize(wgu, gsg)
+    dq, dsc = oracle.nvfp4_quantize(wd, gsd)
+    gub = torch.from_numpy(rng.normal(0, 0.02, 2 * I)).to(torch.bfloat16)
+    db = torch.from_numpy(rng.normal(0, 0.02, H)).to(torch.bfloat16)
+    r = oracle.expert_mlp_nvfp4(xq, xs, guq, gus, gsg, gub, dq, dsc, gsd, db)
+    g = oracle.nvfp4_dequant(xq, xs, 1.0) @ oracle.nvfp4_dequant(guq, gus, gsg).T + gub.float().double().numpy()
+    h = (g[:I] * scipy.special.expit(g[:I]) * g[I:]).astype(np.float32).astype(np.float64)
+    np.testing.assert_allclose(r["h"], h, rtol=1e-6, atol=1e-9)
+    hq, hs = oracle.nvfp4_quantize(r["h"])
+    np.testing.assert_array_equal(r["hq"], hq)
+    y = oracle.nvfp4_dequant(hq, hs, 1.0) @ oracle.nvfp4_dequant(dq, dsc, gsd).T + db.float().double().numpy()
+    np.testing.assert_allclose(r["y"], y, rtol=1e-12, atol=1e-12)
