@@ -627,7 +627,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_case(T: int, calls: int):
+def run_case(T: int, calls: int, plan=None, act_format: str = "mxfp8"):
     """A small profiling target: one layer (about 2.3 GB of packed weights on the
     device), ``calls`` forward calls on the default stream, then the device status."""
     import torch
@@ -641,12 +641,14 @@ def run_case(T: int, calls: int):
     del w
     rw, rb = [t.cuda() for t in ms.make_router(0, H, E, hot_experts=16 if T == 32 else 0, hot_bias=1.0)]
     x = ms.make_tokens(0, T, H).cuda()
+    if plan:
+        moe.set_plan(int(plan[0]), plan[1], plan[2])
     ws = moe.alloc_workspace(dims, T, k)
     for _ in range(calls):
-        moe.forward(dims, x, rw, rb, packed, k, workspace=ws)
+        moe.forward(dims, x, rw, rb, packed, k, workspace=ws, act_format=act_format)
     torch.cuda.synchronize()
     st = moe.device_status(ws)
-    print(f"case T={T}: {calls} calls, device status {st}", flush=True)
+    print(f"case T={T} plan={plan} act={act_format}: {calls} calls, device status {st}", flush=True)
     if st != 0:
         raise SystemExit(1)
 
@@ -745,6 +747,9 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="plan sweep: median step time of every tile-height and routing-path candidate per T")
     ap.add_argument("--sweep-t", type=int, nargs="*", default=None, help="token counts of the plan sweep")
+    ap.add_argument("--plan", nargs=3, default=None, metavar=("TILE_ROWS", "ROUTE", "EXPERT"),
+                    help="with --case: force a plan (tile rows, routing path, expert kernel)")
+    ap.add_argument("--act", default="mxfp8", choices=["mxfp8", "mxfp4"], help="with --case: activation format")
     ap.add_argument("--case", type=int, default=None, metavar="T",
                     help="profiling run: one gpt-oss-shaped layer at T tokens, warmup + steps plain "
                          "forward calls, no timing and no JSON line (T=32 uses the skewed router)")
@@ -752,7 +757,7 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.case is not None:
-        run_case(args.case, args.warmup + args.steps)
+        run_case(args.case, args.warmup + args.steps, args.plan, args.act)
     elif args.sweep:
         run_sweep(args)
     elif args.impl == "reference":

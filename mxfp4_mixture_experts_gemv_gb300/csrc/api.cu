@@ -295,12 +295,11 @@ moe_status forward_impl(moe_dims d, bool fp4, const void* hidden, int32_t T, con
   // Many tokens: a streaming pass after the expert kernel, which would otherwise
   // stall on the slot loads of every completed token.
   b.fused_combine = L.tile_rows <= 32;
-  // expert kernel: full 128-row token tiles take the tokens-on-M kernel (two
-  // weight tiles per MMA), smaller tiles the weights-on-M kernel
+  // expert kernel: weights-on-M by default (the plan sweep measured the
+  // tokens-on-M kernel slower at 2048 and 4096 tokens and even at 8192); the
+  // tokens-on-M kernel runs when the plan asks for it
   const int forced_expert = moe::plan_expert();
-  const bool tokens_m = !fp4 && L.tile_rows == 128 &&
-                        (forced_expert == moe::kExpertAuto || forced_expert == moe::kExpertTokensM) &&
-                        forced_expert != moe::kExpertWeightsM;
+  const bool tokens_m = !fp4 && L.tile_rows == 128 && forced_expert == moe::kExpertTokensM;
   if (forced_expert == moe::kExpertTokensM && !tokens_m)
     return fail(MOE_ERR_UNSUPPORTED_SHAPE, "the tokens-on-M expert kernel needs 128-row tiles and MXFP8 activations");
   if (tokens_m)

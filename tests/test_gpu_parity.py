@@ -268,7 +268,7 @@ def test_forced_route_that_does_not_fit_is_refused():
 def test_gpt_oss_parity_at_the_plan_cutoffs(gpt_layer, T):
     """Either side of every automatic cutoff: cluster / grid routing at 8, grid /
     tensor-core routing at 32, and the token-tile heights 8 / 16 / 32 / 64 / 128
-    at 128, 256, 512 and 1024 (128-row tiles take the tokens-on-M expert kernel).
+    at 128, 256, 512 and 1024.
     Routing, grouping and the gathered rows are checked for every token, the
     output on up to 24 tokens (the oracle runs one token per host thread)."""
     cpu_inp, dev_inp, packed = _gpt_inputs(gpt_layer, T)
