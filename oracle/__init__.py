@@ -90,6 +90,13 @@ def lib():
             L.oracle_nvfp4_value.argtypes = [ctypes.c_int, ctypes.c_int, d]
             L.oracle_expert_mlp_nvfp4.restype = None
             L.oracle_expert_mlp_nvfp4.argtypes = [p, p, i64, i64, p, p, d, p, p, p, d, p, p, p, p, p]
+            L.oracle_convert_mxfp4_to_nvfp4.restype = None
+            L.oracle_convert_mxfp4_to_nvfp4.argtypes = [p, p, i64, i64, d, p, p]
+            L.oracle_mxfp4_amax.restype = d
+            L.oracle_mxfp4_amax.argtypes = [p, p, i64, i64]
+            L.oracle_moe_forward_nvfp4.restype = None
+            L.oracle_moe_forward_nvfp4.argtypes = [p, i64, i64, i64, i64, i32, p, p, p, p, p, p, p, p,
+                                                   p, p, p, p, p, p, p, p, p]
             L.oracle_rmsnorm_bf16.restype = None
             L.oracle_rmsnorm_bf16.argtypes = [p, i64, i64, d, p]
             _lib = L
@@ -227,6 +234,28 @@ def expert_mlp(xq, xs, gu_blocks, gu_scales, gu_bias, d_blocks, d_scales, d_bias
     return dict(g=g, h=h, hq=hq, hs=hs, y=y)
 
 
+def mxfp4_amax(blocks, scales) -> float:
+    """Largest magnitude of an MXFP4 tensor (checkpoint layout, any leading dims)."""
+    b = _np(blocks, np.uint8)
+    s = _np(scales, np.uint8)
+    nb = s.shape[-1]
+    rows = s.size // nb
+    return lib().oracle_mxfp4_amax(_ptr(b), _ptr(s), rows, nb * 32)
+
+
+def convert_mxfp4_to_nvfp4(blocks, scales, gs: float):
+    """MXFP4 rows [rows, K/32, 16] + [rows, K/32] -> NVFP4 (codes [rows, K] one per byte,
+    E4M3 scale codes [rows, K/16]) with global scale gs."""
+    b = _np(blocks, np.uint8)
+    s = _np(scales, np.uint8)
+    rows, nb = s.shape[-2], s.shape[-1]
+    K = nb * 32
+    codes = np.empty((rows, K), np.uint8)
+    sc = np.empty((rows, K // 16), np.uint8)
+    lib().oracle_convert_mxfp4_to_nvfp4(_ptr(b), _ptr(s), rows, K, float(gs), _ptr(codes), _ptr(sc))
+    return codes, sc
+
+
 def moe_forward(x, router_w, router_b, gu_blocks, gu_scales, gu_bias, d_blocks, d_scales, d_bias,
                 k: int, intermediates: bool = False, act_format: str = "mxfp8"):
     """The whole layer -> dict(out fp64 [T,H], logits, ids, w, xq, xs[, h, hq, hs]).
@@ -240,6 +269,8 @@ def moe_forward(x, router_w, router_b, gu_blocks, gu_scales, gu_bias, d_blocks, 
     T, H = xx.shape
     E = wr.shape[0]
     I = gus.shape[1] // 2
+    if act_format == "nvfp4":
+        return _moe_forward_nvfp4(xx, wr, br, gub, gus, gubias, db, ds, dbias, T, H, I, E, k, intermediates)
     out = np.empty((T, H), np.float64)
     logits = np.empty((T, E), np.float64)
     ids = np.empty((T, k), np.int32)
@@ -352,3 +383,24 @@ def expert_mlp_nvfp4(xq, xs, gu_codes, gu_sc, gu_gs, gu_bias, d_codes, d_sc, d_g
     lib().oracle_expert_mlp_nvfp4(_ptr(xq), _ptr(xs), H, I, _ptr(guc), _ptr(gus), float(gu_gs), _ptr(gub),
                                   _ptr(dc), _ptr(ds), float(d_gs), _ptr(db), _ptr(h), _ptr(hq), _ptr(hs), _ptr(y))
     return dict(h=h, hq=hq, hs=hs, y=y)
+
+
+def _moe_forward_nvfp4(xx, wr, br, gub, gus, gubias, db, ds, dbias, T, H, I, E, k, intermediates):
+    out = np.empty((T, H), np.float64)
+    logits = np.empty((T, E), np.float64)
+    ids = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float64)
+    xq = np.empty((T, H), np.uint8)
+    xs = np.empty((T, H // 16), np.uint8)
+    h = hq = hs = None
+    if intermediates:
+        h = np.empty((T, k, I), np.float64)
+        hq = np.empty((T, k, I), np.uint8)
+        hs = np.empty((T, k, I // 16), np.uint8)
+    lib().oracle_moe_forward_nvfp4(_ptr(xx), T, H, I, E, k, _ptr(wr), _ptr(br), _ptr(gub), _ptr(gus),
+                                   _ptr(gubias), _ptr(db), _ptr(ds), _ptr(dbias), _ptr(out), _ptr(logits),
+                                   _ptr(ids), _ptr(w), _ptr(xq), _ptr(xs), _ptr(h), _ptr(hq), _ptr(hs))
+    r = dict(out=out, logits=logits, ids=ids, w=w, xq=xq, xs=xs)
+    if intermediates:
+        r.update(h=h, hq=hq, hs=hs)
+    return r

@@ -468,6 +468,76 @@ void oracle_expert_mlp_nvfp4(const uint8_t* xq, const uint8_t* xs, int64_t H, in
   if (hs_out) std::copy(hs.begin(), hs.end(), hs_out);
 }
 
+// Convert one MXFP4 projection's rows [rows, K] (checkpoint layout) to NVFP4 with
+// global scale gs: codes [rows, K] one per byte, E4M3 scale codes [rows, K/16].
+void oracle_convert_mxfp4_to_nvfp4(const uint8_t* blocks, const uint8_t* scales, int64_t rows, int64_t K, double gs,
+                                   uint8_t* codes, uint8_t* sc) {
+  std::vector<double> w(K);
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t c = 0; c < K; ++c) w[c] = mxfp4_weight(blocks, scales, K, r, c);
+    oracle_nvfp4_quantize(w.data(), K, gs, codes + r * K, sc + r * (K / 16));
+  }
+}
+
+// Largest magnitude of an MXFP4 tensor of n_rows rows of K elements.
+double oracle_mxfp4_amax(const uint8_t* blocks, const uint8_t* scales, int64_t rows, int64_t K) {
+  double m = 0.0;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < K; ++c) m = std::max(m, std::fabs(mxfp4_weight(blocks, scales, K, r, c)));
+  return m;
+}
+
+// The whole layer in the NVFP4 variant: the MXFP4 expert weights converted to
+// NVFP4 per projection (global scale from the projection's amax over all experts),
+// the activations x and h quantised to NVFP4 with unit global scale, routing and
+// combine as in oracle_moe_forward_fmt.  Arguments as there; xs has H/16 scale
+// codes per token and hs I/16 per (token, slot); codes one per byte.
+void oracle_moe_forward_nvfp4(const uint16_t* x, int64_t T, int64_t H, int64_t I, int64_t E, int32_t k,
+                              const uint16_t* router_w, const uint16_t* router_b, const uint8_t* gu_blocks,
+                              const uint8_t* gu_scales, const uint16_t* gu_bias, const uint8_t* d_blocks,
+                              const uint8_t* d_scales, const uint16_t* d_bias, double* out, double* logits_out,
+                              int32_t* ids_out, double* w_out, uint8_t* xq_out, uint8_t* xs_out, double* h_out,
+                              uint8_t* hq_out, uint8_t* hs_out) {
+  std::vector<double> logits(T * E), w(T * k), xrow(H), y(H);
+  std::vector<int32_t> ids(T * k);
+  std::vector<uint8_t> xq(H), xs(H / 16);
+  oracle_route(x, router_w, router_b, T, H, E, k, logits.data(), ids.data(), w.data());
+  const double gs_gu = oracle_nvfp4_global_scale(oracle_mxfp4_amax(gu_blocks, gu_scales, E * 2 * I, H));
+  const double gs_d = oracle_nvfp4_global_scale(oracle_mxfp4_amax(d_blocks, d_scales, E * H, I));
+  std::vector<std::vector<uint8_t>> guc(E), gus(E), dc(E), ds(E);
+  for (int64_t t = 0; t < T; ++t)
+    for (int32_t j = 0; j < k; ++j) {
+      const int64_t e = ids[t * k + j];
+      if (!guc[e].empty()) continue;
+      guc[e].resize(2 * I * H);
+      gus[e].resize(2 * I * (H / 16));
+      dc[e].resize(H * I);
+      ds[e].resize(H * (I / 16));
+      oracle_convert_mxfp4_to_nvfp4(gu_blocks + e * 2 * I * (H / 2), gu_scales + e * 2 * I * (H / 32), 2 * I, H,
+                                    gs_gu, guc[e].data(), gus[e].data());
+      oracle_convert_mxfp4_to_nvfp4(d_blocks + e * H * (I / 2), d_scales + e * H * (I / 32), H, I, gs_d,
+                                    dc[e].data(), ds[e].data());
+    }
+  for (int64_t t = 0; t < T; ++t) {
+    for (int64_t c = 0; c < H; ++c) xrow[c] = bf16_to_double(x[t * H + c]);
+    oracle_nvfp4_quantize(xrow.data(), H, 1.0, xq.data(), xs.data());
+    if (xq_out) std::copy(xq.begin(), xq.end(), xq_out + t * H);
+    if (xs_out) std::copy(xs.begin(), xs.end(), xs_out + t * (H / 16));
+    for (int64_t c = 0; c < H; ++c) out[t * H + c] = 0.0;
+    for (int32_t j = 0; j < k; ++j) {
+      const int64_t e = ids[t * k + j], tj = t * k + j;
+      oracle_expert_mlp_nvfp4(xq.data(), xs.data(), H, I, guc[e].data(), gus[e].data(), gs_gu, gu_bias + e * 2 * I,
+                              dc[e].data(), ds[e].data(), gs_d, d_bias + e * H, h_out ? h_out + tj * I : nullptr,
+                              hq_out ? hq_out + tj * I : nullptr, hs_out ? hs_out + tj * (I / 16) : nullptr,
+                              y.data());
+      for (int64_t c = 0; c < H; ++c) out[t * H + c] += w[t * k + j] * y[c];
+    }
+  }
+  if (logits_out) std::copy(logits.begin(), logits.end(), logits_out);
+  if (ids_out) std::copy(ids.begin(), ids.end(), ids_out);
+  if (w_out) std::copy(w.begin(), w.end(), w_out);
+}
+
 // RMSNorm with unit gain: x / sqrt(mean(x^2) + eps), rounded to bf16 (RNE).
 void oracle_rmsnorm_bf16(const double* x, int64_t T, int64_t H, double eps, uint16_t* out) {
   for (int64_t t = 0; t < T; ++t) {

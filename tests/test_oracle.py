@@ -585,3 +585,36 @@ def test_expert_mlp_nvfp4_matches_dequantised_dense_path():
     np.testing.assert_array_equal(r["hq"], hq)
     y = oracle.nvfp4_dequant(hq, hs, 1.0) @ oracle.nvfp4_dequant(dq, dsc, gsd).T + db.float().double().numpy()
     np.testing.assert_allclose(r["y"], y, rtol=1e-12, atol=1e-12)
+
+
+def test_nvfp4_layer_matches_its_steps_and_brute_force():
+    """The NVFP4 layer against its pinned steps composed in numpy: the conversion
+    of every used expert (dequantise MXFP4, global scale from the projection's
+    amax over all experts, NVFP4 quantisation), the NVFP4 expert MLP, and the
+    routing-weighted sum; and the projections' amax against a dense dequantisation."""
+    import moe_synth as ms
+    shape = ms.LayerShape(T=5, H=64, I=64, E=4, k=2)
+    inp = ms.make_layer(shape, seed=12)
+    w = (inp.gate_up_blocks, inp.gate_up_scales, inp.gate_up_bias, inp.down_blocks, inp.down_scales, inp.down_bias)
+    r = oracle.moe_forward(inp.x, inp.router_w, inp.router_b, *w, k=2, intermediates=True, act_format="nvfp4")
+    amax_gu = np.abs(oracle.dequant_mxfp4(inp.gate_up_blocks.reshape(-1, 2, 16), inp.gate_up_scales.reshape(-1, 2))).max()
+    assert oracle.mxfp4_amax(inp.gate_up_blocks, inp.gate_up_scales) == amax_gu
+    gs_gu = oracle.nvfp4_global_scale(amax_gu)
+    gs_d = oracle.nvfp4_global_scale(oracle.mxfp4_amax(inp.down_blocks, inp.down_scales))
+    _, ids, wts = oracle.route(inp.x, inp.router_w, inp.router_b, 2)
+    np.testing.assert_array_equal(r["ids"], ids)
+    want = np.zeros((5, 64))
+    for t in range(5):
+        xq, xs = oracle.nvfp4_quantize(inp.x[t].float().double().numpy())
+        np.testing.assert_array_equal(r["xq"][t], xq)
+        for j in range(2):
+            e = int(ids[t, j])
+            gc, gsc = oracle.convert_mxfp4_to_nvfp4(inp.gate_up_blocks[e], inp.gate_up_scales[e], gs_gu)
+            q2, s2 = oracle.nvfp4_quantize(oracle.dequant_mxfp4(inp.gate_up_blocks[e], inp.gate_up_scales[e]), gs_gu)
+            np.testing.assert_array_equal(gc, q2)
+            np.testing.assert_array_equal(gsc, s2)
+            dc, dsc = oracle.convert_mxfp4_to_nvfp4(inp.down_blocks[e], inp.down_scales[e], gs_d)
+            m = oracle.expert_mlp_nvfp4(xq, xs, gc, gsc, gs_gu, inp.gate_up_bias[e], dc, dsc, gs_d, inp.down_bias[e])
+            np.testing.assert_array_equal(r["hq"][t, j], m["hq"])
+            want[t] += wts[t, j] * m["y"]
+    np.testing.assert_allclose(r["out"], want, rtol=1e-12, atol=1e-12)
