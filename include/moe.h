@@ -127,6 +127,24 @@ size_t moe_packed_size(moe_dims d);
 moe_status moe_pack_weights(moe_dims d, const moe_mxfp4_weights *src, void *packed,
                             size_t packed_bytes, void *stream);
 
+/*
+ * NVFP4 variant of the weights: the checkpoint-layout MXFP4 tensors converted to
+ * NVFP4 while packing, by the method of "GPT-OSS-120B on DGX Spark: From MXFP4 to
+ * NVFP4", "Conversion Methodology": dequantise each MXFP4 block (E2M1 value times
+ * 2^(scale - 127)), then per 16-element block take the amax, choose the E4M3
+ * block scale E4M3(amax / (6 gs)) and quantise the elements to E2M1 (round to
+ * nearest even, saturating at 6), with a global scale gs = amax / (6 * 448) per
+ * projection over all experts (this library's reading: the page returns "a global
+ * scale factor" without its rule).  Same layout otherwise (gate/up interleave,
+ * tile-contiguous data, fp32 biases); two scale atoms per k-tile; the global
+ * scales' source amax is kept in the header.  H and I must be multiples of 64
+ * (else MOE_ERR_UNSUPPORTED_SHAPE).  Sizes, ownership, ordering and errors as
+ * moe_pack_weights.
+ */
+size_t moe_packed_size_nvfp4(moe_dims d);
+moe_status moe_pack_weights_nvfp4(moe_dims d, const moe_mxfp4_weights *src, void *packed,
+                                  size_t packed_bytes, void *stream);
+
 /* Workspace bytes moe_forward needs for up to T tokens with top_k (0 for
  * unsupported dims or arguments).  The workspace has no counterpart on the
  * pages: it holds this library's intermediates (logits, grouping, quantised
@@ -174,12 +192,26 @@ moe_status moe_forward(moe_dims d, const void *hidden, int32_t T, const void *ro
  * "Performance Optimizations" (native FP4 x FP4 block-scale MMA as the next
  * step after FP8 x FP4); the activation rule is this library's reading of
  * "Numerical Accuracy" (full-scale block activation quantisation), the same as
- * for MXFP8.  Same arguments, weights, workspace and errors as moe_forward (an
- * unknown act_format is MOE_ERR_INVALID_ARG); in the MXFP4 format the workspace's
- * xq, xp and hq sections hold two codes per byte (rows of H/2 and I/2 bytes).
+ * for MXFP8.
+ *   MOE_ACT_NVFP4  the NVFP4 variant: `packed` must come from moe_pack_weights_nvfp4
+ *                  (the weights converted to NVFP4); x and h are quantised to
+ *                  NVFP4 (E2M1 in 16-element blocks with an E4M3 scale each,
+ *                  amax / 6 rounded to nearest even, unit global scale), and the
+ *                  MMA is tcgen05 kind::mxf4nvf4.  Passages: "GPT-OSS-120B on DGX
+ *                  Spark: From MXFP4 to NVFP4", "The MXFP4 -> NVFP4 Conversion";
+ *                  "GPT-OSS-120B with MXFP4 on DGX Spark (SM121/GB10)", "New
+ *                  Features" (NVFP4 format support, group size 16).  Routing takes
+ *                  the tensor-core path at every T.
+ * Same arguments, workspace and errors as moe_forward (an unknown act_format is
+ * MOE_ERR_INVALID_ARG); in the FP4 formats the workspace's xq, xp and hq sections
+ * hold two codes per byte (rows of H/2 and I/2 bytes).  A packed buffer whose
+ * header does not match the forward (other dims, or MXFP4 weights for the NVFP4
+ * format and the reverse) runs no expert unit and reports MOE_ERR_TIMEOUT-class
+ * status bit 0x20 through moe_get_device_status; the output is then not written.
  */
 #define MOE_ACT_MXFP8 0
 #define MOE_ACT_MXFP4 1
+#define MOE_ACT_NVFP4 2
 moe_status moe_forward_act(moe_dims d, int32_t act_format, const void *hidden, int32_t T,
                            const void *router_w, const void *router_b, const void *packed, int32_t top_k,
                            void *out, void *workspace, size_t workspace_bytes, void *stream);
@@ -206,7 +238,7 @@ moe_status moe_forward_act(moe_dims d, int32_t act_format, const void *hidden, i
  *    overlap on the GPU (concurrent streams or host threads) race on it:
  *    serialise them.
  */
-#define MOE_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+#define MOE_STATIC_SCRATCH_BYTES ((size_t)24 << 20)
 moe_status moe_forward_static_scratch(moe_dims d, const void *hidden, int32_t T, const void *router_w,
                                       const void *router_b, const void *packed, int32_t top_k, void *out,
                                       void *stream);

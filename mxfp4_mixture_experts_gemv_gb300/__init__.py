@@ -24,7 +24,8 @@ STATUS_NAMES = {
 }
 
 # Every symbol the C ABI exports (include/moe.h).
-EXPORTED = ["moe_packed_size", "moe_pack_weights", "moe_workspace_size", "moe_workspace_layout_get",
+EXPORTED = ["moe_packed_size", "moe_pack_weights", "moe_packed_size_nvfp4", "moe_pack_weights_nvfp4",
+            "moe_workspace_size", "moe_workspace_layout_get",
             "moe_forward", "moe_forward_act", "moe_forward_static_scratch", "moe_static_scratch_status", "moe_static_scratch_bytes",
             "moe_get_device_status", "moe_set_wait_limit_ns", "moe_get_wait_limit_ns",
             "moe_debug_hold_waits", "moe_set_plan", "moe_profile_begin", "moe_profile_end", "moe_residual_rmsnorm",
@@ -70,6 +71,10 @@ def lib() -> ctypes.CDLL:
         L.moe_packed_size.argtypes = [Dims]
         L.moe_pack_weights.restype = st
         L.moe_pack_weights.argtypes = [Dims, ctypes.POINTER(Weights), vp, sz, vp]
+        L.moe_packed_size_nvfp4.restype = sz
+        L.moe_packed_size_nvfp4.argtypes = [Dims]
+        L.moe_pack_weights_nvfp4.restype = st
+        L.moe_pack_weights_nvfp4.argtypes = [Dims, ctypes.POINTER(Weights), vp, sz, vp]
         L.moe_workspace_size.restype = sz
         L.moe_workspace_size.argtypes = [Dims, i32, i32]
         L.moe_workspace_layout_get.restype = st
@@ -161,11 +166,16 @@ def _alloc_aligned(nbytes: int, device) -> torch.Tensor:
 
 
 def pack_weights(dims: LayerDims, gate_up_blocks, gate_up_scales, gate_up_bias, down_blocks,
-                 down_scales, down_bias, packed: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """Repack checkpoint-layout MXFP4 expert weights (CUDA tensors) into the forward layout."""
-    n = packed_size(dims)
+                 down_scales, down_bias, packed: torch.Tensor | None = None, stream=None,
+                 nvfp4: bool = False) -> torch.Tensor:
+    """Repack checkpoint-layout MXFP4 expert weights (CUDA tensors) into the forward layout
+    (converted to NVFP4 with nvfp4=True, for the NVFP4 forward)."""
+    L = lib()
+    size_fn, pack_fn = (L.moe_packed_size_nvfp4, L.moe_pack_weights_nvfp4) if nvfp4 else (L.moe_packed_size,
+                                                                                        L.moe_pack_weights)
+    n = size_fn(dims.c())
     if n == 0:
-        _check(lib().moe_pack_weights(dims.c(), None, None, 0, None))
+        _check(pack_fn(dims.c(), None, None, 0, None))
     if packed is None:
         packed = _alloc_aligned(n, gate_up_blocks.device)
     w = Weights(_dev_ptr(gate_up_blocks, "gate_up_blocks", torch.uint8),
@@ -174,8 +184,8 @@ def pack_weights(dims: LayerDims, gate_up_blocks, gate_up_scales, gate_up_bias, 
                 _dev_ptr(down_blocks, "down_blocks", torch.uint8),
                 _dev_ptr(down_scales, "down_scales", torch.uint8),
                 _dev_ptr(down_bias, "down_bias", torch.bfloat16))
-    _check(lib().moe_pack_weights(dims.c(), ctypes.byref(w), _dev_ptr(packed, "packed"),
-                                  packed.numel() * packed.element_size(), _stream(stream)))
+    _check(pack_fn(dims.c(), ctypes.byref(w), _dev_ptr(packed, "packed"), packed.numel() * packed.element_size(),
+                   _stream(stream)))
     return packed
 
 
@@ -183,7 +193,7 @@ def alloc_workspace(dims: LayerDims, T: int, top_k: int, device="cuda") -> torch
     return _alloc_aligned(max(workspace_size(dims, T, top_k), 256), device)
 
 
-ACT_FORMATS = {"mxfp8": 0, "mxfp4": 1}
+ACT_FORMATS = {"mxfp8": 0, "mxfp4": 1, "nvfp4": 2}
 
 
 def forward(dims: LayerDims, hidden: torch.Tensor, router_w: torch.Tensor, router_b: torch.Tensor,

@@ -147,6 +147,35 @@ moe_status moe_pack_weights(moe_dims d, const moe_mxfp4_weights* src, void* pack
   return MOE_OK;
 }
 
+size_t moe_packed_size_nvfp4(moe_dims d) {
+  moe::PackedHeader h;
+  if (check_dims(d) != MOE_OK || !moe::packed_layout(d, &h, moe::kWeightsNvfp4)) return 0;
+  return (size_t)h.total;
+}
+
+moe_status moe_pack_weights_nvfp4(moe_dims d, const moe_mxfp4_weights* src, void* packed, size_t packed_bytes,
+                                  void* stream) {
+  moe_status st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if (d.H % 64 || d.I % 64)
+    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "NVFP4 packing needs H and I multiples of 64 (H=%d I=%d)", d.H, d.I);
+  if (!src || !packed) return fail(MOE_ERR_INVALID_ARG, "null src or packed pointer");
+  if (!src->gate_up_blocks || !src->gate_up_scales || !src->gate_up_bias || !src->down_blocks ||
+      !src->down_scales || !src->down_bias)
+    return fail(MOE_ERR_INVALID_ARG, "null weight tensor pointer");
+  if (!aligned(packed, 256)) return fail(MOE_ERR_ALIGNMENT, "packed buffer must be 256-byte aligned");
+  if (!aligned(src->gate_up_blocks, 16) || !aligned(src->down_blocks, 16))
+    return fail(MOE_ERR_ALIGNMENT, "*_blocks tensors must be 16-byte aligned");
+  moe::PackedHeader h;
+  moe::packed_layout(d, &h, moe::kWeightsNvfp4);
+  if (packed_bytes < h.total)
+    return fail(MOE_ERR_BAD_PACKED_HEADER, "packed buffer has %zu bytes, %llu needed", packed_bytes,
+                (unsigned long long)h.total);
+  cudaError_t e = moe::launch_pack_nvfp4(h, *src, static_cast<uint8_t*>(packed), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "NVFP4 pack kernels");
+  return MOE_OK;
+}
+
 size_t moe_workspace_size(moe_dims d, int32_t T, int32_t top_k) {
   moe_workspace_layout l;
   if (check_dims(d) != MOE_OK || T < 0 || top_k <= 0 || !moe::workspace_layout(d, T, top_k, &l)) return 0;
@@ -166,8 +195,8 @@ moe_status moe_workspace_layout_get(moe_dims d, int32_t T, int32_t top_k, moe_wo
 
 namespace {
 
-// The forward for either activation format (MXFP8, or MXFP4 with fp4).
-moe_status forward_impl(moe_dims d, bool fp4, const void* hidden, int32_t T, const void* router_w,
+// The forward for every activation format (moe::ActFormat).
+moe_status forward_impl(moe_dims d, int fmt, const void* hidden, int32_t T, const void* router_w,
                         const void* router_b, const void* packed, int32_t top_k, void* out, void* workspace,
                         size_t workspace_bytes, void* stream) {
   moe_status st = moe::check_forward_args(d, hidden, T, router_w, router_b, packed, top_k, out);
@@ -178,8 +207,9 @@ moe_status forward_impl(moe_dims d, bool fp4, const void* hidden, int32_t T, con
   moe::workspace_layout(d, T, top_k, &L);
   if (workspace_bytes < L.total)
     return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "workspace has %zu bytes, %zu needed", workspace_bytes, L.total);
+  const bool fp4 = fmt == moe::kActMxfp4;  // the routing kernels' MXFP4 quantisation
   moe::PackedHeader h;
-  moe::packed_layout(d, &h);
+  moe::packed_layout(d, &h, fmt == moe::kActNvfp4 ? moe::kWeightsNvfp4 : moe::kWeightsMxfp4);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -198,9 +228,13 @@ moe_status forward_impl(moe_dims d, bool fp4, const void* hidden, int32_t T, con
   // grid, else the tensor-core router with separate grouping and gather passes
   const int forced = moe::plan_route();
   const bool cluster_fits = moe::route_cluster_fits(T, d.E, d.H), grid_fits = moe::route_small_fits(T, d.H);
-  const int route = forced != moe::kRouteAuto
+  // NVFP4 activations are quantised by the gather pass of the tensor-core path only
+  const int route = fmt == moe::kActNvfp4 && forced == moe::kRouteAuto ? moe::kRouteTensorCore
+                    : forced != moe::kRouteAuto
                         ? forced
                         : (cluster_fits ? moe::kRouteCluster : (grid_fits ? moe::kRouteGrid : moe::kRouteTensorCore));
+  if (fmt == moe::kActNvfp4 && route != moe::kRouteTensorCore)
+    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "NVFP4 activations take the tensor-core routing path only");
   if ((route == moe::kRouteCluster && !cluster_fits) || (route == moe::kRouteGrid && !grid_fits))
     return fail(MOE_ERR_UNSUPPORTED_SHAPE, "the forced routing path %d does not fit T=%d", route, T);
   // The cluster routing kernel clears the status words and counters itself; the
@@ -272,7 +306,7 @@ moe_status forward_impl(moe_dims d, bool fp4, const void* hidden, int32_t T, con
                             reinterpret_cast<int32_t*>(at(L.y)), s);
     if (e != cudaSuccess) return cuda_fail(e, "grouping kernel");
     e = moe::launch_gather_quant(static_cast<const uint16_t*>(hidden), inv_pos, tiles, L.max_tiles, T, top_k, d.H,
-                                 fp4, at(L.xq), at(L.xs), at(L.xp), at(L.xp_sf), s);
+                                 fmt, at(L.xq), at(L.xs), at(L.xp), at(L.xp_sf), s);
     if (e != cudaSuccess) return cuda_fail(e, "gather kernel");
   }
   mark(1);
@@ -299,13 +333,13 @@ moe_status forward_impl(moe_dims d, bool fp4, const void* hidden, int32_t T, con
   // tokens-on-M kernel slower at 2048 and 4096 tokens and even at 8192); the
   // tokens-on-M kernel runs when the plan asks for it
   const int forced_expert = moe::plan_expert();
-  const bool tokens_m = !fp4 && L.tile_rows == 128 && forced_expert == moe::kExpertTokensM;
+  const bool tokens_m = fmt == moe::kActMxfp8 && L.tile_rows == 128 && forced_expert == moe::kExpertTokensM;
   if (forced_expert == moe::kExpertTokensM && !tokens_m)
     return fail(MOE_ERR_UNSUPPORTED_SHAPE, "the tokens-on-M expert kernel needs 128-row tiles and MXFP8 activations");
   if (tokens_m)
     e = moe::launch_expert_swap(h, pk, b, T, top_k, L.max_tiles, sms, s);
   else
-    e = moe::launch_expert_mlp(h, pk, b, T, top_k, L.max_tiles, L.tile_rows, sms, fp4, s);
+    e = moe::launch_expert_mlp(h, pk, b, T, top_k, L.max_tiles, L.tile_rows, sms, fmt, s);
   if (e != cudaSuccess) return cuda_fail(e, "expert MLP kernel");
   if (!b.fused_combine) {
     e = moe::launch_combine(b.y, inv_pos, w, T, top_k, d.H, static_cast<uint16_t*>(out), s);
@@ -322,17 +356,17 @@ extern "C" {
 moe_status moe_forward(moe_dims d, const void* hidden, int32_t T, const void* router_w, const void* router_b,
                        const void* packed, int32_t top_k, void* out, void* workspace, size_t workspace_bytes,
                        void* stream) {
-  return forward_impl(d, false, hidden, T, router_w, router_b, packed, top_k, out, workspace, workspace_bytes,
-                      stream);
+  return forward_impl(d, moe::kActMxfp8, hidden, T, router_w, router_b, packed, top_k, out, workspace,
+                      workspace_bytes, stream);
 }
 
 moe_status moe_forward_act(moe_dims d, int32_t act_format, const void* hidden, int32_t T, const void* router_w,
                            const void* router_b, const void* packed, int32_t top_k, void* out, void* workspace,
                            size_t workspace_bytes, void* stream) {
-  if (act_format != MOE_ACT_MXFP8 && act_format != MOE_ACT_MXFP4)
+  if (act_format != MOE_ACT_MXFP8 && act_format != MOE_ACT_MXFP4 && act_format != MOE_ACT_NVFP4)
     return fail(MOE_ERR_INVALID_ARG, "unknown activation format %d", act_format);
-  return forward_impl(d, act_format == MOE_ACT_MXFP4, hidden, T, router_w, router_b, packed, top_k, out, workspace,
-                      workspace_bytes, stream);
+  const int fmt = act_format == MOE_ACT_MXFP4 ? moe::kActMxfp4 : act_format == MOE_ACT_NVFP4 ? moe::kActNvfp4 : moe::kActMxfp8;
+  return forward_impl(d, fmt, hidden, T, router_w, router_b, packed, top_k, out, workspace, workspace_bytes, stream);
 }
 
 moe_status moe_residual_rmsnorm(float* x_res, const void* layer_out, int32_t T, int32_t H, float eps, void* hidden,

@@ -34,16 +34,29 @@ constexpr int kTileK = 128;   // contraction elements per pipeline stage
 constexpr int kAtomBytes = 512;
 constexpr int kTileRowBytes = kTileK / 2;  // packed bytes of one tile row
 
+// Weight formats of a packed buffer: MXFP4 (E2M1, one E8M0 scale per 32
+// elements) or NVFP4 (E2M1, one E4M3 scale per 16 elements and a global fp32
+// scale per projection).  An NVFP4 buffer holds two scale atoms per k-tile: atom
+// j covers the 16-element blocks 4j..4j+3 of the tile's 128 elements, byte
+// (r%32)*16 + (r/32)*4 + (block%4) for tile row r.
+enum : int32_t { kWeightsMxfp4 = 0, kWeightsNvfp4 = 1 };
+
 struct PackedHeader {
   uint32_t magic, version;
   int32_t E, H, I, Hp, Ip, gu_mtiles, d_mtiles, gu_ktiles, d_ktiles;
-  int32_t gu_rows_stored, d_rows_stored, pad0;
+  int32_t gu_rows_stored, d_rows_stored, wfmt;
   uint64_t off_gu_data, off_gu_sf, off_gu_bias, off_d_data, off_d_sf, off_d_bias, total;
 };
 
+// NVFP4 buffers: the largest magnitude of each projection's weights (fp32 bits,
+// gate_up then down) sits at this offset of the 1 KB header area; the global
+// scale of a projection is amax / (6 * 448) (nvfp4_global_scale).
+constexpr uint32_t kAmaxOffset = 512;
+__host__ __device__ inline float nvfp4_global_scale(float amax) { return amax > 0.f ? amax / 2688.0f : 1.0f; }
+
 inline int64_t round_up(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
 
-inline bool packed_layout(const moe_dims& d, PackedHeader* hd) {
+inline bool packed_layout(const moe_dims& d, PackedHeader* hd, int32_t wfmt = kWeightsMxfp4) {
   if (d.E <= 0 || d.H <= 0 || d.I <= 0) return false;
   if (d.E > 256 || d.H % 32 || d.I % 64) return false;
   PackedHeader h = {};
@@ -58,13 +71,15 @@ inline bool packed_layout(const moe_dims& d, PackedHeader* hd) {
   h.d_ktiles = h.Ip / kTileK;
   h.gu_rows_stored = 2 * d.I;
   h.d_rows_stored = (int32_t)round_up(d.H, 64);
+  h.wfmt = wfmt;
+  const int atoms = wfmt == kWeightsNvfp4 ? 2 : 1;  // scale atoms per k-tile
   uint64_t off = 1024;
   auto take = [&](uint64_t bytes) { uint64_t o = off; off = (uint64_t)round_up(off + bytes, 1024); return o; };
   h.off_gu_data = take((uint64_t)d.E * h.gu_rows_stored * h.gu_ktiles * kTileRowBytes);
-  h.off_gu_sf = take((uint64_t)d.E * h.gu_mtiles * h.gu_ktiles * kAtomBytes);
+  h.off_gu_sf = take((uint64_t)d.E * h.gu_mtiles * h.gu_ktiles * atoms * kAtomBytes);
   h.off_gu_bias = take((uint64_t)d.E * 2 * d.I * 4);
   h.off_d_data = take((uint64_t)d.E * h.d_rows_stored * h.d_ktiles * kTileRowBytes);
-  h.off_d_sf = take((uint64_t)d.E * h.d_mtiles * h.d_ktiles * kAtomBytes);
+  h.off_d_sf = take((uint64_t)d.E * h.d_mtiles * h.d_ktiles * atoms * kAtomBytes);
   h.off_d_bias = take((uint64_t)d.E * d.H * 4);
   h.total = off;
   *hd = h;
@@ -135,17 +150,20 @@ inline bool workspace_layout(const moe_dims& d, int T, int k, moe_workspace_layo
   l.logits = take((size_t)T * d.E * 4);
   l.topk_ids = take((size_t)TK * 4);
   l.topk_w = take((size_t)TK * 4);
+  // sized for every activation format: one code byte per element, one scale per
+  // 16 elements (NVFP4; the 32-element formats use half), two scale atoms per
+  // k-tile (NVFP4; the others use the first of each pair's space)
   l.xq = take((size_t)T * d.H);
-  l.xs = take((size_t)T * (d.H / 32));
+  l.xs = take((size_t)T * (d.H / 16));
   l.counts = take((size_t)d.E * 4);
   l.offsets = take((size_t)(d.E + 1) * 4);
   l.sorted_rows = take((size_t)TK * 4);
   l.inv_pos = take((size_t)TK * 4);
   l.tiles = take((size_t)(4 + 4 * max_tiles) * 4);
   l.xp = take((size_t)TK * d.H + 256);
-  l.xp_sf = take((size_t)max_tiles * kth * kAtomBytes);
+  l.xp_sf = take((size_t)max_tiles * kth * 2 * kAtomBytes);
   l.hq = take((size_t)TK * d.I + 256);
-  l.hq_sf = take((size_t)max_tiles * kti * kAtomBytes);
+  l.hq_sf = take((size_t)max_tiles * kti * 2 * kAtomBytes);
   l.y = take((size_t)TK * d.H * 4);
   l.total = o;
   l.max_tiles = (int32_t)max_tiles;
@@ -161,6 +179,7 @@ enum : uint32_t {
   kStatusTimeoutEpilogue = 1u << 2,
   kStatusTimeoutDrain = 1u << 3,
   kStatusTimeoutRouting = 1u << 4,  // the small-batch routing grid's barrier
+  kStatusBadWeights = 1u << 5,      // the packed buffer's header does not match the forward
 };
 
 // Bounded waits give up after this many nanoseconds unless the host sets
@@ -188,6 +207,8 @@ moe_status report_error(moe_status st, const char* fmt, ...);
 // Kernel launchers (defined in the .cu files).
 cudaError_t launch_pack(const moe_dims& d, const PackedHeader& h, const moe_mxfp4_weights& w,
                         uint8_t* packed, cudaStream_t s);
+// The MXFP4 checkpoint converted to NVFP4 while packing (h.wfmt == kWeightsNvfp4).
+cudaError_t launch_pack_nvfp4(const PackedHeader& h, const moe_mxfp4_weights& w, uint8_t* packed, cudaStream_t s);
 cudaError_t launch_router_tc(const uint16_t* x, const uint16_t* wr, const uint16_t* br, int T, int H, int E, int k,
                              float* logits, int32_t* ids, float* w, uint32_t* status, cudaStream_t s);
 // Grouping in two passes over chunks of pairs; `scratch` holds one count per
@@ -195,10 +216,13 @@ cudaError_t launch_router_tc(const uint16_t* x, const uint16_t* wr, const uint16
 cudaError_t launch_permute(const int32_t* ids, int TK, int k, int E, int tile_rows, int max_tiles,
                            int32_t* counts, int32_t* offsets, int32_t* sorted_rows, int32_t* inv_pos,
                            int32_t* tiles, int32_t* scratch, cudaStream_t s);
-// Activations are quantised to MXFP8 (fp4 false: one E4M3 code byte per element)
-// or MXFP4 (fp4 true: two E2M1 codes per byte), one E8M0 scale per 32 elements.
+// Activation formats: MXFP8 (one E4M3 code byte per element, one E8M0 scale per
+// 32), MXFP4 (two E2M1 codes per byte, one E8M0 scale per 32) and NVFP4 (two
+// E2M1 codes per byte, one E4M3 scale per 16, unit global scale; scale atoms in
+// pairs per k-tile as in an NVFP4 weight buffer).
+enum ActFormat : int { kActMxfp8 = 0, kActMxfp4 = 1, kActNvfp4 = 2 };
 cudaError_t launch_gather_quant(const uint16_t* x, const int32_t* inv_pos, const int32_t* tiles, int max_tiles, int T,
-                                int k, int H, bool fp4, uint8_t* xq, uint8_t* xs, uint8_t* xp, uint8_t* xp_sf,
+                                int k, int H, int fmt, uint8_t* xq, uint8_t* xs, uint8_t* xp, uint8_t* xp_sf,
                                 cudaStream_t s);
 
 cudaError_t launch_residual_rmsnorm(float* x_res, const uint16_t* layer_out, int T, int H, float eps,
@@ -264,10 +288,10 @@ struct ExpertMlpBuffers {
 // out[t] = bf16(sum_j w[t][j] * y[inv_pos[t][j]]), slots in order, fp32 sums.
 cudaError_t launch_combine(const float* y, const int32_t* inv_pos, const float* topk_w, int T, int k, int H,
                            uint16_t* out, cudaStream_t s);
-// fp4: activations (xp, hq) in MXFP4 and the tcgen05 kind::mxf4 MMA; else MXFP8
-// and kind::mxf8f6f4.
+// fmt: activations (xp, hq) in MXFP8 (tcgen05 kind::mxf8f6f4), MXFP4
+// (kind::mxf4) or NVFP4 with NVFP4 weights (kind::mxf4nvf4).
 cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, const ExpertMlpBuffers& b, int T, int k,
-                              int max_tiles, int tile_rows, int num_sms, bool fp4, cudaStream_t s);
+                              int max_tiles, int tile_rows, int num_sms, int fmt, cudaStream_t s);
 // The same layer for 128-row token tiles with the tokens in the MMA M slot and two
 // weight tiles in N (MXFP8 activations); y is combined by launch_combine.
 cudaError_t launch_expert_swap(const PackedHeader& h, const uint8_t* packed, const ExpertMlpBuffers& b, int T, int k,

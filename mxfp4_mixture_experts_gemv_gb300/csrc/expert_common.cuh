@@ -70,6 +70,12 @@ __device__ __forceinline__ int act_box_index(int rows) {
 struct Maps {
   CUtensorMap gu2, gu, gut, d2, d, dt;
   CUtensorMap xp[kActBoxes], hq[kActBoxes];
+  // Fewer, larger copies stream faster: four k-tiles of a 128-row weight tile (512
+  // consecutive rows) as one box of two 256-row planes, and the activation rows of
+  // every k-tile of a pipeline stage as one box of k-tile planes (grouped x only:
+  // all its rows are written before the expert kernel starts).
+  CUtensorMap gu4, d4;
+  CUtensorMap xp3[kActBoxes];
 };
 
 // Tensor maps (host).  Weights: the tile-contiguous packed layout as 2-D rows of
@@ -81,5 +87,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
 bool make_weight_map(CUtensorMap* map, const uint8_t* base, int64_t total_rows, int box_rows);
 bool make_weight_map_packed(CUtensorMap* map, const uint8_t* base, int64_t total_rows, int box_rows);
 bool make_act_map(CUtensorMap* map, const uint8_t* base, int row_bytes, int rows, int box_rows, bool fp4);
+// Weights as planes of 256 rows (two planes per box): dims {128 codes, rows, 2}.
+bool make_weight_map_x2(CUtensorMap* map, const uint8_t* base, int64_t total_rows, bool packed);
+// Activations as k-tile planes: dims {128 elements, rows, ceil(K/128)} with the
+// k-tile plane stride one k-tile of a row; a box covers `planes` consecutive k-tiles
+// of box_rows rows.  The last k-tile of a row runs past the row end into the next
+// row (or into the buffer's zeroed slack after the last row), where the weights it
+// multiplies are zero padding.
+bool make_act_map_planes(CUtensorMap* map, const uint8_t* base, int row_bytes, int rows, int K, int box_rows,
+                         int planes, bool fp4);
 
 }  // namespace moe

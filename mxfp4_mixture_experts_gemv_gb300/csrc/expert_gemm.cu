@@ -70,15 +70,18 @@ constexpr uint32_t smem_row_bytes() { return FP4 ? 64u : 128u; }
 // MMA and epilogue warps through a small queue in shared memory.
 constexpr int kTileQ = 4;
 
-template <int BN, bool FP4>
+template <int BN, bool FP4, bool NV>
 struct GemmCfg {
+  static_assert(FP4 || !NV, "NVFP4 operands are FP4");
   static constexpr int kKS = stage_ktiles<BN>();
+  static constexpr int kSfAtoms = NV ? 2 : 1;  // scale atoms per k-tile and operand (16- or 32-element blocks)
   static constexpr uint32_t kRow = smem_row_bytes<FP4>();
   static constexpr uint32_t kA1 = kTileM * kRow;        // smem per weight k-tile (16 KB unpacked, 8 KB packed)
   static constexpr uint32_t kB1 = BN * kRow;            // BN activation rows per k-tile
   static constexpr uint32_t kA = kKS * kA1;
   static constexpr uint32_t kB = kKS * kB1;
-  static constexpr uint32_t kSF = 2 * kKS * kAtomBytes;  // scale atoms of A (first half) and B
+  static constexpr uint32_t kSF = 2 * kKS * kSfAtoms * kAtomBytes;  // scale atoms of A (first half) and B
+  static constexpr uint32_t kSfCols = 8 * kKS * kSfAtoms;            // tmem columns of one stage's scales
   static constexpr uint32_t kStage = kA + kB + kSF;
   // gate_up epilogue: accumulator chunks of kCW token columns are transposed
   // through shared memory (a token tile of at most 16 rows needs one 16-wide chunk)
@@ -87,10 +90,12 @@ struct GemmCfg {
   static_assert(kXbuf >= BN * 16 * 4, "combine staging lives in the transpose buffer");
   static constexpr uint32_t kBars = 1024;
   static constexpr uint32_t kBudget = 227 * 1024 - 1024 - kXbuf - kBars;
-  static constexpr int kStages = (kBudget / kStage) > 8 ? 8 : (int)(kBudget / kStage);
+  static constexpr int kStagesSmem = (kBudget / kStage) > 8 ? 8 : (int)(kBudget / kStage);
+  static constexpr int kStagesTmem = (int)(256 / kSfCols);
+  static constexpr int kStages = kStagesSmem < kStagesTmem ? kStagesSmem : kStagesTmem;
   static constexpr uint32_t kSmem = 1024 + kStages * kStage + kBars + kXbuf;
   static_assert(kStages >= 2, "pipeline too shallow");
-  static_assert(256 + 8 * kKS * kStages <= 512, "tmem columns");
+  static_assert(256 + kSfCols * kStages <= 512, "tmem columns");
   // barriers (stages, accumulators, drain, tile queue), tmem slot, tile queue, combine list
   static_assert((2 * kStages + 5 + 2 * kTileQ) * 8 + 16 + 16 * (kTileQ + 1) + 4 * (BN + 1) + 16 <= kBars, "barrier area");
 };
@@ -120,6 +125,8 @@ struct MlpParams {
   int I, H, k;
   int weights_evict_first;  // weights are read once per forward: let them leave L2 first
   int fused_combine;  // the down epilogue also combines the k slots of completed tokens
+  const PackedHeader* hdr;   // the packed buffer's header, checked against what this launch expects
+  PackedHeader want;         // (magic, version, dims and weight format)
 };
 
 struct TileRef {
@@ -141,10 +148,11 @@ __device__ __forceinline__ TileRef tile_ref(int tile, int n_gu, const MlpParams&
   return r;
 }
 
-template <int BN, bool FP4>
+template <int BN, bool FP4, bool NV>
 __global__ void __launch_bounds__(192, 1)
     expert_mlp_kernel(const __grid_constant__ Maps maps, const MlpParams p) {
-  using C = GemmCfg<BN, FP4>;
+  using C = GemmCfg<BN, FP4, NV>;
+  constexpr int SA = C::kSfAtoms;
   constexpr int kKS = C::kKS;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -206,7 +214,12 @@ __global__ void __launch_bounds__(192, 1)
   // Everything above overlaps the previous kernel (programmatic dependent
   // launch); the tile list and activations it produced are read only after this.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int n_btiles = p.tiles[0];
+  // a packed buffer of other dims or another weight format runs no unit
+  const PackedHeader& hd = *p.hdr;
+  const bool hdr_ok = hd.magic == p.want.magic && hd.version == p.want.version && hd.E == p.want.E &&
+                      hd.H == p.want.H && hd.I == p.want.I && hd.wfmt == p.want.wfmt;
+  if (!hdr_ok && threadIdx.x == 0) atomicOr(p.status, kStatusBadWeights);
+  const int n_btiles = hdr_ok ? p.tiles[0] : 0;
   const int n_gu = n_btiles * p.gu_mtiles;
   const int total = n_gu + n_btiles * p.d_mtiles;
   const int4* tl = reinterpret_cast<const int4*>(p.tiles + 4);
@@ -250,8 +263,8 @@ __global__ void __launch_bounds__(192, 1)
       int next = total;
       const int m_tiles = r.gu ? p.gu_mtiles : p.d_mtiles;
       const int rows_stored = r.gu ? p.gu_rows_stored : p.d_rows_stored;
-      const uint8_t* sfa = (r.gu ? p.gu_sfa : p.d_sfa) + ((int64_t)td.x * m_tiles + r.m) * k_tiles * kAtomBytes;
-      const uint8_t* sfb = (r.gu ? p.xp_sf : p.hq_sf) + (int64_t)r.b * k_tiles * kAtomBytes;
+      const uint8_t* sfa = (r.gu ? p.gu_sfa : p.d_sfa) + ((int64_t)td.x * m_tiles + r.m) * k_tiles * SA * kAtomBytes;
+      const uint8_t* sfb = (r.gu ? p.xp_sf : p.hq_sf) + (int64_t)r.b * k_tiles * SA * kAtomBytes;
       const int rows_m = min(kTileM, rows_stored - r.m * kTileM);  // 64 for a tail m-tile
       const int bi = min(act_box_index(td.z), kActBoxes - 1);
       const CUtensorMap* bmap = r.gu ? &maps.xp[bi] : &maps.hq[bi];
@@ -263,6 +276,10 @@ __global__ void __launch_bounds__(192, 1)
       auto issue_a = [&](int ss, int kt, int nk) {
         const int a_rows = rows_m * nk;
         const int row0 = row0_unit + kt * rows_m;
+        if (a_rows == 512) {  // two 256-row planes in one box
+          tma_load_3d_hint(sA + ss * C::kA, r.gu ? &maps.gu4 : &maps.d4, &full[ss], 0, row0, 0, wpol);
+          return;
+        }
         for (int off = 0; off < a_rows;) {
           const int c = a_rows - off >= 256 ? 256 : a_rows - off >= 128 ? 128 : 64;
           const CUtensorMap* amap = r.gu ? (c == 256 ? &maps.gu2 : (c == 128 ? &maps.gu : &maps.gut))
@@ -271,13 +288,20 @@ __global__ void __launch_bounds__(192, 1)
           off += c;
         }
       };
-      // activation (B) copies of stage slot `ss` covering k-tiles kt..kt+nk-1
+      // activation (B) copies of stage slot `ss` covering k-tiles kt..kt+nk-1: k-tile
+      // j at j * box rows; grouped x as one box of kKS k-tile planes (a short last
+      // stage reads planes past K, which TMA fills with zeros), hq one box per k-tile
+      const uint32_t b_plane = (uint32_t)act_box_rows(bi) * C::kRow;
       auto issue_b = [&](int ss, int kt, int nk) {
-        for (int j = 0; j < nk; ++j)
-          tma_load_2d(sB + ss * C::kB + j * C::kB1, bmap, &full[ss], (kt + j) * (int)C::kRow, td.y);
+        if (r.gu) {
+          tma_load_3d(sB + ss * C::kB, &maps.xp3[bi], &full[ss], 0, td.y, kt);
+        } else {
+          for (int j = 0; j < nk; ++j)
+            tma_load_2d(sB + ss * C::kB + j * b_plane, bmap, &full[ss], (kt + j) * (int)C::kRow, td.y);
+        }
       };
       auto stage_bytes = [&](int nk) {
-        return (uint32_t)(rows_m * nk * kTileRowBytes + nk * (b_bytes + 2 * kAtomBytes));
+        return (uint32_t)(rows_m * nk * kTileRowBytes + (r.gu ? kKS : nk) * b_bytes + nk * 2 * SA * kAtomBytes);
       };
       // A down unit's hq is ready once all gate_up m-tiles of its token tile are
       // counted.  If it is not ready yet, the unit's first stages get their weight
@@ -297,7 +321,8 @@ __global__ void __launch_bounds__(192, 1)
           for (int j = 0; j < pend_n; ++j) {
             const int kk = pend_kt + j * kKS, nn = min(kKS, k_tiles - kk), ss = (pend_s + j) % S;
             issue_b(ss, kk, nn);
-            bulk_g2s(sSF + ss * C::kSF + kKS * kAtomBytes, sfb + kk * kAtomBytes, nn * kAtomBytes, &full[ss]);
+            bulk_g2s(sSF + ss * C::kSF + kKS * SA * kAtomBytes, sfb + kk * SA * kAtomBytes, nn * SA * kAtomBytes,
+                     &full[ss]);
           }
         __syncwarp();
         pend_n = 0;
@@ -325,15 +350,15 @@ __global__ void __launch_bounds__(192, 1)
             issue_a(s, kt, nk);
             issue_b(s, kt, nk);
             uint8_t* sf = sSF + s * C::kSF;
-            bulk_g2s_hint(sf, sfa + kt * kAtomBytes, nk * kAtomBytes, &full[s], wpol);
-            bulk_g2s(sf + kKS * kAtomBytes, sfb + kt * kAtomBytes, nk * kAtomBytes, &full[s]);
+            bulk_g2s_hint(sf, sfa + kt * SA * kAtomBytes, nk * SA * kAtomBytes, &full[s], wpol);
+            bulk_g2s(sf + kKS * SA * kAtomBytes, sfb + kt * SA * kAtomBytes, nk * SA * kAtomBytes, &full[s]);
           }
           __syncwarp();
         } else {
           if (elect_one()) {
             mbar_arrive_expect_tx(&full[s], stage_bytes(nk));
             issue_a(s, kt, nk);
-            bulk_g2s_hint(sSF + s * C::kSF, sfa + kt * kAtomBytes, nk * kAtomBytes, &full[s], wpol);
+            bulk_g2s_hint(sSF + s * C::kSF, sfa + kt * SA * kAtomBytes, nk * SA * kAtomBytes, &full[s], wpol);
           }
           __syncwarp();
           if (pend_n == 0) {
@@ -397,6 +422,8 @@ __global__ void __launch_bounds__(192, 1)
       const int4 td = make_int4(q.y, q.z, q.w, 0);
       const int k_tiles = r.gu ? p.gu_ktiles : p.d_ktiles;
       const int rows_m = min(kTileM, (r.gu ? p.gu_rows_stored : p.d_rows_stored) - r.m * kTileM);
+      // activation k-tile j sits j box heights into the stage (the producer's layout)
+      const uint32_t b_plane = (uint32_t)act_box_rows(min(act_box_index(td.z), kActBoxes - 1)) * C::kRow;
       if (!mbar_wait_warp(&tempty[acc], aph ^ 1u, p.wait_ns)) {
         if (lane == 0) {
           atomicOr(p.status, kStatusTimeoutMma);
@@ -409,8 +436,9 @@ __global__ void __launch_bounds__(192, 1)
       // B rows past the unit's rows are never read back
       const uint32_t n_mma = (uint32_t)max(16, min(BN, (td.z + 15) & ~15));
       const uint32_t d_tmem = tmem + (uint32_t)acc * 128u;
-      const uint32_t idesc0 = FP4 ? idesc_mxf8f6f4(128, n_mma, 1 /*E2M1*/, 1 /*E2M1*/, 0, 0)
-                                  : idesc_mxf8f6f4(128, n_mma, 5 /*E2M1*/, 0 /*E4M3*/, 0, 0);
+      uint32_t idesc0 = FP4 ? idesc_mxf8f6f4(128, n_mma, 1 /*E2M1*/, 1 /*E2M1*/, 0, 0)
+                            : idesc_mxf8f6f4(128, n_mma, 5 /*E2M1*/, 0 /*E4M3*/, 0, 0);
+      if (NV) idesc0 &= ~(1u << 23);  // block scales in UE4M3, not UE8M0
       for (int kt = 0; kt < k_tiles; kt += kKS) {
         const int nk = min(kKS, k_tiles - kt);
         if (!mbar_wait_warp(&full[s], ph, p.wait_ns)) {
@@ -422,18 +450,29 @@ __global__ void __launch_bounds__(192, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t sf_t = tmem + 256u + (uint32_t)s * (8u * kKS);
+        const uint32_t sf_t = tmem + 256u + (uint32_t)s * C::kSfCols;
         const uint32_t sf_s = smem_u32(sSF + s * C::kSF);
         const uint32_t a_s = smem_u32(sA + s * C::kA);
         const uint32_t b_s = smem_u32(sB + s * C::kB);
         if (elect_one()) {
           for (int j = 0; j < nk; ++j) {
-            const uint32_t sfa_t = sf_t + 8u * j, sfb_t = sfa_t + 4u;
-            tmem_cp_32x128b_x4(sfa_t, sdesc_sf_atom(sf_s + j * kAtomBytes));
-            tmem_cp_32x128b_x4(sfb_t, sdesc_sf_atom(sf_s + (kKS + j) * kAtomBytes));
+            // this k-tile's scale atoms: A then B, SA each, four columns per atom
+            const uint32_t sfa_t = sf_t + 8u * SA * j, sfb_t = sfa_t + 4u * SA;
+#pragma unroll
+            for (int aa = 0; aa < SA; ++aa) {
+              tmem_cp_32x128b_x4(sfa_t + 4u * aa, sdesc_sf_atom(sf_s + (j * SA + aa) * kAtomBytes));
+              tmem_cp_32x128b_x4(sfb_t + 4u * aa, sdesc_sf_atom(sf_s + ((kKS + j) * SA + aa) * kAtomBytes));
+            }
             // weight k-tile j starts rows_m rows into the stage (a swizzle-atom multiple)
-            const uint32_t a_j = a_s + (uint32_t)(j * rows_m) * C::kRow, b_j = b_s + j * C::kB1;
-            if constexpr (FP4) {
+            const uint32_t a_j = a_s + (uint32_t)(j * rows_m) * C::kRow, b_j = b_s + (uint32_t)j * b_plane;
+            if constexpr (NV) {
+              // two MMAs of K = 64, each with the four 16-element block scales of one atom
+              const uint64_t ad = sdesc_sw64(a_j), bd = sdesc_sw64(b_j);
+#pragma unroll
+              for (uint32_t kk = 0; kk < 2; ++kk)
+                umma_mxf4nvf4(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc0, sfa_t + 4u * kk, sfb_t + 4u * kk,
+                              (kt + j + (int)kk) != 0);
+            } else if constexpr (FP4) {
               // two MMAs of K = 64 (32 bytes of each 64-byte row); each takes two of the
               // row's four block scales, starting at byte 2kk
               const uint64_t ad = sdesc_sw64(a_j), bd = sdesc_sw64(b_j);
@@ -478,6 +517,13 @@ __global__ void __launch_bounds__(192, 1)
     int acc = 0;
     uint32_t aph = 0;
     bool ok = true;
+    // NVFP4 weights carry a global scale per projection (the activations' is 1)
+    const float gs_gu = NV ? nvfp4_global_scale(__uint_as_float(reinterpret_cast<const uint32_t*>(
+                                 reinterpret_cast<const uint8_t*>(p.hdr) + kAmaxOffset)[0]))
+                           : 1.0f;
+    const float gs_d = NV ? nvfp4_global_scale(__uint_as_float(reinterpret_cast<const uint32_t*>(
+                                reinterpret_cast<const uint8_t*>(p.hdr) + kAmaxOffset)[1]))
+                          : 1.0f;
     auto bias_of = [&](const TileRef& rr, const int4& t4) -> float {
       if (rr.gu) return p.gu_bias[(int64_t)t4.x * 2 * p.I + rr.m * kTileM + row];
       const int o = rr.m * kTileM + row;
@@ -539,7 +585,9 @@ __global__ void __launch_bounds__(192, 1)
             for (int j = 0; j < 16; ++j) r0[j] = r1[j] = 0;
           }
 #pragma unroll
-          for (int j = 0; j < CW; ++j) xbuf[row * XS + j] = __uint_as_float(j < 16 ? r0[j] : r1[j - 16]) + bias_v;
+          for (int j = 0; j < CW; ++j)
+            xbuf[row * XS + j] = (NV ? __uint_as_float(j < 16 ? r0[j] : r1[j - 16]) * gs_gu
+                                     : __uint_as_float(j < 16 ? r0[j] : r1[j - 16])) + bias_v;
           named_barrier_sync(1, 128);
           const int n = c0 + jt;
           float h[16];
@@ -557,11 +605,17 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) h[i] = 0.f;
           }
-          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+          if (!NV) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));  // MX blocks span the lane pair
           const int sx = FP4 ? mx_scale_exp<2>(amax) : mx_scale_exp<8>(amax);
           const float inv = mx_pow2_neg(sx);
           uint32_t pk[4];
-          if constexpr (FP4) {
+          uint32_t nsc = 0;  // NVFP4: this half block is one 16-element block with its own E4M3 scale
+          if constexpr (NV) {
+            uint32_t p2[2];
+            nsc = nvfp4_block16(h, 1.0f, p2);
+            pk[0] = p2[0];
+            pk[1] = p2[1];
+          } else if constexpr (FP4) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) h[i] *= inv;
             pk[0] = cvt_e2m1x8(h);
@@ -580,7 +634,20 @@ __global__ void __launch_bounds__(192, 1)
               *reinterpret_cast<uint2*>(p.hq + (int64_t)(td.y + n) * (p.I / 2) + col / 2) = make_uint2(pk[0], pk[1]);
             else
               *reinterpret_cast<uint4*>(p.hq + (int64_t)(td.y + n) * p.I + col) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            if (hh == 0) {
+            if (NV) {
+              // 16-element block q = 2 kb + hh: k-tile q / 8, atom (q / 4) % 2, byte q % 4
+              const int qb = 2 * kb + hh;
+              uint8_t* wd = p.hq_sf + (((int64_t)r.b * p.d_ktiles + (qb >> 3)) * 2 + ((qb >> 2) & 1)) * kAtomBytes +
+                            (n & 31) * 16 + (n >> 5) * 4;
+              wd[qb & 3] = (uint8_t)nsc;
+              // the last real block also zeroes the scales of the padding blocks after it
+              // in its k-tile (zero data past I; their scale must not be a NaN code)
+              const int last = (p.I >> 4) - 1;
+              if (qb == last) {
+                for (int j = (qb & 3) + 1; j < 4; ++j) wd[j] = 0;
+                if (((qb >> 2) & 1) == 0) *reinterpret_cast<uint32_t*>(wd + kAtomBytes) = 0u;
+              }
+            } else if (hh == 0) {
               uint8_t* wd = p.hq_sf + ((int64_t)r.b * p.d_ktiles + (kb >> 2)) * kAtomBytes + (n & 31) * 16 + (n >> 5) * 4;
               wd[kb & 3] = (uint8_t)(sx + 127);
               // the last real block also sets the padding blocks of its word (zero
@@ -610,7 +677,9 @@ __global__ void __launch_bounds__(192, 1)
               for (int j = 0; j < 32; ++j) {
                 const int n = c0 + j;
                 if (n < rows)
-                  p.y[(int64_t)(td.y + n) * p.H + orow] = __uint_as_float(j < 16 ? r0[j] : r1[j - 16]) + bias_v;
+                  p.y[(int64_t)(td.y + n) * p.H + orow] =
+                      (NV ? __uint_as_float(j < 16 ? r0[j] : r1[j - 16]) * gs_d : __uint_as_float(j < 16 ? r0[j] : r1[j - 16])) +
+                      bias_v;
               }
             }
           }
@@ -682,13 +751,13 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-template <int BN, bool FP4>
+template <int BN, bool FP4, bool NV>
 cudaError_t launch_bn(const Maps& m, const MlpParams& p, int grid, cudaStream_t s) {
-  using C = GemmCfg<BN, FP4>;
+  using C = GemmCfg<BN, FP4, NV>;
   static bool attr = false;
   if (!attr) {
     cudaError_t e =
-        cudaFuncSetAttribute(expert_mlp_kernel<BN, FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+        cudaFuncSetAttribute(expert_mlp_kernel<BN, FP4, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
@@ -707,7 +776,7 @@ cudaError_t launch_bn(const Maps& m, const MlpParams& p, int grid, cudaStream_t 
   attrs[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, expert_mlp_kernel<BN, FP4>, m, p);
+  return cudaLaunchKernelEx(&cfg, expert_mlp_kernel<BN, FP4, NV>, m, p);
 }
 
 }  // namespace
@@ -768,27 +837,56 @@ bool make_act_map(CUtensorMap* map, const uint8_t* base, int row_bytes, int rows
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_weight_map_x2(CUtensorMap* map, const uint8_t* base, int64_t total_rows, bool packed) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {packed ? (cuuint64_t)kTileRowBytes : (cuuint64_t)kTileK, (cuuint64_t)total_rows, 2};
+  cuuint64_t strides[2] = {(cuuint64_t)kTileRowBytes, (cuuint64_t)256 * kTileRowBytes};
+  cuuint32_t box[3] = {packed ? (cuuint32_t)kTileRowBytes : (cuuint32_t)kTileK, 256, 2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(map, packed ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3,
+             const_cast<uint8_t*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             packed ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_act_map_planes(CUtensorMap* map, const uint8_t* base, int row_bytes, int rows, int K, int box_rows,
+                         int planes, bool fp4) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t kbytes = fp4 ? (cuuint64_t)kTileRowBytes : (cuuint64_t)kTileK;  // one k-tile of a row
+  cuuint64_t dims[3] = {kbytes, (cuuint64_t)rows, (cuuint64_t)((K + kTileK - 1) / kTileK)};
+  cuuint64_t strides[2] = {(cuuint64_t)row_bytes, kbytes};
+  cuuint32_t box[3] = {(cuuint32_t)kbytes, (cuuint32_t)box_rows, (cuuint32_t)planes};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, fp4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Encoded descriptors depend only on these values, so they are reused across calls.
 struct MapKey {
   const uint8_t* packed;
   const uint8_t* xp;
   const uint8_t* hq;
   int E, H, I, TK, tile_rows;
-  bool fp4;
+  int fmt;                       // activation format, which also fixes the weight layout
+  uint64_t off_gu_data, off_d_data;  // the packed sections the weight maps point into
   bool operator==(const MapKey& o) const {
     return packed == o.packed && xp == o.xp && hq == o.hq && E == o.E && H == o.H && I == o.I && TK == o.TK &&
-           tile_rows == o.tile_rows && fp4 == o.fp4;
+           tile_rows == o.tile_rows && fmt == o.fmt && off_gu_data == o.off_gu_data && off_d_data == o.off_d_data;
   }
 };
 
 cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, const ExpertMlpBuffers& b, int T, int k,
-                              int max_tiles, int tile_rows, int num_sms, bool fp4, cudaStream_t s) {
+                              int max_tiles, int tile_rows, int num_sms, int fmt, cudaStream_t s) {
   const int TK = T * k;
+  const bool fp4 = fmt != kActMxfp8;
   static std::mutex mu;
   static MapKey keys[32];
   static Maps cache[32];
   static int n_cached = 0, next_slot = 0;
-  const MapKey key{packed, b.xp, b.hq, h.E, h.H, h.I, TK, tile_rows, fp4};
+  const MapKey key{packed, b.xp, b.hq, h.E, h.H, h.I, TK, tile_rows, fmt, h.off_gu_data, h.off_d_data};
   Maps m;
   bool hit = false;
   {
@@ -804,6 +902,9 @@ cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, cons
   const int64_t gu_rows = (int64_t)h.E * h.gu_rows_stored * h.gu_ktiles;
   const int64_t d_rows = (int64_t)h.E * h.d_rows_stored * h.d_ktiles;
   auto wmap = fp4 ? make_weight_map_packed : make_weight_map;
+  if (!make_weight_map_x2(&m.gu4, packed + h.off_gu_data, (int64_t)h.E * h.gu_rows_stored * h.gu_ktiles, fp4) ||
+      !make_weight_map_x2(&m.d4, packed + h.off_d_data, (int64_t)h.E * h.d_rows_stored * h.d_ktiles, fp4))
+    return cudaErrorInvalidValue;
   if (!wmap(&m.gu2, packed + h.off_gu_data, gu_rows, 2 * kTileM) ||
       !wmap(&m.gu, packed + h.off_gu_data, gu_rows, kTileM) || !wmap(&m.gut, packed + h.off_gu_data, gu_rows, 64) ||
       !wmap(&m.d2, packed + h.off_d_data, d_rows, 2 * kTileM) || !wmap(&m.d, packed + h.off_d_data, d_rows, kTileM) ||
@@ -812,7 +913,9 @@ cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, cons
   for (int i = 0; i < kActBoxes; ++i) {
     // boxes taller than the token tile are never used; encode them at its height
     const int rows = std::min(act_box_rows(i), tile_rows);
-    if (!make_act_map(&m.xp[i], b.xp, fp4 ? h.H / 2 : h.H, TK, rows, fp4) ||
+    if (!make_act_map_planes(&m.xp3[i], b.xp, fp4 ? h.H / 2 : h.H, TK, h.H, rows, tile_rows == 8 ? 4 : tile_rows <= 32 ? 3 : 2,
+                             fp4) ||
+        !make_act_map(&m.xp[i], b.xp, fp4 ? h.H / 2 : h.H, TK, rows, fp4) ||
         !make_act_map(&m.hq[i], b.hq, fp4 ? h.I / 2 : h.I, TK, rows, fp4))
       return cudaErrorInvalidValue;
   }
@@ -855,13 +958,20 @@ cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, cons
   // read once per forward
   p.weights_evict_first = (int64_t)T * k <= (int64_t)h.E * tile_rows;
   p.fused_combine = b.fused_combine ? 1 : 0;
+  p.hdr = reinterpret_cast<const PackedHeader*>(packed);
+  p.want = h;
   const int grid = (int)std::min<int64_t>(num_sms, (int64_t)max_tiles * (h.gu_mtiles + h.d_mtiles));
   switch (tile_rows) {
-    case 8: return fp4 ? launch_bn<8, true>(m, p, grid, s) : launch_bn<8, false>(m, p, grid, s);
-    case 16: return fp4 ? launch_bn<16, true>(m, p, grid, s) : launch_bn<16, false>(m, p, grid, s);
-    case 32: return fp4 ? launch_bn<32, true>(m, p, grid, s) : launch_bn<32, false>(m, p, grid, s);
-    case 64: return fp4 ? launch_bn<64, true>(m, p, grid, s) : launch_bn<64, false>(m, p, grid, s);
-    case 128: return fp4 ? launch_bn<128, true>(m, p, grid, s) : launch_bn<128, false>(m, p, grid, s);
+    case 8: return fmt == kActNvfp4 ? launch_bn<8, true, true>(m, p, grid, s)
+                 : fp4 ? launch_bn<8, true, false>(m, p, grid, s) : launch_bn<8, false, false>(m, p, grid, s);
+    case 16: return fmt == kActNvfp4 ? launch_bn<16, true, true>(m, p, grid, s)
+                  : fp4 ? launch_bn<16, true, false>(m, p, grid, s) : launch_bn<16, false, false>(m, p, grid, s);
+    case 32: return fmt == kActNvfp4 ? launch_bn<32, true, true>(m, p, grid, s)
+                  : fp4 ? launch_bn<32, true, false>(m, p, grid, s) : launch_bn<32, false, false>(m, p, grid, s);
+    case 64: return fmt == kActNvfp4 ? launch_bn<64, true, true>(m, p, grid, s)
+                  : fp4 ? launch_bn<64, true, false>(m, p, grid, s) : launch_bn<64, false, false>(m, p, grid, s);
+    case 128: return fmt == kActNvfp4 ? launch_bn<128, true, true>(m, p, grid, s)
+                   : fp4 ? launch_bn<128, true, false>(m, p, grid, s) : launch_bn<128, false, false>(m, p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -133,8 +133,14 @@ constexpr int kGatherWarps = 8;
 
 __global__ void __launch_bounds__(32 * kGatherWarps) gather_tok_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ inv_pos, const int32_t* __restrict__ tiles,
-    int max_tiles, int T, int k, int H, int fp4, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
+    int max_tiles, int T, int k, int H, int fmt, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
     uint8_t* __restrict__ xp, uint8_t* __restrict__ xp_sf) {
+  const int fp4 = fmt != kActMxfp8 ? 1 : 0;  // codes two per byte
+  const bool nv = fmt == kActNvfp4;          // two E4M3 scales per 32-element block
+  // the 256 bytes after the last grouped row are read (as zero padding) by the
+  // expert kernel's k-tile-plane boxes: keep them zero
+  if (blockIdx.x == 0 && threadIdx.x < 16)
+    reinterpret_cast<uint4*>(xp + (int64_t)T * k * (H >> fp4))[threadIdx.x] = make_uint4(0, 0, 0, 0);
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ int2 s_tl[];  // [max_tiles]: {row0, rows}
   const int n_tiles = min(tiles[0], max_tiles);
@@ -175,24 +181,44 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_tok_kernel(
       const int blk = b0 + 32 * u + lane;
       if (b0 + 32 * u >= nbh) break;  // whole warp
       uint4 c[2];
-      uint32_t sc = 127u;  // padding blocks past H carry the neutral scale
+      // padding blocks past H carry the neutral E8M0 scale, or the zero E4M3 scale
+      uint32_t sc = nv ? 0u : 127u;
       if (blk < nbh) {
-        sc = quant_block_act(v[u], c, fp4);
+        if (nv) {
+          float f[32];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float g[8];
+            bf16x8(v[u][q], g);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[8 * q + i] = g[i];
+          }
+          uint32_t p0[2], p1[2];
+          const uint32_t s0 = nvfp4_block16(f, 1.0f, p0), s1 = nvfp4_block16(f + 16, 1.0f, p1);
+          c[0] = make_uint4(p0[0], p0[1], p1[0], p1[1]);
+          sc = s0 | (s1 << 8);
+          *reinterpret_cast<uint16_t*>(xs + (int64_t)t * (H / 16) + 2 * blk) = (uint16_t)sc;
+        } else {
+          sc = quant_block_act(v[u], c, fp4);
+          xs[(int64_t)t * nbh + blk] = (uint8_t)sc;
+        }
         store_block_codes(xq + (int64_t)t * (H >> fp4) + blk * (32 >> fp4), c, fp4);
-        xs[(int64_t)t * nbh + blk] = (uint8_t)sc;
       }
-      // the scales of the four blocks of a 128-element k-tile form one word of the
-      // row's atom entry: lanes 4i..4i+3 hold them, lane 4i stores the word
-      const uint32_t word = sc | (__shfl_down_sync(0xffffffffu, sc, 1) << 8) |
-                            (__shfl_down_sync(0xffffffffu, sc, 2) << 16) | (__shfl_down_sync(0xffffffffu, sc, 3) << 24);
+      // the scales of a 128-element k-tile form one word of the row's atom entry
+      // (lanes 4i..4i+3 hold them, lane 4i stores it), or for NVFP4 two words in the
+      // tile's two atoms (lanes 4i and 4i+2 store them, padding blocks included)
+      const uint32_t word = nv ? (sc | (__shfl_down_sync(0xffffffffu, sc, 1) << 16))
+                               : (sc | (__shfl_down_sync(0xffffffffu, sc, 1) << 8) |
+                                  (__shfl_down_sync(0xffffffffu, sc, 2) << 16) |
+                                  (__shfl_down_sync(0xffffffffu, sc, 3) << 24));
+      const bool writes_word = nv ? ((lane & 1) == 0 && (blk >> 2) < kth) : ((lane & 3) == 0 && blk < nbh);
       for (int j = 0; j < k; ++j) {
         const int pj = __shfl_sync(0xffffffffu, p, j), bj = __shfl_sync(0xffffffffu, b, j),
                   nj = __shfl_sync(0xffffffffu, n, j);
-        if (blk < nbh) {
-          store_block_codes(xp + (int64_t)pj * (H >> fp4) + blk * (32 >> fp4), c, fp4);
-          if ((lane & 3) == 0)
-            *reinterpret_cast<uint32_t*>(xp_sf + ((int64_t)bj * kth + (blk >> 2)) * kAtomBytes + (nj & 31) * 16 +
-                                         (nj >> 5) * 4) = word;
+        if (blk < nbh) store_block_codes(xp + (int64_t)pj * (H >> fp4) + blk * (32 >> fp4), c, fp4);
+        if (writes_word) {
+          const int64_t atom = nv ? ((int64_t)bj * kth + (blk >> 2)) * 2 + ((lane >> 1) & 1) : (int64_t)bj * kth + (blk >> 2);
+          *reinterpret_cast<uint32_t*>(xp_sf + atom * kAtomBytes + (nj & 31) * 16 + (nj >> 5) * 4) = word;
         }
       }
     }
@@ -259,7 +285,7 @@ cudaError_t launch_permute(const int32_t* ids, int TK, int k, int E, int tile_ro
 }
 
 cudaError_t launch_gather_quant(const uint16_t* x, const int32_t* inv_pos, const int32_t* tiles, int max_tiles, int T,
-                                int k, int H, bool fp4, uint8_t* xq, uint8_t* xs, uint8_t* xp, uint8_t* xp_sf,
+                                int k, int H, int fmt, uint8_t* xq, uint8_t* xs, uint8_t* xp, uint8_t* xp_sf,
                                 cudaStream_t s) {
   const size_t smem = (size_t)max_tiles * sizeof(int2);
   if (smem > 48 * 1024) {
@@ -267,7 +293,7 @@ cudaError_t launch_gather_quant(const uint16_t* x, const int32_t* inv_pos, const
     if (e != cudaSuccess) return e;
   }
   gather_tok_kernel<<<(T + kGatherWarps - 1) / kGatherWarps, 32 * kGatherWarps, smem, s>>>(
-      x, inv_pos, tiles, max_tiles, T, k, H, fp4 ? 1 : 0, xq, xs, xp, xp_sf);
+      x, inv_pos, tiles, max_tiles, T, k, H, fmt, xq, xs, xp, xp_sf);
   return cudaGetLastError();
 }
 

@@ -91,6 +91,32 @@ __device__ __forceinline__ uint8_t quant_block_vals_fp4(const uint4 (&v)[4], uin
   return (uint8_t)(s + 127);
 }
 
+// E4M3 code -> fp32 (exact; codes from a saturating conversion, never NaN).
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+  const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+  const float v = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0.001953125f;  // m * 2^-9
+  return (c & 0x80u) ? -v : v;
+}
+
+// NVFP4 quantisation of one 16-element block with global scale gs: scale code =
+// E4M3(amax / (6 gs)) with round-to-nearest-even and saturation at 448, element
+// codes = E2M1(v / (scale * gs)) likewise (zero codes if the scale is zero), the
+// divisions in IEEE fp32.  The 16 codes, two per byte (lower-index element in
+// the low nibble), in pk[0..1]; returns the scale code.
+__device__ __forceinline__ uint32_t nvfp4_block16(const float* v, float gs, uint32_t (&pk)[2]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const uint32_t sc = cvt_e4m3x2(__fdiv_rn(amax, __fmul_rn(6.0f, gs)), 0.f) & 0xFFu;
+  const float sv = __fmul_rn(e4m3_value(sc), gs);
+  float x[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) x[i] = sv == 0.f ? 0.f : __fdiv_rn(v[i], sv);
+  pk[0] = cvt_e2m1x8(x);
+  pk[1] = cvt_e2m1x8(x + 8);
+  return sc;
+}
+
 // Either activation format: MXFP8 (fp4 false; 32 code bytes in c[0..1]) or
 // MXFP4 (fp4 true; 16 code bytes in c[0]).
 __device__ __forceinline__ uint8_t quant_block_act(const uint4 (&v)[4], uint4 (&c)[2], bool fp4) {

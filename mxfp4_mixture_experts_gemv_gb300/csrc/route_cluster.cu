@@ -115,6 +115,10 @@ __global__ void __launch_bounds__(kRcThreads, 1) route_cluster_kernel(const Rout
     // them before any report
     if (rank == 0) *reinterpret_cast<uint4*>(a.zero) = make_uint4(0u, 0u, 0u, 0u);
   }
+  // the 256 bytes after the last grouped row are read (as zero padding) by the
+  // expert kernel's k-tile-plane boxes: keep them zero
+  if (rank == 0 && tid >= 32 && tid < 48)
+    reinterpret_cast<uint4*>(a.xp + (int64_t)TK * (H >> a.fp4))[tid - 32] = make_uint4(0, 0, 0, 0);
   // biases of this CTA's experts (in flight with the copies)
   if (tid < ne) s_bias[tid] = __uint_as_float((uint32_t)a.br[e0 + tid] << 16);
   __syncthreads();  // the barrier's initialisation is visible to every thread

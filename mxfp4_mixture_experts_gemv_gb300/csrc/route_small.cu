@@ -65,6 +65,11 @@ __global__ void __launch_bounds__(kThreads) route_small_kernel(const RouteSmallA
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int TK = T * k;
 
+  // the 256 bytes after the last grouped row are read (as zero padding) by the
+  // expert kernel's k-tile-plane boxes: keep them zero
+  if (blockIdx.x == 0 && tid < 16)
+    reinterpret_cast<uint4*>(a.xp + (int64_t)TK * (H >> a.fp4))[tid] = make_uint4(0, 0, 0, 0);
+
   // ------------------------------------------------------------ phase A: logits of expert e
   {
     // stage the router row and the T token rows in shared memory with async copies

@@ -32,7 +32,42 @@ class GpuRun:
 
     @property
     def fp4(self) -> bool:
-        return self.act_format == "mxfp4"
+        return self.act_format in ("mxfp4", "nvfp4")
+
+    @property
+    def nv(self) -> bool:
+        return self.act_format == "nvfp4"
+
+    @property
+    def block(self) -> int:
+        """Elements per activation scale: 16 for NVFP4, 32 for the MX formats."""
+        return 16 if self.nv else 32
+
+    def atom_scales(self, section, rows_of, n_rows, K, n_blocks=None):
+        """Scale codes of the listed grouped rows from a scale-atom section: [rows, blocks].
+        MX formats: one atom per 128-element k-tile, byte (n%32)*16 + (n/32)*4 + block%4;
+        NVFP4: two atoms per k-tile, atom (block/4)%2 of k-tile block/8."""
+        L = self.layout
+        kt = (K + 127) // 128
+        atoms = self.section(section, (L.max_tiles, kt, 2, 512) if self.nv else (L.max_tiles, kt, 512),
+                             torch.uint8).numpy()
+        tiles = self.section("tiles", (4 + 4 * L.max_tiles,), torch.int32).numpy()
+        td = tiles[4:4 + 4 * tiles[0]].reshape(-1, 4)
+        pos = np.asarray(rows_of, np.int64)
+        b = np.searchsorted(td[:, 1], pos, side="right") - 1
+        n = pos - td[b, 1]
+        nb = n_blocks if n_blocks is not None else (8 if self.nv else 4) * kt
+        kb = np.arange(nb)
+        byte = ((n % 32) * 16 + (n // 32) * 4)[:, None] + (kb % 4)[None, :]
+        if self.nv:
+            return atoms[b[:, None], (kb // 8)[None, :], ((kb // 4) % 2)[None, :], byte]
+        return atoms[b[:, None], (kb // 4)[None, :], byte]
+
+    def scale_values(self, codes):
+        """Scale multipliers of scale codes: 2^(code - 127) (E8M0) or the E4M3 value."""
+        if self.nv:
+            return _code_table(False)[codes]
+        return np.ldexp(1.0, codes.astype(np.int64) - 127)
 
     def codes(self, name, rows, cols):
         """Activation codes of a workspace section, one code per element: E4M3 bytes,
@@ -45,11 +80,11 @@ class GpuRun:
         return moe.view(self.ws, getattr(self.layout, name), shape, dtype).cpu()
 
 
-def pack(inp: ms.LayerInputs):
+def pack(inp: ms.LayerInputs, nvfp4: bool = False):
     s = inp.shape
     dims = moe.LayerDims(s.E, s.H, s.I)
     packed = moe.pack_weights(dims, inp.gate_up_blocks, inp.gate_up_scales, inp.gate_up_bias,
-                              inp.down_blocks, inp.down_scales, inp.down_bias)
+                              inp.down_blocks, inp.down_scales, inp.down_bias, nvfp4=nvfp4)
     return dims, packed
 
 
@@ -142,7 +177,7 @@ def H_gamma(n: int) -> float:
 def check_quantised_x(run: GpuRun, xq_ref, xs_ref):
     T, H = xq_ref.shape
     xq = run.codes("xq", T, H)
-    xs = run.section("xs", (T, H // 32), torch.uint8).numpy()
+    xs = run.section("xs", (T, H // run.block), torch.uint8).numpy()
     np.testing.assert_array_equal(zero_codes_equal(xq, run.fp4), zero_codes_equal(xq_ref, run.fp4))
     np.testing.assert_array_equal(xs, xs_ref)
 
@@ -156,17 +191,10 @@ def check_gathered(run: GpuRun, T: int, sr: np.ndarray, xq_ref: np.ndarray, xs_r
     TK = T * k
     xp = run.codes("xp", TK, H)
     np.testing.assert_array_equal(zero_codes_equal(xp, run.fp4), zero_codes_equal(xq_ref[sr // k], run.fp4))
-    kth = (H + 127) // 128
-    xp_sf = run.section("xp_sf", (L.max_tiles, kth, 512), torch.uint8).numpy()
-    tiles = run.section("tiles", (4 + 4 * L.max_tiles,), torch.int32).numpy()
-    td = tiles[4:4 + 4 * tiles[0]].reshape(-1, 4)
-    pos = np.arange(TK)
-    b = np.searchsorted(td[:, 1], pos, side="right") - 1
-    n = pos - td[b, 1]
-    kb = np.arange(4 * kth)
-    sc = xp_sf[b[:, None], kb[None, :] // 4, ((n % 32) * 16 + (n // 32) * 4)[:, None] + (kb % 4)[None, :]]
-    want = np.full((TK, 4 * kth), 127, np.uint8)
-    want[:, :H // 32] = xs_ref[sr // k]
+    sc = run.atom_scales("xp_sf", np.arange(TK), TK, H)
+    # padding blocks past H: the neutral E8M0 scale, or the zero E4M3 scale
+    want = np.full(sc.shape, 0 if run.nv else 127, np.uint8)
+    want[:, :H // run.block] = xs_ref[sr // k]
     np.testing.assert_array_equal(sc, want)
 
 
@@ -225,6 +253,10 @@ def compare_out(got: np.ndarray, want: np.ndarray, what="", allow=None, bf16_rou
 _TABLES = {}
 
 
+def e4m3_values():
+    return _code_table(False)
+
+
 def _code_table(fp4: bool):
     """Value of every activation code from the oracle's decoders (E2M1 or E4M3)."""
     if fp4 not in _TABLES:
@@ -239,16 +271,9 @@ def gpu_hq(run: GpuRun, T: int, inv: np.ndarray):
     L = run.layout
     TK = run.out.shape[0] * k
     hq = run.codes("hq", TK, I)
-    kti = (I + 127) // 128
-    hq_sf = run.section("hq_sf", (L.max_tiles, kti, 512), torch.uint8).numpy()
-    tiles = run.section("tiles", (4 + 4 * L.max_tiles,), torch.int32).numpy()
-    td = tiles[4:4 + 4 * tiles[0]].reshape(-1, 4)
     pos = inv.reshape(-1).astype(np.int64)
-    b = np.searchsorted(td[:, 1], pos, side="right") - 1
-    n = pos - td[b, 1]
-    kb = np.arange(I // 32)
-    sc = hq_sf[b[:, None], kb[None, :] // 4, ((n % 32) * 16 + (n // 32) * 4)[:, None] + (kb % 4)[None, :]]
-    return hq[pos].reshape(-1, k, I), sc.reshape(-1, k, I // 32)
+    sc = run.atom_scales("hq_sf", pos, TK, I, n_blocks=I // run.block)
+    return hq[pos].reshape(-1, k, I), sc.reshape(-1, k, I // run.block)
 
 
 def check_intermediate(run: GpuRun, ref: dict, inp_cpu: ms.LayerInputs, inv: np.ndarray, tokens=None,
@@ -267,8 +292,9 @@ def check_intermediate(run: GpuRun, ref: dict, inp_cpu: ms.LayerInputs, inv: np.
     mag = 0x7 if run.fp4 else 0x7F
     gq, gs = gpu_hq(run, T, inv)
     rq, rs = ref["hq"], ref["hs"]
-    gv = e4[gq] * np.ldexp(1.0, np.repeat(gs.astype(np.int64), 32, axis=-1) - 127)
-    rv = e4[rq] * np.ldexp(1.0, np.repeat(rs.astype(np.int64), 32, axis=-1) - 127)
+    B = run.block
+    gv = e4[gq] * np.repeat(run.scale_values(gs), B, axis=-1)
+    rv = e4[rq] * np.repeat(run.scale_values(rs), B, axis=-1)
     h = ref["h"]
     allow = np.zeros(T)
     flips = 0
@@ -276,14 +302,19 @@ def check_intermediate(run: GpuRun, ref: dict, inp_cpu: ms.LayerInputs, inv: np.
     for t, j in zip(*np.nonzero((gv != rv).any(axis=-1))):
         e = int(ref["ids"][t, j])
         bad = np.nonzero(gv[t, j] != rv[t, j])[0]
-        for blk in np.unique(bad // 32):
-            sl = slice(32 * blk, 32 * blk + 32)
+        for blk in np.unique(bad // B):
+            sl = slice(B * blk, B * blk + B)
             if gs[t, j, blk] != rs[t, j, blk]:
                 amax = np.abs(h[t, j, sl]).max()
-                edge = 2.0 ** np.round(np.log2(amax))
-                assert abs(amax - edge) <= rel_mid * amax, f"pair {(t, j)} block {blk}: scale differs away from a power of two"
+                if run.nv:
+                    # the E4M3 block scale flips where amax / 6 sits at the midpoint of two scale values
+                    mid_s = 0.5 * (e4m3_values()[int(gs[t, j, blk])] + e4m3_values()[int(rs[t, j, blk])])
+                    assert abs(amax / 6 - mid_s) <= rel_mid * amax / 6, f"pair {(t, j)} block {blk}: scale differs away from a midpoint"
+                else:
+                    edge = 2.0 ** np.round(np.log2(amax))
+                    assert abs(amax - edge) <= rel_mid * amax, f"pair {(t, j)} block {blk}: scale differs away from a power of two"
             else:
-                for i in bad[(bad >= 32 * blk) & (bad < 32 * blk + 32)]:
+                for i in bad[(bad >= B * blk) & (bad < B * blk + B)]:
                     mid = 0.5 * (gv[t, j, i] + rv[t, j, i])
                     a, b = int(gq[t, j, i]), int(rq[t, j, i])
                     # neighbours: magnitudes one code apart with the same sign, or either side of zero
@@ -293,7 +324,12 @@ def check_intermediate(run: GpuRun, ref: dict, inp_cpu: ms.LayerInputs, inv: np.
                     assert abs(h[t, j, i] - mid) <= rel_mid * abs(h[t, j, i]), \
                         f"pair {(t, j)} elem {i}: h={h[t, j, i]!r} not at the midpoint {mid!r}"
         if e not in colmax:
-            colmax[e] = np.abs(oracle.dequant_mxfp4(inp_cpu.down_blocks[e], inp_cpu.down_scales[e])).max(axis=0)
+            wd = oracle.dequant_mxfp4(inp_cpu.down_blocks[e], inp_cpu.down_scales[e])
+            if run.nv:  # the NVFP4 weights: the MXFP4 ones re-quantised, within one block-scale unit
+                gsd = oracle.nvfp4_global_scale(oracle.mxfp4_amax(inp_cpu.down_blocks, inp_cpu.down_scales))
+                wd = oracle.nvfp4_dequant(*oracle.convert_mxfp4_to_nvfp4(inp_cpu.down_blocks[e], inp_cpu.down_scales[e],
+                                                                          gsd), gsd)
+            colmax[e] = np.abs(wd).max(axis=0)
         allow[t] += ref["w"][t, j] * float((np.abs(gv[t, j] - rv[t, j]) * colmax[e]).sum())
         flips += bad.size
     total = T * k * I

@@ -23,7 +23,7 @@ def L():
 def _declared_functions():
     src = open(os.path.join(ROOT, "include", "moe.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_header_declarations_match_binding():
@@ -160,5 +160,5 @@ def test_plan_override_is_checked_and_sizes_follow_it(L):
 
 
 def test_forward_act_rejects_unknown_formats(L):
-    assert L.moe_forward_act(GPT.c(), 2, FAKE, 4, FAKE, FAKE, FAKE, 4, FAKE, FAKE, 1 << 40, None) == 1
+    assert L.moe_forward_act(GPT.c(), 3, FAKE, 4, FAKE, FAKE, FAKE, 4, FAKE, FAKE, 1 << 40, None) == 1
     assert b"activation format" in L.moe_last_error()

@@ -56,13 +56,15 @@ def _full_check(inp_cpu, run, strict=True):
     return ref
 
 
-@pytest.mark.parametrize("act_format", ["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("act_format", ["mxfp8", "mxfp4", "nvfp4"])
 @pytest.mark.parametrize("name", list(SMALL_CASES))
 def test_small_layer_parity(name, act_format):
     shape, seed = SMALL_CASES[name]
+    if act_format == "nvfp4" and (shape.H % 64 or shape.I % 64):
+        pytest.skip("NVFP4 packing needs H and I multiples of 64")
     inp = ms.make_layer(shape, seed=seed)
     dev = inp.to("cuda")
-    _, packed = mc.pack(dev)
+    _, packed = mc.pack(dev, nvfp4=act_format == "nvfp4")
     run = mc.run_gpu(dev, packed, act_format=act_format)
     _full_check(inp, run, strict=False)
 
@@ -167,6 +169,19 @@ def gpt_layer():
     return dims, packed, w, cpu
 
 
+_NV_PACKED = {}
+
+
+def _nvfp4_packed(gpt_layer):
+    """The gpt-oss layer's weights converted to NVFP4 (packed once per module)."""
+    dims, packed, w, cpu = gpt_layer
+    key = packed.data_ptr()
+    if key not in _NV_PACKED:
+        _NV_PACKED.clear()
+        _NV_PACKED[key] = moe.pack_weights(dims, *w, nvfp4=True)
+    return _NV_PACKED[key]
+
+
 def _gpt_inputs(gpt_layer, T, hot=0, hot_bias=0.0):
     dims, packed, w, cpu = gpt_layer
     shape = ms.LayerShape(T=T, H=dims.H, I=dims.I, E=dims.E, k=4)
@@ -177,20 +192,24 @@ def _gpt_inputs(gpt_layer, T, hot=0, hot_bias=0.0):
     return cpu_inp, dev_inp, packed
 
 
-@pytest.mark.parametrize("act_format", ["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("act_format", ["mxfp8", "mxfp4", "nvfp4"])
 @pytest.mark.parametrize("T,hot", [(4, 0), (32, 16)], ids=["decode_t4", "decode_t32_skewed"])
 def test_gpt_oss_decode_parity(gpt_layer, T, hot, act_format):
     cpu_inp, dev_inp, packed = _gpt_inputs(gpt_layer, T, hot, 1.0 if hot else 0.0)
+    if act_format == "nvfp4":
+        packed = _nvfp4_packed(gpt_layer)
     run = mc.run_gpu(dev_inp, packed, act_format=act_format)
     _full_check(cpu_inp, run)
 
 
-@pytest.mark.parametrize("act_format", ["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("act_format", ["mxfp8", "mxfp4", "nvfp4"])
 def test_gpt_oss_prefill_sampled_parity(gpt_layer, act_format):
     """T = 2048 with the launch configuration of the benchmark; all ids and the
     whole grouping are checked, the output on a sample of tokens."""
     T = 2048
     cpu_inp, dev_inp, packed = _gpt_inputs(gpt_layer, T)
+    if act_format == "nvfp4":
+        packed = _nvfp4_packed(gpt_layer)
     run = mc.run_gpu(dev_inp, packed, act_format=act_format)
     logits, ids_ref, _ = oracle.route(cpu_inp.x, cpu_inp.router_w, cpu_inp.router_b, 4)
     ties = mc.check_routing(run, cpu_inp.x, cpu_inp.router_w, cpu_inp.router_b, logits)
@@ -286,3 +305,62 @@ def test_gpt_oss_parity_at_the_plan_cutoffs(gpt_layer, T):
     ref = mc.oracle_tokens_parallel(cpu_inp, sample)
     allow, _ = mc.check_intermediate(run, ref, cpu_inp, inv.reshape(T, 4)[sample])
     mc.compare_out(mc.bf16_to_f64(run.out)[sample], ref["out"], f"T={T}", allow=allow)
+
+
+def test_nvfp4_pack_matches_the_oracle_conversion():
+    """The NVFP4 repacker, unpacked from its tiles and scale atoms, equals the oracle's
+    conversion of the MXFP4 checkpoint (codes and E4M3 scales of every row, bit-exact),
+    and it records each projection's amax, from which both sides take the global scale."""
+    shape = ms.LayerShape(T=1, H=256, I=192, E=3, k=1)
+    inp = ms.make_layer(shape, seed=23)
+    dev = inp.to("cuda")
+    _, packed = mc.pack(dev, nvfp4=True)
+    pk = packed.cpu().numpy()
+    E, H, I = shape.E, shape.H, shape.I
+    assert pk[52:56].view(np.int32)[0] == 1  # weight format: NVFP4
+    offs = pk[56:112].view(np.uint64)
+    gu_data, gu_sf, gu_b, d_data, d_sf, d_b, total = (int(o) for o in offs)
+    assert total == moe.lib().moe_packed_size_nvfp4(moe.LayerDims(E, H, I).c())
+    amax = pk[512:520].view(np.float32).astype(np.float64)
+    assert amax[0] == oracle.mxfp4_amax(inp.gate_up_blocks, inp.gate_up_scales)
+    assert amax[1] == oracle.mxfp4_amax(inp.down_blocks, inp.down_scales)
+
+    def check(data_off, sf_off, rows, rows_stored, K, blocks, scales, src_row):
+        kt_n, mt_n = (K + 127) // 128, (rows_stored + 127) // 128
+        gs = oracle.nvfp4_global_scale(oracle.mxfp4_amax(blocks, scales))
+        flat = pk[data_off:data_off + E * rows_stored * kt_n * 64]
+        sfa = pk[sf_off:sf_off + E * mt_n * kt_n * 2 * 512].reshape(E, mt_n, kt_n, 2, 512)
+        untiled = _untile(flat, E, rows_stored, kt_n * 128)
+        for e in range(E):
+            want_c, want_s = oracle.convert_mxfp4_to_nvfp4(blocks[e], scales[e], gs)
+            got = np.empty((rows_stored, kt_n * 128), np.uint8)
+            got[:, 0::2] = untiled[e] & 15
+            got[:, 1::2] = untiled[e] >> 4
+            r = np.arange(rows)
+            np.testing.assert_array_equal(got[r, :K], want_c[src_row(r)])
+            assert (got[:, K:] == 0).all() and (got[rows:] == 0).all()
+            q = np.arange(K // 16)
+            byte = ((r % 32) * 16 + ((r % 128) // 32) * 4)[:, None] + (q % 4)[None, :]
+            s = sfa[e, (r // 128)[:, None], (q // 8)[None, :], ((q // 4) % 2)[None, :], byte]
+            np.testing.assert_array_equal(s, want_s[src_row(r)])
+
+    gu_src = np.vectorize(lambda pr: (64 * (pr // 128) + pr % 128) if pr % 128 < 64 else (I + 64 * (pr // 128) + pr % 128 - 64))
+    check(gu_data, gu_sf, 2 * I, 2 * I, H, inp.gate_up_blocks.numpy(), inp.gate_up_scales.numpy(), gu_src)
+    check(d_data, d_sf, H, 256, I, inp.down_blocks.numpy(), inp.down_scales.numpy(), lambda r: r)
+
+
+def test_formats_alternate_on_one_packed_address():
+    """The same device address packed as MXFP4, then NVFP4, then MXFP4 again (the
+    caching allocator hands freed buffers back): each forward must use the layout
+    of the buffer it is given, not descriptors cached for the previous one."""
+    shape = ms.LayerShape(T=5, H=128, I=64, E=6, k=2)
+    inp = ms.make_layer(shape, seed=44)
+    dev = inp.to("cuda")
+    dims = moe.LayerDims(shape.E, shape.H, shape.I)
+    n = max(moe.packed_size(dims), moe.lib().moe_packed_size_nvfp4(dims.c()))
+    buf = moe._alloc_aligned(n, "cuda")
+    for fmt in ("mxfp8", "nvfp4", "mxfp4", "nvfp4"):
+        w = (dev.gate_up_blocks, dev.gate_up_scales, dev.gate_up_bias, dev.down_blocks, dev.down_scales, dev.down_bias)
+        packed = moe.pack_weights(dims, *w, packed=buf, nvfp4=fmt == "nvfp4")
+        run = mc.run_gpu(dev, packed, act_format=fmt)
+        _full_check(inp, run, strict=False)
