@@ -40,6 +40,9 @@ K_TOP = 4
 # checkpoint-format bytes of one expert (packed E2M1 + E8M0 scales + bf16 bias)
 GU_BYTES = 2 * I * (H // 2) + 2 * I * (H // 32) + 2 * I * 2
 D_BYTES = H * (I // 2) + H * (I // 32) + H * 2
+# NVFP4 weights: E4M3 block scales per 16 elements instead of E8M0 per 32
+GU_BYTES_NV = 2 * I * (H // 2) + 2 * I * (H // 16) + 2 * I * 2
+D_BYTES_NV = H * (I // 2) + H * (I // 16) + H * 2
 FLOP_PER_ROW = 2 * (H * 2 * I + I * H)
 
 
@@ -224,14 +227,14 @@ def run_reference(args):
 class Layers:
     """Independently seeded packed layers rotated through the steps."""
 
-    def __init__(self, n: int, device, seed: int = 0):
+    def __init__(self, n: int, device, seed: int = 0, nvfp4: bool = False):
         import mxfp4_mixture_experts_gemv_gb300 as moe
         self.moe = moe
         self.dims = moe.LayerDims(E, H, I)
         self.packed, self.router = [], []
         for l in range(n):
             w = ms.make_expert_weights(seed, H, I, E, layer=l, device=device)
-            self.packed.append(moe.pack_weights(self.dims, *w))
+            self.packed.append(moe.pack_weights(self.dims, *w, nvfp4=nvfp4))
             torch.cuda.synchronize()
             del w
         self.n = n
@@ -328,8 +331,8 @@ def _workload(layers: Layers, T: int, hot: int, hot_bias: float, steps: int, war
     ms_step = _max_over_ranks(dist, ms_total / steps, device)
     seq = [act[i % layers.n] for i in range(steps)]
     n_act = sum(seq) / len(seq)
-    gu_bytes = n_act * GU_BYTES
-    d_bytes = n_act * D_BYTES
+    gu_bytes = n_act * (GU_BYTES_NV if act_format == "nvfp4" else GU_BYTES)
+    d_bytes = n_act * (D_BYTES_NV if act_format == "nvfp4" else D_BYTES)
     step_bytes = gu_bytes + d_bytes + E * H * 2 + E * 2 + 2 * T * H * 2
     flop = T * K_TOP * FLOP_PER_ROW + 2 * T * E * H
     stage_avg = {k: v / max(calls, 1) for k, v in stage_ms.items()}
@@ -402,6 +405,58 @@ def _stack(layers: Layers, n_layers: int, T: int, steps: int, warmup: int, devic
             "algorithmic_bytes": step_bytes, "gbs": step_bytes / (ms_step * 1e-3) / 1e9,
             "tflops": flop / (ms_step * 1e-3) / 1e12, "timing": "CUDA graph of the whole step" if graph else
             "stream of C-ABI calls", "clocks": clocks.summary()}
+
+
+def _dense(N: int, K: int, T: int, steps: int, warmup: int, device, hbm_peak: float, fp8_peak: float):
+    """One dense MXFP4 linear (bf16 weights of the given shape quantised on the device)
+    at T tokens: the default path, and for T <= 4 both forced paths.  Enough weight
+    copies rotate through the steps to exceed L2; each step is one graph replay."""
+    import mxfp4_mixture_experts_gemv_gb300 as moe
+    copies = max(1, -(-(256 << 20) // (N * K // 2)))
+    packs = []
+    for c in range(copies):
+        g = torch.Generator(device=device).manual_seed(1000 + c)
+        wt = (torch.randn(N, K, generator=g, device=device) * 0.05).to(torch.bfloat16)
+        b = (torch.randn(N, generator=g, device=device) * 0.02).to(torch.bfloat16)
+        packs.append(moe.dense_pack(*moe.dense_quantize_weights(wt), b))
+        del wt
+    x = ms.make_tokens(7, T, K).to(device)
+    out = torch.empty((T, N), dtype=torch.bfloat16, device=device)
+    ws = moe._alloc_aligned(max(moe.lib().moe_dense_workspace_size(N, K, T), 256), device)
+    res = {"N": N, "K": K, "T": T, "weight_copies_rotated": copies}
+    wbytes = N * (K // 2) + N * (K // 32) + N * 4
+    step_bytes = wbytes + T * K * 2 + T * N * 2
+    for path in (["auto", "cuda_cores", "weights_m"] if T <= 4 else ["auto"]):
+        moe.set_plan(0, "auto", path)
+        try:
+            for i in range(warmup):
+                moe.dense_forward(N, K, x, packs[i % copies], out=out, workspace=ws)
+            graphs = []
+            for i in range(steps):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    moe.dense_forward(N, K, x, packs[i % copies], out=out, workspace=ws)
+                graphs.append(g)
+            torch.cuda.synchronize()
+            stream = torch.cuda.current_stream()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for g in graphs:
+                g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / steps
+            del graphs
+        finally:
+            moe.set_plan(0, "auto")
+        res[path] = {"us_per_call": us, "gbs": step_bytes / (us * 1e-6) / 1e9,
+                     "hbm_frac": step_bytes / (us * 1e-6) / 1e9 / hbm_peak,
+                     "tflops": 2.0 * T * N * K / (us * 1e-6) / 1e12,
+                     "tflops_frac_of_fp8_peak": 2.0 * T * N * K / (us * 1e-6) / 1e12 / fp8_peak}
+    res["algorithmic_bytes"] = step_bytes
+    del packs
+    torch.cuda.empty_cache()
+    return res
 
 
 def _e2e(layers: Layers, w: dict, steps: int, warmup: int, device, dist):
@@ -560,6 +615,31 @@ def run_ours(args):
                 "expert_mlp_tflops_frac_of_fp4_peak": expert_flop / (mlp_ms * 1e-3) / 1e12 / fp4_peak,
                 "stage_ms": w["stage_ms"], "clocks": w["clocks"]}
             del w
+
+    if not args.no_extra:
+        # the NVFP4 variant: the MXFP4 layers converted to NVFP4 while packing, NVFP4
+        # activations (tcgen05 kind::mxf4nvf4)
+        nv_layers = Layers(args.layers, device, nvfp4=True)
+        for name, T, n in (("nvfp4_decode_t4", 4, args.steps), ("nvfp4_prefill_t2048", 2048, max(10, args.steps // 5))):
+            w = _workload(nv_layers, T, 0, 0.0, n, min(args.warmup, 3), device, dist, act_format="nvfp4")
+            mlp_ms = w["stage_ms"].get("expert_mlp", 0) or float("nan")
+            expert_flop = T * K_TOP * FLOP_PER_ROW
+            extra[name] = {
+                "T": T, "act_format": "nvfp4", "tokens_per_s": _replica_tokens_per_s(world, T, w["ms_per_step"]),
+                "ms_per_step": w["ms_per_step"], "active_experts": w["active_experts"],
+                "algorithmic_bytes": w["step_bytes"], "gbs": w["gbs"], "hbm_frac": w["gbs"] / hbm_peak,
+                "tflops": w["tflops"],
+                "expert_mlp_gbs": (w["gu_bytes"] + w["d_bytes"]) / (mlp_ms * 1e-3) / 1e9,
+                "expert_mlp_tflops": expert_flop / (mlp_ms * 1e-3) / 1e12,
+                "expert_mlp_tflops_frac_of_fp4_peak": expert_flop / (mlp_ms * 1e-3) / 1e12 / fp4_peak,
+                "stage_ms": w["stage_ms"], "clocks": w["clocks"]}
+            del w
+        del nv_layers
+        torch.cuda.empty_cache()
+        # dense MXFP4 linears of the same model: attention projections and LM head
+        for name, N, K, T in (("dense_qkv_t4", 5120, 2880, 4), ("dense_o_t4", 2880, 4096, 4),
+                              ("dense_lm_head_t1", 201088, 2880, 1), ("dense_qkv_t2048", 5120, 2880, 2048)):
+            extra[name] = _dense(N, K, T, args.steps, min(args.warmup, 3), device, hbm_peak, fp8_peak)
 
     if not args.no_extra and not args.no_stack:
         n_l = 36

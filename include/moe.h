@@ -293,6 +293,41 @@ uint64_t moe_get_wait_limit_ns(void);
 moe_status moe_debug_hold_waits(int32_t which);
 
 /*
+ * Dense MXFP4 linears: out = MXFP8(x) . W^T + b, for the attention projections and
+ * the LM head ("GPT-OSS-120B with MXFP4 on DGX Spark (SM121/GB10)", section "What's
+ * Included", "Full MXFP4 Quantization Stack": QKV projections, O projections and
+ * the LM head in MXFP4; section "Performance Optimizations": a CUDA-core path for
+ * M <= 4 beside the tensor cores).  W is [N, K] (N outputs, K inputs), x bf16
+ * [T, K], b bf16 [N] (optional), out bf16 [T, N]; x is quantised per 32-element
+ * block to MXFP8 exactly as in the MoE layer.  N must be a multiple of 64 and K
+ * of 32 (else MOE_ERR_UNSUPPORTED_SHAPE).  All pointers are device pointers owned
+ * by the caller; everything is asynchronous on `stream`.
+ *
+ * moe_dense_quantize_weights: BF16 weights w [N, K] -> MXFP4 in the checkpoint
+ *   layout, blocks [N, K/32, 16] (two E2M1 codes per byte, even element in the low
+ *   nibble) and E8M0 scales [N, K/32], by the activations' block rule (shared
+ *   exponent floor(log2 amax) - 2, E2M1 round-to-nearest-even, saturating at 6);
+ *   the checkpoint keeps these projections in BF16 ("GPT-OSS-120B on DGX Spark:
+ *   From MXFP4 to NVFP4", "MXFP4 Tensor Structure").
+ * moe_dense_pack: MXFP4 checkpoint-layout W (+ bias, may be NULL) -> the packed
+ *   form moe_dense_forward streams (moe_dense_packed_size bytes, 256-byte aligned).
+ * moe_dense_forward: T = 0 is a no-op; the workspace (256-byte aligned,
+ *   moe_dense_workspace_size bytes) holds the quantised input and, for a few
+ *   tokens, K-chunk partial sums.  A few tokens (T <= 4) take the CUDA-core path
+ *   (a GEMV streaming the packed weights), more the tensor-core path (the MoE
+ *   layer's block-scaled GEMM with one expert); moe_set_plan can force either
+ *   (MOE_EXPERT_CUDA_CORES / MOE_EXPERT_WEIGHTS_M).
+ */
+size_t moe_dense_packed_size(int32_t N, int32_t K);
+moe_status moe_dense_quantize_weights(int32_t N, int32_t K, const void *w, void *blocks, void *scales,
+                                      void *stream);
+moe_status moe_dense_pack(int32_t N, int32_t K, const void *blocks, const void *scales, const void *bias,
+                          void *packed, size_t packed_bytes, void *stream);
+size_t moe_dense_workspace_size(int32_t N, int32_t K, int32_t T);
+moe_status moe_dense_forward(int32_t N, int32_t K, const void *x, int32_t T, const void *packed, void *out,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Residual stream of a stack of MoE layers, x <- x + moe(rmsnorm(x)) (the
  * stacked-layer workload; RMSNorm with unit gain; 36 MoE layers per model,
  * "GPT-OSS-120B on DGX Spark: From MXFP4 to NVFP4", section "GPT-OSS-120B
@@ -327,6 +362,7 @@ moe_status moe_residual_rmsnorm(float *x_res, const void *layer_out, int32_t T, 
 #define MOE_EXPERT_AUTO 0
 #define MOE_EXPERT_WEIGHTS_M 1
 #define MOE_EXPERT_TOKENS_M 2
+#define MOE_EXPERT_CUDA_CORES 3 /* dense linears only: the CUDA-core path (T <= 4) */
 moe_status moe_set_plan(int32_t tile_rows, int32_t route, int32_t expert_kernel);
 
 /*

@@ -29,7 +29,8 @@ EXPORTED = ["moe_packed_size", "moe_pack_weights", "moe_packed_size_nvfp4", "moe
             "moe_forward", "moe_forward_act", "moe_forward_static_scratch", "moe_static_scratch_status", "moe_static_scratch_bytes",
             "moe_get_device_status", "moe_set_wait_limit_ns", "moe_get_wait_limit_ns",
             "moe_debug_hold_waits", "moe_set_plan", "moe_profile_begin", "moe_profile_end", "moe_residual_rmsnorm",
-            "moe_last_error", "moe_version"]
+            "moe_dense_packed_size", "moe_dense_quantize_weights", "moe_dense_pack", "moe_dense_workspace_size",
+            "moe_dense_forward", "moe_last_error", "moe_version"]
 STAGES = ["routing", "expert_mlp"]
 
 
@@ -105,6 +106,16 @@ def lib() -> ctypes.CDLL:
         L.moe_profile_begin.argtypes = [i32]
         L.moe_profile_end.restype = st
         L.moe_profile_end.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int32)]
+        L.moe_dense_packed_size.restype = sz
+        L.moe_dense_packed_size.argtypes = [i32, i32]
+        L.moe_dense_quantize_weights.restype = st
+        L.moe_dense_quantize_weights.argtypes = [i32, i32, vp, vp, vp, vp]
+        L.moe_dense_pack.restype = st
+        L.moe_dense_pack.argtypes = [i32, i32, vp, vp, vp, vp, sz, vp]
+        L.moe_dense_workspace_size.restype = sz
+        L.moe_dense_workspace_size.argtypes = [i32, i32, i32]
+        L.moe_dense_forward.restype = st
+        L.moe_dense_forward.argtypes = [i32, i32, vp, i32, vp, vp, vp, sz, vp]
         L.moe_last_error.restype = ctypes.c_char_p
         L.moe_last_error.argtypes = []
         L.moe_version.restype = ctypes.c_uint32
@@ -280,7 +291,7 @@ def wait_limit_ns() -> int:
 
 
 ROUTES = {"auto": 0, "cluster": 1, "grid": 2, "tensor_core": 3}
-EXPERT_KERNELS = {"auto": 0, "weights_m": 1, "tokens_m": 2}
+EXPERT_KERNELS = {"auto": 0, "weights_m": 1, "tokens_m": 2, "cuda_cores": 3}
 
 
 def set_plan(tile_rows: int = 0, route: str = "auto", expert: str = "auto"):
@@ -307,3 +318,42 @@ def view(workspace: torch.Tensor, offset: int, shape, dtype) -> torch.Tensor:
         n *= s
     nbytes = n * torch.empty(0, dtype=dtype).element_size()
     return workspace[offset:offset + nbytes].view(dtype).view(*shape)
+
+
+# ----------------------------------------------------------------------- dense MXFP4 linears
+def dense_quantize_weights(w: torch.Tensor, stream=None):
+    """bf16 [N, K] -> (MXFP4 blocks uint8 [N, K/32, 16], E8M0 scales uint8 [N, K/32])."""
+    N, K = w.shape
+    blocks = torch.empty((N, K // 32, 16), dtype=torch.uint8, device=w.device)
+    scales = torch.empty((N, K // 32), dtype=torch.uint8, device=w.device)
+    _check(lib().moe_dense_quantize_weights(N, K, _dev_ptr(w, "w", torch.bfloat16), _dev_ptr(blocks, "blocks"),
+                                            _dev_ptr(scales, "scales"), _stream(stream)))
+    return blocks, scales
+
+
+def dense_pack(blocks: torch.Tensor, scales: torch.Tensor, bias: torch.Tensor | None = None, stream=None):
+    """MXFP4 checkpoint-layout W [N, K/32, 16] + [N, K/32] (+ bf16 bias [N]) -> packed buffer."""
+    N, nb = scales.shape
+    K = nb * 32
+    n = lib().moe_dense_packed_size(N, K)
+    if n == 0:
+        _check(lib().moe_dense_pack(N, K, None, None, None, None, 0, None))
+    packed = _alloc_aligned(n, blocks.device)
+    _check(lib().moe_dense_pack(N, K, _dev_ptr(blocks, "blocks", torch.uint8), _dev_ptr(scales, "scales", torch.uint8),
+                                None if bias is None else _dev_ptr(bias, "bias", torch.bfloat16),
+                                _dev_ptr(packed, "packed"), n, _stream(stream)))
+    return packed
+
+
+def dense_forward(N: int, K: int, x: torch.Tensor, packed: torch.Tensor, out: torch.Tensor | None = None,
+                  workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """bf16 x [T, K] -> bf16 out [T, N] = MXFP8(x) . W^T + b."""
+    T = x.shape[0]
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = _alloc_aligned(max(lib().moe_dense_workspace_size(N, K, T), 256), x.device)
+    _check(lib().moe_dense_forward(N, K, _dev_ptr(x, "x", torch.bfloat16), T, _dev_ptr(packed, "packed"),
+                                   _dev_ptr(out, "out", torch.bfloat16), _dev_ptr(workspace, "workspace"),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out

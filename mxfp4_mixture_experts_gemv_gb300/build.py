@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_gb300.so")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
-SOURCES = ["api.cu", "pack.cu", "router_tc.cu", "permute.cu", "expert_gemm.cu", "expert_swap.cu", "route_small.cu", "route_cluster.cu", "stack.cu", "static_scratch.cu"]
+SOURCES = ["api.cu", "pack.cu", "router_tc.cu", "permute.cu", "expert_gemm.cu", "expert_swap.cu", "dense.cu", "route_small.cu", "route_cluster.cu", "stack.cu", "static_scratch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

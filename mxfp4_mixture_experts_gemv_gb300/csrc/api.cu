@@ -369,6 +369,104 @@ moe_status moe_forward_act(moe_dims d, int32_t act_format, const void* hidden, i
   return forward_impl(d, fmt, hidden, T, router_w, router_b, packed, top_k, out, workspace, workspace_bytes, stream);
 }
 
+// ---------------------------------------------------------------- dense MXFP4 linears
+size_t moe_dense_packed_size(int32_t N, int32_t K) {
+  moe::PackedHeader h;
+  return moe::dense_layout(N, K, &h) ? (size_t)h.total : 0;
+}
+
+moe_status moe_dense_quantize_weights(int32_t N, int32_t K, const void* w, void* blocks, void* scales, void* stream) {
+  if (N <= 0 || K <= 0 || K % 32) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "N=%d K=%d (K a multiple of 32)", N, K);
+  if (!w || !blocks || !scales) return fail(MOE_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(w, 16) || !aligned(blocks, 16)) return fail(MOE_ERR_ALIGNMENT, "w and blocks must be 16-byte aligned");
+  cudaError_t e = moe::launch_dense_quantize_weights(N, K, static_cast<const uint16_t*>(w), static_cast<uint8_t*>(blocks),
+                                                     static_cast<uint8_t*>(scales), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "dense weight quantiser");
+  return MOE_OK;
+}
+
+moe_status moe_dense_pack(int32_t N, int32_t K, const void* blocks, const void* scales, const void* bias, void* packed,
+                          size_t packed_bytes, void* stream) {
+  moe::PackedHeader h;
+  if (!moe::dense_layout(N, K, &h))
+    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "N=%d K=%d (N a multiple of 64, K of 32)", N, K);
+  if (!blocks || !scales || !packed) return fail(MOE_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(packed, 256)) return fail(MOE_ERR_ALIGNMENT, "packed buffer must be 256-byte aligned");
+  if (!aligned(blocks, 16)) return fail(MOE_ERR_ALIGNMENT, "blocks must be 16-byte aligned");
+  if (packed_bytes < h.total)
+    return fail(MOE_ERR_BAD_PACKED_HEADER, "packed buffer has %zu bytes, %llu needed", packed_bytes,
+                (unsigned long long)h.total);
+  cudaError_t e = moe::launch_dense_pack(h, static_cast<const uint8_t*>(blocks), static_cast<const uint8_t*>(scales),
+                                         static_cast<const uint16_t*>(bias), static_cast<uint8_t*>(packed),
+                                         static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "dense pack kernels");
+  return MOE_OK;
+}
+
+size_t moe_dense_workspace_size(int32_t N, int32_t K, int32_t T) {
+  moe::DenseWorkspace w;
+  moe::PackedHeader h;
+  if (!moe::dense_layout(N, K, &h) || T < 0 || !moe::dense_workspace(N, K, T, num_sms(), &w)) return 0;
+  return w.total;
+}
+
+moe_status moe_dense_forward(int32_t N, int32_t K, const void* x, int32_t T, const void* packed, void* out,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  moe::PackedHeader h;
+  if (!moe::dense_layout(N, K, &h))
+    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "N=%d K=%d (N a multiple of 64, K of 32)", N, K);
+  if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T=%d < 0", T);
+  if (T == 0) return MOE_OK;
+  if ((int64_t)T * (N > K ? N : K) >= (int64_t)1 << 31) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "T*max(N,K) >= 2^31");
+  if (!x || !packed || !out || !workspace) return fail(MOE_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(x, 16) || !aligned(out, 16)) return fail(MOE_ERR_ALIGNMENT, "x and out must be 16-byte aligned");
+  if (!aligned(packed, 256) || !aligned(workspace, 256))
+    return fail(MOE_ERR_ALIGNMENT, "packed and workspace must be 256-byte aligned");
+  const int sms = num_sms();
+  moe::DenseWorkspace L;
+  moe::dense_workspace(N, K, T, sms, &L);
+  if (workspace_bytes < L.total)
+    return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "workspace has %zu bytes, %zu needed", workspace_bytes, L.total);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const uint8_t* pk = static_cast<const uint8_t*>(packed);
+  // a few tokens on the CUDA cores (the plan may force either path; the measured
+  // default is in dense_cuda_cores_for)
+  const int forced = moe::plan_expert();
+  const bool cores = forced == moe::kExpertCudaCores || (forced == moe::kExpertAuto && moe::dense_cuda_cores_for(T, N, K));
+  if (cores && T > 4) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "the CUDA-core dense path takes at most 4 tokens");
+  cudaError_t e;
+  if (cores) {
+    e = moe::launch_dense_gemv(h, pk, static_cast<const uint16_t*>(x), T, L.k_chunks,
+                               reinterpret_cast<float*>(ws + L.partial), static_cast<uint16_t*>(out), s);
+    if (e != cudaSuccess) return cuda_fail(e, "dense GEMV kernels");
+    return MOE_OK;
+  }
+  int32_t* tiles = reinterpret_cast<int32_t*>(ws + L.tiles);
+  int32_t* inv_pos = reinterpret_cast<int32_t*>(ws + L.inv_pos);
+  e = moe::launch_dense_prep(T, L.tile_rows, L.max_tiles, L.zero_bytes, ws, tiles, inv_pos, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dense grouping kernel");
+  e = moe::launch_gather_quant(static_cast<const uint16_t*>(x), inv_pos, tiles, L.max_tiles, T, 1, K, moe::kActMxfp8,
+                               ws + L.xq, ws + L.xs, ws + L.xp, ws + L.xp_sf, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dense quantiser");
+  moe::ExpertMlpBuffers b = {};
+  b.xp = ws + L.xp;
+  b.xp_sf = ws + L.xp_sf;
+  b.hq = ws + L.xp;      // the down units' activation operand: the quantised input
+  b.hq_sf = ws + L.xp_sf;
+  b.out = static_cast<uint16_t*>(out);
+  b.tiles = tiles;
+  b.inv_pos = inv_pos;
+  b.done_gu = reinterpret_cast<int32_t*>(ws + L.done);
+  b.done_tok = reinterpret_cast<int32_t*>(ws + L.done);
+  b.sched = reinterpret_cast<int32_t*>(ws + L.sched);
+  b.status = reinterpret_cast<uint32_t*>(ws + L.status);
+  b.fused_combine = false;
+  e = moe::launch_expert_mlp(h, pk, b, T, 1, L.max_tiles, L.tile_rows, sms, moe::kActMxfp8, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dense GEMM kernel");
+  return MOE_OK;
+}
+
 moe_status moe_residual_rmsnorm(float* x_res, const void* layer_out, int32_t T, int32_t H, float eps, void* hidden,
                                 void* stream) {
   if (T < 0 || H <= 0 || H % 4 || !(eps > 0.f)) return fail(MOE_ERR_INVALID_ARG, "bad residual/rmsnorm arguments");
@@ -436,7 +534,7 @@ moe_status moe_set_plan(int32_t tile_rows, int32_t route, int32_t expert_kernel)
   if (tile_rows != 0 && tile_rows != 8 && tile_rows != 16 && tile_rows != 32 && tile_rows != 64 && tile_rows != 128)
     return fail(MOE_ERR_INVALID_ARG, "tile_rows=%d is not 0, 8, 16, 32, 64 or 128", tile_rows);
   if (route < MOE_ROUTE_AUTO || route > MOE_ROUTE_TENSOR_CORE) return fail(MOE_ERR_INVALID_ARG, "route=%d", route);
-  if (expert_kernel < MOE_EXPERT_AUTO || expert_kernel > MOE_EXPERT_TOKENS_M)
+  if (expert_kernel < MOE_EXPERT_AUTO || expert_kernel > MOE_EXPERT_CUDA_CORES)
     return fail(MOE_ERR_INVALID_ARG, "expert_kernel=%d", expert_kernel);
   g_plan_tile_rows.store(tile_rows, std::memory_order_relaxed);
   g_plan_route.store(route, std::memory_order_relaxed);

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -39,7 +41,7 @@ constexpr int kTileRowBytes = kTileK / 2;  // packed bytes of one tile row
 // scale per projection).  An NVFP4 buffer holds two scale atoms per k-tile: atom
 // j covers the 16-element blocks 4j..4j+3 of the tile's 128 elements, byte
 // (r%32)*16 + (r/32)*4 + (block%4) for tile row r.
-enum : int32_t { kWeightsMxfp4 = 0, kWeightsNvfp4 = 1 };
+enum : int32_t { kWeightsMxfp4 = 0, kWeightsNvfp4 = 1, kWeightsDense = 2 };
 
 struct PackedHeader {
   uint32_t magic, version;
@@ -86,6 +88,36 @@ inline bool packed_layout(const moe_dims& d, PackedHeader* hd, int32_t wfmt = kW
   return true;
 }
 
+// A dense MXFP4 linear (N outputs, K inputs) packed like one expert's down
+// projection: E = 1, H = N output rows (padded to a multiple of 64; a 64-row tail
+// tile), I = K contraction elements (padded to a multiple of 128), one scale atom
+// per 128 x 128 tile, fp32 bias; no gate_up section.
+inline bool dense_layout(int N, int K, PackedHeader* hd) {
+  if (N <= 0 || K <= 0 || N % 64 || K % 32) return false;
+  PackedHeader h = {};
+  h.magic = kPackedMagic;
+  h.version = kPackedVersion;
+  h.E = 1; h.H = N; h.I = K;
+  h.Hp = (int32_t)round_up(N, kTileK);
+  h.Ip = (int32_t)round_up(K, kTileK);
+  h.gu_mtiles = 0;
+  h.d_mtiles = (int32_t)((N + kTileM - 1) / kTileM);
+  h.gu_ktiles = 0;
+  h.d_ktiles = h.Ip / kTileK;
+  h.gu_rows_stored = 0;
+  h.d_rows_stored = N;
+  h.wfmt = kWeightsDense;
+  uint64_t off = 1024;
+  auto take = [&](uint64_t bytes) { uint64_t o = off; off = (uint64_t)round_up(off + bytes, 1024); return o; };
+  h.off_gu_data = h.off_gu_sf = h.off_gu_bias = off;
+  h.off_d_data = take((uint64_t)h.d_rows_stored * h.d_ktiles * kTileRowBytes);
+  h.off_d_sf = take((uint64_t)h.d_mtiles * h.d_ktiles * kAtomBytes);
+  h.off_d_bias = take((uint64_t)N * 4);
+  h.total = off;
+  *hd = h;
+  return true;
+}
+
 // Row (in 64-byte units) of the first row of data tile (e, m, kt) in the
 // tile-contiguous layout; `rows_stored` rows per expert, the last m-tile may be short.
 __host__ __device__ inline int64_t tile_row0(int e, int m, int kt, int rows_stored, int k_tiles) {
@@ -111,7 +143,7 @@ bool route_cluster_fits(int T, int E, int H);
 // Measurement overrides of the plan (moe_set_plan), process-wide: token rows per
 // tile (0 = automatic) and the routing path (kRouteAuto = automatic).
 enum : int { kRouteAuto = 0, kRouteCluster = 1, kRouteGrid = 2, kRouteTensorCore = 3 };
-enum : int { kExpertAuto = 0, kExpertWeightsM = 1, kExpertTokensM = 2 };
+enum : int { kExpertAuto = 0, kExpertWeightsM = 1, kExpertTokensM = 2, kExpertCudaCores = 3 };
 int plan_tile_rows();
 int plan_route();
 int plan_expert();
@@ -227,6 +259,65 @@ cudaError_t launch_gather_quant(const uint16_t* x, const int32_t* inv_pos, const
 
 cudaError_t launch_residual_rmsnorm(float* x_res, const uint16_t* layer_out, int T, int H, float eps,
                                     uint16_t* hidden, cudaStream_t s);
+
+// Token counts up to this take the dense linears' CUDA-core path by default.
+constexpr int kDenseCudaCoresMaxT = 4;
+
+// Workspace of a dense linear for T tokens: offsets from its base.
+struct DenseWorkspace {
+  size_t status, done, sched, zero_bytes, tiles, inv_pos, xq, xs, xp, xp_sf, partial, total;
+  int max_tiles, tile_rows, k_chunks;
+};
+inline bool dense_workspace(int N, int K, int T, int num_sms, DenseWorkspace* w) {
+  if (N <= 0 || K <= 0 || T < 0) return false;
+  DenseWorkspace d = {};
+  d.tile_rows = tile_rows_for(T, 1, 1);
+  d.max_tiles = T / d.tile_rows + 2;
+  const int kt = (K + kTileK - 1) / kTileK, mt = (N + kTileM - 1) / kTileM;
+  // K chunks of the CUDA-core path: about two CTAs per SM, and at most 96 k-tiles
+  // (4 tokens x 96 x 128 fp32 = 192 KiB of shared memory) per chunk
+  d.k_chunks = std::max((kt + 95) / 96, std::max(1, std::min(kt, (2 * num_sms + mt - 1) / mt)));
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t r = o; o = align256(o + bytes); return r; };
+  d.status = take(16);
+  d.done = take((size_t)d.max_tiles * 4);
+  d.sched = take(16);
+  d.zero_bytes = o;
+  d.tiles = take((size_t)(4 + 4 * d.max_tiles) * 4);
+  d.inv_pos = take((size_t)T * 4);
+  d.xq = take((size_t)T * K);
+  d.xs = take((size_t)T * (K / 16));
+  d.xp = take((size_t)T * K + 256);
+  d.xp_sf = take((size_t)d.max_tiles * kt * 2 * kAtomBytes);
+  d.partial = take((size_t)d.k_chunks * std::min(T, 4) * N * 4);
+  d.total = o;
+  *w = d;
+  return true;
+}
+
+// Dense linear for T tokens on the CUDA cores (else the tensor cores), from the
+// measured crossover on GB300: the GEMV wins by launching fewer kernels while its
+// per-element decode (E2M1 -> f16 -> f32 conversions) costs less than the tensor
+// path's fixed overhead, which holds up to about 2^26 multiply-adds (T * N * K) at
+// T <= 4; the LM head (201,088 x 2880) at T = 1 is already faster on the tensor cores.
+constexpr int64_t kDenseCudaCoresMaxMacs = (int64_t)1 << 26;
+inline bool dense_cuda_cores_for(int T, int N, int K) {
+  return T <= kDenseCudaCoresMaxT && (int64_t)T * N * K <= kDenseCudaCoresMaxMacs;
+}
+
+// Dense linears (dense.cu).
+cudaError_t launch_dense_quantize_weights(int N, int K, const uint16_t* w, uint8_t* blocks, uint8_t* scales,
+                                          cudaStream_t s);
+cudaError_t launch_dense_pack(const PackedHeader& h, const uint8_t* blocks, const uint8_t* scales, const uint16_t* bias,
+                              uint8_t* packed, cudaStream_t s);
+// identity grouping of T tokens in tiles of tile_rows (the tile list and inv_pos),
+// and the zeroing of the workspace's first zero_bytes (status word, counters)
+cudaError_t launch_dense_prep(int T, int tile_rows, int max_tiles, size_t zero_bytes, uint8_t* workspace,
+                              int32_t* tiles, int32_t* inv_pos, cudaStream_t s);
+// CUDA-core path for a few tokens: out (or fp32 partial sums over K chunks) of
+// MXFP8(x) . W^T + b; k_chunks > 1 writes partial[c][t][n] and a second pass sums.
+cudaError_t launch_dense_gemv(const PackedHeader& h, const uint8_t* packed, const uint16_t* x, int T, int k_chunks,
+                              float* partial, uint16_t* out, cudaStream_t s);
 
 struct RouteSmallOut {
   float* logits;

@@ -127,6 +127,7 @@ struct MlpParams {
   int fused_combine;  // the down epilogue also combines the k slots of completed tokens
   const PackedHeader* hdr;   // the packed buffer's header, checked against what this launch expects
   PackedHeader want;         // (magic, version, dims and weight format)
+  int dense;                 // a dense linear: down units only, B = the quantised input, bf16 out + bias
 };
 
 struct TileRef {
@@ -676,10 +677,15 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
                 const int n = c0 + j;
-                if (n < rows)
-                  p.y[(int64_t)(td.y + n) * p.H + orow] =
+                if (n < rows) {
+                  const float v =
                       (NV ? __uint_as_float(j < 16 ? r0[j] : r1[j - 16]) * gs_d : __uint_as_float(j < 16 ? r0[j] : r1[j - 16])) +
                       bias_v;
+                  if (p.dense)  // a dense linear: row td.y + n of the grouped order is that token
+                    p.out[(int64_t)(td.y + n) * p.H + orow] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+                  else
+                    p.y[(int64_t)(td.y + n) * p.H + orow] = v;
+                }
               }
             }
           }
@@ -899,14 +905,17 @@ cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, cons
       }
   }
   if (!hit) {
-  const int64_t gu_rows = (int64_t)h.E * h.gu_rows_stored * h.gu_ktiles;
   const int64_t d_rows = (int64_t)h.E * h.d_rows_stored * h.d_ktiles;
   auto wmap = fp4 ? make_weight_map_packed : make_weight_map;
-  if (!make_weight_map_x2(&m.gu4, packed + h.off_gu_data, (int64_t)h.E * h.gu_rows_stored * h.gu_ktiles, fp4) ||
+  // a dense linear has no gate_up section: its (unused) gate_up maps alias the weights
+  const uint64_t off_gu = h.gu_rows_stored ? h.off_gu_data : h.off_d_data;
+  const int64_t gu_rows = h.gu_rows_stored ? (int64_t)h.E * h.gu_rows_stored * h.gu_ktiles
+                                           : (int64_t)h.E * h.d_rows_stored * h.d_ktiles;
+  if (!make_weight_map_x2(&m.gu4, packed + off_gu, gu_rows, fp4) ||
       !make_weight_map_x2(&m.d4, packed + h.off_d_data, (int64_t)h.E * h.d_rows_stored * h.d_ktiles, fp4))
     return cudaErrorInvalidValue;
-  if (!wmap(&m.gu2, packed + h.off_gu_data, gu_rows, 2 * kTileM) ||
-      !wmap(&m.gu, packed + h.off_gu_data, gu_rows, kTileM) || !wmap(&m.gut, packed + h.off_gu_data, gu_rows, 64) ||
+  if (!wmap(&m.gu2, packed + off_gu, gu_rows, 2 * kTileM) || !wmap(&m.gu, packed + off_gu, gu_rows, kTileM) ||
+      !wmap(&m.gut, packed + off_gu, gu_rows, 64) ||
       !wmap(&m.d2, packed + h.off_d_data, d_rows, 2 * kTileM) || !wmap(&m.d, packed + h.off_d_data, d_rows, kTileM) ||
       !wmap(&m.dt, packed + h.off_d_data, d_rows, 64))
     return cudaErrorInvalidValue;
@@ -960,6 +969,7 @@ cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, cons
   p.fused_combine = b.fused_combine ? 1 : 0;
   p.hdr = reinterpret_cast<const PackedHeader*>(packed);
   p.want = h;
+  p.dense = h.wfmt == kWeightsDense ? 1 : 0;
   const int grid = (int)std::min<int64_t>(num_sms, (int64_t)max_tiles * (h.gu_mtiles + h.d_mtiles));
   switch (tile_rows) {
     case 8: return fmt == kActNvfp4 ? launch_bn<8, true, true>(m, p, grid, s)

@@ -146,7 +146,7 @@ def test_wait_limit_and_hold_mask_are_checked_on_host(L):
 def test_plan_override_is_checked_and_sizes_follow_it(L):
     assert L.moe_set_plan(12, 0, 0) == 1           # not a tile height the kernels have
     assert L.moe_set_plan(0, 7, 0) == 1            # unknown routing path
-    assert L.moe_set_plan(0, 0, 3) == 1            # unknown expert kernel
+    assert L.moe_set_plan(0, 0, 4) == 1            # unknown expert kernel
     base = moe.workspace_layout(GPT, 1024, 4)
     assert base.tile_rows == 64
     try:
@@ -162,3 +162,46 @@ def test_plan_override_is_checked_and_sizes_follow_it(L):
 def test_forward_act_rejects_unknown_formats(L):
     assert L.moe_forward_act(GPT.c(), 3, FAKE, 4, FAKE, FAKE, FAKE, 4, FAKE, FAKE, 1 << 40, None) == 1
     assert b"activation format" in L.moe_last_error()
+
+
+def test_dense_sizes_and_host_checks(L):
+    # packed: 1 KiB header, then 64-byte rows per 128-wide k-tile (K padded to 128),
+    # 512-byte scale atoms per (128-row, 128-wide) tile, fp32 biases; 1 KiB sections
+    N, K = 320, 288
+    kt, mt = 3, 3
+    up = lambda b: (b + 1023) // 1024 * 1024
+    want = 1024 + up(N * kt * 64) + up(mt * kt * 512) + up(N * 4)
+    assert L.moe_dense_packed_size(N, K) == want
+    assert L.moe_dense_packed_size(100, 256) == 0    # N a multiple of 64
+    assert L.moe_dense_packed_size(128, 250) == 0    # K a multiple of 32
+    assert L.moe_dense_workspace_size(128, 256, -1) == 0
+    assert L.moe_dense_quantize_weights(128, 250, FAKE, FAKE, FAKE, None) == 2
+    assert L.moe_dense_quantize_weights(128, 256, None, FAKE, FAKE, None) == 1
+    assert L.moe_dense_quantize_weights(128, 256, FAKE + 2, FAKE, FAKE, None) == 3
+    n = L.moe_dense_packed_size(128, 256)
+    assert L.moe_dense_pack(100, 256, FAKE, FAKE, None, FAKE, n, None) == 2
+    assert L.moe_dense_pack(128, 256, None, FAKE, None, FAKE, n, None) == 1
+    assert L.moe_dense_pack(128, 256, FAKE, FAKE, None, FAKE + 64, n, None) == 3
+    assert L.moe_dense_pack(128, 256, FAKE, FAKE, None, FAKE, n - 1, None) == 5
+    ws = L.moe_dense_workspace_size(128, 256, 4)
+    assert ws > 0
+    fwd = lambda **kw: L.moe_dense_forward(kw.get("N", 128), 256, kw.get("x", FAKE), kw.get("T", 4), kw.get("pk", FAKE),
+                                           kw.get("out", FAKE), kw.get("ws", FAKE), kw.get("ws_bytes", ws), None)
+    assert fwd(N=100) == 2
+    assert fwd(T=-1) == 1
+    assert fwd(T=0) == 0                             # no-op
+    assert fwd(x=0) == 1 and fwd(out=0) == 1
+    assert fwd(x=FAKE + 8) == 3 and fwd(pk=FAKE + 16) == 3
+    assert fwd(ws_bytes=ws - 1) == 4
+    try:
+        moe.set_plan(0, "auto", "cuda_cores")
+        assert fwd(T=5, ws_bytes=1 << 30) == 2 and b"at most 4 tokens" in L.moe_last_error()
+    finally:
+        moe.set_plan(0, "auto")
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU failure path")
+def test_dense_forward_fails_loudly_without_a_gpu(L):
+    ws = L.moe_dense_workspace_size(128, 256, 4)
+    assert L.moe_dense_forward(128, 256, FAKE, 4, FAKE, FAKE, FAKE, ws, None) == 6
+    assert b"cudaError" in L.moe_last_error()
