@@ -85,7 +85,8 @@ typedef struct {
   size_t status;       /* uint32 [4]: device status words (0 = ok)                  */
   size_t done_gu;      /* int32 [max_tiles]: finished gate_up tiles per token tile  */
   size_t done_tok;     /* int32 [T, ceil(H/128)]: finished down slots per block     */
-  size_t grid_bar;     /* int32[2]: grid routing arrivals, expert tiles claimed     */
+  size_t grid_bar;     /* int32[4]: grid routing arrivals, expert tiles claimed,
+                          cluster routing's tile-list flag and finished-CTA count */
   size_t zero_bytes;   /* bytes from offset 0 the forward zeroes before it starts   */
   size_t logits;       /* fp32 [T, E] router logits                                 */
   size_t topk_ids;     /* int32 [T, k]                                              */
@@ -282,7 +283,9 @@ uint64_t moe_get_wait_limit_ns(void);
  *                                   more gate_up completion than exists;
  *   MOE_DEBUG_HOLD_ROUTING_BARRIER  the small-batch routing grid (8 < T <= 32)
  *                                   waits at its grid barrier for one more CTA
- *                                   than it has.
+ *                                   than it has; after the cluster routing kernel
+ *                                   (T <= 8) the expert kernel waits for one more
+ *                                   routing CTA than published its grouped rows.
  * Such a forward reports MOE_ERR_TIMEOUT through moe_get_device_status after a
  * few wait limits (pair the hook with a short moe_set_wait_limit_ns), its output
  * is not valid, and the device stays usable.  0 restores normal forwards.

@@ -251,6 +251,7 @@ moe_status forward_impl(moe_dims d, int fmt, const void* hidden, int32_t T, cons
     if (pev) cudaEventRecordWithFlags(pev[i], s, cudaEventRecordExternal);
   };
   mark(0);
+  int route_ctas = 0;  // routing CTAs that publish through the flags (cluster path)
   if (cluster_route) {
     // a few tokens: routing, grouping and quantise-on-gather in one cluster
     moe::RouteClusterOut o;
@@ -269,8 +270,10 @@ moe_status forward_impl(moe_dims d, int fmt, const void* hidden, int32_t T, cons
     o.zero = reinterpret_cast<uint32_t*>(ws);
     o.zero_words = (int)(L.zero_bytes / 4);
     o.status = status;
+    o.flags = reinterpret_cast<int32_t*>(at(L.grid_bar)) + 2;
     e = moe::launch_route_cluster(static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(router_w),
-                                  static_cast<const uint16_t*>(router_b), T, d.H, d.E, top_k, L.tile_rows, fp4, o, s);
+                                  static_cast<const uint16_t*>(router_b), T, d.H, d.E, top_k, L.tile_rows, fp4, o,
+                                  &route_ctas, s);
     if (e != cudaSuccess) return cuda_fail(e, "cluster routing kernel");
   } else if (route == moe::kRouteGrid) {
     // decode: routing, quantisation, grouping and gather in one launch
@@ -310,7 +313,7 @@ moe_status forward_impl(moe_dims d, int fmt, const void* hidden, int32_t T, cons
     if (e != cudaSuccess) return cuda_fail(e, "gather kernel");
   }
   mark(1);
-  moe::ExpertMlpBuffers b;
+  moe::ExpertMlpBuffers b = {};
   b.xp = at(L.xp);
   b.xp_sf = at(L.xp_sf);
   b.hq = at(L.hq);
@@ -325,6 +328,12 @@ moe_status forward_impl(moe_dims d, int fmt, const void* hidden, int32_t T, cons
   b.done_tok = reinterpret_cast<int32_t*>(at(L.done_tok));
   b.sched = reinterpret_cast<int32_t*>(at(L.grid_bar)) + 1;  // word 0 is the grid routing barrier
   b.status = status;
+  // The expert kernel follows the cluster routing kernel through the flags (words 2
+  // and 3 of the section): weight copies once the tile list is published, activation
+  // copies once every routing CTA has written its grouped rows.  A debug hold asks it
+  // to wait for one routing CTA more than there are.
+  b.route_flags = reinterpret_cast<int32_t*>(at(L.grid_bar)) + 2;
+  b.route_ctas = route_ctas == 0 ? 0 : route_ctas + ((moe::debug_hold_waits() & MOE_DEBUG_HOLD_ROUTING_BARRIER) ? 1 : 0);
   // A few tokens: the down epilogue combines (no extra launch on the decode path).
   // Many tokens: a streaming pass after the expert kernel, which would otherwise
   // stall on the slot loads of every completed token.

@@ -355,9 +355,12 @@ struct RouteClusterOut {
   uint32_t* zero;  // the workspace's zero-initialised words, cleared by the kernel
   int zero_words;
   uint32_t* status;
+  int32_t* flags;  // two words inside the zero-initialised ones: tile list published, CTAs done
 };
+// *ctas: the routing CTAs the launch runs (the count the second flag reaches)
 cudaError_t launch_route_cluster(const uint16_t* x, const uint16_t* wr, const uint16_t* br, int T, int H, int E,
-                                 int k, int tile_rows, bool fp4, const RouteClusterOut& o, cudaStream_t s);
+                                 int k, int tile_rows, bool fp4, const RouteClusterOut& o, int* ctas,
+                                 cudaStream_t s);
 
 struct ExpertMlpBuffers {
   const uint8_t* xp;        // gate_up B rows [TK][H]
@@ -375,6 +378,12 @@ struct ExpertMlpBuffers {
   int32_t* sched;  // tile claim counter, zero at launch
   uint32_t* status;
   bool fused_combine;  // false: launch_combine sums the slots after the expert kernel
+  // Routing that publishes its results through two flags (tile list, then CTAs
+  // whose grouped rows are written) while it still runs: the expert kernel starts
+  // its weight copies on the first and its activation copies when the second
+  // reaches route_ctas.  route_ctas = 0: the routing grid completes first.
+  const int32_t* route_flags;
+  int route_ctas;
 };
 // out[t] = bf16(sum_j w[t][j] * y[inv_pos[t][j]]), slots in order, fp32 sums.
 cudaError_t launch_combine(const float* y, const int32_t* inv_pos, const float* topk_w, int T, int k, int H,

@@ -10,22 +10,10 @@ namespace moe {
 
 // Where a bounded wait expired: role (1 producer/empty, 2 mma/accumulator, 3 mma/full,
 // 4 epilogue, 5 producer/dependency, 6 producer/tile queue, 7 mma/tile queue; 8 is the
-// cluster routing kernel's copies), tile (or queue position) and k-step, packed for the
+// cluster routing kernel's copies, 9 the expert kernel's wait for the routing flags), tile (or queue position) and k-step, packed for the
 // second status word.
 __device__ __forceinline__ uint32_t wait_site(uint32_t role, int tile, int kt) {
   return (role << 28) | ((uint32_t)min(tile, 0xFFFF) << 12) | (uint32_t)min(kt, 0xFFF);
-}
-
-__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Release increment: every write that happens-before it (this CTA's, ordered by
-// the preceding barrier) is visible to whoever acquires the counter.
-__device__ __forceinline__ void red_add_release_gpu(int32_t* p, int v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Increment with acquire and release: returns the previous value; the caller sees

@@ -128,6 +128,9 @@ struct MlpParams {
   const PackedHeader* hdr;   // the packed buffer's header, checked against what this launch expects
   PackedHeader want;         // (magic, version, dims and weight format)
   int dense;                 // a dense linear: down units only, B = the quantised input, bf16 out + bias
+  int max_tiles;             // capacity of the tile list (entries past its count are not meaningful)
+  const int32_t* route_flags;  // routing still running: [0] tile list published, [1] CTAs done
+  int route_ctas;              // the count [1] reaches; 0 = the routing grid completed first
 };
 
 struct TileRef {
@@ -212,15 +215,42 @@ __global__ void __launch_bounds__(192, 1)
     }
   }
   __syncwarp();
-  // Everything above overlaps the previous kernel (programmatic dependent
-  // launch); the tile list and activations it produced are read only after this.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  // a packed buffer of other dims or another weight format runs no unit
+  // The packed buffer was written before the previous kernel began, so its header
+  // can be read while that kernel runs.  A buffer of other dims or another weight
+  // format runs no unit.
   const PackedHeader& hd = *p.hdr;
   const bool hdr_ok = hd.magic == p.want.magic && hd.version == p.want.version && hd.E == p.want.E &&
                       hd.H == p.want.H && hd.I == p.want.I && hd.wfmt == p.want.wfmt;
+  // Everything above overlaps the previous kernel (programmatic dependent
+  // launch).  Its tile list is read only after that grid completes, or, for a
+  // routing kernel that publishes its results while it runs, after its first flag
+  // (the grouped activations then wait for the second, in the producer).
+  // Every counter of the forward, the claim counter included, was cleared before
+  // this kernel could start (by a memset or a kernel earlier in the stream, or by
+  // the cluster routing kernel before it let this one launch), so the first claim
+  // is taken now, while the routing results are still on their way.
+  int first_claim = 0;
+  if (warp == 0 && lane == 0) first_claim = atomicAdd(p.sched, 1);
+  __shared__ int s_routed;
+  bool routed = true;
+  if (p.route_ctas == 0) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+  } else {
+    if (threadIdx.x == 0) {
+      bool got = ld_acquire_gpu(p.route_flags) != 0;
+      const uint64_t t0 = global_timer_ns();
+      while (!got && global_timer_ns() - t0 <= p.wait_ns) got = ld_acquire_gpu(p.route_flags) != 0;
+      if (!got) {
+        atomicOr(p.status, kStatusTimeoutProducer);
+        atomicCAS(p.status + 1, 0u, wait_site(9, 0, 0));
+      }
+      s_routed = got ? 1 : 0;
+    }
+    __syncthreads();
+    routed = s_routed != 0;
+  }
   if (!hdr_ok && threadIdx.x == 0) atomicOr(p.status, kStatusBadWeights);
-  const int n_btiles = hdr_ok ? p.tiles[0] : 0;
+  const int n_btiles = hdr_ok && routed ? p.tiles[0] : 0;
   const int n_gu = n_btiles * p.gu_mtiles;
   const int total = n_gu + n_btiles * p.d_mtiles;
   const int4* tl = reinterpret_cast<const int4*>(p.tiles + 4);
@@ -232,14 +262,28 @@ __global__ void __launch_bounds__(192, 1)
     int64_t issued = 0;
     bool ok = true;
     const uint64_t wpol = l2_policy(p.weights_evict_first != 0);
-    // Units are claimed from the counter in increasing order, the first one at
-    // the start; later claims are issued several stages before the current
+    // Units are claimed from the counter in increasing order, the first one before
+    // the routing results are read; later claims are issued several stages before the current
     // unit's last loads and their descriptor fetched two stages before them, so
     // neither round trip stalls the copies.
-    int claim = 0;
-    if (lane == 0) claim = atomicAdd(p.sched, 1);
+    // The first claim and the first tile-list entries travel together: lane i
+    // loads entry i, so a first unit among them needs no further round trip.
+    bool xp_ready = p.route_ctas == 0;  // the grouped activations may be read
+    int claim = first_claim;
+    const int4 pre = lane < min(p.max_tiles, 32) ? tl[lane] : make_int4(0, 0, 0, 0);
     int tile = __shfl_sync(0xffffffffu, claim, 0);
-    int4 td_next = tile < total ? tl[tile_ref(tile, n_gu, p).b] : make_int4(0, 0, 0, 0);
+    int4 td_next = make_int4(0, 0, 0, 0);
+    if (tile < total) {
+      const int b0 = tile_ref(tile, n_gu, p).b;
+      if (b0 < 32) {
+        td_next.x = __shfl_sync(0xffffffffu, pre.x, b0);
+        td_next.y = __shfl_sync(0xffffffffu, pre.y, b0);
+        td_next.z = __shfl_sync(0xffffffffu, pre.z, b0);
+        td_next.w = __shfl_sync(0xffffffffu, pre.w, b0);
+      } else {
+        td_next = tl[b0];
+      }
+    }
     for (int i = 0; ok; ++i) {
       const int4 td = td_next;
       // hand the tile (or the end, -1) to the MMA and epilogue warps
@@ -308,9 +352,15 @@ __global__ void __launch_bounds__(192, 1)
       // counted.  If it is not ready yet, the unit's first stages get their weight
       // copies only, and the activation copies of those stages follow the
       // (bounded) wait.
-      const int dep_target = p.gu_mtiles + p.dep_extra;
-      bool dep_ok = r.gu || __all_sync(0xffffffffu, ld_acquire_gpu(p.done_gu + r.b) >= dep_target);
-      if (!r.gu && dep_ok) fence_proxy_async_global();  // hq was written by generic stores; TMA reads it
+      // (a gate_up unit's grouped activations are ready once every routing CTA that
+      // publishes through the flags has counted in)
+      const int32_t* dep_ctr = r.gu ? p.route_flags + 1 : p.done_gu + r.b;
+      const int dep_target = r.gu ? p.route_ctas : p.gu_mtiles + p.dep_extra;
+      // (until a gate_up unit has seen the routing flag, its first stages stream
+      // weights only and the flag is read after their copies are out)
+      bool dep_ok = r.gu ? xp_ready : __all_sync(0xffffffffu, ld_acquire_gpu(dep_ctr) >= dep_target);
+      // hq and the flagged xp were written by generic stores; TMA reads them
+      if (dep_ok && (!r.gu || p.route_ctas != 0)) fence_proxy_async_global();
       bool dep_timeout = false;
       int pend_s = 0, pend_kt = 0, pend_n = 0;  // stages waiting for their activation copies
       // activation copies of the stages that wait for them.  After an expired wait
@@ -367,19 +417,20 @@ __global__ void __launch_bounds__(192, 1)
             pend_kt = kt;
           }
           ++pend_n;
-          dep_ok = __all_sync(0xffffffffu, ld_acquire_gpu(p.done_gu + r.b) >= dep_target);
-          // keep streaming weights while the intermediate is not ready, until every
+          dep_ok = __all_sync(0xffffffffu, ld_acquire_gpu(dep_ctr) >= dep_target);
+          // keep streaming weights while the activations are not ready, until every
           // stage slot is taken or this is the unit's last stage
           if (!dep_ok && (pend_n >= S || kt + kKS >= k_tiles)) {
-            if (!wait_counter_warp(p.done_gu + r.b, dep_target, p.wait_ns)) {
+            if (!wait_counter_warp(dep_ctr, dep_target, p.wait_ns)) {
               if (lane == 0) {
                 atomicOr(p.status, kStatusTimeoutProducer);
-                atomicCAS(p.status + 1, 0u, wait_site(5, tile, kt));
+                atomicCAS(p.status + 1, 0u, wait_site(r.gu ? 9 : 5, tile, kt));
               }
               dep_timeout = true;
             }
             dep_ok = true;
           }
+          if (dep_ok && r.gu) xp_ready = true;
           if (dep_ok) flush_pending();
         }
         ++issued;
@@ -755,6 +806,8 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // a routing grid followed through its flags completes before this one does
+  if (p.route_ctas != 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <int BN, bool FP4, bool NV>
@@ -951,6 +1004,9 @@ cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, cons
   p.done_gu = b.done_gu;
   p.done_tok = b.done_tok;
   p.sched = b.sched;
+  p.max_tiles = max_tiles;
+  p.route_flags = b.route_flags;
+  p.route_ctas = b.route_ctas;
   p.status = b.status;
   p.wait_ns = wait_limit_ns();
   p.dep_extra = (debug_hold_waits() & MOE_DEBUG_HOLD_DOWN_UNITS) ? 1 : 0;

@@ -52,6 +52,7 @@ struct RouteClusterArgs {
   uint32_t* zero;  // words cleared for this forward (status and the expert kernel's counters)
   int zero_words;
   uint32_t* status;
+  int32_t* flags;  // [0] tile list published, [1] routing CTAs whose grouped rows are written
   uint64_t wait_ns;
   int fp4;  // activation format: 0 MXFP8 (32 code bytes per block), 1 MXFP4 (16)
 };
@@ -95,8 +96,6 @@ __global__ void __launch_bounds__(kRcThreads, 1) route_cluster_kernel(const Rout
   __shared__ float s_w[TM * 8];
   __shared__ int s_off[256], s_toff[256];  // of the experts the pairs use
   __shared__ __align__(8) uint64_t s_bar;
-  // the expert kernel may start its prologue now; it waits for this grid's results
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = a.T, H = a.H, E = a.E, k = a.k, TK = T * k;
   const int rank = (int)cluster_ctarank(), ncta = (int)cluster_nctarank();
@@ -111,17 +110,23 @@ __global__ void __launch_bounds__(kRcThreads, 1) route_cluster_kernel(const Rout
     mbar_arrive_expect_tx(&s_bar, bw + bx);
     if (bw) bulk_g2s(s_wr, a.wr + (int64_t)e0 * H, bw, &s_bar);
     bulk_g2s(s_x, a.x, bx, &s_bar);
-    // this forward's status words, cleared before the cluster barrier that orders
-    // them before any report
-    if (rank == 0) *reinterpret_cast<uint4*>(a.zero) = make_uint4(0u, 0u, 0u, 0u);
   }
-  // the 256 bytes after the last grouped row are read (as zero padding) by the
-  // expert kernel's k-tile-plane boxes: keep them zero
-  if (rank == 0 && tid >= 32 && tid < 48)
-    reinterpret_cast<uint4*>(a.xp + (int64_t)TK * (H >> a.fp4))[tid - 32] = make_uint4(0, 0, 0, 0);
+  // The expert kernel may start once every CTA has let it (programmatic dependent
+  // launch).  It then follows this grid through the two flags, so CTA 0 first
+  // clears them, this forward's status words and the expert kernel's counters
+  // (while the copies are in flight), and makes that visible.
+  if (rank == 0) {
+    for (int i = tid; i < a.zero_words; i += kRcThreads) a.zero[i] = 0u;
+    // the 256 bytes after the last grouped row are read (as zero padding) by the
+    // expert kernel's k-tile-plane boxes: keep them zero
+    if (tid >= 32 && tid < 48)
+      reinterpret_cast<uint4*>(a.xp + (int64_t)TK * (H >> a.fp4))[tid - 32] = make_uint4(0, 0, 0, 0);
+    __threadfence();
+  }
   // biases of this CTA's experts (in flight with the copies)
   if (tid < ne) s_bias[tid] = __uint_as_float((uint32_t)a.br[e0 + tid] << 16);
-  __syncthreads();  // the barrier's initialisation is visible to every thread
+  __syncthreads();  // the barrier's initialisation (and CTA 0's clearing) is visible to every thread
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const bool staged = mbar_wait(&s_bar, 0, a.wait_ns);
 
   // logits of this CTA's experts, kG at a time: thread = 16-byte column chunk(s),
@@ -185,7 +190,6 @@ __global__ void __launch_bounds__(kRcThreads, 1) route_cluster_kernel(const Rout
     store_block_codes(a.xq + (int64_t)ut * (H >> a.fp4) + ukb * (32 >> a.fp4), qc, a.fp4);
     a.xs[(int64_t)ut * nbh + ukb] = qs;
   }
-  for (int i = 4 + rank + ncta * tid; i < a.zero_words; i += ncta * kRcThreads) a.zero[i] = 0u;
 
   cluster_wait();  // every CTA has every logit; no CTA touches another's shared memory after this
   if (!staged && tid == 0) {
@@ -195,7 +199,14 @@ __global__ void __launch_bounds__(kRcThreads, 1) route_cluster_kernel(const Rout
   for (int t = warp; t < T; t += kRcThreads / 32) topk_softmax_warp(s_log[t], E, k, s_ids + t * k, s_w + t * k, lane);
   __syncthreads();
   if (warp == 0) {
-    group_pairs_small_warp(s_ids, TK, a.tshift, s_off, s_toff, s_sorted, s_inv, rank == 0 ? a.tiles : nullptr, lane);
+    group_pairs_small_warp(s_ids, TK, E, a.tshift, s_off, s_toff, s_sorted, s_inv, rank == 0 ? a.tiles : nullptr, lane);
+    if (rank == 0) {
+      // publish the tile list (the counters were cleared and fenced at the start):
+      // the expert kernel may now read it and start its weight copies.  The release
+      // store orders the warp's tile writes, ordered before it by the warp barrier.
+      __syncwarp();
+      if (lane == 0) st_release_gpu(a.flags, 1);
+    }
   } else {
     // meanwhile: this CTA's experts' logits, and (CTA 0) the selection and the
     // per-expert counts and offsets (stage outputs)
@@ -233,6 +244,12 @@ __global__ void __launch_bounds__(kRcThreads, 1) route_cluster_kernel(const Rout
         for (int jj = (ukb & 3) + 1; jj < 4; ++jj) wd[jj] = 127;
     }
   }
+  // this CTA's grouped rows and scale bytes (and CTA 0's weights and permutation,
+  // which the combine reads) are written: count it in, so that the expert kernel's
+  // activation copies may read them
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) red_add_release_gpu(a.flags + 1, 1);
 }
 
 int g_cluster_size[64];  // per device: 0 = not chosen yet
@@ -248,7 +265,7 @@ bool route_cluster_fits(int T, int E, int H) {
 }
 
 cudaError_t launch_route_cluster(const uint16_t* x, const uint16_t* wr, const uint16_t* br, int T, int H, int E,
-                                 int k, int tile_rows, bool fp4, const RouteClusterOut& o, cudaStream_t s) {
+                                 int k, int tile_rows, bool fp4, const RouteClusterOut& o, int* ctas, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -289,7 +306,8 @@ cudaError_t launch_route_cluster(const uint16_t* x, const uint16_t* wr, const ui
   const int epc = (E + csize - 1) / csize;
   RouteClusterArgs a{x, wr, br, T, H, E, k, __builtin_ctz((unsigned)tile_rows), o.logits, o.ids, o.w, o.xq, o.xs,
                      o.counts, o.offsets, o.sorted_rows, o.inv_pos, o.tiles, o.xp, o.xp_sf, o.zero,
-                     o.zero_words, o.status, wait_limit_ns(), fp4 ? 1 : 0};
+                     o.zero_words, o.status, o.flags, wait_limit_ns(), fp4 ? 1 : 0};
+  *ctas = csize;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(csize);
   cfg.blockDim = dim3(kRcThreads);

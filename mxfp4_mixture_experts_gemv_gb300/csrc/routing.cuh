@@ -98,69 +98,77 @@ __device__ __forceinline__ void group_pairs_warp(const int32_t* ids, int TK, int
   }
 }
 
-// Warp: the same grouping for at most 64 pairs, by ranking instead of counting.
-// Pair f's key (expert << 6 | f) is unique, so its rank among all keys is its
-// grouped row (stable within an expert); the pairs of smaller experts give the
-// expert's offset, the pairs of the same expert its count, and the first pair of
-// every used expert places that expert's tiles after the tiles of the smaller
-// used experts.  Writes sorted[p], inv[f], and for every used expert e off[e] and
-// toff[e]; when `tiles` is given also the tile list ({expert, row0, rows, 0} at
-// tiles + 4 + 4i, the count in tiles[0]).  Nothing here touches experts no pair
-// uses.
-__device__ __forceinline__ void group_pairs_small_warp(const int32_t* ids, int TK, int tshift, int* off, int* toff,
-                                                       int* sorted, int* inv, int32_t* tiles, int lane) {
+// Warp: the same grouping for at most 64 pairs (lane l holds pairs l and l + 32)
+// and E <= 256 experts, without a pass over the pairs per pair.  A pair's grouped
+// row is its expert's offset plus the number of earlier pairs (smaller f) of the
+// same expert: within each half of the pairs that ordinal comes from the lanes
+// holding the same expert (match.any), and the second half adds the first half's
+// count of that expert.  The per-expert counts are a histogram in off[], turned
+// into exclusive offsets, together with the tile offsets, by one warp scan over
+// the experts (lane l holds experts l*per .. l*per + per - 1).  Writes sorted[p],
+// inv[f], off[e] and toff[e] for every e < E; when `tiles` is given also the tile
+// list ({expert, row0, rows, 0} at tiles + 4 + 4i, the count in tiles[0]).
+__device__ __forceinline__ void group_pairs_small_warp(const int32_t* ids, int TK, int E, int tshift, int* off,
+                                                       int* toff, int* sorted, int* inv, int32_t* tiles, int lane) {
   const int f0 = lane, f1 = lane + 32;
-  const int id0 = f0 < TK ? ids[f0] : 0x3FFFFFF, id1 = f1 < TK ? ids[f1] : 0x3FFFFFF;
-  const int key0 = f0 < TK ? (id0 << 6) | f0 : 0x7FFFFFFF, key1 = f1 < TK ? (id1 << 6) | f1 : 0x7FFFFFFF;
-  int rank0 = 0, rank1 = 0, less0 = 0, less1 = 0, same0 = 0, same1 = 0;
-  for (int g = 0; g < 32; ++g) {
-    const int ka = __shfl_sync(0xffffffffu, key0, g), kb = __shfl_sync(0xffffffffu, key1, g);
-    const int ia = ka >> 6, ib = kb >> 6;
-    rank0 += (ka < key0) + (kb < key0);
-    rank1 += (ka < key1) + (kb < key1);
-    less0 += (ia < id0) + (ib < id0);
-    less1 += (ia < id1) + (ib < id1);
-    same0 += (ia == id0) + (ib == id0);
-    same1 += (ia == id1) + (ib == id1);
-  }
+  const bool v0 = f0 < TK, v1 = f1 < TK;
+  const int id0 = v0 ? ids[f0] : 0, id1 = v1 ? ids[f1] : 0;
+  for (int e = lane; e < E; e += 32) off[e] = 0;
+  __syncwarp();
+  // lanes without a pair get keys no expert has
+  const unsigned lt = (1u << lane) - 1u;
+  const unsigned m0 = __match_any_sync(0xffffffffu, v0 ? id0 : -1 - lane);
+  const unsigned m1 = __match_any_sync(0xffffffffu, v1 ? id1 : -1 - lane);
+  if (v0 && (m0 & lt) == 0) off[id0] = __popc(m0);  // first-half count, by the group's first lane
+  __syncwarp();
+  const int ord0 = __popc(m0 & lt);
+  const int ord1 = v1 ? off[id1] + __popc(m1 & lt) : 0;
+  __syncwarp();
+  if (v1 && (m1 & lt) == 0) off[id1] += __popc(m1);  // plus the second half's
+  __syncwarp();
+  // exclusive scan of (tiles << 16 | count) over the experts
+  const int per = (E + 31) >> 5, e_lo = lane * per;
   const int tr = 1 << tshift;
-  // the first pair of each used expert carries its tile count
-  const bool first0 = f0 < TK && rank0 == less0, first1 = f1 < TK && rank1 == less1;
-  const int tc0 = first0 ? (same0 + tr - 1) >> tshift : 0, tc1 = first1 ? (same1 + tr - 1) >> tshift : 0;
-  int tpre0 = 0, tpre1 = 0;
-  for (int g = 0; g < 32; ++g) {
-    const int ia = __shfl_sync(0xffffffffu, id0, g), ib = __shfl_sync(0xffffffffu, id1, g);
-    const int ta = __shfl_sync(0xffffffffu, tc0, g), tb = __shfl_sync(0xffffffffu, tc1, g);
-    tpre0 += (ia < id0 ? ta : 0) + (ib < id0 ? tb : 0);
-    tpre1 += (ia < id1 ? ta : 0) + (ib < id1 ? tb : 0);
-  }
-  if (f0 < TK) {
-    sorted[rank0] = f0;
-    inv[f0] = rank0;
-  }
-  if (f1 < TK) {
-    sorted[rank1] = f1;
-    inv[f1] = rank1;
-  }
-  if (first0) {
-    off[id0] = less0;
-    toff[id0] = tpre0;
-    if (tiles)
-      for (int i = 0; i < tc0; ++i)
-        reinterpret_cast<int4*>(tiles + 4)[tpre0 + i] = make_int4(id0, less0 + i * tr, min(tr, same0 - i * tr), 0);
-  }
-  if (first1) {
-    off[id1] = less1;
-    toff[id1] = tpre1;
-    if (tiles)
-      for (int i = 0; i < tc1; ++i)
-        reinterpret_cast<int4*>(tiles + 4)[tpre1 + i] = make_int4(id1, less1 + i * tr, min(tr, same1 - i * tr), 0);
-  }
-  if (tiles) {
-    int n = tc0 + tc1;
+  int cnt[8];
+  int mine = 0;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
-    if (lane == 0) tiles[0] = n;
+  for (int i = 0; i < 8; ++i) {
+    const int e = e_lo + i;
+    cnt[i] = i < per && e < E ? off[e] : 0;
+    mine += (((cnt[i] + tr - 1) >> tshift) << 16) + cnt[i];
+  }
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  int run = incl - mine;
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = e_lo + i;
+    if (i < per && e < E) {
+      const int o = run & 0xFFFF, to = run >> 16;
+      off[e] = o;
+      toff[e] = to;
+      if (tiles)
+        for (int t = 0; t * tr < cnt[i]; ++t)
+          reinterpret_cast<int4*>(tiles + 4)[to + t] = make_int4(e, o + t * tr, min(tr, cnt[i] - t * tr), 0);
+      run += (((cnt[i] + tr - 1) >> tshift) << 16) + cnt[i];
+    }
+  }
+  if (tiles && lane == 31) tiles[0] = incl >> 16;
+  __syncwarp();
+  if (v0) {
+    const int r = off[id0] + ord0;
+    sorted[r] = f0;
+    inv[f0] = r;
+  }
+  if (v1) {
+    const int r = off[id1] + ord1;
+    sorted[r] = f1;
+    inv[f1] = r;
   }
 }
 

@@ -55,9 +55,14 @@ def test_held_down_units_time_out_and_the_device_stays_usable(T):
     _normal_forward_meets_the_oracle(inp, dev, packed)
 
 
-def test_held_routing_barrier_times_out_and_the_device_stays_usable():
-    shape = ms.LayerShape(T=20, H=256, I=256, E=8, k=2)  # the small-batch grid routing path
-    inp, dev, packed, st = _forward_with_held_waits(shape, moe.HOLD_ROUTING_BARRIER, seed=41)
+@pytest.mark.parametrize("T", [20, 4], ids=["grid_route_barrier", "cluster_route_flags"])
+def test_held_routing_barrier_times_out_and_the_device_stays_usable(T):
+    """T = 20: the small-batch routing grid waits at its barrier for one CTA more
+    than it has.  T = 4: the expert kernel waits for one more cluster-routing CTA
+    than published its grouped rows (the flag it follows the running routing by)."""
+    shape = ms.LayerShape(T=T, H=256, I=256, E=8, k=2)
+    inp, dev, packed, st = _forward_with_held_waits(shape, moe.HOLD_ROUTING_BARRIER, seed=41 + T)
     assert st == 7, moe.STATUS_NAMES.get(st, st)
+    assert "device wait expired" in moe.lib().moe_last_error().decode()
     _normal_forward_meets_the_oracle(inp, dev, packed)
 
