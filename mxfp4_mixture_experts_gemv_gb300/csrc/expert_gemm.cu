@@ -57,8 +57,14 @@ namespace {
 // faster (measured with the same copies alone: three stages of four k-tiles
 // reach 6.8 TB/s where six stages of two reach 5.9 TB/s), so the smallest token
 // tile, whose activation slots are small, takes four k-tiles per stage.
-template <int BN>
-constexpr int stage_ktiles() { return BN == 8 ? 4 : (BN <= 32 ? 3 : 2); }
+// k-tiles per pipeline stage for token tiles of bn rows (the kernel's stage layout
+// and the host's k-tile-plane activation boxes both follow it).  Measured at
+// decode (8-row tiles): unpacked E2M1 weights (32 KB of smem per 4 k-tiles) run
+// best with three stages of four k-tiles (T = 4: 50.0 us against 51.2 with two of
+// six, 54 with two of five, 52.6 with four of three, 58.2 with six of two); packed
+// FP4 operands (half the smem) with stages of six (FP4 x FP4 49.3 against 50.9 us,
+// NVFP4 69.1 against 71.9).
+constexpr int stage_ktiles_for(int bn, bool fp4) { return bn == 8 ? (fp4 ? 6 : 4) : (bn <= 32 ? 3 : 2); }
 
 // Shared-memory bytes of one 128-element k-tile row of an operand: 128 for E4M3
 // and for E2M1 weights unpacked by TMA for kind::mxf8f6f4 (16 codes per 16-byte
@@ -73,7 +79,7 @@ constexpr int kTileQ = 4;
 template <int BN, bool FP4, bool NV>
 struct GemmCfg {
   static_assert(FP4 || !NV, "NVFP4 operands are FP4");
-  static constexpr int kKS = stage_ktiles<BN>();
+  static constexpr int kKS = stage_ktiles_for(BN, FP4);
   static constexpr int kSfAtoms = NV ? 2 : 1;  // scale atoms per k-tile and operand (16- or 32-element blocks)
   static constexpr uint32_t kRow = smem_row_bytes<FP4>();
   static constexpr uint32_t kA1 = kTileM * kRow;        // smem per weight k-tile (16 KB unpacked, 8 KB packed)
@@ -975,7 +981,7 @@ cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, cons
   for (int i = 0; i < kActBoxes; ++i) {
     // boxes taller than the token tile are never used; encode them at its height
     const int rows = std::min(act_box_rows(i), tile_rows);
-    if (!make_act_map_planes(&m.xp3[i], b.xp, fp4 ? h.H / 2 : h.H, TK, h.H, rows, tile_rows == 8 ? 4 : tile_rows <= 32 ? 3 : 2,
+    if (!make_act_map_planes(&m.xp3[i], b.xp, fp4 ? h.H / 2 : h.H, TK, h.H, rows, stage_ktiles_for(tile_rows, fp4),
                              fp4) ||
         !make_act_map(&m.xp[i], b.xp, fp4 ? h.H / 2 : h.H, TK, rows, fp4) ||
         !make_act_map(&m.hq[i], b.hq, fp4 ? h.I / 2 : h.I, TK, rows, fp4))
