@@ -228,13 +228,15 @@ moe_status forward_impl(moe_dims d, int fmt, const void* hidden, int32_t T, cons
   // grid, else the tensor-core router with separate grouping and gather passes
   const int forced = moe::plan_route();
   const bool cluster_fits = moe::route_cluster_fits(T, d.E, d.H), grid_fits = moe::route_small_fits(T, d.H);
-  // NVFP4 activations are quantised by the gather pass of the tensor-core path only
-  const int route = fmt == moe::kActNvfp4 && forced == moe::kRouteAuto ? moe::kRouteTensorCore
-                    : forced != moe::kRouteAuto
+  // NVFP4 activations are quantised by the cluster kernel and by the gather pass of the
+  // tensor-core path (not by the grid routing kernel)
+  const bool nv = fmt == moe::kActNvfp4;
+  const int route = forced != moe::kRouteAuto
                         ? forced
-                        : (cluster_fits ? moe::kRouteCluster : (grid_fits ? moe::kRouteGrid : moe::kRouteTensorCore));
-  if (fmt == moe::kActNvfp4 && route != moe::kRouteTensorCore)
-    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "NVFP4 activations take the tensor-core routing path only");
+                        : (cluster_fits ? moe::kRouteCluster
+                                        : (grid_fits && !nv ? moe::kRouteGrid : moe::kRouteTensorCore));
+  if (nv && route == moe::kRouteGrid)
+    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "NVFP4 activations take the cluster or tensor-core routing path");
   if ((route == moe::kRouteCluster && !cluster_fits) || (route == moe::kRouteGrid && !grid_fits))
     return fail(MOE_ERR_UNSUPPORTED_SHAPE, "the forced routing path %d does not fit T=%d", route, T);
   // The cluster routing kernel clears the status words and counters itself; the
@@ -272,7 +274,7 @@ moe_status forward_impl(moe_dims d, int fmt, const void* hidden, int32_t T, cons
     o.status = status;
     o.flags = reinterpret_cast<int32_t*>(at(L.grid_bar)) + 2;
     e = moe::launch_route_cluster(static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(router_w),
-                                  static_cast<const uint16_t*>(router_b), T, d.H, d.E, top_k, L.tile_rows, fp4, o,
+                                  static_cast<const uint16_t*>(router_b), T, d.H, d.E, top_k, L.tile_rows, fmt, o,
                                   &route_ctas, s);
     if (e != cudaSuccess) return cuda_fail(e, "cluster routing kernel");
   } else if (route == moe::kRouteGrid) {

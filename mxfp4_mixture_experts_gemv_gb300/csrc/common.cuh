@@ -359,7 +359,7 @@ struct RouteClusterOut {
 };
 // *ctas: the routing CTAs the launch runs (the count the second flag reaches)
 cudaError_t launch_route_cluster(const uint16_t* x, const uint16_t* wr, const uint16_t* br, int T, int H, int E,
-                                 int k, int tile_rows, bool fp4, const RouteClusterOut& o, int* ctas,
+                                 int k, int tile_rows, int fmt, const RouteClusterOut& o, int* ctas,
                                  cudaStream_t s);
 
 struct ExpertMlpBuffers {

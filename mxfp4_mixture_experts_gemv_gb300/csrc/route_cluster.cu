@@ -54,7 +54,8 @@ struct RouteClusterArgs {
   uint32_t* status;
   int32_t* flags;  // [0] tile list published, [1] routing CTAs whose grouped rows are written
   uint64_t wait_ns;
-  int fp4;  // activation format: 0 MXFP8 (32 code bytes per block), 1 MXFP4 (16)
+  int fp4;  // activation codes: 0 MXFP8 (32 code bytes per block), 1 E2M1 (16)
+  int nv;   // 1: NVFP4 (two E4M3 scales per 32-element block, unit global scale)
 };
 
 // Sum-reduce N values held by every lane of a warp so that each lane ends up
@@ -184,11 +185,26 @@ __global__ void __launch_bounds__(kRcThreads, 1) route_cluster_kernel(const Rout
   const bool has_u = u < T * nbh;
   const int ut = has_u ? u / nbh : 0, ukb = has_u ? u - ut * nbh : 0;
   uint4 qc[2];
-  uint8_t qs = 0;
+  uint32_t qs = 0;  // the block's scale code (NVFP4: the two 16-element blocks' codes, low byte first)
   if (has_u) {
-    qs = quant_block_regs_act(s_x + (size_t)ut * H + ukb * 32, qc, a.fp4);
+    if (a.nv) {
+      float f[32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float g[8];
+        bf16x8(reinterpret_cast<const uint4*>(s_x + (size_t)ut * H + ukb * 32)[q], g);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[8 * q + i] = g[i];
+      }
+      uint32_t p0[2], p1[2];
+      qs = nvfp4_block16(f, 1.0f, p0) | (nvfp4_block16(f + 16, 1.0f, p1) << 8);
+      qc[0] = make_uint4(p0[0], p0[1], p1[0], p1[1]);
+      *reinterpret_cast<uint16_t*>(a.xs + (int64_t)ut * (H / 16) + 2 * ukb) = (uint16_t)qs;
+    } else {
+      qs = quant_block_regs_act(s_x + (size_t)ut * H + ukb * 32, qc, a.fp4);
+      a.xs[(int64_t)ut * nbh + ukb] = (uint8_t)qs;
+    }
     store_block_codes(a.xq + (int64_t)ut * (H >> a.fp4) + ukb * (32 >> a.fp4), qc, a.fp4);
-    a.xs[(int64_t)ut * nbh + ukb] = qs;
   }
 
   cluster_wait();  // every CTA has every logit; no CTA touches another's shared memory after this
@@ -238,10 +254,22 @@ __global__ void __launch_bounds__(kRcThreads, 1) route_cluster_kernel(const Rout
       store_block_codes(a.xp + (int64_t)p * (H >> a.fp4) + ukb * (32 >> a.fp4), qc, a.fp4);
       const int r_in_e = p - s_off[e];
       const int b = s_toff[e] + (r_in_e >> a.tshift), n = r_in_e & ((1 << a.tshift) - 1);
-      uint8_t* wd = a.xp_sf + ((int64_t)b * kth + ka) * kAtomBytes + (n & 31) * 16 + (n >> 5) * 4;
-      wd[ukb & 3] = qs;
-      if (ukb == nbh - 1)
-        for (int jj = (ukb & 3) + 1; jj < 4; ++jj) wd[jj] = 127;
+      const int row_off = (n & 31) * 16 + (n >> 5) * 4;
+      if (a.nv) {
+        // a k-tile's eight 16-element blocks fill two atoms; 32-element block s of the
+        // k-tile is half-word s & 1 of atom (s >> 1) & 1.  The last real block also
+        // gives the padding blocks after it the zero scale.
+        uint8_t* atoms = a.xp_sf + ((int64_t)b * kth + ka) * 2 * kAtomBytes + row_off;
+        const int sl = ukb & 3;
+        reinterpret_cast<uint16_t*>(atoms + ((sl >> 1) & 1) * kAtomBytes)[sl & 1] = (uint16_t)qs;
+        if (ukb == nbh - 1)
+          for (int jj = sl + 1; jj < 4; ++jj) reinterpret_cast<uint16_t*>(atoms + ((jj >> 1) & 1) * kAtomBytes)[jj & 1] = 0;
+      } else {
+        uint8_t* wd = a.xp_sf + ((int64_t)b * kth + ka) * kAtomBytes + row_off;
+        wd[ukb & 3] = (uint8_t)qs;
+        if (ukb == nbh - 1)
+          for (int jj = (ukb & 3) + 1; jj < 4; ++jj) wd[jj] = 127;
+      }
     }
   }
   // this CTA's grouped rows and scale bytes (and CTA 0's weights and permutation,
@@ -265,7 +293,7 @@ bool route_cluster_fits(int T, int E, int H) {
 }
 
 cudaError_t launch_route_cluster(const uint16_t* x, const uint16_t* wr, const uint16_t* br, int T, int H, int E,
-                                 int k, int tile_rows, bool fp4, const RouteClusterOut& o, int* ctas, cudaStream_t s) {
+                                 int k, int tile_rows, int fmt, const RouteClusterOut& o, int* ctas, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -306,7 +334,8 @@ cudaError_t launch_route_cluster(const uint16_t* x, const uint16_t* wr, const ui
   const int epc = (E + csize - 1) / csize;
   RouteClusterArgs a{x, wr, br, T, H, E, k, __builtin_ctz((unsigned)tile_rows), o.logits, o.ids, o.w, o.xq, o.xs,
                      o.counts, o.offsets, o.sorted_rows, o.inv_pos, o.tiles, o.xp, o.xp_sf, o.zero,
-                     o.zero_words, o.status, o.flags, wait_limit_ns(), fp4 ? 1 : 0};
+                     o.zero_words, o.status, o.flags, wait_limit_ns(), fmt != kActMxfp8 ? 1 : 0,
+                     fmt == kActNvfp4 ? 1 : 0};
   *ctas = csize;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(csize);
