@@ -63,8 +63,9 @@ namespace {
 // best with three stages of four k-tiles (T = 4: 50.0 us against 51.2 with two of
 // six, 54 with two of five, 52.6 with four of three, 58.2 with six of two); packed
 // FP4 operands (half the smem) with stages of six (FP4 x FP4 49.3 against 50.9 us,
-// NVFP4 69.1 against 71.9).
-constexpr int stage_ktiles_for(int bn, bool fp4) { return bn == 8 ? (fp4 ? 6 : 4) : (bn <= 32 ? 3 : 2); }
+// NVFP4 69.1 against 71.9).  FP4 stages hold an even number of k-tiles: the MXFP4
+// activation boxes span two k-tiles (256 elements, 128-byte rows).
+constexpr int stage_ktiles_for(int bn, bool fp4) { return bn == 8 ? (fp4 ? 6 : 4) : (bn <= 32 ? (fp4 ? 4 : 3) : 2); }
 
 // Shared-memory bytes of one 128-element k-tile row of an operand: 128 for E4M3
 // and for E2M1 weights unpacked by TMA for kind::mxf8f6f4 (16 codes per 16-byte
@@ -82,6 +83,13 @@ struct GemmCfg {
   static constexpr int kKS = stage_ktiles_for(BN, FP4);
   static constexpr int kSfAtoms = NV ? 2 : 1;  // scale atoms per k-tile and operand (16- or 32-element blocks)
   static constexpr uint32_t kRow = smem_row_bytes<FP4>();
+  // MXFP4 activations (kind::mxf4): 128-byte shared-memory rows of 256 elements, one
+  // TMA box row per two k-tiles (TMA lands box rows at a fixed rate per SM, whatever
+  // their width); NVFP4 keeps 64-byte rows, one per k-tile
+  static constexpr bool kWideB = FP4 && !NV;
+  static constexpr uint32_t kBRow = kWideB ? 128u : kRow;
+  static constexpr int kBPlanes = kWideB ? kKS / 2 : kKS;  // activation planes of a grouped-x stage
+  static_assert(!kWideB || kKS % 2 == 0, "MXFP4 activation stages span whole pairs of k-tiles");
   static constexpr uint32_t kA1 = kTileM * kRow;        // smem per weight k-tile (16 KB unpacked, 8 KB packed)
   static constexpr uint32_t kB1 = BN * kRow;            // BN activation rows per k-tile
   static constexpr uint32_t kA = kKS * kA1;
@@ -319,7 +327,7 @@ __global__ void __launch_bounds__(192, 1)
       const int rows_m = min(kTileM, rows_stored - r.m * kTileM);  // 64 for a tail m-tile
       const int bi = min(act_box_index(td.z), kActBoxes - 1);
       const CUtensorMap* bmap = r.gu ? &maps.xp[bi] : &maps.hq[bi];
-      const uint32_t b_bytes = (uint32_t)act_box_rows(bi) * C::kRow;
+      const uint32_t b_bytes = (uint32_t)act_box_rows(bi) * C::kBRow;  // one box plane
       const int row0_unit = (int)tile_row0(td.x, r.m, 0, rows_stored, k_tiles);
       // weight (A) copies of stage slot `ss`: the nk weight tiles are rows_m * nk
       // consecutive 64-byte rows (128 bytes each in shared memory when unpacked),
@@ -339,20 +347,23 @@ __global__ void __launch_bounds__(192, 1)
           off += c;
         }
       };
-      // activation (B) copies of stage slot `ss` covering k-tiles kt..kt+nk-1: k-tile
-      // j at j * box rows; grouped x as one box of kKS k-tile planes (a short last
-      // stage reads planes past K, which TMA fills with zeros), hq one box per k-tile
-      const uint32_t b_plane = (uint32_t)act_box_rows(bi) * C::kRow;
+      // activation (B) copies of stage slot `ss` covering k-tiles kt..kt+nk-1: plane j
+      // (one k-tile, or two for MXFP4) at j * box rows; grouped x as one box of the
+      // stage's planes (a short last stage reads planes past K, which TMA fills with
+      // zeros), hq one box per plane
+      const uint32_t b_plane = (uint32_t)act_box_rows(bi) * C::kBRow;
       auto issue_b = [&](int ss, int kt, int nk) {
         if (r.gu) {
-          tma_load_3d(sB + ss * C::kB, &maps.xp3[bi], &full[ss], 0, td.y, kt);
+          tma_load_3d(sB + ss * C::kB, &maps.xp3[bi], &full[ss], 0, td.y, C::kWideB ? kt / 2 : kt);
         } else {
-          for (int j = 0; j < nk; ++j)
-            tma_load_2d(sB + ss * C::kB + j * b_plane, bmap, &full[ss], (kt + j) * (int)C::kRow, td.y);
+          const int np = C::kWideB ? (nk + 1) / 2 : nk, p0 = C::kWideB ? kt / 2 : kt;
+          for (int j = 0; j < np; ++j)
+            tma_load_2d(sB + ss * C::kB + j * b_plane, bmap, &full[ss], (p0 + j) * (int)C::kBRow, td.y);
         }
       };
       auto stage_bytes = [&](int nk) {
-        return (uint32_t)(rows_m * nk * kTileRowBytes + (r.gu ? kKS : nk) * b_bytes + nk * 2 * SA * kAtomBytes);
+        const int b_planes = r.gu ? C::kBPlanes : (C::kWideB ? (nk + 1) / 2 : nk);
+        return (uint32_t)(rows_m * nk * kTileRowBytes + b_planes * b_bytes + nk * 2 * SA * kAtomBytes);
       };
       // A down unit's hq is ready once all gate_up m-tiles of its token tile are
       // counted.  If it is not ready yet, the unit's first stages get their weight
@@ -480,8 +491,8 @@ __global__ void __launch_bounds__(192, 1)
       const int4 td = make_int4(q.y, q.z, q.w, 0);
       const int k_tiles = r.gu ? p.gu_ktiles : p.d_ktiles;
       const int rows_m = min(kTileM, (r.gu ? p.gu_rows_stored : p.d_rows_stored) - r.m * kTileM);
-      // activation k-tile j sits j box heights into the stage (the producer's layout)
-      const uint32_t b_plane = (uint32_t)act_box_rows(min(act_box_index(td.z), kActBoxes - 1)) * C::kRow;
+      // activation plane j sits j box heights into the stage (the producer's layout)
+      const uint32_t b_plane = (uint32_t)act_box_rows(min(act_box_index(td.z), kActBoxes - 1)) * C::kBRow;
       if (!mbar_wait_warp(&tempty[acc], aph ^ 1u, p.wait_ns)) {
         if (lane == 0) {
           atomicOr(p.status, kStatusTimeoutMma);
@@ -522,7 +533,8 @@ __global__ void __launch_bounds__(192, 1)
               tmem_cp_32x128b_x4(sfb_t + 4u * aa, sdesc_sf_atom(sf_s + ((kKS + j) * SA + aa) * kAtomBytes));
             }
             // weight k-tile j starts rows_m rows into the stage (a swizzle-atom multiple)
-            const uint32_t a_j = a_s + (uint32_t)(j * rows_m) * C::kRow, b_j = b_s + (uint32_t)j * b_plane;
+            const uint32_t a_j = a_s + (uint32_t)(j * rows_m) * C::kRow,
+                           b_j = b_s + (uint32_t)(C::kWideB ? j >> 1 : j) * b_plane;
             if constexpr (NV) {
               // two MMAs of K = 64, each with the four 16-element block scales of one atom
               const uint64_t ad = sdesc_sw64(a_j), bd = sdesc_sw64(b_j);
@@ -531,9 +543,10 @@ __global__ void __launch_bounds__(192, 1)
                 umma_mxf4nvf4(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc0, sfa_t + 4u * kk, sfb_t + 4u * kk,
                               (kt + j + (int)kk) != 0);
             } else if constexpr (FP4) {
-              // two MMAs of K = 64 (32 bytes of each 64-byte row); each takes two of the
-              // row's four block scales, starting at byte 2kk
-              const uint64_t ad = sdesc_sw64(a_j), bd = sdesc_sw64(b_j);
+              // two MMAs of K = 64 (32 bytes of each 64-byte weight row; the activation row
+              // holds two k-tiles, this one in its first or second 64 bytes); each takes
+              // two of the row's four block scales, starting at byte 2kk
+              const uint64_t ad = sdesc_sw64(a_j), bd = sdesc_sw128(b_j) + 4u * (uint32_t)(j & 1);
 #pragma unroll
               for (uint32_t kk = 0; kk < 2; ++kk) {
                 const uint32_t idesc = idesc0 | ((2u * kk) << 4) | ((2u * kk) << 29);
@@ -981,10 +994,14 @@ cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, cons
   for (int i = 0; i < kActBoxes; ++i) {
     // boxes taller than the token tile are never used; encode them at its height
     const int rows = std::min(act_box_rows(i), tile_rows);
-    if (!make_act_map_planes(&m.xp3[i], b.xp, fp4 ? h.H / 2 : h.H, TK, h.H, rows, stage_ktiles_for(tile_rows, fp4),
-                             fp4) ||
-        !make_act_map(&m.xp[i], b.xp, fp4 ? h.H / 2 : h.H, TK, rows, fp4) ||
-        !make_act_map(&m.hq[i], b.hq, fp4 ? h.I / 2 : h.I, TK, rows, fp4))
+    // MXFP4 activations travel as 128-byte rows of 256 elements (byte-typed boxes with
+    // the 128-byte swizzle, one plane per two k-tiles); NVFP4 as 64-byte rows
+    const bool wide = fp4 && fmt != kActNvfp4, narrow = fp4 && !wide;
+    const int kst = stage_ktiles_for(tile_rows, fp4);
+    if (!make_act_map_planes(&m.xp3[i], b.xp, fp4 ? h.H / 2 : h.H, TK, wide ? h.H / 2 : h.H, rows,
+                             wide ? kst / 2 : kst, narrow) ||
+        !make_act_map(&m.xp[i], b.xp, fp4 ? h.H / 2 : h.H, TK, rows, narrow) ||
+        !make_act_map(&m.hq[i], b.hq, fp4 ? h.I / 2 : h.I, TK, rows, narrow))
       return cudaErrorInvalidValue;
   }
     std::lock_guard<std::mutex> lk(mu);
