@@ -60,10 +60,10 @@ struct Maps {
   CUtensorMap xp[kActBoxes], hq[kActBoxes];
   // Fewer, larger copies stream faster: four k-tiles of a 128-row weight tile (512
   // consecutive rows) as one box of two 256-row planes, and the activation rows of
-  // every k-tile of a pipeline stage as one box of k-tile planes (grouped x only:
-  // all its rows are written before the expert kernel starts).
+  // every k-tile of a pipeline stage as one box of k-tile planes (grouped x, and the
+  // intermediate read by the down units).
   CUtensorMap gu4, d4;
-  CUtensorMap xp3[kActBoxes];
+  CUtensorMap xp3[kActBoxes], hq3[kActBoxes];
 };
 
 // Tensor maps (host).  Weights: the tile-contiguous packed layout as 2-D rows of

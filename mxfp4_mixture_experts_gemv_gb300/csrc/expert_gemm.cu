@@ -143,6 +143,7 @@ struct MlpParams {
   PackedHeader want;         // (magic, version, dims and weight format)
   int dense;                 // a dense linear: down units only, B = the quantised input, bf16 out + bias
   int max_tiles;             // capacity of the tile list (entries past its count are not meaningful)
+  int TK;                    // grouped rows (token, slot pairs)
   const int32_t* route_flags;  // routing still running: [0] tile list published, [1] CTAs done
   int route_ctas;              // the count [1] reaches; 0 = the routing grid completed first
 };
@@ -326,7 +327,6 @@ __global__ void __launch_bounds__(192, 1)
       const uint8_t* sfb = (r.gu ? p.xp_sf : p.hq_sf) + (int64_t)r.b * k_tiles * SA * kAtomBytes;
       const int rows_m = min(kTileM, rows_stored - r.m * kTileM);  // 64 for a tail m-tile
       const int bi = min(act_box_index(td.z), kActBoxes - 1);
-      const CUtensorMap* bmap = r.gu ? &maps.xp[bi] : &maps.hq[bi];
       const uint32_t b_bytes = (uint32_t)act_box_rows(bi) * C::kBRow;  // one box plane
       const int row0_unit = (int)tile_row0(td.x, r.m, 0, rows_stored, k_tiles);
       // weight (A) copies of stage slot `ss`: the nk weight tiles are rows_m * nk
@@ -347,23 +347,19 @@ __global__ void __launch_bounds__(192, 1)
           off += c;
         }
       };
-      // activation (B) copies of stage slot `ss` covering k-tiles kt..kt+nk-1: plane j
-      // (one k-tile, or two for MXFP4) at j * box rows; grouped x as one box of the
-      // stage's planes (a short last stage reads planes past K, which TMA fills with
-      // zeros), hq one box per plane
+      // activation (B) copies of stage slot `ss` covering k-tiles kt..kt+nk-1: one box
+      // of the stage's planes (plane j, one k-tile or two for MXFP4, at j * box rows) of
+      // grouped x or of the intermediate; a short last stage reads planes past K, which
+      // TMA fills with zeros, and a last row's last plane reads the zeroed 256 bytes
+      // after the rows
       const uint32_t b_plane = (uint32_t)act_box_rows(bi) * C::kBRow;
       auto issue_b = [&](int ss, int kt, int nk) {
-        if (r.gu) {
-          tma_load_3d(sB + ss * C::kB, &maps.xp3[bi], &full[ss], 0, td.y, C::kWideB ? kt / 2 : kt);
-        } else {
-          const int np = C::kWideB ? (nk + 1) / 2 : nk, p0 = C::kWideB ? kt / 2 : kt;
-          for (int j = 0; j < np; ++j)
-            tma_load_2d(sB + ss * C::kB + j * b_plane, bmap, &full[ss], (p0 + j) * (int)C::kBRow, td.y);
-        }
+        (void)nk;
+        tma_load_3d(sB + ss * C::kB, r.gu ? &maps.xp3[bi] : &maps.hq3[bi], &full[ss], 0, td.y,
+                    C::kWideB ? kt / 2 : kt);
       };
       auto stage_bytes = [&](int nk) {
-        const int b_planes = r.gu ? C::kBPlanes : (C::kWideB ? (nk + 1) / 2 : nk);
-        return (uint32_t)(rows_m * nk * kTileRowBytes + b_planes * b_bytes + nk * 2 * SA * kAtomBytes);
+        return (uint32_t)(rows_m * nk * kTileRowBytes + C::kBPlanes * b_bytes + nk * 2 * SA * kAtomBytes);
       };
       // A down unit's hq is ready once all gate_up m-tiles of its token tile are
       // counted.  If it is not ready yet, the unit's first stages get their weight
@@ -635,6 +631,11 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const uint32_t tb = tmem + (uint32_t)acc * 128u + ((uint32_t)(32 * q) << 16);
       if (r.gu) {
+        // the 256 bytes after the last intermediate row are read (as zero padding) by the
+        // down units' plane boxes: the tile holding the last row clears them before it
+        // counts its m-tile 0 (which every down unit of that tile waits for)
+        if (r.m == 0 && td.y + td.z == p.TK && et < 16)
+          reinterpret_cast<uint4*>(p.hq + (int64_t)p.TK * (FP4 ? p.I / 2 : p.I))[et] = make_uint4(0, 0, 0, 0);
         // accumulator rows 0..63 = gate, 64..127 = up of intermediate columns 64m..64m+63
         // SwiGLU + MXFP8 of a 32-column chunk, transposed through shared memory:
         // thread et takes token column jt of the chunk and 16 rows (half hh = et & 1)
@@ -1000,6 +1001,8 @@ cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, cons
     const int kst = stage_ktiles_for(tile_rows, fp4);
     if (!make_act_map_planes(&m.xp3[i], b.xp, fp4 ? h.H / 2 : h.H, TK, wide ? h.H / 2 : h.H, rows,
                              wide ? kst / 2 : kst, narrow) ||
+        !make_act_map_planes(&m.hq3[i], b.hq, fp4 ? h.I / 2 : h.I, TK, wide ? h.I / 2 : h.I, rows,
+                             wide ? kst / 2 : kst, narrow) ||
         !make_act_map(&m.xp[i], b.xp, fp4 ? h.H / 2 : h.H, TK, rows, narrow) ||
         !make_act_map(&m.hq[i], b.hq, fp4 ? h.I / 2 : h.I, TK, rows, narrow))
       return cudaErrorInvalidValue;
@@ -1028,6 +1031,7 @@ cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, cons
   p.done_tok = b.done_tok;
   p.sched = b.sched;
   p.max_tiles = max_tiles;
+  p.TK = TK;
   p.route_flags = b.route_flags;
   p.route_ctas = b.route_ctas;
   p.status = b.status;
