@@ -296,11 +296,13 @@ inline bool dense_workspace(int N, int K, int T, int num_sms, DenseWorkspace* w)
 }
 
 // Dense linear for T tokens on the CUDA cores (else the tensor cores), from the
-// measured crossover on GB300: the GEMV wins by launching fewer kernels while its
-// per-element decode (E2M1 -> f16 -> f32 conversions) costs less than the tensor
-// path's fixed overhead, which holds up to about 2^26 multiply-adds (T * N * K) at
-// T <= 4; the LM head (201,088 x 2880) at T = 1 is already faster on the tensor cores.
-constexpr int64_t kDenseCudaCoresMaxMacs = (int64_t)1 << 26;
+// measured crossover on GB300 (graph-replayed calls, weights streamed from HBM): the
+// GEMV launches fewer kernels but decodes every element on the CUDA cores (E2M1 ->
+// f16 -> f32), so it wins up to about 2^25 multiply-adds (T * N * K): 2880 x 2880 at
+// T = 4 14.6 against 16.3 us, 5120 x 2880 at T = 2 15.0 against 16.2; from about
+// 4.7e7 the tensor cores win (2880 x 4096 at T = 4 16.9 against 18.5 us, 16384 x 2880
+// at T = 1 17.3 against 24.8, the LM head 201,088 x 2880 at T = 1 66 against 134).
+constexpr int64_t kDenseCudaCoresMaxMacs = (int64_t)1 << 25;
 inline bool dense_cuda_cores_for(int T, int N, int K) {
   return T <= kDenseCudaCoresMaxT && (int64_t)T * N * K <= kDenseCudaCoresMaxMacs;
 }
