@@ -22,7 +22,7 @@ TOPK_W_ATOL = 1e-6
 
 
 @dataclasses.dataclass
-class GpuRun:
+class GpuForward:
     dims: moe.LayerDims
     k: int
     out: torch.Tensor
@@ -103,7 +103,7 @@ def zero_codes_equal(codes: np.ndarray, fp4: bool) -> np.ndarray:
     return c
 
 
-def run_gpu(inp: ms.LayerInputs, packed, x=None, poison: int | None = None, act_format: str = "mxfp8") -> GpuRun:
+def run_gpu(inp: ms.LayerInputs, packed, x=None, poison: int | None = None, act_format: str = "mxfp8") -> GpuForward:
     s = inp.shape
     dims = moe.LayerDims(s.E, s.H, s.I)
     x = inp.x if x is None else x
@@ -115,7 +115,7 @@ def run_gpu(inp: ms.LayerInputs, packed, x=None, poison: int | None = None, act_
     moe.forward(dims, x, inp.router_w, inp.router_b, packed, s.k, out=out, workspace=ws, act_format=act_format)
     st = moe.device_status(ws)
     assert st == moe.MOE_OK, moe.STATUS_NAMES.get(st, st)
-    return GpuRun(dims, s.k, out, ws, moe.workspace_layout(dims, T, s.k), act_format)
+    return GpuForward(dims, s.k, out, ws, moe.workspace_layout(dims, T, s.k), act_format)
 
 
 def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
@@ -126,7 +126,7 @@ def _widen(bits: np.ndarray) -> np.ndarray:
     return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def check_routing(run: GpuRun, x_cpu, wr_cpu, br_cpu, logits_ref: np.ndarray):
+def check_routing(run: GpuForward, x_cpu, wr_cpu, br_cpu, logits_ref: np.ndarray):
     """Router ids: equal to the oracle's, or a valid selection under fp32 near-ties.
 
     Returns the set of tokens whose ids differ (accepted near-ties)."""
@@ -174,7 +174,7 @@ def H_gamma(n: int) -> float:
     return n * u / (1 - n * u)
 
 
-def check_quantised_x(run: GpuRun, xq_ref, xs_ref):
+def check_quantised_x(run: GpuForward, xq_ref, xs_ref):
     T, H = xq_ref.shape
     xq = run.codes("xq", T, H)
     xs = run.section("xs", (T, H // run.block), torch.uint8).numpy()
@@ -182,7 +182,7 @@ def check_quantised_x(run: GpuRun, xq_ref, xs_ref):
     np.testing.assert_array_equal(xs, xs_ref)
 
 
-def check_gathered(run: GpuRun, T: int, sr: np.ndarray, xq_ref: np.ndarray, xs_ref: np.ndarray):
+def check_gathered(run: GpuForward, T: int, sr: np.ndarray, xq_ref: np.ndarray, xs_ref: np.ndarray):
     """The grouped MXFP8 rows, bit-exact: row p holds the oracle's codes of token
     sorted_rows[p] // k, and its scale-atom entry the token's block scales (127 on
     the padding blocks past H/32)."""
@@ -198,7 +198,7 @@ def check_gathered(run: GpuRun, T: int, sr: np.ndarray, xq_ref: np.ndarray, xs_r
     np.testing.assert_array_equal(sc, want)
 
 
-def check_grouping(run: GpuRun, T: int):
+def check_grouping(run: GpuForward, T: int):
     E, k = run.dims.E, run.k
     ids = run.section("topk_ids", (T, k), torch.int32).numpy()
     cnt, off, sr, inv = oracle.permute(ids, E)
@@ -265,7 +265,7 @@ def _code_table(fp4: bool):
     return _TABLES[fp4]
 
 
-def gpu_hq(run: GpuRun, T: int, inv: np.ndarray):
+def gpu_hq(run: GpuForward, T: int, inv: np.ndarray):
     """GPU intermediate codes and scale codes per (token, slot): [T,k,I], [T,k,I/32]."""
     I, k = run.dims.I, run.k
     L = run.layout
@@ -276,7 +276,7 @@ def gpu_hq(run: GpuRun, T: int, inv: np.ndarray):
     return hq[pos].reshape(-1, k, I), sc.reshape(-1, k, I // run.block)
 
 
-def check_intermediate(run: GpuRun, ref: dict, inp_cpu: ms.LayerInputs, inv: np.ndarray, tokens=None,
+def check_intermediate(run: GpuForward, ref: dict, inp_cpu: ms.LayerInputs, inv: np.ndarray, tokens=None,
                        rel_mid=2e-4):
     """Compare the GPU's MXFP8 intermediate with the oracle's for every (token, slot).
 

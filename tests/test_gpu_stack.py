@@ -134,7 +134,7 @@ def _teacher_forced_stack(T):
             # routing and grouping of every token, on the GPU's own input
             x_t = torch.from_numpy(hid_bits.view(np.int16)).view(torch.bfloat16)
             logits = _oracle_route_all(hid_bits, rw, rb, pool)
-            run = mc.GpuRun(dims, K, out, ws, layout)
+            run = mc.GpuForward(dims, K, out, ws, layout)
             ties = mc.check_routing(run, x_t, rw, rb, logits)
             n_ties += len(ties)
             cnt, off, sr, inv = mc.check_grouping(run, T)
