@@ -45,7 +45,8 @@ def _normal_forward_meets_the_oracle(inp, dev, packed):
     mc.compare_out(mc.bf16_to_f64(run.out), ref["out"], "after timeout", bf16_rounding=True)
 
 
-@pytest.mark.parametrize("T", [4, 20, 64], ids=["cluster_route", "grid_route", "tensor_core_route"])
+@pytest.mark.parametrize("T", [4, 20, 64, 300],
+                         ids=["cluster_route", "grid_route", "tensor_core_route", "tensor_core_route_128_row_tiles"])
 def test_held_down_units_time_out_and_the_device_stays_usable(T):
     shape = ms.LayerShape(T=T, H=256, I=256, E=8, k=2)
     inp, dev, packed, st = _forward_with_held_waits(shape, moe.HOLD_DOWN_UNITS, seed=30 + T)
