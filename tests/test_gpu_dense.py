@@ -59,16 +59,23 @@ def test_dense_forward_matches_the_oracle(N, K, T, path):
     mc.compare_out(mc.bf16_to_f64(out), ref, f"dense {N}x{K} T={T} {path}", bf16_rounding=True)
 
 
-@pytest.mark.parametrize("N,K,T", [(5120, 2880, 4), (2880, 4096, 4), (5120, 2880, 64), (2880, 4096, 200)],
-                         ids=["qkv_t4", "o_t4", "qkv_t64", "o_t200"])
-def test_dense_gpt_oss_projection_shapes(N, K, T):
+@pytest.mark.parametrize("N,K,T,path", [(5120, 2880, 4, "auto"), (2880, 4096, 4, "auto"), (5120, 2880, 64, "auto"),
+                                         (2880, 4096, 200, "auto"), (5120, 2880, 4, "cuda_cores"),
+                                         (2880, 4096, 2, "cuda_cores")],
+                         ids=["qkv_t4", "o_t4", "qkv_t64", "o_t200", "qkv_t4_cuda_cores", "o_t2_cuda_cores"])
+def test_dense_gpt_oss_projection_shapes(N, K, T, path):
     """gpt-oss-120b's attention projections (hidden 2880, 64 query and 8 KV heads of
-    64: QKV 5120 outputs, O 2880 outputs from 4096), outputs of a token sample."""
+    64: QKV 5120 outputs, O 2880 outputs from 4096), outputs of a token sample; the
+    CUDA-core cases split K over up to 14 chunks per weight tile and sum them in order."""
     w, b = _weights(N, K, seed=N ^ K)
     x = ms.make_tokens(32, T, K)
     blocks, scales = moe.dense_quantize_weights(w.cuda())
     packed = moe.dense_pack(blocks, scales, b.cuda())
-    out = mc.bf16_to_f64(moe.dense_forward(N, K, x.cuda(), packed))
+    moe.set_plan(0, "auto", path)
+    try:
+        out = mc.bf16_to_f64(moe.dense_forward(N, K, x.cuda(), packed))
+    finally:
+        moe.set_plan(0, "auto")
     rows = sorted(set(np.linspace(0, T - 1, min(T, 8)).astype(int).tolist()))
     ref = _oracle_rows(x, blocks.cpu(), scales.cpu(), b, rows)
     mc.compare_out(out[rows], ref, f"dense {N}x{K} T={T}")
