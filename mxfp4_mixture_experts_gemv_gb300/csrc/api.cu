@@ -455,10 +455,10 @@ moe_status moe_dense_forward(int32_t N, int32_t K, const void* x, int32_t T, con
   }
   int32_t* tiles = reinterpret_cast<int32_t*>(ws + L.tiles);
   int32_t* inv_pos = reinterpret_cast<int32_t*>(ws + L.inv_pos);
-  e = moe::launch_dense_prep(T, L.tile_rows, L.max_tiles, L.zero_bytes, ws, tiles, inv_pos, s);
-  if (e != cudaSuccess) return cuda_fail(e, "dense grouping kernel");
+  // the quantiser also lays out the identity grouping and clears the counters
   e = moe::launch_gather_quant(static_cast<const uint16_t*>(x), inv_pos, tiles, L.max_tiles, T, 1, K, moe::kActMxfp8,
-                               ws + L.xq, ws + L.xs, ws + L.xp, ws + L.xp_sf, s);
+                               ws + L.xq, ws + L.xs, ws + L.xp, ws + L.xp_sf, s, L.tile_rows,
+                               reinterpret_cast<uint32_t*>(ws), (int)(L.zero_bytes / 4));
   if (e != cudaSuccess) return cuda_fail(e, "dense quantiser");
   moe::ExpertMlpBuffers b = {};
   b.xp = ws + L.xp;

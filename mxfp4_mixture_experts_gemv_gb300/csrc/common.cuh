@@ -253,9 +253,12 @@ cudaError_t launch_permute(const int32_t* ids, int TK, int k, int E, int tile_ro
 // E2M1 codes per byte, one E4M3 scale per 16, unit global scale; scale atoms in
 // pairs per k-tile as in an NVFP4 weight buffer).
 enum ActFormat : int { kActMxfp8 = 0, kActMxfp4 = 1, kActNvfp4 = 2 };
-cudaError_t launch_gather_quant(const uint16_t* x, const int32_t* inv_pos, const int32_t* tiles, int max_tiles, int T,
+// dense_tile_rows > 0: a dense linear (k = 1, identity grouping); the kernel also
+// writes the tile list and inv_pos and clears the first zero_words words at zero.
+cudaError_t launch_gather_quant(const uint16_t* x, int32_t* inv_pos, int32_t* tiles, int max_tiles, int T,
                                 int k, int H, int fmt, uint8_t* xq, uint8_t* xs, uint8_t* xp, uint8_t* xp_sf,
-                                cudaStream_t s);
+                                cudaStream_t s, int dense_tile_rows = 0, uint32_t* zero = nullptr,
+                                int zero_words = 0);
 
 cudaError_t launch_residual_rmsnorm(float* x_res, const uint16_t* layer_out, int T, int H, float eps,
                                     uint16_t* hidden, cudaStream_t s);
@@ -297,11 +300,11 @@ inline bool dense_workspace(int N, int K, int T, int num_sms, DenseWorkspace* w)
 
 // Dense linear for T tokens on the CUDA cores (else the tensor cores), from the
 // measured crossover on GB300 (graph-replayed calls, weights streamed from HBM): the
-// GEMV launches fewer kernels but decodes every element on the CUDA cores (E2M1 ->
-// f16 -> f32), so it wins up to about 2^25 multiply-adds (T * N * K): 2880 x 2880 at
-// T = 4 14.6 against 16.3 us, 5120 x 2880 at T = 2 15.0 against 16.2; from about
-// 4.7e7 the tensor cores win (2880 x 4096 at T = 4 16.9 against 18.5 us, 16384 x 2880
-// at T = 1 17.3 against 24.8, the LM head 201,088 x 2880 at T = 1 66 against 134).
+// GEMV has no quantise-and-place pass but decodes every element on the CUDA cores
+// (E2M1 -> f16 -> f32), so it wins up to about 2^25 multiply-adds (T * N * K): 2880 x
+// 2880 at T = 4 14.9 against 15.3 us, 5120 x 2880 at T = 2 15.2 against 15.2; from
+// about 4.7e7 the tensor cores win (2880 x 4096 at T = 4 16.7 against 18.7 us, 16384 x
+// 2880 at T = 1 16.8 against 24.7, the LM head 201,088 x 2880 at T = 1 65 against 134).
 constexpr int64_t kDenseCudaCoresMaxMacs = (int64_t)1 << 25;
 inline bool dense_cuda_cores_for(int T, int N, int K) {
   return T <= kDenseCudaCoresMaxT && (int64_t)T * N * K <= kDenseCudaCoresMaxMacs;
@@ -312,10 +315,6 @@ cudaError_t launch_dense_quantize_weights(int N, int K, const uint16_t* w, uint8
                                           cudaStream_t s);
 cudaError_t launch_dense_pack(const PackedHeader& h, const uint8_t* blocks, const uint8_t* scales, const uint16_t* bias,
                               uint8_t* packed, cudaStream_t s);
-// identity grouping of T tokens in tiles of tile_rows (the tile list and inv_pos),
-// and the zeroing of the workspace's first zero_bytes (status word, counters)
-cudaError_t launch_dense_prep(int T, int tile_rows, int max_tiles, size_t zero_bytes, uint8_t* workspace,
-                              int32_t* tiles, int32_t* inv_pos, cudaStream_t s);
 // CUDA-core path for a few tokens: out (or fp32 partial sums over K chunks) of
 // MXFP8(x) . W^T + b; k_chunks > 1 writes partial[c][t][n] and a second pass sums.
 cudaError_t launch_dense_gemv(const PackedHeader& h, const uint8_t* packed, const uint16_t* x, int T, int k_chunks,

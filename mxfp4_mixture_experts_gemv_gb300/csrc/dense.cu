@@ -89,21 +89,6 @@ __global__ void dense_pack_sf_kernel(DensePackArgs a) {
   if (blockIdx.x == 0 && threadIdx.x == 0) *reinterpret_cast<PackedHeader*>(a.packed) = h;
 }
 
-// Identity grouping of the T tokens in tiles of tile_rows (tile list, inv_pos), and
-// the reset of the status word and the expert kernel's counters (the first
-// zero_words 32-bit words of the workspace).
-__global__ void dense_prep_kernel(int T, int tile_rows, int max_tiles, int zero_words, uint32_t* __restrict__ zero,
-                                  int32_t* __restrict__ tiles, int32_t* __restrict__ inv_pos) {
-  const int n_tiles = min((T + tile_rows - 1) / tile_rows, max_tiles);
-  const int n = max(max(T, n_tiles), zero_words);
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-    if (i < zero_words) zero[i] = 0u;
-    if (i < T) inv_pos[i] = i;
-    if (i < n_tiles) reinterpret_cast<int4*>(tiles + 4)[i] = make_int4(0, i * tile_rows, min(tile_rows, T - i * tile_rows), 0);
-  }
-  if (blockIdx.x == 0 && threadIdx.x == 0) tiles[0] = n_tiles;
-}
-
 // Eight E2M1 codes (one 32-bit word, lower-index element in the low nibble) ->
 // eight fp32 values, by the hardware E2M1 -> f16x2 conversion.
 __device__ __forceinline__ void e2m1x8_to_f32(uint32_t w, float (&f)[8]) {
@@ -232,15 +217,6 @@ cudaError_t launch_dense_pack(const PackedHeader& h, const uint8_t* blocks, cons
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   dense_pack_sf_kernel<<<512, 256, 0, s>>>(a);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_dense_prep(int T, int tile_rows, int max_tiles, size_t zero_bytes, uint8_t* workspace,
-                              int32_t* tiles, int32_t* inv_pos, cudaStream_t s) {
-  const int zero_words = (int)(zero_bytes / 4);
-  const int n = std::max(std::max(T, zero_words), 1);
-  dense_prep_kernel<<<std::max(1, std::min(1024, (n + 255) / 256)), 256, 0, s>>>(
-      T, tile_rows, max_tiles, zero_words, reinterpret_cast<uint32_t*>(workspace), tiles, inv_pos);
   return cudaGetLastError();
 }
 

@@ -131,31 +131,52 @@ __global__ void __launch_bounds__(kPermThreads) perm_scatter_kernel(
 // left as they are: they only feed accumulator columns that are discarded.
 constexpr int kGatherWarps = 8;
 
+// dense_tr > 0 (a dense linear, k = 1): the grouping is the identity in tiles of
+// dense_tr rows; block 0 writes that tile list and inv_pos and clears the expert
+// kernel's zero_words counters (which it reads only after this grid completes).
 __global__ void __launch_bounds__(32 * kGatherWarps) gather_tok_kernel(
-    const uint16_t* __restrict__ x, const int32_t* __restrict__ inv_pos, const int32_t* __restrict__ tiles,
+    const uint16_t* __restrict__ x, int32_t* __restrict__ inv_pos, int32_t* __restrict__ tiles,
     int max_tiles, int T, int k, int H, int fmt, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
-    uint8_t* __restrict__ xp, uint8_t* __restrict__ xp_sf) {
+    uint8_t* __restrict__ xp, uint8_t* __restrict__ xp_sf, int dense_tr, uint32_t* __restrict__ zero,
+    int zero_words) {
   const int fp4 = fmt != kActMxfp8 ? 1 : 0;  // codes two per byte
   const bool nv = fmt == kActNvfp4;          // two E4M3 scales per 32-element block
   // the 256 bytes after the last grouped row are read (as zero padding) by the
   // expert kernel's k-tile-plane boxes: keep them zero
   if (blockIdx.x == 0 && threadIdx.x < 16)
     reinterpret_cast<uint4*>(xp + (int64_t)T * k * (H >> fp4))[threadIdx.x] = make_uint4(0, 0, 0, 0);
+  if (dense_tr > 0 && blockIdx.x == 0) {
+    // the expert kernel takes its first work ticket before it waits for this grid:
+    // the counters are cleared and made visible before the dependents may launch
+    const int n_tiles = min((T + dense_tr - 1) / dense_tr, max_tiles);
+    for (int i = threadIdx.x; i < max(n_tiles, zero_words); i += blockDim.x) {
+      if (i < zero_words) zero[i] = 0u;
+      if (i < n_tiles) reinterpret_cast<int4*>(tiles + 4)[i] = make_int4(0, i * dense_tr, min(dense_tr, T - i * dense_tr), 0);
+    }
+    if (threadIdx.x == 0) tiles[0] = n_tiles;
+    __threadfence();
+    __syncthreads();
+  }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   extern __shared__ int2 s_tl[];  // [max_tiles]: {row0, rows}
-  const int n_tiles = min(tiles[0], max_tiles);
+  const int n_tiles = dense_tr > 0 ? 0 : min(tiles[0], max_tiles);
   for (int i = threadIdx.x; i < n_tiles; i += blockDim.x) {
     const int4 td = reinterpret_cast<const int4*>(tiles + 4)[i];
     s_tl[i] = make_int2(td.y, td.z);
   }
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kGatherWarps + warp;
   if (t >= T) return;  // whole warp
   const int nbh = H / 32, kth = (H + kTileK - 1) / kTileK;
   // lanes j < k: grouped row p of slot j, its tile b and row n in the tile
   int p = 0, b = 0, n = 0;
-  if (lane < k) {
+  if (dense_tr > 0) {
+    if (lane == 0) inv_pos[t] = t;
+    p = t;
+    b = t / dense_tr;
+    n = t - b * dense_tr;
+  } else if (lane < k) {
     p = inv_pos[(int64_t)t * k + lane];
     int lo = 0, hi = n_tiles - 1;
     while (lo < hi) {  // last tile whose first row is <= p (tiles are in row order)
@@ -284,16 +305,16 @@ cudaError_t launch_permute(const int32_t* ids, int TK, int k, int E, int tile_ro
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather_quant(const uint16_t* x, const int32_t* inv_pos, const int32_t* tiles, int max_tiles, int T,
+cudaError_t launch_gather_quant(const uint16_t* x, int32_t* inv_pos, int32_t* tiles, int max_tiles, int T,
                                 int k, int H, int fmt, uint8_t* xq, uint8_t* xs, uint8_t* xp, uint8_t* xp_sf,
-                                cudaStream_t s) {
-  const size_t smem = (size_t)max_tiles * sizeof(int2);
+                                cudaStream_t s, int dense_tile_rows, uint32_t* zero, int zero_words) {
+  const size_t smem = dense_tile_rows > 0 ? 16 : (size_t)max_tiles * sizeof(int2);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(gather_tok_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
   gather_tok_kernel<<<(T + kGatherWarps - 1) / kGatherWarps, 32 * kGatherWarps, smem, s>>>(
-      x, inv_pos, tiles, max_tiles, T, k, H, fmt, xq, xs, xp, xp_sf);
+      x, inv_pos, tiles, max_tiles, T, k, H, fmt, xq, xs, xp, xp_sf, dense_tile_rows, zero, zero_words);
   return cudaGetLastError();
 }
 
