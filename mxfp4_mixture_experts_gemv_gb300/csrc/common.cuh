@@ -397,5 +397,7 @@ cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, cons
 // weight tiles in N (MXFP8 activations); y is combined by launch_combine.
 cudaError_t launch_expert_swap(const PackedHeader& h, const uint8_t* packed, const ExpertMlpBuffers& b, int T, int k,
                                int max_tiles, int num_sms, cudaStream_t s);
+// whether the packed layer's weight tiles pair up as the tokens-on-M kernel reads them
+bool expert_swap_supported(const PackedHeader& h);
 
 }  // namespace moe

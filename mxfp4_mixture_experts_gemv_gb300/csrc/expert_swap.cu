@@ -17,8 +17,9 @@
 // intermediates of an MX block, in one thread's accumulator columns, so the SwiGLU
 // and the MXFP8 quantisation of h run in registers without a transpose.
 // The 256-column accumulator leaves no room in tensor memory for a second one and
-// the scale columns, so the accumulator is single-buffered: the producer keeps
-// filling its stages while the epilogue drains it.
+// the scale columns, so the accumulator is single-buffered: each epilogue warp
+// copies its 128 columns to registers and releases the accumulator before the
+// SwiGLU, quantisation and stores, so the next unit's MMAs overlap them.
 //
 // Scheduling is the weights-on-M kernel's: units claimed by running CTAs from one
 // counter in increasing order, gate_up units first; a down unit's producer waits
@@ -367,24 +368,28 @@ __global__ void __launch_bounds__(kSwThreads, 1)
       tc_fence_after();
       const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kTileM * half);
       const bool store = ok && n < rows;
+      // the warp's 128 accumulator columns go to registers first and the accumulator
+      // is released at once, so the next unit's MMAs overlap the math and the stores
+      uint32_t acc[128];
+      if (present && ok) {
+#pragma unroll
+        for (int c = 0; c < 128; c += 16) tmem_ld_32x32b_x16(tb + (uint32_t)c, *reinterpret_cast<uint32_t(*)[16]>(acc + c));
+        tmem_ld_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty);
       if (present && r.gu) {
         // columns 0..63 of this tile are gate rows 64 mt.., 64..127 the matching up rows
         const float* bias = p.gu_bias + (int64_t)e * 2 * p.I + (int64_t)mt * kTileM;
+#pragma unroll
         for (int blk = 0; blk < 2; ++blk) {
-          uint32_t g0[16], g1[16], u0[16], u1[16];
-          if (ok) {
-            tmem_ld_32x32b_x16(tb + 32u * blk, g0);
-            tmem_ld_32x32b_x16(tb + 32u * blk + 16u, g1);
-            tmem_ld_32x32b_x16(tb + 64u + 32u * blk, u0);
-            tmem_ld_32x32b_x16(tb + 64u + 32u * blk + 16u, u1);
-            tmem_ld_wait();
-          }
           float h[32];
           float amax = 0.f;
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const float g = __uint_as_float(c < 16 ? g0[c] : g1[c - 16]) + __ldg(bias + 32 * blk + c);
-            const float up = __uint_as_float(c < 16 ? u0[c] : u1[c - 16]) + __ldg(bias + 64 + 32 * blk + c);
+            const float g = __uint_as_float(acc[32 * blk + c]) + __ldg(bias + 32 * blk + c);
+            const float up = __uint_as_float(acc[64 + 32 * blk + c]) + __ldg(bias + 64 + 32 * blk + c);
             h[c] = __fdividef(g, 1.0f + __expf(-g)) * up;  // rel. error ~1e-6, far below an E4M3 step
             amax = fmaxf(amax, fabsf(h[c]));
           }
@@ -410,35 +415,27 @@ __global__ void __launch_bounds__(kSwThreads, 1)
               for (int jj = (kb & 3) + 1; jj < 4; ++jj) wd[jj] = 127;
           }
         }
-      } else if (present) {
+      } else if (present && store) {
         const float* bias = p.d_bias + (int64_t)e * p.H + (int64_t)mt * kTileM;
         float* yrow = p.y + (int64_t)(row0 + n) * p.H + (int64_t)mt * kTileM;
-        for (int c0 = 0; c0 < wrows; c0 += 32) {
-          uint32_t v0[16], v1[16];
-          if (ok) {
-            tmem_ld_32x32b_x16(tb + (uint32_t)c0, v0);
-            tmem_ld_32x32b_x16(tb + (uint32_t)c0 + 16u, v1);
-            tmem_ld_wait();
-          }
-          if (store) {
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          if (c0 < wrows) {
 #pragma unroll
             for (int c = 0; c < 32; c += 4) {
               const int f = mt * kTileM + c0 + c;
               if (f < p.H) {  // H is a multiple of 32: whole groups of four are in or out
                 float4 o;
-                o.x = __uint_as_float(c < 16 ? v0[c] : v1[c - 16]) + __ldg(bias + c0 + c);
-                o.y = __uint_as_float(c + 1 < 16 ? v0[c + 1] : v1[c - 15]) + __ldg(bias + c0 + c + 1);
-                o.z = __uint_as_float(c + 2 < 16 ? v0[c + 2] : v1[c - 14]) + __ldg(bias + c0 + c + 2);
-                o.w = __uint_as_float(c + 3 < 16 ? v0[c + 3] : v1[c - 13]) + __ldg(bias + c0 + c + 3);
+                o.x = __uint_as_float(acc[c0 + c]) + __ldg(bias + c0 + c);
+                o.y = __uint_as_float(acc[c0 + c + 1]) + __ldg(bias + c0 + c + 1);
+                o.z = __uint_as_float(acc[c0 + c + 2]) + __ldg(bias + c0 + c + 2);
+                o.w = __uint_as_float(acc[c0 + c + 3]) + __ldg(bias + c0 + c + 3);
                 *reinterpret_cast<float4*>(yrow + c0 + c) = o;
               }
             }
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty);
       if (r.gu) {
         // every hq byte of this unit is stored: count it
         named_barrier_sync(1, kSwEpiThreads);
