@@ -64,6 +64,9 @@ struct Maps {
   // intermediate read by the down units).
   CUtensorMap gu4, d4;
   CUtensorMap xp3[kActBoxes], hq3[kActBoxes];
+  // The tokens-on-M kernel's pairs of consecutive 128-row weight tiles: one k-tile of
+  // both tiles as one box, and both tiles' scale atoms of that k-tile as one box.
+  CUtensorMap gup, dp, gusf, dsf;
 };
 
 // Tensor maps (host).  Weights: the tile-contiguous packed layout as 2-D rows of

@@ -197,6 +197,8 @@ __global__ void __launch_bounds__(kSwThreads, 1)
       const int w0row = (int)tile_row0(td.x, m0, 0, rows_stored, k_tiles);
       const int w1row = nm == 2 ? (int)tile_row0(td.x, m0 + 1, 0, rows_stored, k_tiles) : 0;
       const uint32_t bytes = (uint32_t)(act_box_rows(bi) * kTileK + (rw0 + rw1) * kTileRowBytes + (1 + nm) * kAtomBytes);
+      // two full weight tiles take the pair boxes
+      const bool pair = nm == 2 && rw0 == kTileM && rw1 == kTileM;
       const int claim_st = max(0, k_tiles - 8), fetch_st = max(0, k_tiles - 3);
       int next = total;
       if (!r.gu) {
@@ -228,14 +230,22 @@ __global__ void __launch_bounds__(kSwThreads, 1)
         if (elect_one()) {
           mbar_arrive_expect_tx(&full[s], bytes);
           uint8_t* b_s = sB + s * kSwB;
-          tma_load_2d_hint(b_s, w0map, &full[s], 0, w0row + kt * rw0, wpol);
-          if (nm == 2) tma_load_2d_hint(b_s + rw0 * kTileK, w1map, &full[s], 0, w1row + kt * rw1, wpol);
-          tma_load_2d(sA + s * kSwA, amap, &full[s], kt * kTileK, td.y);
           uint8_t* sf = sSF + s * kSwSF;
+          if (pair) {
+            // k-tile kt of both weight tiles (rows kt*128.. of tiles m0 and m0+1 of
+            // expert e) and their two scale atoms, one box each
+            tma_load_4d_hint(b_s, r.gu ? &maps.gup : &maps.dp, &full[s], 0, kt * kTileM, m0, td.x, wpol);
+            tma_load_3d_hint(sf + kAtomBytes, r.gu ? &maps.gusf : &maps.dsf, &full[s], 0, kt, td.x * m_tiles + m0,
+                             wpol);
+          } else {
+            tma_load_2d_hint(b_s, w0map, &full[s], 0, w0row + kt * rw0, wpol);
+            if (nm == 2) tma_load_2d_hint(b_s + rw0 * kTileK, w1map, &full[s], 0, w1row + kt * rw1, wpol);
+            bulk_g2s_hint(sf + kAtomBytes, sfw + kt * kAtomBytes, kAtomBytes, &full[s], wpol);
+            if (nm == 2)
+              bulk_g2s_hint(sf + 2 * kAtomBytes, sfw + (k_tiles + kt) * kAtomBytes, kAtomBytes, &full[s], wpol);
+          }
+          tma_load_2d(sA + s * kSwA, amap, &full[s], kt * kTileK, td.y);
           bulk_g2s(sf, sfx + kt * kAtomBytes, kAtomBytes, &full[s]);
-          bulk_g2s_hint(sf + kAtomBytes, sfw + kt * kAtomBytes, kAtomBytes, &full[s], wpol);
-          if (nm == 2)
-            bulk_g2s_hint(sf + 2 * kAtomBytes, sfw + (k_tiles + kt) * kAtomBytes, kAtomBytes, &full[s], wpol);
         }
         __syncwarp();
         ++issued;
@@ -454,6 +464,38 @@ __global__ void __launch_bounds__(kSwThreads, 1)
 
 }  // namespace
 
+// One k-tile of two consecutive 128-row weight tiles of an expert as one box: the
+// tile-contiguous layout seen as 4-D {128 codes, row within the m-tile (k-tile kt
+// at rows 128 kt..), m-tile, expert}; full m-tiles only (a 64-row tail tile is read
+// by the 2-D maps).
+bool make_weight_pair_map(CUtensorMap* map, const uint8_t* base, int E, int rows_stored, int k_tiles) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)kTileK, (cuuint64_t)kTileM * k_tiles, (cuuint64_t)(rows_stored / kTileM),
+                        (cuuint64_t)E};
+  cuuint64_t strides[3] = {(cuuint64_t)kTileRowBytes, (cuuint64_t)kTileM * k_tiles * kTileRowBytes,
+                           (cuuint64_t)rows_stored * k_tiles * kTileRowBytes};
+  cuuint32_t box[4] = {kTileK, kTileM, 2, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, const_cast<uint8_t*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The scale atoms [E][m_tiles][k_tiles][512 bytes] as 3-D {128 words, k-tile,
+// (expert, m-tile)}: a box holds the atoms of one k-tile of two consecutive m-tiles.
+bool make_scale_pair_map(CUtensorMap* map, const uint8_t* base, int E, int m_tiles, int k_tiles) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)(kAtomBytes / 4), (cuuint64_t)k_tiles, (cuuint64_t)E * m_tiles};
+  cuuint64_t strides[2] = {(cuuint64_t)kAtomBytes, (cuuint64_t)k_tiles * kAtomBytes};
+  cuuint32_t box[3] = {kAtomBytes / 4, 1, 2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint8_t*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool expert_swap_supported(const PackedHeader& h) {
   // the weight tiles of a projection pair up, a 64-row tail tile only as the last
   return h.gu_rows_stored % kTileM == 0;
@@ -493,6 +535,16 @@ cudaError_t launch_expert_swap(const PackedHeader& h, const uint8_t* packed, con
         !make_weight_map(&m.gut, packed + h.off_gu_data, gu_rows, 64) ||
         !make_weight_map(&m.d, packed + h.off_d_data, d_rows, kTileM) ||
         !make_weight_map(&m.dt, packed + h.off_d_data, d_rows, 64))
+      return cudaErrorInvalidValue;
+    // pair boxes exist for projections with at least two full 128-row weight tiles
+    // (the only ones whose units take them)
+    if (h.gu_rows_stored >= 2 * kTileM &&
+        (!make_weight_pair_map(&m.gup, packed + h.off_gu_data, h.E, h.gu_rows_stored, h.gu_ktiles) ||
+         !make_scale_pair_map(&m.gusf, packed + h.off_gu_sf, h.E, h.gu_mtiles, h.gu_ktiles)))
+      return cudaErrorInvalidValue;
+    if (h.d_rows_stored >= 2 * kTileM &&
+        (!make_weight_pair_map(&m.dp, packed + h.off_d_data, h.E, h.d_rows_stored, h.d_ktiles) ||
+         !make_scale_pair_map(&m.dsf, packed + h.off_d_sf, h.E, h.d_mtiles, h.d_ktiles)))
       return cudaErrorInvalidValue;
     for (int i = 0; i < kActBoxes; ++i) {
       const int rows = act_box_rows(i);
