@@ -156,6 +156,13 @@ size_t moe_workspace_size(moe_dims d, int32_t T, int32_t top_k);
 moe_status moe_workspace_layout_get(moe_dims d, int32_t T, int32_t top_k,
                                     moe_workspace_layout *out);
 
+/* The same for moe_forward_act in activation format act_format (MOE_ACT_*): the
+ * section offsets and total are those of moe_workspace_layout_get; tile_rows and
+ * max_tiles are the ones that format's forward uses.  An unknown format is
+ * MOE_ERR_INVALID_ARG. */
+moe_status moe_workspace_layout_act(moe_dims d, int32_t T, int32_t top_k, int32_t act_format,
+                                    moe_workspace_layout *out);
+
 /*
  * One MoE layer forward for T tokens: the layer defined at the top of this
  * file.  Passages: "GPT-OSS-120B on DGX Spark: From MXFP4 to NVFP4", section

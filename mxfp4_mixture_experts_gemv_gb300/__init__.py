@@ -25,7 +25,7 @@ STATUS_NAMES = {
 
 # Every symbol the C ABI exports (include/moe.h).
 EXPORTED = ["moe_packed_size", "moe_pack_weights", "moe_packed_size_nvfp4", "moe_pack_weights_nvfp4",
-            "moe_workspace_size", "moe_workspace_layout_get",
+            "moe_workspace_size", "moe_workspace_layout_get", "moe_workspace_layout_act",
             "moe_forward", "moe_forward_act", "moe_forward_static_scratch", "moe_static_scratch_status", "moe_static_scratch_bytes",
             "moe_get_device_status", "moe_set_wait_limit_ns", "moe_get_wait_limit_ns",
             "moe_debug_hold_waits", "moe_set_plan", "moe_profile_begin", "moe_profile_end", "moe_residual_rmsnorm",
@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
         L.moe_workspace_size.argtypes = [Dims, i32, i32]
         L.moe_workspace_layout_get.restype = st
         L.moe_workspace_layout_get.argtypes = [Dims, i32, i32, ctypes.POINTER(WorkspaceLayout)]
+        L.moe_workspace_layout_act.restype = st
+        L.moe_workspace_layout_act.argtypes = [Dims, i32, i32, i32, ctypes.POINTER(WorkspaceLayout)]
         L.moe_forward.restype = st
         L.moe_forward.argtypes = [Dims, vp, i32, vp, vp, vp, i32, vp, vp, sz, vp]
         L.moe_forward_act.restype = st
@@ -163,9 +165,11 @@ def workspace_size(dims: LayerDims, T: int, top_k: int) -> int:
     return lib().moe_workspace_size(dims.c(), T, top_k)
 
 
-def workspace_layout(dims: LayerDims, T: int, top_k: int) -> WorkspaceLayout:
+def workspace_layout(dims: LayerDims, T: int, top_k: int, act_format: str = "mxfp8") -> WorkspaceLayout:
+    """Section offsets of the workspace (the same for every activation format) and
+    the tile height / tile capacity the forward in ``act_format`` uses."""
     out = WorkspaceLayout()
-    _check(lib().moe_workspace_layout_get(dims.c(), T, top_k, ctypes.byref(out)))
+    _check(lib().moe_workspace_layout_act(dims.c(), T, top_k, ACT_FORMATS[act_format], ctypes.byref(out)))
     return out
 
 

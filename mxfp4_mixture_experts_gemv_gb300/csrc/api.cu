@@ -183,11 +183,18 @@ size_t moe_workspace_size(moe_dims d, int32_t T, int32_t top_k) {
 }
 
 moe_status moe_workspace_layout_get(moe_dims d, int32_t T, int32_t top_k, moe_workspace_layout* out) {
+  return moe_workspace_layout_act(d, T, top_k, MOE_ACT_MXFP8, out);
+}
+
+moe_status moe_workspace_layout_act(moe_dims d, int32_t T, int32_t top_k, int32_t act_format,
+                                    moe_workspace_layout* out) {
   moe_status st = check_dims(d);
   if (st != MOE_OK) return st;
   if (!out || T < 0 || top_k <= 0 || top_k > 8 || top_k > d.E)
     return fail(MOE_ERR_INVALID_ARG, "bad layout query (T=%d top_k=%d)", T, top_k);
-  moe::workspace_layout(d, T, top_k, out);
+  if (act_format != MOE_ACT_MXFP8 && act_format != MOE_ACT_MXFP4 && act_format != MOE_ACT_NVFP4)
+    return fail(MOE_ERR_INVALID_ARG, "unknown activation format %d", act_format);
+  moe::workspace_layout(d, T, top_k, out, act_format);
   return MOE_OK;
 }
 
@@ -204,7 +211,7 @@ moe_status forward_impl(moe_dims d, int fmt, const void* hidden, int32_t T, cons
   if (!workspace) return fail(MOE_ERR_INVALID_ARG, "null workspace");
   if (!aligned(workspace, 256)) return fail(MOE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
   moe_workspace_layout L;
-  moe::workspace_layout(d, T, top_k, &L);
+  moe::workspace_layout(d, T, top_k, &L, fmt);
   if (workspace_bytes < L.total)
     return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "workspace has %zu bytes, %zu needed", workspace_bytes, L.total);
   const bool fp4 = fmt == moe::kActMxfp4;  // the routing kernels' MXFP4 quantisation

@@ -148,34 +148,58 @@ int plan_tile_rows();
 int plan_route();
 int plan_expert();
 
-// Token rows per tile of the grouped GEMM, from the measured plan sweep on the
-// gpt-oss-shaped layer (E = 128, top-4): twice the average rows per expert,
-// rounded up to a power of two, within [8, 128].  Small tiles take the pipeline
-// shape that streams weights fastest (four k-tiles per stage) and most experts
-// still fit one tile, so each weight byte is read once; the fastest tile height
-// in the sweep was 8 rows up to T = 128 (2 to 4 rows per expert on average),
-// then 16, 32, 64 at T = 256, 512, 1024 and 128 from T = 2048.
-inline int tile_rows_for(int T, int k, int E) {
-  if (const int forced = plan_tile_rows()) return forced;
+// Activation formats: MXFP8 (one E4M3 code byte per element, one E8M0 scale per
+// 32), MXFP4 (two E2M1 codes per byte, one E8M0 scale per 32) and NVFP4 (two
+// E2M1 codes per byte, one E4M3 scale per 16, unit global scale; scale atoms in
+// pairs per k-tile as in an NVFP4 weight buffer).
+enum ActFormat : int { kActMxfp8 = 0, kActMxfp4 = 1, kActNvfp4 = 2 };
+
+// Token rows per tile of the grouped GEMM for the weights-on-M kernel, from the
+// measured plan sweep on the gpt-oss-shaped layer (E = 128, top-4): twice the
+// average rows per expert, rounded up to a power of two, within [8, 128].  Small
+// tiles take the pipeline shape that streams weights fastest (four k-tiles per
+// stage) and most experts still fit one tile, so each weight byte is read once;
+// the fastest height in the sweep was 8 rows up to T = 128 (2 to 4 rows per
+// expert on average), then 16, 32, 64 at T = 256, 512, 1024 and 128 from 2048.
+inline int tile_rows_weights_m(int T, int k, int E) {
   const int64_t avg = ((int64_t)T * k + E - 1) / E;  // average token rows per expert
   int tr = 8;
   while (tr < 128 && tr < 2 * avg) tr *= 2;
   return tr;
 }
 
+// Average token rows per expert from which MXFP8 layers take 128-row tiles and the
+// tokens-on-M kernel: measured fastest from 8 rows per expert (T = 256 on the
+// gpt-oss layer, 327.7 against 330.2 us for 16-row tiles; T = 512 338 against 354;
+// T = 1024 361 against 369) up to T = 8192.
+constexpr int kTokensMMinAvgRows = 8;
+
+// The tile height of a layer forward in activation format fmt (the plan's, if it
+// forces one).
+inline int tile_rows_for(int T, int k, int E, int fmt) {
+  if (const int forced = plan_tile_rows()) return forced;
+  const int64_t avg = ((int64_t)T * k + E - 1) / E;
+  if (fmt == kActMxfp8 && avg >= kTokensMMinAvgRows) return 128;
+  return tile_rows_weights_m(T, k, E);
+}
+
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-inline bool workspace_layout(const moe_dims& d, int T, int k, moe_workspace_layout* L) {
+inline bool workspace_layout(const moe_dims& d, int T, int k, moe_workspace_layout* L, int fmt = kActMxfp8) {
   if (T < 0 || k <= 0) return false;
   const int64_t TK = (int64_t)T * k;
-  const int tr = tile_rows_for(T, k, d.E);
+  const int tr = tile_rows_for(T, k, d.E, fmt);
   const int64_t max_tiles = TK / tr + (TK < d.E ? TK : d.E) + 1;
+  // the sections that scale with the tile count are sized for the smallest tile
+  // height any activation format takes, so every format has the same offsets
+  const int tr_min = plan_tile_rows() ? tr : std::min(tr, tile_rows_weights_m(T, k, d.E));
+  const int64_t cap_tiles = TK / tr_min + (TK < d.E ? TK : d.E) + 1;
   const int64_t kth = (d.H + kTileK - 1) / kTileK, kti = (d.I + kTileK - 1) / kTileK;
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t r = o; o = align256(o + bytes); return r; };
   moe_workspace_layout l = {};
   l.status = take(16);
-  l.done_gu = take((size_t)max_tiles * 4);
+  l.done_gu = take((size_t)cap_tiles * 4);
   l.done_tok = take((size_t)T * ((d.H + kTileM - 1) / kTileM) * 4);
   l.grid_bar = take(16);
   l.zero_bytes = o;  // status words and the counters above start at zero every forward
@@ -191,11 +215,11 @@ inline bool workspace_layout(const moe_dims& d, int T, int k, moe_workspace_layo
   l.offsets = take((size_t)(d.E + 1) * 4);
   l.sorted_rows = take((size_t)TK * 4);
   l.inv_pos = take((size_t)TK * 4);
-  l.tiles = take((size_t)(4 + 4 * max_tiles) * 4);
+  l.tiles = take((size_t)(4 + 4 * cap_tiles) * 4);
   l.xp = take((size_t)TK * d.H + 256);
-  l.xp_sf = take((size_t)max_tiles * kth * 2 * kAtomBytes);
+  l.xp_sf = take((size_t)cap_tiles * kth * 2 * kAtomBytes);
   l.hq = take((size_t)TK * d.I + 256);
-  l.hq_sf = take((size_t)max_tiles * kti * 2 * kAtomBytes);
+  l.hq_sf = take((size_t)cap_tiles * kti * 2 * kAtomBytes);
   l.y = take((size_t)TK * d.H * 4);
   l.total = o;
   l.max_tiles = (int32_t)max_tiles;
@@ -248,11 +272,6 @@ cudaError_t launch_router_tc(const uint16_t* x, const uint16_t* wr, const uint16
 cudaError_t launch_permute(const int32_t* ids, int TK, int k, int E, int tile_rows, int max_tiles,
                            int32_t* counts, int32_t* offsets, int32_t* sorted_rows, int32_t* inv_pos,
                            int32_t* tiles, int32_t* scratch, cudaStream_t s);
-// Activation formats: MXFP8 (one E4M3 code byte per element, one E8M0 scale per
-// 32), MXFP4 (two E2M1 codes per byte, one E8M0 scale per 32) and NVFP4 (two
-// E2M1 codes per byte, one E4M3 scale per 16, unit global scale; scale atoms in
-// pairs per k-tile as in an NVFP4 weight buffer).
-enum ActFormat : int { kActMxfp8 = 0, kActMxfp4 = 1, kActNvfp4 = 2 };
 // dense_tile_rows > 0: a dense linear (k = 1, identity grouping); the kernel also
 // writes the tile list and inv_pos and clears the first zero_words words at zero.
 cudaError_t launch_gather_quant(const uint16_t* x, int32_t* inv_pos, int32_t* tiles, int max_tiles, int T,
@@ -274,7 +293,7 @@ struct DenseWorkspace {
 inline bool dense_workspace(int N, int K, int T, int num_sms, DenseWorkspace* w) {
   if (N <= 0 || K <= 0 || T < 0) return false;
   DenseWorkspace d = {};
-  d.tile_rows = tile_rows_for(T, 1, 1);
+  d.tile_rows = plan_tile_rows() ? plan_tile_rows() : tile_rows_weights_m(T, 1, 1);
   d.max_tiles = T / d.tile_rows + 2;
   const int kt = (K + kTileK - 1) / kTileK, mt = (N + kTileM - 1) / kTileM;
   // K chunks of the CUDA-core path: about two CTAs per SM, and at most 96 k-tiles

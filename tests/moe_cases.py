@@ -115,7 +115,7 @@ def run_gpu(inp: ms.LayerInputs, packed, x=None, poison: int | None = None, act_
     moe.forward(dims, x, inp.router_w, inp.router_b, packed, s.k, out=out, workspace=ws, act_format=act_format)
     st = moe.device_status(ws)
     assert st == moe.MOE_OK, moe.STATUS_NAMES.get(st, st)
-    return GpuForward(dims, s.k, out, ws, moe.workspace_layout(dims, T, s.k), act_format)
+    return GpuForward(dims, s.k, out, ws, moe.workspace_layout(dims, T, s.k, act_format), act_format)
 
 
 def bf16_to_f64(t: torch.Tensor) -> np.ndarray:

@@ -71,9 +71,19 @@ def test_workspace_layout_sections_are_disjoint_and_aligned():
         offs = [getattr(lay, n) for n in names]
         assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
         assert lay.total == moe.workspace_size(GPT, T, 4)
-        # the measured table: 8 rows up to T = 128, then 16, 32, 64, and 128 from 2048
-        want = 8 if T <= 128 else 16 if T <= 256 else 32 if T <= 512 else 64 if T <= 1024 else 128
+        # the measured table: 128-row tiles (tokens-on-M) from 8 rows per expert on
+        # average (T >= 225 here), below that twice the average rounded up to a power of
+        # two from 8 (8 rows up to T = 128)
+        avg = -(-T * 4 // 128)
+        want = 128 if avg >= 8 else 8 if T <= 128 else 16
         assert lay.tile_rows == want
+        # the FP4 formats keep the weights-on-M table, at the same offsets
+        want4 = 8 if T <= 128 else 16 if T <= 256 else 32 if T <= 512 else 64 if T <= 1024 else 128
+        for fmt in ("mxfp4", "nvfp4"):
+            l4 = moe.workspace_layout(GPT, T, 4, fmt)
+            assert l4.tile_rows == want4
+            assert [getattr(l4, n) for n in names] == offs and l4.total == lay.total
+            assert l4.max_tiles >= T * 4 // l4.tile_rows + min(T * 4, 128)
         # enough tiles for any routing: every expert's partial tile plus full tiles
         assert lay.max_tiles >= T * 4 // lay.tile_rows + min(T * 4, 128)
 
@@ -148,7 +158,7 @@ def test_plan_override_is_checked_and_sizes_follow_it(L):
     assert L.moe_set_plan(0, 7, 0) == 1            # unknown routing path
     assert L.moe_set_plan(0, 0, 4) == 1            # unknown expert kernel
     base = moe.workspace_layout(GPT, 1024, 4)
-    assert base.tile_rows == 64
+    assert base.tile_rows == 128
     try:
         moe.set_plan(8, "tensor_core")
         lay = moe.workspace_layout(GPT, 1024, 4)
@@ -156,7 +166,7 @@ def test_plan_override_is_checked_and_sizes_follow_it(L):
         assert moe.workspace_size(GPT, 1024, 4) == lay.total
     finally:
         moe.set_plan(0, "auto")
-    assert moe.workspace_layout(GPT, 1024, 4).tile_rows == 64
+    assert moe.workspace_layout(GPT, 1024, 4).tile_rows == 128
 
 
 def test_forward_act_rejects_unknown_formats(L):

@@ -283,11 +283,12 @@ def test_forced_route_that_does_not_fit_is_refused():
         moe.set_plan(0, "auto")
 
 
-@pytest.mark.parametrize("T", [8, 9, 32, 33, 128, 129, 256, 257, 512, 513, 1024, 1025, 2048])
+@pytest.mark.parametrize("T", [8, 9, 32, 33, 128, 129, 224, 225, 512, 1024, 2048])
 def test_gpt_oss_parity_at_the_plan_cutoffs(gpt_layer, T):
     """Either side of every automatic cutoff: cluster / grid routing at 8, grid /
-    tensor-core routing at 32, and the token-tile heights 8 / 16 / 32 / 64 / 128
-    at 128, 256, 512 and 1024.
+    tensor-core routing at 32, token tiles of 8 / 16 rows at 128, and 16-row tiles
+    (weights-on-M kernel) / 128-row tiles (tokens-on-M kernel) at 224 (7 / 8 rows
+    per expert on average); then the tokens-on-M kernel at 512, 1024 and 2048.
     Routing, grouping and the gathered rows are checked for every token, the
     output on up to 24 tokens (the oracle runs one token per host thread)."""
     cpu_inp, dev_inp, packed = _gpt_inputs(gpt_layer, T)
