@@ -45,18 +45,27 @@ namespace {
 
 constexpr int kSwThreads = 320;
 constexpr int kSwEpiThreads = 256;
-constexpr int kSwStages = 4;
 constexpr int kSwQ = 4;                            // tile queue entries
-constexpr uint32_t kSwA = kTileM * kTileK;         // 16 KB: 128 token rows x 128 E4M3 codes
-constexpr uint32_t kSwB = 2 * kTileM * kTileK;     // 32 KB: 256 weight rows, E2M1 unpacked to bytes
 constexpr uint32_t kSwSF = 3 * kAtomBytes;         // scale atoms: tokens, weight tile 0, weight tile 1
-constexpr uint32_t kSwStage = kSwA + kSwB + kSwSF;
 constexpr uint32_t kSwBars = 1024;
-constexpr uint32_t kSwSmem = 1024 + kSwStages * kSwStage + kSwBars;
 constexpr uint32_t kSwSfCols = 12;                 // tmem columns of one stage's scales (4 per atom)
-static_assert(kSwSmem <= 227 * 1024, "shared memory");
-static_assert(256 + kSwSfCols * kSwStages <= 512, "tensor memory columns");
-static_assert((2 * kSwStages + 3 + 2 * kSwQ) * 8 + 16 + 16 * (kSwQ + 1) <= kSwBars, "barrier area");
+
+// Stage shapes.  MXFP8 activations (kind::mxf8f6f4): 128 token rows of 128 E4M3
+// codes (16 KB) and 256 weight rows with the E2M1 codes unpacked to bytes (32 KB),
+// four stages.  MXFP4 activations (kind::mxf4): both operands packed, two codes per
+// byte (8 KB + 16 KB), so twice the stages fit.
+template <bool FP4>
+struct SwCfg {
+  static constexpr int kStages = FP4 ? 8 : 4;
+  static constexpr uint32_t kRowA = FP4 ? 64 : kTileK;  // bytes of a token row's k-tile
+  static constexpr uint32_t kA = kTileM * kRowA;
+  static constexpr uint32_t kB = 2 * kTileM * (FP4 ? 64 : kTileK);
+  static constexpr uint32_t kStage = kA + kB + kSwSF;
+  static constexpr uint32_t kSmem = 1024 + kStages * kStage + kSwBars;
+  static_assert(kSmem <= 227 * 1024, "shared memory");
+  static_assert(256 + kSwSfCols * kStages <= 512, "tensor memory columns");
+  static_assert((2 * kStages + 3 + 2 * kSwQ) * 8 + 16 + 16 * (kSwQ + 1) <= kSwBars, "barrier area");
+};
 
 struct SwapParams {
   const uint8_t* gu_sfa;  // gate_up weight scale atoms [E][gu_mtiles][gu_ktiles][512]
@@ -94,8 +103,12 @@ __device__ __forceinline__ Unit unit_ref(int u, int n_gu, int gp, int dp) {
   return r;
 }
 
+template <bool FP4>
 __global__ void __launch_bounds__(kSwThreads, 1)
     expert_swap_kernel(const __grid_constant__ Maps maps, const SwapParams p) {
+  using C = SwCfg<FP4>;
+  constexpr int kSwStages = C::kStages;
+  constexpr uint32_t kSwA = C::kA, kSwB = C::kB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -196,7 +209,8 @@ __global__ void __launch_bounds__(kSwThreads, 1)
       const CUtensorMap* w1map = r.gu ? (rw1 == kTileM ? &maps.gu : &maps.gut) : (rw1 == kTileM ? &maps.d : &maps.dt);
       const int w0row = (int)tile_row0(td.x, m0, 0, rows_stored, k_tiles);
       const int w1row = nm == 2 ? (int)tile_row0(td.x, m0 + 1, 0, rows_stored, k_tiles) : 0;
-      const uint32_t bytes = (uint32_t)(act_box_rows(bi) * kTileK + (rw0 + rw1) * kTileRowBytes + (1 + nm) * kAtomBytes);
+      const uint32_t bytes =
+          (uint32_t)(act_box_rows(bi) * C::kRowA + (rw0 + rw1) * kTileRowBytes + (1 + nm) * kAtomBytes);
       // two full weight tiles take the pair boxes
       const bool pair = nm == 2 && rw0 == kTileM && rw1 == kTileM;
       const int claim_st = max(0, k_tiles - 8), fetch_st = max(0, k_tiles - 3);
@@ -239,12 +253,13 @@ __global__ void __launch_bounds__(kSwThreads, 1)
                              wpol);
           } else {
             tma_load_2d_hint(b_s, w0map, &full[s], 0, w0row + kt * rw0, wpol);
-            if (nm == 2) tma_load_2d_hint(b_s + rw0 * kTileK, w1map, &full[s], 0, w1row + kt * rw1, wpol);
+            if (nm == 2)
+              tma_load_2d_hint(b_s + rw0 * (FP4 ? kTileRowBytes : kTileK), w1map, &full[s], 0, w1row + kt * rw1, wpol);
             bulk_g2s_hint(sf + kAtomBytes, sfw + kt * kAtomBytes, kAtomBytes, &full[s], wpol);
             if (nm == 2)
               bulk_g2s_hint(sf + 2 * kAtomBytes, sfw + (k_tiles + kt) * kAtomBytes, kAtomBytes, &full[s], wpol);
           }
-          tma_load_2d(sA + s * kSwA, amap, &full[s], kt * kTileK, td.y);
+          tma_load_2d(sA + s * kSwA, amap, &full[s], kt * (int)C::kRowA, td.y);
           bulk_g2s(sf, sfx + kt * kAtomBytes, kAtomBytes, &full[s]);
         }
         __syncwarp();
@@ -295,7 +310,8 @@ __global__ void __launch_bounds__(kSwThreads, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t idesc0 = idesc_mxf8f6f4(128, (uint32_t)n_mma, 0 /*E4M3*/, 5 /*E2M1*/, 0, 0);
+      const uint32_t idesc0 = FP4 ? idesc_mxf8f6f4(128, (uint32_t)n_mma, 1 /*E2M1*/, 1 /*E2M1*/, 0, 0)
+                                  : idesc_mxf8f6f4(128, (uint32_t)n_mma, 0 /*E4M3*/, 5 /*E2M1*/, 0, 0);
       for (int kt = 0; kt < k_tiles; ++kt) {
         if (!mbar_wait_warp(&full[s], ph, p.wait_ns)) {
           if (lane == 0) {
@@ -312,12 +328,24 @@ __global__ void __launch_bounds__(kSwThreads, 1)
           tmem_cp_32x128b_x4(sf_t, sdesc_sf_atom(sf_s));                      // A: token scales
           tmem_cp_32x128b_x4(sf_t + 4u, sdesc_sf_atom(sf_s + kAtomBytes));    // B: weight rows 0..127
           if (nm == 2) tmem_cp_32x128b_x4(sf_t + 8u, sdesc_sf_atom(sf_s + 2 * kAtomBytes));  // rows 128..255
-          const uint64_t ad = sdesc_sw128(smem_u32(sA + s * kSwA));
-          const uint64_t bd = sdesc_sw128(smem_u32(sB + s * kSwB));
+          if constexpr (FP4) {
+            // two MMAs of K = 64 (32 bytes of each 64-byte row); MMA kk takes block
+            // scales 2kk and 2kk + 1 of each row
+            const uint64_t ad = sdesc_sw64(smem_u32(sA + s * kSwA));
+            const uint64_t bd = sdesc_sw64(smem_u32(sB + s * kSwB));
 #pragma unroll
-          for (uint32_t kk = 0; kk < 4; ++kk) {
-            const uint32_t idesc = idesc0 | (kk << 4) | (kk << 29);
-            umma_mxf8f6f4(tmem, ad + 2u * kk, bd + 2u * kk, idesc, sf_t, sf_t + 4u, (kt + (int)kk) != 0);
+            for (uint32_t kk = 0; kk < 2; ++kk) {
+              const uint32_t idesc = idesc0 | ((2u * kk) << 4) | ((2u * kk) << 29);
+              umma_mxf4(tmem, ad + 2u * kk, bd + 2u * kk, idesc, sf_t, sf_t + 4u, (kt + (int)kk) != 0);
+            }
+          } else {
+            const uint64_t ad = sdesc_sw128(smem_u32(sA + s * kSwA));
+            const uint64_t bd = sdesc_sw128(smem_u32(sB + s * kSwB));
+#pragma unroll
+            for (uint32_t kk = 0; kk < 4; ++kk) {
+              const uint32_t idesc = idesc0 | (kk << 4) | (kk << 29);
+              umma_mxf8f6f4(tmem, ad + 2u * kk, bd + 2u * kk, idesc, sf_t, sf_t + 4u, (kt + (int)kk) != 0);
+            }
           }
           umma_commit(&empty[s]);
         }
@@ -403,19 +431,32 @@ __global__ void __launch_bounds__(kSwThreads, 1)
             h[c] = __fdividef(g, 1.0f + __expf(-g)) * up;  // rel. error ~1e-6, far below an E4M3 step
             amax = fmaxf(amax, fabsf(h[c]));
           }
-          const int sx = mx_scale_exp<8>(amax);
+          const int sx = FP4 ? mx_scale_exp<2>(amax) : mx_scale_exp<8>(amax);
           const float inv = mx_pow2_neg(sx);
           uint32_t pk[8];
+          if constexpr (FP4) {
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint32_t lo = cvt_e4m3x2(h[4 * c] * inv, h[4 * c + 1] * inv);
-            const uint32_t hi = cvt_e4m3x2(h[4 * c + 2] * inv, h[4 * c + 3] * inv);
-            pk[c] = lo | (hi << 16);
+            for (int c = 0; c < 32; ++c) h[c] *= inv;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) pk[c] = cvt_e2m1x8(h + 8 * c);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint32_t lo = cvt_e4m3x2(h[4 * c] * inv, h[4 * c + 1] * inv);
+              const uint32_t hi = cvt_e4m3x2(h[4 * c + 2] * inv, h[4 * c + 3] * inv);
+              pk[c] = lo | (hi << 16);
+            }
           }
           if (store) {
-            uint4* dst = reinterpret_cast<uint4*>(p.hq + (int64_t)(row0 + n) * p.I + mt * 64 + 32 * blk);
-            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            if constexpr (FP4) {
+              // 32 codes, two per byte: 16 bytes at intermediate column mt * 64 + 32 blk
+              *reinterpret_cast<uint4*>(p.hq + (int64_t)(row0 + n) * (p.I / 2) + mt * 32 + 16 * blk) =
+                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(p.hq + (int64_t)(row0 + n) * p.I + mt * 64 + 32 * blk);
+              dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
             const int kb = 2 * mt + blk;  // MX block of the intermediate
             uint8_t* wd = p.hq_sf + ((int64_t)r.b * p.d_ktiles + (kb >> 2)) * kAtomBytes + (n & 31) * 16 + (n >> 5) * 4;
             wd[kb & 3] = (uint8_t)(sx + 127);
@@ -468,17 +509,20 @@ __global__ void __launch_bounds__(kSwThreads, 1)
 // tile-contiguous layout seen as 4-D {128 codes, row within the m-tile (k-tile kt
 // at rows 128 kt..), m-tile, expert}; full m-tiles only (a 64-row tail tile is read
 // by the 2-D maps).
-bool make_weight_pair_map(CUtensorMap* map, const uint8_t* base, int E, int rows_stored, int k_tiles) {
+bool make_weight_pair_map(CUtensorMap* map, const uint8_t* base, int E, int rows_stored, int k_tiles, bool packed) {
   auto enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[4] = {(cuuint64_t)kTileK, (cuuint64_t)kTileM * k_tiles, (cuuint64_t)(rows_stored / kTileM),
-                        (cuuint64_t)E};
+  // unpacked by TMA for kind::mxf8f6f4 (128 codes per row, 128-byte swizzle), or the
+  // packed bytes for kind::mxf4 (64 bytes per row, 64-byte swizzle)
+  const cuuint64_t inner = packed ? (cuuint64_t)kTileRowBytes : (cuuint64_t)kTileK;
+  cuuint64_t dims[4] = {inner, (cuuint64_t)kTileM * k_tiles, (cuuint64_t)(rows_stored / kTileM), (cuuint64_t)E};
   cuuint64_t strides[3] = {(cuuint64_t)kTileRowBytes, (cuuint64_t)kTileM * k_tiles * kTileRowBytes,
                            (cuuint64_t)rows_stored * k_tiles * kTileRowBytes};
-  cuuint32_t box[4] = {kTileK, kTileM, 2, 1};
+  cuuint32_t box[4] = {(cuuint32_t)inner, kTileM, 2, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, const_cast<uint8_t*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return enc(map, packed ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4,
+             const_cast<uint8_t*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             packed ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -502,20 +546,23 @@ bool expert_swap_supported(const PackedHeader& h) {
 }
 
 cudaError_t launch_expert_swap(const PackedHeader& h, const uint8_t* packed, const ExpertMlpBuffers& b, int T, int k,
-                               int max_tiles, int num_sms, cudaStream_t s) {
+                               int max_tiles, int num_sms, int fmt, cudaStream_t s) {
+  if (fmt != kActMxfp8 && fmt != kActMxfp4) return cudaErrorInvalidValue;
+  const bool fp4 = fmt == kActMxfp4;
   const int TK = T * k;
   struct Key {
     const uint8_t *packed, *xp, *hq;
-    int E, H, I, TK;
+    int E, H, I, TK, fp4;
     bool operator==(const Key& o) const {
-      return packed == o.packed && xp == o.xp && hq == o.hq && E == o.E && H == o.H && I == o.I && TK == o.TK;
+      return packed == o.packed && xp == o.xp && hq == o.hq && E == o.E && H == o.H && I == o.I && TK == o.TK &&
+             fp4 == o.fp4;
     }
   };
   static std::mutex mu;
   static Key keys[32];
   static Maps cache[32];
   static int n_cached = 0, next_slot = 0;
-  const Key key{packed, b.xp, b.hq, h.E, h.H, h.I, TK};
+  const Key key{packed, b.xp, b.hq, h.E, h.H, h.I, TK, fp4 ? 1 : 0};
   Maps m;
   bool hit = false;
   {
@@ -531,24 +578,25 @@ cudaError_t launch_expert_swap(const PackedHeader& h, const uint8_t* packed, con
     m = Maps{};
     const int64_t gu_rows = (int64_t)h.E * h.gu_rows_stored * h.gu_ktiles;
     const int64_t d_rows = (int64_t)h.E * h.d_rows_stored * h.d_ktiles;
-    if (!make_weight_map(&m.gu, packed + h.off_gu_data, gu_rows, kTileM) ||
-        !make_weight_map(&m.gut, packed + h.off_gu_data, gu_rows, 64) ||
-        !make_weight_map(&m.d, packed + h.off_d_data, d_rows, kTileM) ||
-        !make_weight_map(&m.dt, packed + h.off_d_data, d_rows, 64))
+    auto wmap = fp4 ? make_weight_map_packed : make_weight_map;
+    if (!wmap(&m.gu, packed + h.off_gu_data, gu_rows, kTileM) || !wmap(&m.gut, packed + h.off_gu_data, gu_rows, 64) ||
+        !wmap(&m.d, packed + h.off_d_data, d_rows, kTileM) || !wmap(&m.dt, packed + h.off_d_data, d_rows, 64))
       return cudaErrorInvalidValue;
     // pair boxes exist for projections with at least two full 128-row weight tiles
     // (the only ones whose units take them)
     if (h.gu_rows_stored >= 2 * kTileM &&
-        (!make_weight_pair_map(&m.gup, packed + h.off_gu_data, h.E, h.gu_rows_stored, h.gu_ktiles) ||
+        (!make_weight_pair_map(&m.gup, packed + h.off_gu_data, h.E, h.gu_rows_stored, h.gu_ktiles, fp4) ||
          !make_scale_pair_map(&m.gusf, packed + h.off_gu_sf, h.E, h.gu_mtiles, h.gu_ktiles)))
       return cudaErrorInvalidValue;
     if (h.d_rows_stored >= 2 * kTileM &&
-        (!make_weight_pair_map(&m.dp, packed + h.off_d_data, h.E, h.d_rows_stored, h.d_ktiles) ||
+        (!make_weight_pair_map(&m.dp, packed + h.off_d_data, h.E, h.d_rows_stored, h.d_ktiles, fp4) ||
          !make_scale_pair_map(&m.dsf, packed + h.off_d_sf, h.E, h.d_mtiles, h.d_ktiles)))
       return cudaErrorInvalidValue;
     for (int i = 0; i < kActBoxes; ++i) {
       const int rows = act_box_rows(i);
-      if (!make_act_map(&m.xp[i], b.xp, h.H, TK, rows, false) || !make_act_map(&m.hq[i], b.hq, h.I, TK, rows, false))
+      // MXFP4 rows hold two codes per byte; a box is one k-tile (64 bytes) of a row
+      if (!make_act_map(&m.xp[i], b.xp, fp4 ? h.H / 2 : h.H, TK, rows, fp4) ||
+          !make_act_map(&m.hq[i], b.hq, fp4 ? h.I / 2 : h.I, TK, rows, fp4))
         return cudaErrorInvalidValue;
     }
     std::lock_guard<std::mutex> lk(mu);
@@ -581,17 +629,21 @@ cudaError_t launch_expert_swap(const PackedHeader& h, const uint8_t* packed, con
   p.I = h.I;
   p.H = h.H;
   p.weights_evict_first = (int64_t)T * k <= (int64_t)h.E * kTileM;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(expert_swap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSwSmem);
+  static bool attr[2] = {false, false};
+  const uint32_t smem = fp4 ? SwCfg<true>::kSmem : SwCfg<false>::kSmem;
+  if (!attr[fp4]) {
+    cudaError_t e = fp4 ? cudaFuncSetAttribute(expert_swap_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)smem)
+                        : cudaFuncSetAttribute(expert_swap_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)smem);
     if (e != cudaSuccess) return e;
-    attr = true;
+    attr[fp4] = true;
   }
   const int units = max_tiles * ((h.gu_mtiles + 1) / 2 + (h.d_mtiles + 1) / 2);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)std::max(1, std::min(num_sms, units)));
   cfg.blockDim = dim3(kSwThreads);
-  cfg.dynamicSmemBytes = kSwSmem;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   // programmatic dependent launch, as for the weights-on-M kernel: units are
   // claimed at run time by running CTAs, so any subset of resident CTAs finishes
@@ -600,7 +652,8 @@ cudaError_t launch_expert_swap(const PackedHeader& h, const uint8_t* packed, con
   attrs[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, expert_swap_kernel, m, p);
+  return fp4 ? cudaLaunchKernelEx(&cfg, expert_swap_kernel<true>, m, p)
+             : cudaLaunchKernelEx(&cfg, expert_swap_kernel<false>, m, p);
 }
 
 }  // namespace moe
