@@ -773,7 +773,7 @@ def run_sweep(args):
                 ws = moe.alloc_workspace(layers.dims, T, K_TOP, device)
                 for l in range(layers.n):  # warm-up, and the plan must run
                     moe.forward(layers.dims, xs[l], routers[l][0], routers[l][1], layers.packed[l], K_TOP, out=out,
-                                workspace=ws)
+                                workspace=ws, act_format=args.act)
                 st = moe.device_status(ws)
                 if st != moe.MOE_OK:
                     raise RuntimeError(f"device status {st}")
@@ -783,7 +783,7 @@ def run_sweep(args):
                     g = torch.cuda.CUDAGraph()
                     with torch.cuda.graph(g):
                         moe.forward(layers.dims, xs[l], routers[l][0], routers[l][1], layers.packed[l], K_TOP,
-                                    out=out, workspace=ws)
+                                    out=out, workspace=ws, act_format=args.act)
                     graphs.append(g)
                 for g in graphs[:args.warmup]:
                     g.replay()
@@ -799,13 +799,13 @@ def run_sweep(args):
                 del graphs, ws
             finally:
                 moe.set_plan(0, "auto")
-            line = {"sweep": "plan", "T": T, "tile_rows": tr, "route": rt, "expert": ex, "step_us": us,
+            line = {"sweep": "plan", "act": args.act, "T": T, "tile_rows": tr, "route": rt, "expert": ex, "step_us": us,
                     "tokens_per_s": T / (us * 1e-6)}
             rows.append(line)
             print(json.dumps(line), flush=True)
         # the automatic plan, for comparison
         ws = moe.alloc_workspace(layers.dims, T, K_TOP, device)
-        lay = moe.workspace_layout(layers.dims, T, K_TOP)
+        lay = moe.workspace_layout(layers.dims, T, K_TOP, args.act)
         fastest = min(rows, key=lambda r: r["step_us"])
         best[T] = {"fastest": (fastest["tile_rows"], fastest["route"], fastest["expert"], round(fastest["step_us"], 1)),
                    "auto_tile_rows": lay.tile_rows}
@@ -829,7 +829,8 @@ def main():
     ap.add_argument("--sweep-t", type=int, nargs="*", default=None, help="token counts of the plan sweep")
     ap.add_argument("--plan", nargs=3, default=None, metavar=("TILE_ROWS", "ROUTE", "EXPERT"),
                     help="with --case: force a plan (tile rows, routing path, expert kernel)")
-    ap.add_argument("--act", default="mxfp8", choices=["mxfp8", "mxfp4"], help="with --case: activation format")
+    ap.add_argument("--act", default="mxfp8", choices=["mxfp8", "mxfp4"],
+                    help="with --case or --sweep: activation format")
     ap.add_argument("--case", type=int, default=None, metavar="T",
                     help="profiling run: one gpt-oss-shaped layer at T tokens, warmup + steps plain "
                          "forward calls, no timing and no JSON line (T=32 uses the skewed router)")

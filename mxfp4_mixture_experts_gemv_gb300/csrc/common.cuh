@@ -168,10 +168,12 @@ inline int tile_rows_weights_m(int T, int k, int E) {
   return tr;
 }
 
-// Average token rows per expert from which MXFP8 layers take 128-row tiles and the
-// tokens-on-M kernel: measured fastest from 8 rows per expert (T = 256 on the
-// gpt-oss layer, 327.7 against 330.2 us for 16-row tiles; T = 512 338 against 354;
-// T = 1024 361 against 369) up to T = 8192.
+// Average token rows per expert from which MXFP8 and MXFP4 layers take 128-row tiles
+// and the tokens-on-M kernel: measured fastest from 8 rows per expert up to T = 8192
+// on the gpt-oss layer (MXFP8: T = 256 327.7 against 330.2 us for 16-row tiles,
+// T = 512 340 against 348, T = 1024 364 against 371; MXFP4: T = 256 287 against 297,
+// T = 512 295 against 319, T = 1024 322 against 346).  NVFP4 layers keep the
+// weights-on-M kernel.
 constexpr int kTokensMMinAvgRows = 8;
 
 // The tile height of a layer forward in activation format fmt (the plan's, if it
@@ -179,7 +181,7 @@ constexpr int kTokensMMinAvgRows = 8;
 inline int tile_rows_for(int T, int k, int E, int fmt) {
   if (const int forced = plan_tile_rows()) return forced;
   const int64_t avg = ((int64_t)T * k + E - 1) / E;
-  if (fmt == kActMxfp8 && avg >= kTokensMMinAvgRows) return 128;
+  if ((fmt == kActMxfp8 || fmt == kActMxfp4) && avg >= kTokensMMinAvgRows) return 128;
   return tile_rows_weights_m(T, k, E);
 }
 

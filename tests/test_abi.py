@@ -77,11 +77,12 @@ def test_workspace_layout_sections_are_disjoint_and_aligned():
         avg = -(-T * 4 // 128)
         want = 128 if avg >= 8 else 8 if T <= 128 else 16
         assert lay.tile_rows == want
-        # the FP4 formats keep the weights-on-M table, at the same offsets
-        want4 = 8 if T <= 128 else 16 if T <= 256 else 32 if T <= 512 else 64 if T <= 1024 else 128
-        for fmt in ("mxfp4", "nvfp4"):
+        # MXFP4 follows the same table; NVFP4 keeps the weights-on-M table; the
+        # offsets are the same for every format
+        want_nv = 8 if T <= 128 else 16 if T <= 256 else 32 if T <= 512 else 64 if T <= 1024 else 128
+        for fmt, w in (("mxfp4", want), ("nvfp4", want_nv)):
             l4 = moe.workspace_layout(GPT, T, 4, fmt)
-            assert l4.tile_rows == want4
+            assert l4.tile_rows == w
             assert [getattr(l4, n) for n in names] == offs and l4.total == lay.total
             assert l4.max_tiles >= T * 4 // l4.tile_rows + min(T * 4, 128)
         # enough tiles for any routing: every expert's partial tile plus full tiles

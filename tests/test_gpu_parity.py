@@ -302,29 +302,34 @@ def test_forced_route_that_does_not_fit_is_refused():
         moe.set_plan(0, "auto")
 
 
-@pytest.mark.parametrize("T", [8, 9, 32, 33, 128, 129, 224, 225, 512, 1024, 2048])
-def test_gpt_oss_parity_at_the_plan_cutoffs(gpt_layer, T):
+@pytest.mark.parametrize("T,act_format", [(8, "mxfp8"), (9, "mxfp8"), (32, "mxfp8"), (33, "mxfp8"), (128, "mxfp8"),
+                                          (129, "mxfp8"), (224, "mxfp8"), (225, "mxfp8"), (512, "mxfp8"),
+                                          (1024, "mxfp8"), (2048, "mxfp8"), (224, "mxfp4"), (225, "mxfp4"),
+                                          (1024, "mxfp4")])
+def test_gpt_oss_parity_at_the_plan_cutoffs(gpt_layer, T, act_format):
     """Either side of every automatic cutoff: cluster / grid routing at 8, grid /
     tensor-core routing at 32, token tiles of 8 / 16 rows at 128, and 16-row tiles
     (weights-on-M kernel) / 128-row tiles (tokens-on-M kernel) at 224 (7 / 8 rows
-    per expert on average); then the tokens-on-M kernel at 512, 1024 and 2048.
-    Routing, grouping and the gathered rows are checked for every token, the
-    output on up to 24 tokens (the oracle runs one token per host thread)."""
+    per expert on average), for MXFP8 and MXFP4 activations; then the tokens-on-M
+    kernel at 512, 1024 and 2048.  Routing, grouping and the gathered rows are
+    checked for every token, the output on up to 24 tokens (the oracle runs one
+    token per host thread)."""
     cpu_inp, dev_inp, packed = _gpt_inputs(gpt_layer, T)
-    run = mc.run_gpu(dev_inp, packed)
+    run = mc.run_gpu(dev_inp, packed, act_format=act_format)
     logits, _, _ = oracle.route(cpu_inp.x, cpu_inp.router_w, cpu_inp.router_b, 4)
     ties = mc.check_routing(run, cpu_inp.x, cpu_inp.router_w, cpu_inp.router_b, logits)
-    xq, xs = oracle.mxfp8_quantize(mc.bf16_to_f64(cpu_inp.x))
-    mc.check_quantised_x(run, xq, xs)
     cnt, off, sr, inv = mc.check_grouping(run, T)
-    mc.check_gathered(run, T, sr, xq, xs)
+    if act_format == "mxfp8":
+        xq, xs = oracle.mxfp8_quantize(mc.bf16_to_f64(cpu_inp.x))
+        mc.check_quantised_x(run, xq, xs)
+        mc.check_gathered(run, T, sr, xq, xs)
     e_max = int(np.argmax(cnt))
     last = [int(sr[p]) // 4 for p in range(max(off[e_max], off[e_max + 1] - 4), off[e_max + 1])]
     spread = np.linspace(0, T - 1, min(T, 20)).astype(int).tolist()
     sample = sorted(set(spread + last) - ties)
-    ref = mc.oracle_tokens_parallel(cpu_inp, sample)
+    ref = mc.oracle_tokens_parallel(cpu_inp, sample, act_format)
     allow, _ = mc.check_intermediate(run, ref, cpu_inp, inv.reshape(T, 4)[sample])
-    mc.compare_out(mc.bf16_to_f64(run.out)[sample], ref["out"], f"T={T}", allow=allow)
+    mc.compare_out(mc.bf16_to_f64(run.out)[sample], ref["out"], f"T={T} {act_format}", allow=allow)
 
 
 def test_nvfp4_pack_matches_the_oracle_conversion():
