@@ -548,16 +548,24 @@ def _e2e(layers: Layers, w: dict, steps: int, warmup: int, device, dist):
                                  "(own buffers and workspace each); copies overlap the other request's kernels"}}
 
 
+def _source_hash(names) -> str:
+    """First 16 hex digits of the SHA-256 of the named kernel sources, concatenated."""
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "mxfp4_mixture_experts_gemv_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def _traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's sources
+    (the kernel file and the headers it includes) are unchanged."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)[f"{kernel}@{workload}"]
-        src = os.path.join(ROOT, "mxfp4_mixture_experts_gemv_gb300", "csrc", rec["source"])
-        with open(src, "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest()[:16] != rec["source_sha256_16"]:
-                return None
+        if _source_hash(rec["sources"]) != rec["sources_sha256_16"]:
+            return None
         return rec["dram_bytes_per_launch"]
     except Exception:
         return None
