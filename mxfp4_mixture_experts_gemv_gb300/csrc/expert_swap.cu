@@ -2,9 +2,11 @@
 //
 // Same layer as the weights-on-M kernel (expert_gemm.cu): E2M1 weights x E4M3
 // activations, one E8M0 scale per 32 contraction elements on both sides
-// (tcgen05 kind::mxf8f6f4 block-scaled MMA, fp32 accumulation in tensor memory):
+// (tcgen05 kind::mxf8f6f4 block-scaled MMA, fp32 accumulation in tensor memory),
+// or with MXFP4 activations E2M1 x E2M1 (kind::mxf4, FP4 = true):
 //
 //   gate_up units: g = Xp . Wgu[e]^T + bgu[e]; epilogue h = silu(gate) * up, MXFP8(h)
+//                  (MXFP4(h) with MXFP4 activations)
 //   down units:    y = hq . Wd[e]^T + bd[e]
 //
 // A unit is one token tile of up to 128 rows (MMA M = 128; rows past the tile are
