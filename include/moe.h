@@ -358,7 +358,7 @@ moe_status moe_residual_rmsnorm(float *x_res, const void *layer_out, int32_t T, 
  * T <= 8, _GRID T <= 32, _TENSOR_CORE any T) and the expert kernel
  * (MOE_EXPERT_AUTO = the measured default; _WEIGHTS_M = weight rows in the MMA's
  * M slot and token rows in N, any tile height; _TOKENS_M = 128 token rows in M and
- * two 128-row weight tiles in N, 128-row tiles and MXFP8 or MXFP4 activations only).
+ * two 128-row weight tiles in N, 128-row tiles only).
  * Process-wide.  moe_workspace_size
  * and moe_workspace_layout_get follow the tile override, so size workspaces
  * after setting it.  A forced routing path or expert kernel that does not fit

@@ -415,7 +415,7 @@ cudaError_t launch_combine(const float* y, const int32_t* inv_pos, const float* 
 cudaError_t launch_expert_mlp(const PackedHeader& h, const uint8_t* packed, const ExpertMlpBuffers& b, int T, int k,
                               int max_tiles, int tile_rows, int num_sms, int fmt, cudaStream_t s);
 // The same layer for 128-row token tiles with the tokens in the MMA M slot and two
-// weight tiles in N (MXFP8 or MXFP4 activations); y is combined by launch_combine.
+// weight tiles in N (any activation format); y is combined by launch_combine.
 cudaError_t launch_expert_swap(const PackedHeader& h, const uint8_t* packed, const ExpertMlpBuffers& b, int T, int k,
                                int max_tiles, int num_sms, int fmt, cudaStream_t s);
 // whether the packed layer's weight tiles pair up as the tokens-on-M kernel reads them

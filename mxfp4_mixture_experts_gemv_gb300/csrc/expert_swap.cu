@@ -3,10 +3,12 @@
 // Same layer as the weights-on-M kernel (expert_gemm.cu): E2M1 weights x E4M3
 // activations, one E8M0 scale per 32 contraction elements on both sides
 // (tcgen05 kind::mxf8f6f4 block-scaled MMA, fp32 accumulation in tensor memory),
-// or with MXFP4 activations E2M1 x E2M1 (kind::mxf4, FP4 = true):
+// or with MXFP4 activations E2M1 x E2M1 (kind::mxf4, FP4 = true), or NVFP4
+// weights and activations (kind::mxf4nvf4, NV = true: UE4M3 scales per 16
+// elements and a global scale per weight projection):
 //
 //   gate_up units: g = Xp . Wgu[e]^T + bgu[e]; epilogue h = silu(gate) * up, MXFP8(h)
-//                  (MXFP4(h) with MXFP4 activations)
+//                  (MXFP4(h) or NVFP4(h) with FP4 activations)
 //   down units:    y = hq . Wd[e]^T + bd[e]
 //
 // A unit is one token tile of up to 128 rows (MMA M = 128; rows past the tile are
@@ -48,24 +50,29 @@ namespace {
 constexpr int kSwThreads = 320;
 constexpr int kSwEpiThreads = 256;
 constexpr int kSwQ = 4;                            // tile queue entries
-constexpr uint32_t kSwSF = 3 * kAtomBytes;         // scale atoms: tokens, weight tile 0, weight tile 1
 constexpr uint32_t kSwBars = 1024;
-constexpr uint32_t kSwSfCols = 12;                 // tmem columns of one stage's scales (4 per atom)
 
 // Stage shapes.  MXFP8 activations (kind::mxf8f6f4): 128 token rows of 128 E4M3
 // codes (16 KB) and 256 weight rows with the E2M1 codes unpacked to bytes (32 KB),
-// four stages.  MXFP4 activations (kind::mxf4): both operands packed, two codes per
-// byte (8 KB + 16 KB), so twice the stages fit.
-template <bool FP4>
+// four stages.  MXFP4 activations (kind::mxf4) and NVFP4 (kind::mxf4nvf4): both
+// operands packed, two codes per byte (8 KB + 16 KB), so twice the stages fit.
+// Scale atoms per stage: tokens, then weight tile 0 and 1 (one atom each per
+// k-tile; NVFP4 two each, one per 64 elements: tokens a0 a1, tile 0 a0 a1, tile 1
+// a0 a1), four tensor-memory columns per atom.
+template <bool FP4, bool NV>
 struct SwCfg {
   static constexpr int kStages = FP4 ? 8 : 4;
+  static constexpr int kSA = NV ? 2 : 1;  // scale atoms per k-tile and 128 rows
   static constexpr uint32_t kRowA = FP4 ? 64 : kTileK;  // bytes of a token row's k-tile
   static constexpr uint32_t kA = kTileM * kRowA;
   static constexpr uint32_t kB = 2 * kTileM * (FP4 ? 64 : kTileK);
-  static constexpr uint32_t kStage = kA + kB + kSwSF;
+  static constexpr uint32_t kSF = 3 * kSA * kAtomBytes;
+  static constexpr uint32_t kSfCols = 12 * kSA;
+  static constexpr uint32_t kStage = kA + kB + kSF;
   static constexpr uint32_t kSmem = 1024 + kStages * kStage + kSwBars;
+  static_assert(!NV || FP4, "NVFP4 operands are packed");
   static_assert(kSmem <= 227 * 1024, "shared memory");
-  static_assert(256 + kSwSfCols * kStages <= 512, "tensor memory columns");
+  static_assert(256 + kSfCols * kStages <= 512, "tensor memory columns");
   static_assert((2 * kStages + 3 + 2 * kSwQ) * 8 + 16 + 16 * (kSwQ + 1) <= kSwBars, "barrier area");
 };
 
@@ -88,6 +95,7 @@ struct SwapParams {
   int d_mtiles, d_ktiles, d_rows_stored;
   int I, H;
   int weights_evict_first;
+  const float* nv_amax;   // NVFP4 weights: each projection's amax (gate_up, down), for its global scale
 };
 
 struct Unit {
@@ -105,12 +113,12 @@ __device__ __forceinline__ Unit unit_ref(int u, int n_gu, int gp, int dp) {
   return r;
 }
 
-template <bool FP4>
+template <bool FP4, bool NV>
 __global__ void __launch_bounds__(kSwThreads, 1)
     expert_swap_kernel(const __grid_constant__ Maps maps, const SwapParams p) {
-  using C = SwCfg<FP4>;
-  constexpr int kSwStages = C::kStages;
-  constexpr uint32_t kSwA = C::kA, kSwB = C::kB;
+  using C = SwCfg<FP4, NV>;
+  constexpr int kSwStages = C::kStages, SA = C::kSA;
+  constexpr uint32_t kSwA = C::kA, kSwB = C::kB, kSwSF = C::kSF, kSwSfCols = C::kSfCols;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -203,8 +211,8 @@ __global__ void __launch_bounds__(kSwThreads, 1)
       const int m0 = 2 * r.j, nm = min(2, m_tiles - m0);
       const int rw0 = min(kTileM, rows_stored - m0 * kTileM);             // 64 for a tail weight tile
       const int rw1 = nm == 2 ? min(kTileM, rows_stored - (m0 + 1) * kTileM) : 0;
-      const uint8_t* sfw = (r.gu ? p.gu_sfa : p.d_sfa) + ((int64_t)td.x * m_tiles + m0) * k_tiles * kAtomBytes;
-      const uint8_t* sfx = (r.gu ? p.xp_sf : p.hq_sf) + (int64_t)r.b * k_tiles * kAtomBytes;
+      const uint8_t* sfw = (r.gu ? p.gu_sfa : p.d_sfa) + ((int64_t)td.x * m_tiles + m0) * k_tiles * SA * kAtomBytes;
+      const uint8_t* sfx = (r.gu ? p.xp_sf : p.hq_sf) + (int64_t)r.b * k_tiles * SA * kAtomBytes;
       const int bi = min(act_box_index(td.z), kActBoxes - 1);
       const CUtensorMap* amap = r.gu ? &maps.xp[bi] : &maps.hq[bi];
       const CUtensorMap* w0map = r.gu ? (rw0 == kTileM ? &maps.gu : &maps.gut) : (rw0 == kTileM ? &maps.d : &maps.dt);
@@ -212,7 +220,7 @@ __global__ void __launch_bounds__(kSwThreads, 1)
       const int w0row = (int)tile_row0(td.x, m0, 0, rows_stored, k_tiles);
       const int w1row = nm == 2 ? (int)tile_row0(td.x, m0 + 1, 0, rows_stored, k_tiles) : 0;
       const uint32_t bytes =
-          (uint32_t)(act_box_rows(bi) * C::kRowA + (rw0 + rw1) * kTileRowBytes + (1 + nm) * kAtomBytes);
+          (uint32_t)(act_box_rows(bi) * C::kRowA + (rw0 + rw1) * kTileRowBytes + (1 + nm) * SA * kAtomBytes);
       // two full weight tiles take the pair boxes
       const bool pair = nm == 2 && rw0 == kTileM && rw1 == kTileM;
       const int claim_st = max(0, k_tiles - 8), fetch_st = max(0, k_tiles - 3);
@@ -251,18 +259,19 @@ __global__ void __launch_bounds__(kSwThreads, 1)
             // k-tile kt of both weight tiles (rows kt*128.. of tiles m0 and m0+1 of
             // expert e) and their two scale atoms, one box each
             tma_load_4d_hint(b_s, r.gu ? &maps.gup : &maps.dp, &full[s], 0, kt * kTileM, m0, td.x, wpol);
-            tma_load_3d_hint(sf + kAtomBytes, r.gu ? &maps.gusf : &maps.dsf, &full[s], 0, kt, td.x * m_tiles + m0,
-                             wpol);
+            tma_load_3d_hint(sf + SA * kAtomBytes, r.gu ? &maps.gusf : &maps.dsf, &full[s], 0, kt * SA,
+                             td.x * m_tiles + m0, wpol);
           } else {
             tma_load_2d_hint(b_s, w0map, &full[s], 0, w0row + kt * rw0, wpol);
             if (nm == 2)
               tma_load_2d_hint(b_s + rw0 * (FP4 ? kTileRowBytes : kTileK), w1map, &full[s], 0, w1row + kt * rw1, wpol);
-            bulk_g2s_hint(sf + kAtomBytes, sfw + kt * kAtomBytes, kAtomBytes, &full[s], wpol);
+            bulk_g2s_hint(sf + SA * kAtomBytes, sfw + kt * SA * kAtomBytes, SA * kAtomBytes, &full[s], wpol);
             if (nm == 2)
-              bulk_g2s_hint(sf + 2 * kAtomBytes, sfw + (k_tiles + kt) * kAtomBytes, kAtomBytes, &full[s], wpol);
+              bulk_g2s_hint(sf + 2 * SA * kAtomBytes, sfw + (k_tiles + kt) * SA * kAtomBytes, SA * kAtomBytes,
+                            &full[s], wpol);
           }
           tma_load_2d(sA + s * kSwA, amap, &full[s], kt * (int)C::kRowA, td.y);
-          bulk_g2s(sf, sfx + kt * kAtomBytes, kAtomBytes, &full[s]);
+          bulk_g2s(sf, sfx + kt * SA * kAtomBytes, SA * kAtomBytes, &full[s]);
         }
         __syncwarp();
         ++issued;
@@ -312,8 +321,9 @@ __global__ void __launch_bounds__(kSwThreads, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t idesc0 = FP4 ? idesc_mxf8f6f4(128, (uint32_t)n_mma, 1 /*E2M1*/, 1 /*E2M1*/, 0, 0)
-                                  : idesc_mxf8f6f4(128, (uint32_t)n_mma, 0 /*E4M3*/, 5 /*E2M1*/, 0, 0);
+      uint32_t idesc0 = FP4 ? idesc_mxf8f6f4(128, (uint32_t)n_mma, 1 /*E2M1*/, 1 /*E2M1*/, 0, 0)
+                            : idesc_mxf8f6f4(128, (uint32_t)n_mma, 0 /*E4M3*/, 5 /*E2M1*/, 0, 0);
+      if (NV) idesc0 &= ~(1u << 23);  // block scales in UE4M3, not UE8M0
       for (int kt = 0; kt < k_tiles; ++kt) {
         if (!mbar_wait_warp(&full[s], ph, p.wait_ns)) {
           if (lane == 0) {
@@ -327,10 +337,29 @@ __global__ void __launch_bounds__(kSwThreads, 1)
         const uint32_t sf_t = tmem + 256u + (uint32_t)s * kSwSfCols;
         const uint32_t sf_s = smem_u32(sSF + s * kSwSF);
         if (elect_one()) {
-          tmem_cp_32x128b_x4(sf_t, sdesc_sf_atom(sf_s));                      // A: token scales
-          tmem_cp_32x128b_x4(sf_t + 4u, sdesc_sf_atom(sf_s + kAtomBytes));    // B: weight rows 0..127
-          if (nm == 2) tmem_cp_32x128b_x4(sf_t + 8u, sdesc_sf_atom(sf_s + 2 * kAtomBytes));  // rows 128..255
-          if constexpr (FP4) {
+          if constexpr (NV) {
+            // columns: token atoms a0 a1 at 0 and 4; for each 64-element half j the
+            // B scales of weight rows 0..127 then 128..255 side by side at 8 + 8j
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              tmem_cp_32x128b_x4(sf_t + 4u * j, sdesc_sf_atom(sf_s + j * kAtomBytes));
+              tmem_cp_32x128b_x4(sf_t + 8u + 8u * j, sdesc_sf_atom(sf_s + (2 + j) * kAtomBytes));
+              if (nm == 2) tmem_cp_32x128b_x4(sf_t + 12u + 8u * j, sdesc_sf_atom(sf_s + (4 + j) * kAtomBytes));
+            }
+          } else {
+            tmem_cp_32x128b_x4(sf_t, sdesc_sf_atom(sf_s));                      // A: token scales
+            tmem_cp_32x128b_x4(sf_t + 4u, sdesc_sf_atom(sf_s + kAtomBytes));    // B: weight rows 0..127
+            if (nm == 2) tmem_cp_32x128b_x4(sf_t + 8u, sdesc_sf_atom(sf_s + 2 * kAtomBytes));  // rows 128..255
+          }
+          if constexpr (NV) {
+            // two MMAs of K = 64, each with the four 16-element block scales of one atom
+            const uint64_t ad = sdesc_sw64(smem_u32(sA + s * kSwA));
+            const uint64_t bd = sdesc_sw64(smem_u32(sB + s * kSwB));
+#pragma unroll
+            for (uint32_t kk = 0; kk < 2; ++kk)
+              umma_mxf4nvf4(tmem, ad + 2u * kk, bd + 2u * kk, idesc0, sf_t + 4u * kk, sf_t + 8u + 8u * kk,
+                            (kt + (int)kk) != 0);
+          } else if constexpr (FP4) {
             // two MMAs of K = 64 (32 bytes of each 64-byte row); MMA kk takes block
             // scales 2kk and 2kk + 1 of each row
             const uint64_t ad = sdesc_sw64(smem_u32(sA + s * kSwA));
@@ -367,6 +396,9 @@ __global__ void __launch_bounds__(kSwThreads, 1)
     if (!mbar_wait_warp(drain, 0, kDrainLimitNs) && lane == 0) atomicOr(p.status, kStatusTimeoutDrain);
   } else {
     // -------------------------------------------------------------- epilogue
+    // NVFP4 weights carry a global scale per projection (the activations' is 1)
+    const float gs_gu = NV ? nvfp4_global_scale(p.nv_amax[0]) : 1.0f;
+    const float gs_d = NV ? nvfp4_global_scale(p.nv_amax[1]) : 1.0f;
     const int q = warp & 3;            // tmem lane quadrant this warp may read
     const int half = (warp - 2) >> 2;  // accumulator columns [128 half, 128 half + 128)
     const int n = 32 * q + lane;       // token row of the tile == tmem lane
@@ -428,15 +460,24 @@ __global__ void __launch_bounds__(kSwThreads, 1)
           float amax = 0.f;
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const float g = __uint_as_float(acc[32 * blk + c]) + __ldg(bias + 32 * blk + c);
-            const float up = __uint_as_float(acc[64 + 32 * blk + c]) + __ldg(bias + 64 + 32 * blk + c);
+            const float g = __uint_as_float(acc[32 * blk + c]) * gs_gu + __ldg(bias + 32 * blk + c);
+            const float up = __uint_as_float(acc[64 + 32 * blk + c]) * gs_gu + __ldg(bias + 64 + 32 * blk + c);
             h[c] = __fdividef(g, 1.0f + __expf(-g)) * up;  // rel. error ~1e-6, far below an E4M3 step
             amax = fmaxf(amax, fabsf(h[c]));
           }
           const int sx = FP4 ? mx_scale_exp<2>(amax) : mx_scale_exp<8>(amax);
           const float inv = mx_pow2_neg(sx);
           uint32_t pk[8];
-          if constexpr (FP4) {
+          uint32_t nsc[2] = {0u, 0u};  // NVFP4: the E4M3 scales of the two 16-element halves
+          if constexpr (NV) {
+            uint32_t q0[2], q1[2];
+            nsc[0] = nvfp4_block16(h, 1.0f, q0);
+            nsc[1] = nvfp4_block16(h + 16, 1.0f, q1);
+            pk[0] = q0[0];
+            pk[1] = q0[1];
+            pk[2] = q1[0];
+            pk[3] = q1[1];
+          } else if constexpr (FP4) {
 #pragma unroll
             for (int c = 0; c < 32; ++c) h[c] *= inv;
 #pragma unroll
@@ -460,12 +501,29 @@ __global__ void __launch_bounds__(kSwThreads, 1)
               dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
             }
             const int kb = 2 * mt + blk;  // MX block of the intermediate
-            uint8_t* wd = p.hq_sf + ((int64_t)r.b * p.d_ktiles + (kb >> 2)) * kAtomBytes + (n & 31) * 16 + (n >> 5) * 4;
-            wd[kb & 3] = (uint8_t)(sx + 127);
-            // the last real block also sets the padding blocks of its word (zero data
-            // past I; their scale must not be the NaN code)
-            if (kb == (p.I >> 5) - 1)
-              for (int jj = (kb & 3) + 1; jj < 4; ++jj) wd[jj] = 127;
+            if constexpr (NV) {
+              // 16-element block q = 2 kb + hh: k-tile q / 8, atom (q / 4) % 2, byte q % 4
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const int qb = 2 * kb + hh;
+                uint8_t* wd = p.hq_sf + (((int64_t)r.b * p.d_ktiles + (qb >> 3)) * 2 + ((qb >> 2) & 1)) * kAtomBytes +
+                              (n & 31) * 16 + (n >> 5) * 4;
+                wd[qb & 3] = (uint8_t)nsc[hh];
+                // the last real block also zeroes the scales of the padding blocks after
+                // it in its k-tile (zero data past I; their scale must not be a NaN code)
+                if (qb == (p.I >> 4) - 1) {
+                  for (int jj = (qb & 3) + 1; jj < 4; ++jj) wd[jj] = 0;
+                  if (((qb >> 2) & 1) == 0) *reinterpret_cast<uint32_t*>(wd + kAtomBytes) = 0u;
+                }
+              }
+            } else {
+              uint8_t* wd = p.hq_sf + ((int64_t)r.b * p.d_ktiles + (kb >> 2)) * kAtomBytes + (n & 31) * 16 + (n >> 5) * 4;
+              wd[kb & 3] = (uint8_t)(sx + 127);
+              // the last real block also sets the padding blocks of its word (zero data
+              // past I; their scale must not be the NaN code)
+              if (kb == (p.I >> 5) - 1)
+                for (int jj = (kb & 3) + 1; jj < 4; ++jj) wd[jj] = 127;
+            }
           }
         }
       } else if (present && store) {
@@ -479,10 +537,10 @@ __global__ void __launch_bounds__(kSwThreads, 1)
               const int f = mt * kTileM + c0 + c;
               if (f < p.H) {  // H is a multiple of 32: whole groups of four are in or out
                 float4 o;
-                o.x = __uint_as_float(acc[c0 + c]) + __ldg(bias + c0 + c);
-                o.y = __uint_as_float(acc[c0 + c + 1]) + __ldg(bias + c0 + c + 1);
-                o.z = __uint_as_float(acc[c0 + c + 2]) + __ldg(bias + c0 + c + 2);
-                o.w = __uint_as_float(acc[c0 + c + 3]) + __ldg(bias + c0 + c + 3);
+                o.x = __uint_as_float(acc[c0 + c]) * gs_d + __ldg(bias + c0 + c);
+                o.y = __uint_as_float(acc[c0 + c + 1]) * gs_d + __ldg(bias + c0 + c + 1);
+                o.z = __uint_as_float(acc[c0 + c + 2]) * gs_d + __ldg(bias + c0 + c + 2);
+                o.w = __uint_as_float(acc[c0 + c + 3]) * gs_d + __ldg(bias + c0 + c + 3);
                 *reinterpret_cast<float4*>(yrow + c0 + c) = o;
               }
             }
@@ -528,14 +586,15 @@ bool make_weight_pair_map(CUtensorMap* map, const uint8_t* base, int E, int rows
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The scale atoms [E][m_tiles][k_tiles][512 bytes] as 3-D {128 words, k-tile,
-// (expert, m-tile)}: a box holds the atoms of one k-tile of two consecutive m-tiles.
-bool make_scale_pair_map(CUtensorMap* map, const uint8_t* base, int E, int m_tiles, int k_tiles) {
+// The scale atoms [E][m_tiles][k_tiles][atoms][512 bytes] (atoms = 1, or 2 for
+// NVFP4) as 3-D {128 words, (k-tile, atom), (expert, m-tile)}: a box holds the atoms
+// of one k-tile of two consecutive m-tiles.
+bool make_scale_pair_map(CUtensorMap* map, const uint8_t* base, int E, int m_tiles, int k_tiles, int atoms) {
   auto enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)(kAtomBytes / 4), (cuuint64_t)k_tiles, (cuuint64_t)E * m_tiles};
-  cuuint64_t strides[2] = {(cuuint64_t)kAtomBytes, (cuuint64_t)k_tiles * kAtomBytes};
-  cuuint32_t box[3] = {kAtomBytes / 4, 1, 2};
+  cuuint64_t dims[3] = {(cuuint64_t)(kAtomBytes / 4), (cuuint64_t)k_tiles * atoms, (cuuint64_t)E * m_tiles};
+  cuuint64_t strides[2] = {(cuuint64_t)kAtomBytes, (cuuint64_t)k_tiles * atoms * kAtomBytes};
+  cuuint32_t box[3] = {kAtomBytes / 4, (cuuint32_t)atoms, 2};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint8_t*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -549,22 +608,23 @@ bool expert_swap_supported(const PackedHeader& h) {
 
 cudaError_t launch_expert_swap(const PackedHeader& h, const uint8_t* packed, const ExpertMlpBuffers& b, int T, int k,
                                int max_tiles, int num_sms, int fmt, cudaStream_t s) {
-  if (fmt != kActMxfp8 && fmt != kActMxfp4) return cudaErrorInvalidValue;
-  const bool fp4 = fmt == kActMxfp4;
+  if (fmt != kActMxfp8 && fmt != kActMxfp4 && fmt != kActNvfp4) return cudaErrorInvalidValue;
+  const bool fp4 = fmt != kActMxfp8, nv = fmt == kActNvfp4;
+  const int atoms = nv ? 2 : 1;
   const int TK = T * k;
   struct Key {
     const uint8_t *packed, *xp, *hq;
-    int E, H, I, TK, fp4;
+    int E, H, I, TK, fmt;
     bool operator==(const Key& o) const {
       return packed == o.packed && xp == o.xp && hq == o.hq && E == o.E && H == o.H && I == o.I && TK == o.TK &&
-             fp4 == o.fp4;
+             fmt == o.fmt;
     }
   };
   static std::mutex mu;
   static Key keys[32];
   static Maps cache[32];
   static int n_cached = 0, next_slot = 0;
-  const Key key{packed, b.xp, b.hq, h.E, h.H, h.I, TK, fp4 ? 1 : 0};
+  const Key key{packed, b.xp, b.hq, h.E, h.H, h.I, TK, fmt};
   Maps m;
   bool hit = false;
   {
@@ -588,11 +648,11 @@ cudaError_t launch_expert_swap(const PackedHeader& h, const uint8_t* packed, con
     // (the only ones whose units take them)
     if (h.gu_rows_stored >= 2 * kTileM &&
         (!make_weight_pair_map(&m.gup, packed + h.off_gu_data, h.E, h.gu_rows_stored, h.gu_ktiles, fp4) ||
-         !make_scale_pair_map(&m.gusf, packed + h.off_gu_sf, h.E, h.gu_mtiles, h.gu_ktiles)))
+         !make_scale_pair_map(&m.gusf, packed + h.off_gu_sf, h.E, h.gu_mtiles, h.gu_ktiles, atoms)))
       return cudaErrorInvalidValue;
     if (h.d_rows_stored >= 2 * kTileM &&
         (!make_weight_pair_map(&m.dp, packed + h.off_d_data, h.E, h.d_rows_stored, h.d_ktiles, fp4) ||
-         !make_scale_pair_map(&m.dsf, packed + h.off_d_sf, h.E, h.d_mtiles, h.d_ktiles)))
+         !make_scale_pair_map(&m.dsf, packed + h.off_d_sf, h.E, h.d_mtiles, h.d_ktiles, atoms)))
       return cudaErrorInvalidValue;
     for (int i = 0; i < kActBoxes; ++i) {
       const int rows = act_box_rows(i);
@@ -631,15 +691,15 @@ cudaError_t launch_expert_swap(const PackedHeader& h, const uint8_t* packed, con
   p.I = h.I;
   p.H = h.H;
   p.weights_evict_first = (int64_t)T * k <= (int64_t)h.E * kTileM;
-  static bool attr[2] = {false, false};
-  const uint32_t smem = fp4 ? SwCfg<true>::kSmem : SwCfg<false>::kSmem;
-  if (!attr[fp4]) {
-    cudaError_t e = fp4 ? cudaFuncSetAttribute(expert_swap_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)smem)
-                        : cudaFuncSetAttribute(expert_swap_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)smem);
+  p.nv_amax = reinterpret_cast<const float*>(packed + kAmaxOffset);
+  static bool attr[3] = {false, false, false};
+  const uint32_t smem = nv ? SwCfg<true, true>::kSmem : fp4 ? SwCfg<true, false>::kSmem : SwCfg<false, false>::kSmem;
+  auto kernel = nv ? expert_swap_kernel<true, true> : fp4 ? expert_swap_kernel<true, false>
+                                                          : expert_swap_kernel<false, false>;
+  if (!attr[fmt]) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    attr[fp4] = true;
+    attr[fmt] = true;
   }
   const int units = max_tiles * ((h.gu_mtiles + 1) / 2 + (h.d_mtiles + 1) / 2);
   cudaLaunchConfig_t cfg = {};
@@ -654,8 +714,7 @@ cudaError_t launch_expert_swap(const PackedHeader& h, const uint8_t* packed, con
   attrs[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  return fp4 ? cudaLaunchKernelEx(&cfg, expert_swap_kernel<true>, m, p)
-             : cudaLaunchKernelEx(&cfg, expert_swap_kernel<false>, m, p);
+  return cudaLaunchKernelEx(&cfg, kernel, m, p);
 }
 
 }  // namespace moe

@@ -255,16 +255,17 @@ def test_forced_plans_meet_the_oracle(T, tile_rows, route, expert):
         moe.set_plan(0, "auto")
 
 
-@pytest.mark.parametrize("act_format", ["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("act_format", ["mxfp8", "mxfp4", "nvfp4"])
 @pytest.mark.parametrize("expert", ["weights_m", "tokens_m"])
 def test_both_expert_kernels_on_ragged_tails(expert, act_format):
-    """H = 288 (a 64-row down tail tile), I = 192 (three gate_up tiles: one pair and
-    a single), 128-row token tiles with a ragged last tile; MXFP8 and MXFP4
-    activations (kind::mxf8f6f4 and kind::mxf4)."""
-    shape = ms.LayerShape(T=90, H=288, I=192, E=6, k=3)
+    """Ragged shapes: a 64-row down tail tile, three gate_up tiles (one pair and a
+    single), 128-row token tiles with a ragged last tile; MXFP8, MXFP4 and NVFP4
+    activations (kind::mxf8f6f4, kind::mxf4, kind::mxf4nvf4).  H = 288 and I = 192
+    (NVFP4 packing needs multiples of 64: H = 320 there)."""
+    shape = ms.LayerShape(T=90, H=320 if act_format == "nvfp4" else 288, I=192, E=6, k=3)
     inp = ms.make_layer(shape, seed=61)
     dev = inp.to("cuda")
-    _, packed = mc.pack(dev)
+    _, packed = mc.pack(dev, nvfp4=act_format == "nvfp4")
     moe.set_plan(128, "auto", expert)
     try:
         run = mc.run_gpu(dev, packed, act_format=act_format)
@@ -273,17 +274,18 @@ def test_both_expert_kernels_on_ragged_tails(expert, act_format):
         moe.set_plan(0, "auto")
 
 
+@pytest.mark.parametrize("act_format", ["mxfp4", "nvfp4"])
 @pytest.mark.parametrize("T", [20, 300])
-def test_tokens_on_m_kernel_with_mxfp4_activations(T):
-    """The tokens-on-M kernel in its kind::mxf4 form (both operands packed, eight
-    stages) on 128-row token tiles."""
+def test_tokens_on_m_kernel_with_fp4_activations(T, act_format):
+    """The tokens-on-M kernel in its kind::mxf4 and kind::mxf4nvf4 forms (both
+    operands packed, eight stages) on 128-row token tiles."""
     shape = ms.LayerShape(T=T, H=256, I=128, E=8, k=4)
     inp = ms.make_layer(shape, seed=70 + T)
     dev = inp.to("cuda")
-    _, packed = mc.pack(dev)
+    _, packed = mc.pack(dev, nvfp4=act_format == "nvfp4")
     moe.set_plan(128, "auto", "tokens_m")
     try:
-        run = mc.run_gpu(dev, packed, act_format="mxfp4")
+        run = mc.run_gpu(dev, packed, act_format=act_format)
         assert run.layout.tile_rows == 128
         _full_check(inp, run, strict=False)
     finally:
