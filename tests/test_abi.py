@@ -216,3 +216,33 @@ def test_dense_forward_fails_loudly_without_a_gpu(L):
     ws = L.moe_dense_workspace_size(128, 256, 4)
     assert L.moe_dense_forward(128, 256, FAKE, 4, FAKE, FAKE, FAKE, ws, None) == 6
     assert b"cudaError" in L.moe_last_error()
+
+
+def test_workspace_sections_hold_every_formats_tiles():
+    """For random layer shapes and token counts, each activation format's tile height
+    and tile capacity fit the shared section offsets: the tile list, the gate_up
+    counters and both scale-atom sections are sized for the largest tile count any
+    format can produce (every expert's partial tile plus the full tiles)."""
+    import random
+    rng = random.Random(7)
+    for _ in range(300):
+        E = rng.choice([1, 2, 3, 8, 32, 128, 200, 256])
+        k = rng.randint(1, min(8, E))
+        H = 32 * rng.randint(1, 100)
+        I = 64 * rng.randint(1, 50)
+        T = rng.choice([0, 1, rng.randint(1, 64), rng.randint(1, 3000), rng.randint(1, 20000)])
+        dims = moe.LayerDims(E, H, I)
+        lays = {f: moe.workspace_layout(dims, T, k, f) for f in ("mxfp8", "mxfp4", "nvfp4")}
+        base = lays["mxfp8"]
+        kth, kti = -(-H // 128), -(-I // 128)
+        TK = T * k
+        for f, l in lays.items():
+            for name, _ in moe.WorkspaceLayout._fields_[:-2]:
+                if name not in ("max_tiles", "tile_rows"):
+                    assert getattr(l, name) == getattr(base, name), (f, name)
+            assert l.tile_rows in (8, 16, 32, 64, 128)
+            assert l.max_tiles >= TK // l.tile_rows + min(TK, E), (f, E, k, T)
+            assert l.done_tok - l.done_gu >= 4 * l.max_tiles
+            assert l.xp - l.tiles >= (4 + 4 * l.max_tiles) * 4
+            assert l.hq - l.xp_sf >= l.max_tiles * kth * 2 * 512
+            assert l.y - l.hq_sf >= l.max_tiles * kti * 2 * 512
